@@ -1,0 +1,485 @@
+"""KDA benchmark: one JSON line on rank 0.
+
+Workload (one "step"): chunked prefill of 4 sequences x 4096 tokens, 16 heads,
+dk = dv = 128, bf16 inputs, fp32 initial state ~ N(0, 0.01) in, final state
+out (one kda_chunk_fwd call). Inputs (~400 MB) are larger than the 129 MB L2,
+so no flush is needed between steps. The JSON line also carries the decode
+step (256 sequences x 32 heads, fp32 states in HBM) in GB/s of HBM traffic
+and the long-context segment scan (1,048,576 tokens, 8 segments).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Multi-GPU (torchrun): every rank runs its own independent batch (weak
+scaling, no collective on the data path); the timing is the max over ranks.
+"--impl reference" times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PREFILL = dict(B=4, T=4096, H=16, d=128)
+TOKENS_PER_STEP = PREFILL["B"] * PREFILL["T"]
+TOKEN_HEADS = TOKENS_PER_STEP * PREFILL["H"]
+# algorithmic bytes of the prefill path per token-head (bf16 q, k, v, log_alpha,
+# gate in; beta in; o out) and per (sequence, head) state (fp32 in + out)
+BYTES_PER_TOKEN_HEAD = 5 * 128 * 2 + 2 + 128 * 2
+STATE_BYTES = 128 * 128 * 4
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.monotonic(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = []
+        if not inside:  # window shorter than the sampling period: nearest samples
+            inside = [min(self.samples, key=lambda s: abs(s[0] - 0.5 * (t0 + t1)))[1]]
+            note = ["window_shorter_than_sampling"]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons + note,
+                "samples": len(inside)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+_CPU_INPUTS = {}
+
+
+def oracle_prefill_sample(n_tokens: int, threads: int = 0):
+    """Time the fp64 oracle on the first n_tokens of each of the 4 sequences
+    of the prefill workload (all 16 heads). Returns (seconds, token count)."""
+    import oracle
+    from linear_attention_05_gb300 import inputs
+
+    if "prefill" not in _CPU_INPUTS:
+        _CPU_INPUTS["prefill"] = inputs.make("prefill", device="cpu")
+    x = _CPU_INPUTS["prefill"]
+    B_, T_ = PREFILL["B"], PREFILL["T"]
+    idx = np.concatenate([np.arange(b * T_, b * T_ + n_tokens) for b in range(B_)])
+
+    def sel(t):
+        return t[idx].float().numpy()
+
+    args = [sel(x[n]) for n in ("q", "k", "v", "log_alpha", "beta", "gate")]
+    S0 = x["S0"].double().numpy()
+    cu = [i * n_tokens for i in range(B_ + 1)]
+    t0 = time.perf_counter()
+    oracle.forward(*args, S0, cu, n_threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, B_ * n_tokens, oracle.threads() if threads == 0 else threads
+
+
+def cpu_baseline(target_s: float = 12.0):
+    # calibrate on a small sample, then size the measured sample to ~target_s
+    dt, ntok, cores = oracle_prefill_sample(64)
+    per_tok = dt / ntok
+    n = int(min(PREFILL["T"], max(64, target_s / per_tok / PREFILL["B"])))
+    dt, ntok, cores = oracle_prefill_sample(n)
+    return {"value": ntok / dt / 1e6, "unit": "Mtok/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} tokens of each of the 4 sequences x 16 heads "
+                      f"({ntok} tokens, {ntok * 16} token-heads) in {dt:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    steps = []
+    n_tok = None
+    for i in range(args.warmup + args.steps):
+        dt, ntok, cores = oracle_prefill_sample(args.ref_tokens)
+        if i >= args.warmup:
+            steps.append(dt)
+            n_tok = ntok
+    total = sum(steps)
+    val = n_tok * len(steps) / total / 1e6
+    line = {
+        "impl": "reference", "metric": "KDA prefill Mtok/s", "value": round(val, 6),
+        "unit": "Mtok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / len(steps), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill B=4 T=4096 H=16 dk=dv=128 bf16 inputs, fp32 state",
+                   "sample_tokens_per_sequence": args.ref_tokens},
+        "cpu_baseline": {"value": round(val, 6), "unit": "Mtok/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"first {args.ref_tokens} tokens of each of the 4 sequences"
+                                   f" x 16 heads per step"},
+        "e2e": {"value": round(val, 6), "unit": "Mtok/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def time_kernels(fn, steps, stream, n_launch):
+    """Run fn() `steps` times with trace events around each of its launches;
+    returns (total ms, per-launch-index list of ms)."""
+    import linear_attention_05_gb300 as kda
+
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n_launch)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for row in evs:  # create the events before the timed region
+        for b, e in row:
+            b.record(stream)
+            e.record(stream)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        kda.kda_trace_events([b for b, _ in evs[i]], [e for _, e in evs[i]])
+        fn()
+    end.record(stream)
+    kda.kda_trace_events([], [])
+    torch.cuda.synchronize()
+    total = start.elapsed_time(end)
+    per = [sum(evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(steps)) / steps
+           for j in range(n_launch)]
+    return total, per
+
+
+def run_gpu(args, rank, world, local):
+    import linear_attention_05_gb300 as kda
+    from linear_attention_05_gb300 import inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    kda.load()
+    stream = torch.cuda.current_stream()
+
+    w = inputs.WORKLOADS["prefill"]
+    # every rank gets its own batch (weak scaling): shift the seed by rank
+    w_rank = inputs.Workload(w.name, w.lengths, w.H, w.dk, w.dv, w.dtype, w.seed + 1000 * rank,
+                             w.init_state)
+    x = inputs.make(w_rank, device=dev)
+    T, H, d = w.T_total, w.H, w.dk
+    n_seq = len(w.lengths)
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((n_seq, H, d, d), dtype=torch.float32, device=dev)
+    ws_bytes = kda.kda_chunk_fwd_workspace_size(T, n_seq, H, d, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], out,
+                          x["S0"], fs, None, n_seq, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.monotonic()
+    total_ms, per_launch = time_kernels(step, args.steps, stream, 3)
+    t_wall1 = time.monotonic()
+    barrier(world)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    total_ms = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    value = world * TOKENS_PER_STEP / (ms_per_step * 1e-3) / 1e6
+
+    # roofline of the dominant launch (chunk prep or state pass)
+    names = ["kda_chunk_table", "kda_prep_simt", "kda_state_simt"]
+    dom = int(np.argmax(per_launch))
+    alg_bytes = {  # algorithmic bytes per launch of each kernel
+        0: (n_seq + 1) * 4,
+        1: TOKEN_HEADS * (4 * d * 2 + 2),
+        2: TOKEN_HEADS * (2 * d * 2) + 2 * n_seq * H * STATE_BYTES,
+    }
+    achieved = alg_bytes[dom] / (per_launch[dom] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": None, "peak_source": pk["source"],
+                "launch_ms": [round(t, 4) for t in per_launch]}
+
+    # end to end through the public API: pinned host inputs -> device -> host
+    host = {k: v.to("cpu").pin_memory() for k, v in x.items() if k != "cu_seqlens" and v is not None}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    fs_h = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size() + fs_h.numel() * fs_h.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        kda.kda_chunk_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["log_alpha"],
+                          dev_in["beta"], dev_in["gate"], out, dev_in["S0"], fs, None, n_seq,
+                          workspace=ws, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        fs_h.copy_(fs, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    e2e = {"value": round(world * TOKENS_PER_STEP / (e2e_ms * 1e-3) / 1e6, 3), "unit": "Mtok/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": round(e2e_ms, 4)}
+    del host, dev_in
+
+    line = {
+        "metric": "KDA prefill Mtok/s & % tensor peak; decode state GB/s vs GB300 HBM peak",
+        "value": round(value, 3), "unit": "Mtok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; q,k unit-norm N(0,1), v N(0,1), beta/gate sigmoid(N(0,1)), "
+                "log_alpha max(-exp(N(-3,1)), log 0.5))",
+        "config": {"workload": "prefill B=4 T=4096 H=16 dk=dv=128 chunk=64, bf16 inputs, "
+                               "fp32 initial/final state",
+                   "global_batch": PREFILL["B"] * world, "seq_len": PREFILL["T"],
+                   "parallelism": f"independent batch per GPU x{world}",
+                   "l2": "inputs (~400 MB) larger than L2; no flush"},
+        "roofline": roofline, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": 3 * args.steps,
+    }
+
+    if rank == 0 and not args.skip_extra:
+        line["decode"] = bench_decode(dev, pk, stream)
+        line["segment_scan"] = bench_segment_scan(dev, pk, stream)
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def bench_decode(dev, pk, stream, steps=64):
+    """256 sequences x 32 heads, fp32 state (512 MiB) resident; 64 steps, one
+    kda_decode_step call per step with fresh inputs."""
+    import linear_attention_05_gb300 as kda
+    from linear_attention_05_gb300 import inputs
+
+    w = inputs.WORKLOADS["decode"]
+    N, H, d = len(w.lengths), w.H, w.dk
+    S = inputs.state(N, H, d, d, w.seed, device=dev).contiguous()
+    xs = [inputs.tokens(N, H, d, d, w.dtype, w.seed, step=s, device=dev) for s in range(steps)]
+    outs = [torch.empty((N, H, d), dtype=w.dtype, device=dev) for _ in range(steps)]
+
+    def run(i):
+        x = xs[i]
+        kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"],
+                            outs[i], S, stream=stream)
+
+    for i in range(3):
+        run(i)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for b, e in evs:
+        b.record(stream)
+        e.record(stream)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        kda.kda_trace_events([evs[i][0]], [evs[i][1]])
+        run(i)
+    t1.record(stream)
+    kda.kda_trace_events([], [])
+    torch.cuda.synchronize()
+    per_step_ms = t0.elapsed_time(t1) / steps
+    kern_ms = sum(b.elapsed_time(e) for b, e in evs) / steps
+    bytes_step = 2 * N * H * STATE_BYTES + N * H * (5 * d * 2 + 2 + d * 2)
+    gbs = bytes_step / (kern_ms * 1e-3) / 1e9
+    return {"workload": "decode 256 seq x 32 heads, dk=dv=128, bf16 tokens, fp32 state, 64 steps",
+            "value": round(gbs, 1), "unit": "GB/s", "us_per_step": round(per_step_ms * 1e3, 2),
+            "kernel_us": round(kern_ms * 1e3, 2),
+            "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": round(gbs, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                         "bytes_per_launch": bytes_step},
+            "gpu_launches": steps}
+
+
+def bench_segment_scan(dev, pk, stream, reps=2):
+    """1,048,576 tokens x 16 heads, 8 segments of 131,072: summaries, ordered
+    scan, segment re-run from the recovered entry states."""
+    import linear_attention_05_gb300 as kda
+    from linear_attention_05_gb300 import inputs
+
+    w = inputs.WORKLOADS["longctx"]
+    T, H, d, n_seg = w.T_total, w.H, w.dk, w.n_segments
+    x = inputs.make(w, device=dev)
+    cu = torch.arange(0, T + 1, T // n_seg, dtype=torch.int32, device=dev)
+    X = torch.empty((n_seg, H, d, d), dtype=torch.float32, device=dev)
+    Z = torch.empty((n_seg, H, d, d), dtype=torch.float32, device=dev)
+    E = torch.empty_like(Z)
+    Sf = torch.empty((H, d, d), dtype=torch.float32, device=dev)
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((n_seg, H, d, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(kda.kda_chunk_fwd_workspace_size(T, n_seg, H, d, d), dtype=torch.uint8,
+                     device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def run(record):
+        if record:
+            ev[0].record(stream)
+        kda.kda_segment_summary(x["k"], x["v"], x["log_alpha"], x["beta"], cu, n_seg, X, Z,
+                                workspace=ws, stream=stream)
+        if record:
+            ev[1].record(stream)
+        kda.kda_scan_combine(X, Z, None, E, Sf, stream=stream)
+        if record:
+            ev[2].record(stream)
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], out, E,
+                          fs, cu, n_seg, workspace=ws, stream=stream)
+        if record:
+            ev[3].record(stream)
+
+    run(False)
+    torch.cuda.synchronize()
+    tot = [0.0, 0.0, 0.0]
+    for _ in range(reps):
+        run(True)
+        torch.cuda.synchronize()
+        for i in range(3):
+            tot[i] += ev[i].elapsed_time(ev[i + 1]) / reps
+    th = T * H
+    scan_bytes = n_seg * H * (d * d + d * d) * 4 + n_seg * H * d * d * 4 + H * d * d * 4
+    return {"workload": "long context T=1,048,576 H=16 dk=dv=128 bf16, 8 segments",
+            "summary_ms": round(tot[0], 3), "scan_ms": round(tot[1], 4),
+            "rerun_ms": round(tot[2], 3),
+            "value": round(T / ((tot[0] + tot[1] + tot[2]) * 1e-3) / 1e6, 3), "unit": "Mtok/s",
+            "scan_gbs": round(scan_bytes / (tot[1] * 1e-3) / 1e9, 1),
+            "summary_alg_gbs": round(th * (3 * d * 2 + 2) / (tot[0] * 1e-3) / 1e9, 1),
+            "gpu_launches": 7 * reps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=256,
+                    help="reference arm: tokens per sequence timed per step")
+    ap.add_argument("--skip-extra", action="store_true", help="prefill line only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

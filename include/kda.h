@@ -1,0 +1,198 @@
+/*
+ * kda.h - C ABI of libkda: Kimi Delta Attention (KDA) on NVIDIA GB300 (sm_103a).
+ *
+ * KDA keeps, per sequence and head, a state S in R^{dk x dv} (rows = key
+ * channels, columns = value channels) and for every token t does
+ *
+ *     S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T
+ *     o_t = g_t (.) (scale * S_t^T q_t)
+ *
+ * with a_t = exp(log_alpha_t) in (0, 1]^{dk} a per-key-channel retention,
+ * b_t in [0, 1] the write strength and g_t the (already sigmoided) output gate.
+ * Sources: K3 training overview (zuoshipin.com/article/18261) section 2 "KDA"
+ * (channel-wise forget gate, delta-rule corrective write, full-rank output
+ * gate, lower bound on the per-step retention); K3 explainer
+ * (devpress.csdn.net/awstech/6a72dc33...) section 2 (predict from memory,
+ * write the error; delta rule with a channel-wise retention factor).
+ *
+ * Conventions shared by every entry point
+ *  - Ownership: the caller owns every buffer. The library allocates no device
+ *    memory; scratch space is passed in as `workspace` (size from the matching
+ *    *_workspace_size call, 256-byte aligned).
+ *  - Pointers are device pointers to contiguous row-major arrays, 16-byte
+ *    aligned. Token tensors are packed [T_total, H, d]; per-token scalars
+ *    [T_total, H]; states [n, H, dk, dv] fp32 with dv fastest.
+ *  - Work is enqueued on `stream` and is asynchronous. A call returns
+ *    KDA_OK once its kernels are launched; argument errors are returned before
+ *    anything is launched. Problems found on the device (a violated
+ *    precondition under KDA_DEBUG_CHECK, malformed cu_seqlens, a bounded wait
+ *    that ran out) set a per-device error word that kda_get_error() reads.
+ *  - Supported shapes: dk, dv in {64, 128}; chunk = 64. Other values return
+ *    KDA_ERR_UNSUPPORTED. T_total = 0 and empty sequences are valid; an empty
+ *    sequence leaves final = initial.
+ *  - Token tensors are fp32 or bf16 (`dtype`); the output has the input
+ *    dtype; states are always fp32. bf16 results are rounded to nearest even.
+ *  - Precondition (the retention lower bound): log_alpha >= -0.6953125
+ *    (= log 0.5 less one bf16 ulp). Within a 64-token chunk the decay factors
+ *    then stay below 2^64.2, well inside the fp32/bf16 range. The library does
+ *    not clamp; KDA_DEBUG_CHECK reports KDA_ERR_PRECONDITION.
+ *  - No atomics touch outputs: repeated calls give bitwise-equal results.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,  /* NULL / misaligned pointer, negative size, bad combination */
+  KDA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (dk, dv, chunk, dtype) */
+  KDA_ERR_CUDA = 3,         /* a CUDA call or launch failed */
+  KDA_ERR_TIMEOUT = 4,      /* a bounded on-device wait ran out (kda_get_error) */
+  KDA_ERR_PRECONDITION = 5, /* input outside the documented domain (kda_get_error) */
+  KDA_ERR_WORKSPACE = 6     /* workspace NULL or smaller than required */
+} kda_status;
+
+typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
+
+enum {
+  KDA_QK_L2NORM = 1u,  /* normalise q and k rows: x / sqrt(sum x^2 + 1e-6) */
+  KDA_DEBUG_CHECK = 2u /* check log_alpha >= -0.6953125 and beta in [0,1] on device */
+};
+
+/* Library version string, e.g. "libkda 0.1 sm_103a". */
+const char *kda_version(void);
+
+/*
+ * Chunked prefill over packed sequences.
+ * Source: K3 training overview section 4 "FlashKDA": per-chunk update cards
+ * (forget gate, Q/K normalisation, decay, intra-chunk correction matrix) are
+ * prepared in parallel; only the state hand-off and output read-out run in
+ * order. The result equals the token recurrence above.
+ *
+ *  q, k, log_alpha : [T_total, H, dk]   dtype
+ *  v, gate         : [T_total, H, dv]   dtype; gate NULL means g = 1
+ *  beta            : [T_total, H]       dtype, values in [0, 1]
+ *  out             : [T_total, H, dv]   dtype (written)
+ *  initial_state   : [n_seq, H, dk, dv] fp32, or NULL for zero
+ *  final_state     : [n_seq, H, dk, dv] fp32, or NULL (not written)
+ *  cu_seqlens      : device int32 [n_seq + 1], cu[0] = 0, non-decreasing,
+ *                    cu[n_seq] = T_total; NULL means n_seq sequences of
+ *                    T_total / n_seq tokens each (must divide)
+ *  chunk           : 64
+ *  workspace       : >= kda_chunk_fwd_workspace_size(...) bytes
+ * Malformed cu_seqlens found on the device set KDA_ERR_INVALID_ARG in the
+ * error word and the call writes nothing.
+ */
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
+                         const void *log_alpha, const void *beta,
+                         const void *gate, void *out,
+                         const float *initial_state, float *final_state,
+                         const int32_t *cu_seqlens, int n_seq, int64_t T_total,
+                         int H, int dk, int dv, int chunk, float scale,
+                         unsigned flags, kda_dtype dtype, void *workspace,
+                         size_t workspace_bytes, kda_stream_t stream);
+
+size_t kda_chunk_fwd_workspace_size(int64_t T_total, int n_seq, int H, int dk,
+                                    int dv, int chunk, kda_dtype dtype);
+
+/*
+ * One decode step for N sequences, one new token each, against fp32 states
+ * resident in device memory (the recurrence above, applied once).
+ * Source: K3 explainer section 2 (one corrective write per token) and the
+ * prefix-cache section 14 (a fixed-size KDA state per sequence).
+ *
+ *  q, k, log_alpha : [N, H, dk] dtype;  v, gate : [N, H, dv] dtype (gate NULL = 1)
+ *  beta            : [N, H] dtype
+ *  out             : [N, H, dv] dtype (written)
+ *  state           : [n_slots, H, dk, dv] fp32, updated in place
+ *  state_slot      : device int32 [N] giving the state row of sequence n, or
+ *                    NULL for row n. Slots must be distinct and < n_slots
+ *                    (out-of-range slots set KDA_ERR_INVALID_ARG on device
+ *                    and that sequence is skipped).
+ */
+kda_status kda_decode_step(const void *q, const void *k, const void *v,
+                           const void *log_alpha, const void *beta,
+                           const void *gate, void *out, float *state,
+                           const int32_t *state_slot, int n_slots, int N, int H,
+                           int dk, int dv, float scale, unsigned flags,
+                           kda_dtype dtype, kda_stream_t stream);
+
+/*
+ * Context-parallel segment summaries. For each segment s (token range
+ * [cu_segs[s], cu_segs[s+1])) and head: the transition X (dk x dk) and the
+ * zero-init state Z (dk x dv) such that running the segment from any entry
+ * state E gives X E + Z.
+ * Source: K3 training overview section 3 "KDA context parallel": each device
+ * emits two fixed-size pieces, how its segment rewrites existing memory and
+ * the state it builds from empty memory.
+ *
+ *  k, log_alpha : [T_total, H, dk] dtype;  v : [T_total, H, dv];  beta : [T_total, H]
+ *  cu_segs      : device int32 [n_seg + 1] (same rules as cu_seqlens)
+ *  X_out        : [n_seg, H, dk, dk] fp32;  Z_out : [n_seg, H, dk, dv] fp32
+ *  workspace    : >= kda_segment_summary_workspace_size(...) bytes
+ */
+kda_status kda_segment_summary(const void *k, const void *v,
+                               const void *log_alpha, const void *beta,
+                               const int32_t *cu_segs, int n_seg,
+                               int64_t T_total, int H, int dk, int dv,
+                               int chunk, unsigned flags, kda_dtype dtype,
+                               float *X_out, float *Z_out, void *workspace,
+                               size_t workspace_bytes, kda_stream_t stream);
+
+size_t kda_segment_summary_workspace_size(int64_t T_total, int n_seg, int H,
+                                          int dk, int dv, int chunk,
+                                          kda_dtype dtype);
+
+/*
+ * Ordered prefix scan of the segment maps, per head:
+ *   E_0 = S_init (or 0),  E_s = X_{s-1} E_{s-1} + Z_{s-1},
+ *   S_final = X_{n-1} E_{n-1} + Z_{n-1}.
+ * Source: K3 training overview section 3: the summaries are merged in order
+ * by a prefix scan that recovers the exact state before every segment.
+ *
+ *  X : [n_seg, H, dk, dk] fp32;  Z : [n_seg, H, dk, dv] fp32
+ *  S_init      : [H, dk, dv] fp32 or NULL (zero)
+ *  S_entry_out : [n_seg, H, dk, dv] fp32 (E_s), or NULL
+ *  S_final_out : [H, dk, dv] fp32, or NULL
+ * All arithmetic is fp32.
+ */
+kda_status kda_scan_combine(const float *X, const float *Z, int n_seg, int H,
+                            int dk, int dv, const float *S_init,
+                            float *S_entry_out, float *S_final_out,
+                            kda_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word of the
+ * current device. Returns KDA_OK, KDA_ERR_PRECONDITION, KDA_ERR_INVALID_ARG
+ * (malformed cu_seqlens / slots), KDA_ERR_TIMEOUT or KDA_ERR_CUDA.
+ */
+kda_status kda_get_error(kda_stream_t stream);
+
+/*
+ * Tracing. After kda_trace_events(begin, end, n) with n > 0, every entry point
+ * called from this host thread records begin[i] and end[i] (cudaEvent_t
+ * handles, created and owned by the caller) on its stream around its i-th
+ * kernel launch, i < n; launches past n are not traced. kda_chunk_fwd and
+ * kda_segment_summary launch, in order: 0 chunk table, 1 chunk prep,
+ * 2 state pass. n = 0 turns tracing off. Records nothing else and allocates
+ * nothing; the caller reads the elapsed times with cudaEventElapsedTime.
+ */
+kda_status kda_trace_events(void *const *begin, void *const *end, int n);
+
+/* Human-readable message for the last non-OK status on this host thread. */
+const char *kda_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

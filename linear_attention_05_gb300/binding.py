@@ -1,0 +1,278 @@
+"""ctypes binding over libkda: the C ABI's entry points under the same names.
+
+Argument marshalling only. Every step of KDA runs in the library's CUDA
+kernels; this module turns torch tensors into device pointers and sizes,
+passes the current CUDA stream, and raises ``KdaError`` on a non-OK status.
+There is no fallback: if ``libkda.so`` is missing or cannot be loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libkda.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "kda.h")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_CUDA = 3
+KDA_ERR_TIMEOUT = 4
+KDA_ERR_PRECONDITION = 5
+KDA_ERR_WORKSPACE = 6
+STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED",
+                3: "KDA_ERR_CUDA", 4: "KDA_ERR_TIMEOUT", 5: "KDA_ERR_PRECONDITION",
+                6: "KDA_ERR_WORKSPACE"}
+KDA_DTYPE_F32 = 0
+KDA_DTYPE_BF16 = 1
+KDA_QK_L2NORM = 1
+KDA_DEBUG_CHECK = 2
+CHUNK = 64
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def declared_functions(header: str = HEADER):
+    """Names of the functions include/kda.h declares."""
+    txt = open(header).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", txt)))
+
+
+def load(path: str = LIB_PATH):
+    """Load libkda.so (raises if it is missing) and declare the signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"libkda.so not found at {path}; run linear_attention_05_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        P, I, I64, F, U, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                               ctypes.c_uint, ctypes.c_size_t)
+        sig = {
+            "kda_version": ([], ctypes.c_char_p),
+            "kda_last_error_string": ([], ctypes.c_char_p),
+            "kda_chunk_fwd": ([P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, P, SZ, P], I),
+            "kda_chunk_fwd_workspace_size": ([I64, I, I, I, I, I, I], SZ),
+            "kda_decode_step": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, U, I, P], I),
+            "kda_segment_summary": ([P, P, P, P, P, I, I64, I, I, I, I, U, I, P, P, P, SZ, P], I),
+            "kda_segment_summary_workspace_size": ([I64, I, I, I, I, I, I], SZ),
+            "kda_scan_combine": ([P, P, I, I, I, I, P, P, P, P], I),
+            "kda_get_error": ([P], I),
+            "kda_trace_events": ([ctypes.POINTER(P), ctypes.POINTER(P), I], I),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor or None")
+    if t.numel() > 0 and not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return KDA_DTYPE_F32
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(lib, st: int):
+    if st != KDA_OK:
+        raise KdaError(st, lib.kda_last_error_string().decode())
+
+
+def _f32_or_none(t, name):
+    if t is not None and t.dtype != torch.float32:
+        raise ValueError(f"{name} must be float32")
+    return t
+
+
+# ----------------------------------------------------------------------------- raw entry points
+def kda_version() -> str:
+    """Library version string."""
+    return load().kda_version().decode()
+
+
+def kda_last_error_string() -> str:
+    return load().kda_last_error_string().decode()
+
+
+def kda_chunk_fwd_workspace_size(T_total, n_seq, H, dk, dv, chunk=CHUNK, dtype=KDA_DTYPE_BF16):
+    return int(load().kda_chunk_fwd_workspace_size(T_total, n_seq, H, dk, dv, chunk, dtype))
+
+
+def kda_segment_summary_workspace_size(T_total, n_seg, H, dk, dv, chunk=CHUNK, dtype=KDA_DTYPE_BF16):
+    return int(load().kda_segment_summary_workspace_size(T_total, n_seg, H, dk, dv, chunk, dtype))
+
+
+def _workspace(nbytes, device, workspace):
+    if workspace is not None:
+        return workspace, workspace.numel() * workspace.element_size()
+    if nbytes == 0:
+        return None, 0
+    return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
+
+
+def kda_chunk_fwd(q, k, v, log_alpha, beta, gate, out, initial_state, final_state, cu_seqlens,
+                  n_seq, scale=1.0, flags=KDA_QK_L2NORM, workspace=None, stream=None,
+                  chunk=CHUNK):
+    """Chunked prefill; writes ``out`` and (if given) ``final_state``."""
+    lib = load()
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(k)
+    _f32_or_none(initial_state, "initial_state")
+    _f32_or_none(final_state, "final_state")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    need = lib.kda_chunk_fwd_workspace_size(T, n_seq, H, dk, dv, chunk, dt)
+    ws, wsb = _workspace(need, k.device, workspace)
+    st = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(gate),
+                           _ptr(out), _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens),
+                           n_seq, T, H, dk, dv, chunk, float(scale), int(flags), dt, _ptr(ws),
+                           wsb, _stream(stream))
+    _check(lib, st)
+    return out, final_state
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, gate, out, state, state_slot=None, scale=1.0,
+                    flags=KDA_QK_L2NORM, stream=None):
+    """One token per sequence; updates ``state`` in place and writes ``out``."""
+    lib = load()
+    N, H, dk = k.shape
+    dv = v.shape[-1]
+    _f32_or_none(state, "state")
+    if state_slot is not None and state_slot.dtype != torch.int32:
+        raise ValueError("state_slot must be int32")
+    st = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(gate),
+                             _ptr(out), _ptr(state), _ptr(state_slot), state.shape[0], N, H, dk,
+                             dv, float(scale), int(flags), _dtype_code(k), _stream(stream))
+    _check(lib, st)
+    return out
+
+
+def kda_segment_summary(k, v, log_alpha, beta, cu_segs, n_seg, X_out, Z_out,
+                        flags=KDA_QK_L2NORM, workspace=None, stream=None, chunk=CHUNK):
+    """Per-segment transition X and zero-init state Z (fp32)."""
+    lib = load()
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(k)
+    if cu_segs is not None and cu_segs.dtype != torch.int32:
+        raise ValueError("cu_segs must be int32")
+    need = lib.kda_segment_summary_workspace_size(T, n_seg, H, dk, dv, chunk, dt)
+    ws, wsb = _workspace(need, k.device, workspace)
+    st = lib.kda_segment_summary(_ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(cu_segs),
+                                 n_seg, T, H, dk, dv, chunk, int(flags), dt, _ptr(X_out),
+                                 _ptr(Z_out), _ptr(ws), wsb, _stream(stream))
+    _check(lib, st)
+    return X_out, Z_out
+
+
+def kda_scan_combine(X, Z, S_init, S_entry_out, S_final_out, stream=None):
+    """Ordered scan of the segment maps (fp32)."""
+    lib = load()
+    n_seg, H, dk, dv = Z.shape
+    st = lib.kda_scan_combine(_ptr(X), _ptr(Z), n_seg, H, dk, dv, _ptr(S_init),
+                              _ptr(S_entry_out), _ptr(S_final_out), _stream(stream))
+    _check(lib, st)
+    return S_entry_out, S_final_out
+
+
+def kda_get_error(stream=None) -> int:
+    """Synchronise the stream, read and clear the device error word; returns the status."""
+    lib = load()
+    return int(lib.kda_get_error(_stream(stream)))
+
+
+def kda_trace_events(begin, end):
+    """Record torch.cuda.Event pairs around each launch of later calls on this
+    thread (begin[i]/end[i] around launch i); pass empty lists to stop."""
+    lib = load()
+    n = len(begin)
+    if n != len(end):
+        raise ValueError("begin and end must have the same length")
+    for e in list(begin) + list(end):
+        if e.cuda_event == 0:  # torch creates the event lazily
+            e.record()
+    arr_t = ctypes.c_void_p * max(n, 1)
+    b = arr_t(*[e.cuda_event for e in begin])
+    en = arr_t(*[e.cuda_event for e in end])
+    _check(lib, lib.kda_trace_events(b, en, n))
+
+
+# ----------------------------------------------------------------------------- conveniences
+def chunk_fwd(q, k, v, log_alpha, beta, gate=None, initial_state=None, cu_seqlens=None,
+              n_seq=None, scale=1.0, l2norm=True, output_final_state=True, workspace=None,
+              stream=None):
+    """Allocate the outputs with torch and call kda_chunk_fwd."""
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    if n_seq is None:
+        n_seq = (cu_seqlens.numel() - 1) if cu_seqlens is not None else 1
+    out = torch.empty((T, H, dv), dtype=v.dtype, device=v.device)
+    fs = (torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=v.device)
+          if output_final_state else None)
+    kda_chunk_fwd(q, k, v, log_alpha, beta, gate, out, initial_state, fs, cu_seqlens, n_seq,
+                  scale=scale, flags=KDA_QK_L2NORM if l2norm else 0, workspace=workspace,
+                  stream=stream)
+    return out, fs
+
+
+def decode_step(q, k, v, log_alpha, beta, gate, state, state_slot=None, scale=1.0, l2norm=True,
+                stream=None):
+    out = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    return kda_decode_step(q, k, v, log_alpha, beta, gate, out, state, state_slot, scale,
+                           KDA_QK_L2NORM if l2norm else 0, stream)
+
+
+def segment_summary(k, v, log_alpha, beta, cu_segs, l2norm=True, workspace=None, stream=None):
+    n_seg = cu_segs.numel() - 1
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    X = torch.empty((n_seg, H, dk, dk), dtype=torch.float32, device=k.device)
+    Z = torch.empty((n_seg, H, dk, dv), dtype=torch.float32, device=k.device)
+    return kda_segment_summary(k, v, log_alpha, beta, cu_segs, n_seg, X, Z,
+                               KDA_QK_L2NORM if l2norm else 0, workspace, stream)
+
+
+def scan_combine(X, Z, S_init=None, stream=None):
+    n_seg, H, dk, dv = Z.shape
+    E = torch.empty_like(Z)
+    Sf = torch.empty((H, dk, dv), dtype=torch.float32, device=Z.device)
+    return kda_scan_combine(X, Z, S_init, E, Sf, stream)

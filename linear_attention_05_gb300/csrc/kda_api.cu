@@ -1,0 +1,289 @@
+// libkda C ABI: argument validation, workspace carving and launches.
+// Every check here runs before any launch, so a rejected call has no effect.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "../../include/kda.h"
+#include "kda_common.cuh"
+
+namespace {
+
+thread_local char g_msg[512] = "no error";
+
+// caller-owned events recorded around each launch (tracing), per host thread
+constexpr int kMaxTrace = 8;
+thread_local cudaEvent_t g_tr_begin[kMaxTrace], g_tr_end[kMaxTrace];
+thread_local int g_tr_n = 0;
+
+// Records begin/end events around the idx-th launch of an entry point.
+struct Tracer {
+  cudaStream_t st;
+  int idx = 0;
+  explicit Tracer(cudaStream_t s) : st(s) {}
+  template <typename F>
+  cudaError_t operator()(F &&launch) {
+    const int i = idx++;
+    const bool on = i < g_tr_n;
+    if (on) cudaEventRecord(g_tr_begin[i], st);
+    cudaError_t e = launch();
+    if (on) cudaEventRecord(g_tr_end[i], st);
+    return e;
+  }
+};
+
+kda_status fail(kda_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+kda_status cuda_status(cudaError_t e, const char *where) {
+  if (e == cudaSuccess) return KDA_OK;
+  return fail(KDA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool shape_ok(int dk, int dv) { return (dk == 64 || dk == 128) && (dv == 64 || dv == 128); }
+
+#define KDA_REQUIRE(cond, st, ...) \
+  do {                             \
+    if (!(cond)) return fail(st, __VA_ARGS__); \
+  } while (0)
+
+kda_status check_ptr(const void *p, const char *name, bool required) {
+  if (p == nullptr) {
+    if (required) return fail(KDA_ERR_INVALID_ARG, "%s must not be NULL", name);
+    return KDA_OK;
+  }
+  if (!aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return KDA_OK;
+}
+
+#define KDA_CHECK_PTR(p, req)                       \
+  do {                                              \
+    kda_status s_ = check_ptr((p), #p, (req));      \
+    if (s_ != KDA_OK) return s_;                    \
+  } while (0)
+
+kda_status common_checks(int64_t T_total, int n_seq, int H, int dk, int dv, int chunk,
+                         kda_dtype dtype, const int32_t *cu) {
+  KDA_REQUIRE(T_total >= 0 && n_seq >= 0 && H > 0, KDA_ERR_INVALID_ARG,
+              "negative size (T_total=%lld n_seq=%d H=%d)", (long long)T_total, n_seq, H);
+  KDA_REQUIRE(dtype == KDA_DTYPE_F32 || dtype == KDA_DTYPE_BF16, KDA_ERR_UNSUPPORTED,
+              "dtype %d not supported", (int)dtype);
+  KDA_REQUIRE(shape_ok(dk, dv), KDA_ERR_UNSUPPORTED, "dk=%d dv=%d: only 64 or 128", dk, dv);
+  KDA_REQUIRE(chunk == kda::kChunk, KDA_ERR_UNSUPPORTED, "chunk=%d: only 64", chunk);
+  KDA_REQUIRE(T_total < (int64_t)INT32_MAX, KDA_ERR_UNSUPPORTED, "T_total too large");
+  KDA_REQUIRE((int64_t)n_seq * H < (int64_t)INT32_MAX / 4, KDA_ERR_UNSUPPORTED, "too many chains");
+  if (cu == nullptr && n_seq > 0)
+    KDA_REQUIRE(T_total % n_seq == 0, KDA_ERR_INVALID_ARG,
+                "cu_seqlens is NULL but T_total=%lld is not a multiple of n_seq=%d",
+                (long long)T_total, n_seq);
+  if (cu == nullptr && n_seq == 0)
+    KDA_REQUIRE(T_total == 0, KDA_ERR_INVALID_ARG, "n_seq=0 with T_total>0");
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_version(void) { return "libkda 0.1 sm_103a"; }
+
+const char *kda_last_error_string(void) { return g_msg; }
+
+size_t kda_chunk_fwd_workspace_size(int64_t T_total, int n_seq, int H, int dk, int dv,
+                                    int chunk, kda_dtype dtype) {
+  if (common_checks(T_total, n_seq, H, dk, dv, chunk, dtype, (const int32_t *)1) != KDA_OK)
+    return 0;
+  return kda::chunk_ws_bytes(T_total, n_seq, H, dk, dv);
+}
+
+size_t kda_segment_summary_workspace_size(int64_t T_total, int n_seg, int H, int dk, int dv,
+                                          int chunk, kda_dtype dtype) {
+  return kda_chunk_fwd_workspace_size(T_total, n_seg, H, dk, dv, chunk, dtype);
+}
+
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *log_alpha,
+                         const void *beta, const void *gate, void *out,
+                         const float *initial_state, float *final_state,
+                         const int32_t *cu_seqlens, int n_seq, int64_t T_total, int H, int dk,
+                         int dv, int chunk, float scale, unsigned flags, kda_dtype dtype,
+                         void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+  kda_status st = common_checks(T_total, n_seq, H, dk, dv, chunk, dtype, cu_seqlens);
+  if (st != KDA_OK) return st;
+  KDA_REQUIRE((flags & ~(unsigned)(KDA_QK_L2NORM | KDA_DEBUG_CHECK)) == 0, KDA_ERR_INVALID_ARG,
+              "unknown flag bits 0x%x", flags);
+  const bool tokens = T_total > 0;
+  KDA_CHECK_PTR(q, tokens);
+  KDA_CHECK_PTR(k, tokens);
+  KDA_CHECK_PTR(v, tokens);
+  KDA_CHECK_PTR(log_alpha, tokens);
+  KDA_CHECK_PTR(beta, false);
+  KDA_REQUIRE(!tokens || beta != nullptr, KDA_ERR_INVALID_ARG, "beta must not be NULL");
+  KDA_CHECK_PTR(gate, false);
+  KDA_CHECK_PTR(out, tokens);
+  KDA_CHECK_PTR(initial_state, false);
+  KDA_CHECK_PTR(final_state, false);
+  KDA_REQUIRE(cu_seqlens == nullptr || ((uintptr_t)cu_seqlens & 3u) == 0, KDA_ERR_INVALID_ARG,
+              "cu_seqlens is not 4-byte aligned");
+  if (n_seq == 0) return KDA_OK;
+  const size_t need = kda::chunk_ws_bytes(T_total, n_seq, H, dk, dv);
+  KDA_REQUIRE(workspace != nullptr && workspace_bytes >= need, KDA_ERR_WORKSPACE,
+              "workspace %zu bytes, need %zu", workspace_bytes, need);
+  KDA_REQUIRE(((uintptr_t)workspace & 255u) == 0, KDA_ERR_INVALID_ARG,
+              "workspace is not 256-byte aligned");
+  cudaStream_t s = (cudaStream_t)stream;
+  Tracer tr(s);
+  kda::ChunkWs ws = kda::chunk_ws_carve(workspace, T_total, n_seq, H, dk, dv);
+  st = cuda_status(tr([&] { return kda::launch_chunk_table(cu_seqlens, n_seq, T_total, ws, s); }),
+                   "chunk table");
+  if (st != KDA_OK) return st;
+  st = cuda_status(tr([&] {
+                     return kda::launch_prep(q, k, v, log_alpha, beta, cu_seqlens, n_seq, T_total,
+                                             H, dk, dv, flags, dtype, ws, true, s);
+                   }),
+                   "chunk prep");
+  if (st != KDA_OK) return st;
+  return cuda_status(tr([&] {
+                       return kda::launch_state_pass(0, gate, out, initial_state, final_state,
+                                                     nullptr, nullptr, cu_seqlens, n_seq, T_total,
+                                                     H, dk, dv, scale, dtype, ws, s);
+                     }),
+                     "state pass");
+}
+
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *log_alpha,
+                           const void *beta, const void *gate, void *out, float *state,
+                           const int32_t *state_slot, int n_slots, int N, int H, int dk, int dv,
+                           float scale, unsigned flags, kda_dtype dtype, kda_stream_t stream) {
+  KDA_REQUIRE(N >= 0 && H > 0 && n_slots >= 0, KDA_ERR_INVALID_ARG,
+              "negative size (N=%d H=%d n_slots=%d)", N, H, n_slots);
+  KDA_REQUIRE(dtype == KDA_DTYPE_F32 || dtype == KDA_DTYPE_BF16, KDA_ERR_UNSUPPORTED,
+              "dtype %d not supported", (int)dtype);
+  KDA_REQUIRE(shape_ok(dk, dv), KDA_ERR_UNSUPPORTED, "dk=%d dv=%d: only 64 or 128", dk, dv);
+  KDA_REQUIRE((flags & ~(unsigned)(KDA_QK_L2NORM | KDA_DEBUG_CHECK)) == 0, KDA_ERR_INVALID_ARG,
+              "unknown flag bits 0x%x", flags);
+  KDA_REQUIRE((int64_t)N * H < (int64_t)INT32_MAX, KDA_ERR_UNSUPPORTED, "N*H too large");
+  if (N == 0) return KDA_OK;
+  KDA_REQUIRE(state_slot != nullptr || n_slots >= N, KDA_ERR_INVALID_ARG,
+              "n_slots=%d < N=%d without a slot map", n_slots, N);
+  KDA_CHECK_PTR(q, true);
+  KDA_CHECK_PTR(k, true);
+  KDA_CHECK_PTR(v, true);
+  KDA_CHECK_PTR(log_alpha, true);
+  KDA_REQUIRE(beta != nullptr, KDA_ERR_INVALID_ARG, "beta must not be NULL");
+  KDA_CHECK_PTR(gate, false);
+  KDA_CHECK_PTR(out, true);
+  KDA_CHECK_PTR(state, true);
+  KDA_REQUIRE(state_slot == nullptr || ((uintptr_t)state_slot & 3u) == 0, KDA_ERR_INVALID_ARG,
+              "state_slot is not 4-byte aligned");
+  Tracer tr((cudaStream_t)stream);
+  return cuda_status(tr([&] {
+                       return kda::launch_decode(q, k, v, log_alpha, beta, gate, out, state,
+                                                 state_slot, n_slots, N, H, dk, dv, scale, flags,
+                                                 dtype, (cudaStream_t)stream);
+                     }),
+                     "decode");
+}
+
+kda_status kda_segment_summary(const void *k, const void *v, const void *log_alpha,
+                               const void *beta, const int32_t *cu_segs, int n_seg,
+                               int64_t T_total, int H, int dk, int dv, int chunk, unsigned flags,
+                               kda_dtype dtype, float *X_out, float *Z_out, void *workspace,
+                               size_t workspace_bytes, kda_stream_t stream) {
+  kda_status st = common_checks(T_total, n_seg, H, dk, dv, chunk, dtype, cu_segs);
+  if (st != KDA_OK) return st;
+  KDA_REQUIRE((flags & ~(unsigned)(KDA_QK_L2NORM | KDA_DEBUG_CHECK)) == 0, KDA_ERR_INVALID_ARG,
+              "unknown flag bits 0x%x", flags);
+  const bool tokens = T_total > 0;
+  KDA_CHECK_PTR(k, tokens);
+  KDA_CHECK_PTR(v, tokens);
+  KDA_CHECK_PTR(log_alpha, tokens);
+  KDA_REQUIRE(!tokens || beta != nullptr, KDA_ERR_INVALID_ARG, "beta must not be NULL");
+  KDA_CHECK_PTR(X_out, n_seg > 0);
+  KDA_CHECK_PTR(Z_out, n_seg > 0);
+  KDA_REQUIRE(cu_segs == nullptr || ((uintptr_t)cu_segs & 3u) == 0, KDA_ERR_INVALID_ARG,
+              "cu_segs is not 4-byte aligned");
+  if (n_seg == 0) return KDA_OK;
+  const size_t need = kda::chunk_ws_bytes(T_total, n_seg, H, dk, dv);
+  KDA_REQUIRE(workspace != nullptr && workspace_bytes >= need, KDA_ERR_WORKSPACE,
+              "workspace %zu bytes, need %zu", workspace_bytes, need);
+  KDA_REQUIRE(((uintptr_t)workspace & 255u) == 0, KDA_ERR_INVALID_ARG,
+              "workspace is not 256-byte aligned");
+  cudaStream_t s = (cudaStream_t)stream;
+  Tracer tr(s);
+  kda::ChunkWs ws = kda::chunk_ws_carve(workspace, T_total, n_seg, H, dk, dv);
+  st = cuda_status(tr([&] { return kda::launch_chunk_table(cu_segs, n_seg, T_total, ws, s); }),
+                   "chunk table");
+  if (st != KDA_OK) return st;
+  st = cuda_status(tr([&] {
+                     return kda::launch_prep(k, k, v, log_alpha, beta, cu_segs, n_seg, T_total, H,
+                                             dk, dv, flags, dtype, ws, false, s);
+                   }),
+                   "chunk prep");
+  if (st != KDA_OK) return st;
+  return cuda_status(tr([&] {
+                       return kda::launch_state_pass(1, nullptr, nullptr, nullptr, nullptr, X_out,
+                                                     Z_out, cu_segs, n_seg, T_total, H, dk, dv,
+                                                     1.0f, dtype, ws, s);
+                     }),
+                     "summary state pass");
+}
+
+kda_status kda_scan_combine(const float *X, const float *Z, int n_seg, int H, int dk, int dv,
+                            const float *S_init, float *S_entry_out, float *S_final_out,
+                            kda_stream_t stream) {
+  KDA_REQUIRE(n_seg >= 0 && H > 0, KDA_ERR_INVALID_ARG, "negative size (n_seg=%d H=%d)", n_seg,
+              H);
+  KDA_REQUIRE(shape_ok(dk, dv), KDA_ERR_UNSUPPORTED, "dk=%d dv=%d: only 64 or 128", dk, dv);
+  KDA_CHECK_PTR(X, n_seg > 0);
+  KDA_CHECK_PTR(Z, n_seg > 0);
+  KDA_CHECK_PTR(S_init, false);
+  KDA_CHECK_PTR(S_entry_out, false);
+  KDA_CHECK_PTR(S_final_out, false);
+  if (S_entry_out == nullptr && S_final_out == nullptr) return KDA_OK;
+  Tracer tr((cudaStream_t)stream);
+  return cuda_status(tr([&] {
+                       return kda::launch_scan_combine(X, Z, n_seg, H, dk, dv, S_init,
+                                                       S_entry_out, S_final_out,
+                                                       (cudaStream_t)stream);
+                     }),
+                     "scan combine");
+}
+
+kda_status kda_trace_events(void *const *begin, void *const *end, int n) {
+  KDA_REQUIRE(n >= 0 && n <= kMaxTrace, KDA_ERR_INVALID_ARG, "n=%d: 0..%d events", n, kMaxTrace);
+  KDA_REQUIRE(n == 0 || (begin != nullptr && end != nullptr), KDA_ERR_INVALID_ARG,
+              "begin/end must not be NULL");
+  for (int i = 0; i < n; ++i) {
+    KDA_REQUIRE(begin[i] != nullptr && end[i] != nullptr, KDA_ERR_INVALID_ARG,
+                "event %d is NULL", i);
+    g_tr_begin[i] = (cudaEvent_t)begin[i];
+    g_tr_end[i] = (cudaEvent_t)end[i];
+  }
+  g_tr_n = n;
+  return KDA_OK;
+}
+
+kda_status kda_get_error(kda_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e, "stream synchronize");
+  unsigned a = 0, b = 0;
+  if ((e = kda::chunk_take_error(&a)) != cudaSuccess) return cuda_status(e, "error word");
+  if ((e = kda::decode_take_error(&b)) != cudaSuccess) return cuda_status(e, "error word");
+  const unsigned bits = a | b;
+  if (bits & kda::kErrTimeout) return fail(KDA_ERR_TIMEOUT, "a bounded device wait ran out");
+  if (bits & kda::kErrBadSeqlens)
+    return fail(KDA_ERR_INVALID_ARG, "malformed cu_seqlens / cu_segs or state_slot on device");
+  if (bits & kda::kErrPrecondition)
+    return fail(KDA_ERR_PRECONDITION, "log_alpha < -0.6953125 or beta outside [0,1]");
+  return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,545 @@
+// Chunked KDA forward, SIMT fp32 path.
+//
+// The chunked form follows from the recurrence S_t = (I - b k k^T) Diag(a) S + b k v^T
+// (K3 training overview, zuoshipin.com/article/18261, section 2 "KDA") and the
+// FlashKDA split the same page describes in section 4: per-chunk "update cards"
+// are prepared in parallel, and only the state hand-off and read-out run in
+// order. For a 64-token chunk with entry state S, G_r the inclusive running sum
+// of log_alpha inside the chunk, Kt = k*e^{G}, Kh = k*e^{-G}, Qt = q*e^{G},
+// Kd = k*e^{G_C - G}:
+//   M  = strict_lower(diag(b) Kt Kh^T),   P = lower(Qt Kh^T)
+//   (I + M) [W | Ut] = [diag(b) Kt | diag(b) V]            (forward substitution)
+//   U  = Ut - W S
+//   O  = Qt S + P U,        o = scale * g * O
+//   S' = Diag(e^{G_C}) S + Kd^T U
+// Stage A (kda_prep_simt) runs over all (chunk, head) pairs at once and writes
+// W, Ut, Qt, Kd, P and e^{G_C}; stage B (kda_state_simt) walks the chunks of
+// one (sequence, head) in order for a slice of value columns.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kda_common.cuh"
+
+namespace kda {
+
+__device__ unsigned g_chunk_err;
+
+namespace {
+
+constexpr int C = kChunk;
+
+__device__ __forceinline__ void set_err(unsigned bits) { atomicOr(&g_chunk_err, bits); }
+
+// Find the sequence owning global chunk `ci`: largest s with off[s] <= ci.
+__device__ __forceinline__ int find_seq(const int *off, int n_seq, int ci) {
+  int lo = 0, hi = n_seq - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= ci) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void seq_range(const int32_t *cu, int64_t fixed_len, int s,
+                                          int64_t *t0, int64_t *len) {
+  if (cu) {
+    *t0 = cu[s];
+    *len = (int64_t)cu[s + 1] - cu[s];
+  } else {
+    *t0 = (int64_t)s * fixed_len;
+    *len = fixed_len;
+  }
+}
+
+// One block: validate cu_seqlens and build per-sequence chunk offsets.
+__global__ void __launch_bounds__(1024) kda_chunk_table(const int32_t *cu, int n_seq,
+                                                        int64_t T_total, ChunkMeta *meta,
+                                                        int *off) {
+  __shared__ int warp_tot[32];
+  __shared__ int bad;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+  const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
+  // contiguous range of sequences per thread
+  const int per = (n_seq + nt - 1) / nt;
+  const int s_lo = min(n_seq, tid * per), s_hi = min(n_seq, s_lo + per);
+  int local = 0;
+  for (int s = s_lo; s < s_hi; ++s) {
+    int64_t len;
+    if (cu) {
+      len = (int64_t)cu[s + 1] - cu[s];
+      if (len < 0) bad = 1;
+    } else {
+      len = fixed_len;
+    }
+    local += (int)((len + C - 1) / C);
+  }
+  if (cu && tid == 0 && (cu[0] != 0 || (int64_t)cu[n_seq] != T_total)) bad = 1;
+  // block exclusive scan of `local`
+  const int lane = tid & 31, w = tid >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int x = (lane < (nt >> 5)) ? warp_tot[lane] : 0;
+    int xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, xi, o);
+      if (lane >= o) xi += y;
+    }
+    warp_tot[lane] = xi - x;  // exclusive
+  }
+  __syncthreads();
+  int run = warp_tot[w] + incl - local;
+  for (int s = s_lo; s < s_hi; ++s) {
+    off[s] = run;
+    int64_t len = cu ? (int64_t)cu[s + 1] - cu[s] : fixed_len;
+    run += (int)((len + C - 1) / C);
+  }
+  __syncthreads();
+  if (s_hi == n_seq && s_lo < s_hi) off[n_seq] = run;
+  if (n_seq == 0 && tid == 0) off[0] = 0;
+  __syncthreads();
+  if (tid == 0) {
+    meta->invalid = bad;
+    meta->total_chunks = bad ? 0 : off[n_seq];
+    if (bad) set_err(kErrBadSeqlens);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Stage A: per (chunk, head) preparation. 256 threads.
+template <int DK, int DV, typename Tin>
+__global__ void __launch_bounds__(256) kda_prep_simt(
+    const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
+    const Tin *__restrict__ la, const Tin *__restrict__ beta, const int32_t *__restrict__ cu,
+    int n_seq, int64_t fixed_len, int H, unsigned flags, const ChunkMeta *__restrict__ meta,
+    const int *__restrict__ off, float *__restrict__ Wg, float *__restrict__ Ug,
+    float *__restrict__ Qg, float *__restrict__ Kdg, float *__restrict__ Pg,
+    float *__restrict__ Dg, int need_q) {
+  constexpr int LK = DK + 1, LV = DV + 1, LA = C + 1;
+  extern __shared__ float smem[];
+  float *sKt = smem;             // [C][LK]  k*e^{G}, then b*Kt, then W
+  float *sKh = sKt + C * LK;     // [C][LK]  k*e^{-G}
+  float *sQt = sKh + C * LK;     // [C][LK]  q*e^{G}
+  float *sV = sQt + C * LK;      // [C][LV]  v, then b*v, then Ut
+  float *sA = sV + C * LV;       // [C][LA]  strict-lower diag(b) Kt Kh^T
+  float *sB = sA + C * LA;       // [C]      beta
+  float *sGC = sB + C;           // [DK]     e^{G_C}
+
+  const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  if (meta->invalid || ci >= meta->total_chunks) return;
+  const int s = find_seq(off, n_seq, ci);
+  int64_t ts, ls;
+  seq_range(cu, fixed_len, s, &ts, &ls);
+  const int j = ci - off[s];
+  const int64_t t0 = ts + (int64_t)j * C;
+  const int len = (int)min((int64_t)C, ls - (int64_t)j * C);
+
+  // load (rows >= len are zero: no write, no read-out, no decay)
+  for (int e = tid; e < C * DK; e += 256) {
+    int r = e / DK, c = e % DK;
+    float kv = 0.f, qv = 0.f, lv = 0.f;
+    if (r < len) {
+      size_t g = ((size_t)(t0 + r) * H + h) * DK + c;
+      kv = to_f32(k[g]);
+      qv = to_f32(q[g]);
+      lv = to_f32(la[g]);
+      if ((flags & KDA_DEBUG_CHECK) && !(lv >= kLogAlphaMin && lv <= 0.f)) set_err(kErrPrecondition);
+    }
+    sKh[r * LK + c] = kv;
+    sQt[r * LK + c] = qv;
+    sKt[r * LK + c] = lv;
+  }
+  for (int e = tid; e < C * DV; e += 256) {
+    int r = e / DV, c = e % DV;
+    sV[r * LV + c] = r < len ? to_f32(v[((size_t)(t0 + r) * H + h) * DV + c]) : 0.f;
+  }
+  if (tid < C) {
+    float b = tid < len ? to_f32(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+    if ((flags & KDA_DEBUG_CHECK) && tid < len && !(b >= 0.f && b <= 1.f)) set_err(kErrPrecondition);
+    sB[tid] = b;
+  }
+  __syncthreads();
+
+  // L2 normalisation of q and k rows: one warp per row
+  if (flags & KDA_QK_L2NORM) {
+    const int lane = tid & 31, w = tid >> 5;
+    for (int r = w; r < C; r += 8) {
+      float sk = 0.f, sq = 0.f;
+      for (int c = lane; c < DK; c += 32) {
+        float a = sKh[r * LK + c], b = sQt[r * LK + c];
+        sk += a * a;
+        sq += b * b;
+      }
+      sk = warp_sum(sk);
+      sq = warp_sum(sq);
+      float rk = rsqrtf(sk + kL2Eps), rq = rsqrtf(sq + kL2Eps);
+      for (int c = lane; c < DK; c += 32) {
+        sKh[r * LK + c] *= rk;
+        sQt[r * LK + c] *= rq;
+      }
+    }
+    __syncthreads();
+  }
+
+  // running log-decay G per key channel and the decayed operands
+  if (tid < DK) {
+    const int c = tid;
+    float G = 0.f;
+    for (int r = 0; r < C; ++r) {
+      G += sKt[r * LK + c];  // log_alpha (0 on padded rows)
+      float ep = expf(G), en = expf(-G);
+      float kn = sKh[r * LK + c];
+      sKt[r * LK + c] = kn * ep;
+      sKh[r * LK + c] = kn * en;
+      sQt[r * LK + c] *= ep;
+    }
+    sGC[c] = expf(G);
+  }
+  __syncthreads();
+
+  const size_t slab = (size_t)ci * H + h;
+  // Gram blocks: A = strict_lower(diag(b) Kt Kh^T), P = lower(Qt Kh^T); 4x4 per thread
+  {
+    const int rb = (tid >> 4) * 4, cb = (tid & 15) * 4;
+    float a[4][4] = {}, p[4][4] = {};
+    for (int c = 0; c < DK; ++c) {
+      float kt[4], qt[4], kh[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        kt[i] = sKt[(rb + i) * LK + c];
+        qt[i] = sQt[(rb + i) * LK + c];
+        kh[i] = sKh[(cb + i) * LK + c];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          a[i][jj] = fmaf(kt[i], kh[jj], a[i][jj]);
+          p[i][jj] = fmaf(qt[i], kh[jj], p[i][jj]);
+        }
+    }
+    float *Pout = Pg + slab * C * C;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        int r = rb + i, c2 = cb + jj;
+        sA[r * LA + c2] = c2 < r ? sB[r] * a[i][jj] : 0.f;
+        Pout[r * C + c2] = c2 <= r ? p[i][jj] : 0.f;
+      }
+  }
+  __syncthreads();
+
+  // write Qt, Kd = Kh * e^{G_C}, e^{G_C}; scale the right-hand sides by beta
+  float *Qout = Qg + slab * C * DK, *Kdout = Kdg + slab * C * DK;
+  for (int e = tid; e < C * DK; e += 256) {
+    int r = e / DK, c = e % DK;
+    if (need_q) Qout[e] = sQt[r * LK + c];
+    Kdout[e] = sKh[r * LK + c] * sGC[c];
+  }
+  if (tid < DK) Dg[slab * DK + tid] = sGC[tid];
+  for (int e = tid; e < C * DK; e += 256) {
+    int r = e / DK, c = e % DK;
+    sKt[r * LK + c] *= sB[r];
+  }
+  for (int e = tid; e < C * DV; e += 256) {
+    int r = e / DV, c = e % DV;
+    sV[r * LV + c] *= sB[r];
+  }
+  __syncthreads();
+
+  // (I + A) X = [b Kt | b V], forward substitution: one thread per column
+  if (tid < DK + DV) {
+    float *col = tid < DK ? sKt + tid : sV + (tid - DK);
+    const int ld = tid < DK ? LK : LV;
+    for (int r = 1; r < C; ++r) {
+      float acc = col[r * ld];
+      for (int i = 0; i < r; ++i) acc = fmaf(-sA[r * LA + i], col[i * ld], acc);
+      col[r * ld] = acc;
+    }
+  }
+  __syncthreads();
+  float *Wout = Wg + slab * C * DK, *Uout = Ug + slab * C * DV;
+  for (int e = tid; e < C * DK; e += 256) Wout[e] = sKt[(e / DK) * LK + e % DK];
+  for (int e = tid; e < C * DV; e += 256) Uout[e] = sV[(e / DV) * LV + e % DV];
+}
+
+// ---------------------------------------------------------------------------
+// Stage B: sequential state pass for one (sequence, head) and BV value columns.
+// mode 0: prefill (reads Qt/P, writes out and the final state)
+// mode 1: segment summary on the augmented state [X | Z]: columns < DK carry X
+//         (entry = identity, no value input), the rest carry Z (entry = 0).
+constexpr int BV = 32;
+
+template <int DK, int DV, typename Tout>
+__global__ void __launch_bounds__(256) kda_state_simt(
+    int mode, const Tout *__restrict__ gate, Tout *__restrict__ out,
+    const float *__restrict__ S0, float *__restrict__ S_final, float *__restrict__ X_out,
+    float *__restrict__ Z_out, const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len,
+    int H, float scale, const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
+    const float *__restrict__ Wg, const float *__restrict__ Ug, const float *__restrict__ Qg,
+    const float *__restrict__ Kdg, const float *__restrict__ Pg, const float *__restrict__ Dg) {
+  constexpr int LK = DK + 1, LS = BV + 1, LP = C + 1;
+  extern __shared__ float smem[];
+  float *sS = smem;            // [DK][LS]
+  float *sU = sS + DK * LS;    // [C][LS]
+  float *sW = sU + C * LS;     // [C][LK]
+  float *sQ = sW + C * LK;     // [C][LK]
+  float *sKd = sQ + C * LK;    // [C][LK]
+  float *sP = sKd + C * LK;    // [C][LP]
+  float *sD = sP + C * LP;     // [DK]
+
+  if (meta->invalid) return;
+  const int chain = blockIdx.x, s = chain / H, h = chain % H, tid = threadIdx.x;
+  const int j0 = blockIdx.y * BV;
+  const int jt = tid & 31, rt = tid >> 5;  // column lane, row group (8 groups)
+  bool xpart = false;
+  int vcol0 = j0;  // first value column of this slice (mode 0 / Z part)
+  if (mode == 1) {
+    xpart = j0 < DK;
+    vcol0 = j0 - DK;
+  }
+  // entry state
+  for (int c = rt; c < DK; c += 8) {
+    float x = 0.f;
+    if (mode == 0) {
+      if (S0) x = S0[(((size_t)s * H + h) * DK + c) * DV + j0 + jt];
+    } else if (xpart) {
+      x = (c == j0 + jt) ? 1.f : 0.f;
+    }
+    sS[c * LS + jt] = x;
+  }
+  int64_t ts, ls;
+  seq_range(cu, fixed_len, s, &ts, &ls);
+  const int nchunks = (int)((ls + C - 1) / C);
+  const bool write_o = (mode == 0) && out != nullptr;
+  __syncthreads();
+
+  for (int jc = 0; jc < nchunks; ++jc) {
+    const size_t slab = (size_t)(off[s] + jc) * H + h;
+    const int64_t t0 = ts + (int64_t)jc * C;
+    const int len = (int)min((int64_t)C, ls - (int64_t)jc * C);
+    const float *W = Wg + slab * C * DK, *Kd = Kdg + slab * C * DK;
+    for (int e = tid; e < C * DK; e += 256) {
+      int r = e / DK, c = e % DK;
+      sW[r * LK + c] = W[e];
+      sKd[r * LK + c] = Kd[e];
+      if (write_o) sQ[r * LK + c] = Qg[slab * C * DK + e];
+    }
+    for (int e = tid; e < C * BV; e += 256) {
+      int r = e / BV, c = e % BV;
+      sU[r * LS + c] = xpart ? 0.f : Ug[slab * C * DV + (size_t)r * DV + vcol0 + c];
+    }
+    if (write_o)
+      for (int e = tid; e < C * C; e += 256) sP[(e / C) * LP + e % C] = Pg[slab * C * C + e];
+    if (tid < DK) sD[tid] = Dg[slab * DK + tid];
+    __syncthreads();
+
+    // U = Ut - W S   (rows rt, rt+8, ...)
+    float u[C / 8];
+#pragma unroll
+    for (int m = 0; m < C / 8; ++m) u[m] = sU[(rt + 8 * m) * LS + jt];
+    for (int c = 0; c < DK; ++c) {
+      float sv = sS[c * LS + jt];
+#pragma unroll
+      for (int m = 0; m < C / 8; ++m) u[m] = fmaf(-sW[(rt + 8 * m) * LK + c], sv, u[m]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < C / 8; ++m) sU[(rt + 8 * m) * LS + jt] = u[m];
+    __syncthreads();
+
+    if (write_o) {
+      // O = Qt S + P U
+      float o[C / 8] = {};
+      for (int c = 0; c < DK; ++c) {
+        float sv = sS[c * LS + jt];
+#pragma unroll
+        for (int m = 0; m < C / 8; ++m) o[m] = fmaf(sQ[(rt + 8 * m) * LK + c], sv, o[m]);
+      }
+#pragma unroll
+      for (int m = 0; m < C / 8; ++m) {
+        const int r = rt + 8 * m;
+        float acc = o[m];
+        for (int i = 0; i <= r; ++i) acc = fmaf(sP[r * LP + i], sU[i * LS + jt], acc);
+        if (r < len) {
+          size_t g = ((size_t)(t0 + r) * H + h) * DV + j0 + jt;
+          float gv = gate ? to_f32(gate[g]) : 1.f;
+          out[g] = from_f32<Tout>(scale * gv * acc);
+        }
+      }
+    }
+
+    // S = Diag(e^{G_C}) S + Kd^T U
+    float ns[DK / 8];
+#pragma unroll
+    for (int m = 0; m < DK / 8; ++m) {
+      const int c = rt + 8 * m;
+      float acc = sD[c] * sS[c * LS + jt];
+      for (int i = 0; i < C; ++i) acc = fmaf(sKd[i * LK + c], sU[i * LS + jt], acc);
+      ns[m] = acc;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < DK / 8; ++m) sS[(rt + 8 * m) * LS + jt] = ns[m];
+    __syncthreads();
+  }
+
+  // final state
+  for (int c = rt; c < DK; c += 8) {
+    float x = sS[c * LS + jt];
+    if (mode == 0) {
+      if (S_final) S_final[(((size_t)s * H + h) * DK + c) * DV + j0 + jt] = x;
+    } else if (xpart) {
+      X_out[(((size_t)s * H + h) * DK + c) * DK + j0 + jt] = x;
+    } else {
+      Z_out[(((size_t)s * H + h) * DK + c) * DV + vcol0 + jt] = x;
+    }
+  }
+}
+
+template <int DK, int DV>
+constexpr size_t prep_smem() {
+  return sizeof(float) * (3 * C * (DK + 1) + C * (DV + 1) + C * (C + 1) + C + DK);
+}
+template <int DK>
+constexpr size_t state_smem() {
+  return sizeof(float) * (DK * (BV + 1) + C * (BV + 1) + 3 * C * (DK + 1) + C * (C + 1) + DK);
+}
+
+template <int DK, int DV, typename Tin>
+cudaError_t launch_prep_t(const void *q, const void *k, const void *v, const void *la,
+                          const void *beta, const int32_t *cu, int n_seq, int64_t T_total,
+                          int H, unsigned flags, const ChunkWs &ws, bool need_q,
+                          cudaStream_t st) {
+  auto kern = kda_prep_simt<DK, DV, Tin>;
+  constexpr size_t sm = prep_smem<DK, DV>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
+  dim3 grid(ws.max_chunks, H);
+  kern<<<grid, 256, sm, st>>>((const Tin *)q, (const Tin *)k, (const Tin *)v, (const Tin *)la,
+                              (const Tin *)beta, cu, n_seq, fixed_len, H, flags, ws.meta,
+                              ws.seq_chunk_off, ws.W, ws.U, ws.Q, ws.Kd, ws.P, ws.D,
+                              need_q ? 1 : 0);
+  return cudaGetLastError();
+}
+
+template <int DK, int DV, typename Tout>
+cudaError_t launch_state_t(int mode, const void *gate, void *out, const float *S0,
+                           float *S_final, float *X_out, float *Z_out, const int32_t *cu,
+                           int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
+                           cudaStream_t st) {
+  auto kern = kda_state_simt<DK, DV, Tout>;
+  constexpr size_t sm = state_smem<DK>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
+  const int ncols = mode == 0 ? DV : DK + DV;
+  dim3 grid(n_seq * H, ncols / BV);
+  kern<<<grid, 256, sm, st>>>(mode, (const Tout *)gate, (Tout *)out, S0, S_final, X_out, Z_out,
+                              cu, n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.W,
+                              ws.U, ws.Q, ws.Kd, ws.P, ws.D);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+static size_t max_chunks_of(int64_t T_total, int n_seq) {
+  // sum_s ceil(len_s / C) <= T_total / C + n_seq
+  return (size_t)(T_total / C) + (size_t)n_seq + 1;
+}
+
+size_t chunk_ws_bytes(int64_t T_total, int n_seq, int H, int dk, int dv) {
+  const size_t mc = max_chunks_of(T_total, n_seq);
+  size_t b = align_up(sizeof(ChunkMeta), 256);
+  b += align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
+  const size_t per = (size_t)mc * H;
+  b += align_up(sizeof(float) * per * C * dk, 256) * 3;  // W, Q, Kd
+  b += align_up(sizeof(float) * per * C * dv, 256);      // U
+  b += align_up(sizeof(float) * per * C * C, 256);       // P
+  b += align_up(sizeof(float) * per * dk, 256);          // D
+  return b;
+}
+
+ChunkWs chunk_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int dv) {
+  ChunkWs w;
+  const size_t mc = max_chunks_of(T_total, n_seq);
+  char *p = (char *)ws;
+  w.meta = (ChunkMeta *)p;
+  p += align_up(sizeof(ChunkMeta), 256);
+  w.seq_chunk_off = (int *)p;
+  p += align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
+  const size_t per = (size_t)mc * H;
+  w.W = (float *)p;  p += align_up(sizeof(float) * per * C * dk, 256);
+  w.Q = (float *)p;  p += align_up(sizeof(float) * per * C * dk, 256);
+  w.Kd = (float *)p; p += align_up(sizeof(float) * per * C * dk, 256);
+  w.U = (float *)p;  p += align_up(sizeof(float) * per * C * dv, 256);
+  w.P = (float *)p;  p += align_up(sizeof(float) * per * C * C, 256);
+  w.D = (float *)p;
+  w.max_chunks = (int)mc;
+  return w;
+}
+
+cudaError_t launch_chunk_table(const int32_t *cu, int n_seq, int64_t T_total, const ChunkWs &ws,
+                               cudaStream_t st) {
+  kda_chunk_table<<<1, 1024, 0, st>>>(cu, n_seq, T_total, ws.meta, ws.seq_chunk_off);
+  return cudaGetLastError();
+}
+
+#define KDA_DISPATCH_DKDV(dk, dv, ...)                                   \
+  do {                                                                    \
+    if (dk == 128 && dv == 128) { constexpr int DK = 128, DV = 128; __VA_ARGS__; } \
+    else if (dk == 64 && dv == 64) { constexpr int DK = 64, DV = 64; __VA_ARGS__; } \
+    else if (dk == 128 && dv == 64) { constexpr int DK = 128, DV = 64; __VA_ARGS__; } \
+    else { constexpr int DK = 64, DV = 128; __VA_ARGS__; }                \
+  } while (0)
+
+cudaError_t launch_prep(const void *q, const void *k, const void *v, const void *la,
+                        const void *beta, const int32_t *cu, int n_seq, int64_t T_total, int H,
+                        int dk, int dv, unsigned flags, kda_dtype dt, const ChunkWs &ws,
+                        bool need_q, cudaStream_t st) {
+  if (dt == KDA_DTYPE_BF16) {
+    KDA_DISPATCH_DKDV(dk, dv, return launch_prep_t<DK, DV, __nv_bfloat16>(
+                                  q, k, v, la, beta, cu, n_seq, T_total, H, flags, ws, need_q, st));
+  } else {
+    KDA_DISPATCH_DKDV(dk, dv, return launch_prep_t<DK, DV, float>(
+                                  q, k, v, la, beta, cu, n_seq, T_total, H, flags, ws, need_q, st));
+  }
+}
+
+cudaError_t launch_state_pass(int mode, const void *gate, void *out, const float *S0,
+                              float *S_final, float *X_out, float *Z_out, const int32_t *cu,
+                              int n_seq, int64_t T_total, int H, int dk, int dv, float scale,
+                              kda_dtype dt, const ChunkWs &ws, cudaStream_t st) {
+  if (dt == KDA_DTYPE_BF16) {
+    KDA_DISPATCH_DKDV(dk, dv, return launch_state_t<DK, DV, __nv_bfloat16>(
+                                  mode, gate, out, S0, S_final, X_out, Z_out, cu, n_seq,
+                                  T_total, H, scale, ws, st));
+  } else {
+    KDA_DISPATCH_DKDV(dk, dv, return launch_state_t<DK, DV, float>(
+                                  mode, gate, out, S0, S_final, X_out, Z_out, cu, n_seq,
+                                  T_total, H, scale, ws, st));
+  }
+}
+
+cudaError_t chunk_take_error(unsigned *bits) {
+  unsigned v = 0, z = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_chunk_err, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbol(g_chunk_err, &z, sizeof(unsigned));
+  *bits = v;
+  return e;
+}
+
+}  // namespace kda

@@ -1,0 +1,97 @@
+// Internal helpers shared by the libkda translation units (device side).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+constexpr int kChunk = 64;
+// log 0.5 rounded down by one bf16 ulp: the smallest log-retention the chunked
+// kernels accept (64 tokens x 0.6953125 = 44.5, so exp(-Gamma) <= 2^64.2).
+constexpr float kLogAlphaMin = -0.6953125f;
+constexpr float kL2Eps = 1e-6f;
+
+// Bits of the per-translation-unit device error word.
+enum : unsigned {
+  kErrPrecondition = 1u,
+  kErrTimeout = 2u,
+  kErrBadSeqlens = 4u,
+};
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Per-call metadata at the head of the chunk workspace.
+struct ChunkMeta {
+  int total_chunks;  // sum over sequences of ceil(len / 64)
+  int invalid;       // non-zero: cu_seqlens rejected; every kernel exits
+  int pad[62];
+};
+
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) {
+  return (x + a - 1) / a * a;
+}
+
+}  // namespace kda
+
+// Launchers and error-word accessors defined in the kernel translation units.
+namespace kda {
+
+struct ChunkWs {
+  ChunkMeta *meta;
+  int *seq_chunk_off;  // [n_seq + 1]
+  float *W, *U, *Q, *Kd, *P, *D;
+  int max_chunks;
+};
+
+size_t chunk_ws_bytes(int64_t T_total, int n_seq, int H, int dk, int dv);
+ChunkWs chunk_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int dv);
+
+cudaError_t launch_chunk_table(const int32_t *cu, int n_seq, int64_t T_total,
+                               const ChunkWs &ws, cudaStream_t st);
+cudaError_t launch_prep(const void *q, const void *k, const void *v,
+                        const void *la, const void *beta, const int32_t *cu,
+                        int n_seq, int64_t T_total, int H, int dk, int dv,
+                        unsigned flags, kda_dtype dt, const ChunkWs &ws,
+                        bool need_q, cudaStream_t st);
+// mode 0: forward (out, final); mode 1: segment summary (X_out, Z_out)
+cudaError_t launch_state_pass(int mode, const void *gate, void *out,
+                              const float *S0, float *S_final, float *X_out,
+                              float *Z_out, const int32_t *cu, int n_seq,
+                              int64_t T_total, int H, int dk, int dv,
+                              float scale, kda_dtype dt, const ChunkWs &ws,
+                              cudaStream_t st);
+cudaError_t launch_decode(const void *q, const void *k, const void *v,
+                          const void *la, const void *beta, const void *gate,
+                          void *out, float *state, const int32_t *slot,
+                          int n_slots, int N, int H, int dk, int dv,
+                          float scale, unsigned flags, kda_dtype dt,
+                          cudaStream_t st);
+cudaError_t launch_scan_combine(const float *X, const float *Z, int n_seg,
+                                int H, int dk, int dv, const float *S_init,
+                                float *E_out, float *S_final, cudaStream_t st);
+
+// Read-and-clear of each translation unit's device error word.
+cudaError_t chunk_take_error(unsigned *bits);
+cudaError_t decode_take_error(unsigned *bits);
+
+}  // namespace kda

@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: the library loads, exports what include/kda.h
+declares, and rejects bad arguments with the documented status before any
+CUDA call."""
+import ctypes
+
+import pytest
+
+from linear_attention_05_gb300 import binding as B
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return B.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = B.declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version(lib):
+    assert "sm_103a" in B.kda_version()
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+ODD = 0x10001
+
+
+def chunk(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, la=FAKE, beta=FAKE, gate=None, out=FAKE, s0=None, sf=None,
+             cu=None, n_seq=1, T=128, H=2, dk=64, dv=64, chunk=64, scale=1.0, flags=1,
+             dtype=1, ws=FAKE, wsb=0, stream=None)
+    a.update(kw)
+    return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["la"], a["beta"], a["gate"], a["out"],
+                             a["s0"], a["sf"], a["cu"], a["n_seq"], a["T"], a["H"], a["dk"],
+                             a["dv"], a["chunk"], a["scale"], a["flags"], a["dtype"], a["ws"],
+                             a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=96), B.KDA_ERR_UNSUPPORTED),
+    (dict(dv=256), B.KDA_ERR_UNSUPPORTED),
+    (dict(chunk=32), B.KDA_ERR_UNSUPPORTED),
+    (dict(dtype=7), B.KDA_ERR_UNSUPPORTED),
+    (dict(T=-1), B.KDA_ERR_INVALID_ARG),
+    (dict(H=0), B.KDA_ERR_INVALID_ARG),
+    (dict(n_seq=-2), B.KDA_ERR_INVALID_ARG),
+    (dict(q=None), B.KDA_ERR_INVALID_ARG),
+    (dict(beta=None), B.KDA_ERR_INVALID_ARG),
+    (dict(out=None), B.KDA_ERR_INVALID_ARG),
+    (dict(k=ODD), B.KDA_ERR_INVALID_ARG),
+    (dict(gate=ODD), B.KDA_ERR_INVALID_ARG),
+    (dict(sf=ODD), B.KDA_ERR_INVALID_ARG),
+    (dict(cu=FAKE + 2), B.KDA_ERR_INVALID_ARG),
+    (dict(n_seq=3, T=128), B.KDA_ERR_INVALID_ARG),  # 128 tokens do not split into 3 equal seqs
+    (dict(flags=0x80), B.KDA_ERR_INVALID_ARG),
+    (dict(ws=None, wsb=0), B.KDA_ERR_WORKSPACE),
+    (dict(wsb=100), B.KDA_ERR_WORKSPACE),
+])
+def test_chunk_fwd_rejects(lib, kw, status):
+    assert chunk(lib, **kw) == status
+    assert B.kda_last_error_string() != ""
+
+
+def test_chunk_fwd_no_sequences_is_noop(lib):
+    assert chunk(lib, n_seq=0, T=0, q=None, k=None, v=None, la=None, beta=None, out=None,
+                 ws=None) == B.KDA_OK
+
+
+def test_workspace_size(lib):
+    s1 = B.kda_chunk_fwd_workspace_size(4096, 1, 16, 128, 128)
+    s2 = B.kda_chunk_fwd_workspace_size(8192, 1, 16, 128, 128)
+    assert 0 < s1 < s2
+    assert B.kda_chunk_fwd_workspace_size(4096, 1, 16, 96, 128) == 0
+    assert B.kda_segment_summary_workspace_size(4096, 2, 16, 128, 128) > 0
+
+
+def dec(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, la=FAKE, beta=FAKE, gate=None, out=FAKE, state=FAKE,
+             slot=None, n_slots=4, N=4, H=2, dk=128, dv=128, scale=1.0, flags=1, dtype=1,
+             stream=None)
+    a.update(kw)
+    return lib.kda_decode_step(a["q"], a["k"], a["v"], a["la"], a["beta"], a["gate"], a["out"],
+                               a["state"], a["slot"], a["n_slots"], a["N"], a["H"], a["dk"],
+                               a["dv"], a["scale"], a["flags"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=32), B.KDA_ERR_UNSUPPORTED),
+    (dict(N=-1), B.KDA_ERR_INVALID_ARG),
+    (dict(state=None), B.KDA_ERR_INVALID_ARG),
+    (dict(state=ODD), B.KDA_ERR_INVALID_ARG),
+    (dict(n_slots=2), B.KDA_ERR_INVALID_ARG),  # fewer slots than sequences, no slot map
+    (dict(slot=FAKE + 1), B.KDA_ERR_INVALID_ARG),
+    (dict(flags=4), B.KDA_ERR_INVALID_ARG),
+])
+def test_decode_rejects(lib, kw, status):
+    assert dec(lib, **kw) == status
+
+
+def test_decode_zero_sequences_is_noop(lib):
+    assert dec(lib, N=0, q=None) == B.KDA_OK
+
+
+def test_segment_summary_rejects(lib):
+    st = lib.kda_segment_summary(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 256, 2, 64, 64, 64, 1, 1,
+                                 FAKE, FAKE, FAKE, 10, None)
+    assert st == B.KDA_ERR_WORKSPACE
+    st = lib.kda_segment_summary(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 256, 2, 64, 64, 48, 1, 1,
+                                 FAKE, FAKE, FAKE, 10, None)
+    assert st == B.KDA_ERR_UNSUPPORTED
+
+
+def test_scan_combine_rejects(lib):
+    assert lib.kda_scan_combine(None, FAKE, 2, 2, 64, 64, None, FAKE, None, None) == \
+        B.KDA_ERR_INVALID_ARG
+    assert lib.kda_scan_combine(FAKE, FAKE, 2, 2, 64, 80, None, FAKE, None, None) == \
+        B.KDA_ERR_UNSUPPORTED
+    # nothing requested: a no-op
+    assert lib.kda_scan_combine(FAKE, FAKE, 2, 2, 64, 64, None, None, None, None) == B.KDA_OK
