@@ -105,6 +105,33 @@ size_t kda_chunk_fwd_workspace_size(int64_t T_total, int n_seq, int H, int dk,
                                     int dv, int chunk, kda_dtype dtype);
 
 /*
+ * kda_chunk_fwd without a workspace argument, for callers that cannot
+ * allocate device memory where they run the mixer: host frameworks that
+ * reserve the device heap up front and give a kernel only its inputs and
+ * outputs, plugin interfaces with no workspace slot, and code that must not
+ * call cudaMalloc/cudaFree because they can synchronise the device. The K3
+ * pages have no counterpart to this entry point.
+ *
+ * Same arguments, results and status codes as kda_chunk_fwd, minus
+ * workspace/workspace_bytes. Scratch comes from a fixed 64 MiB array in the
+ * library's device memory (held on every device that loads the library until
+ * it is unloaded); problems whose kda_chunk_fwd_workspace_size exceeds 64 MiB
+ * are rejected with KDA_ERR_WORKSPACE before any launch. The call allocates
+ * nothing. All calls on a device share that array: calls whose kernels may
+ * overlap on the GPU (unordered streams) race and give wrong results. The
+ * first call on a device looks up the array's address (cudaGetSymbolAddress);
+ * make that first call before any stream capture.
+ */
+kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                                 const void *log_alpha, const void *beta,
+                                 const void *gate, void *out,
+                                 const float *initial_state, float *final_state,
+                                 const int32_t *cu_seqlens, int n_seq,
+                                 int64_t T_total, int H, int dk, int dv,
+                                 int chunk, float scale, unsigned flags,
+                                 kda_dtype dtype, kda_stream_t stream);
+
+/*
  * One decode step for N sequences, one new token each, against fp32 states
  * resident in device memory (the recurrence above, applied once).
  * Source: K3 explainer section 2 (one corrective write per token) and the

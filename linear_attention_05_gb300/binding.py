@@ -68,6 +68,7 @@ def load(path: str = LIB_PATH):
             "kda_last_error_string": ([], ctypes.c_char_p),
             "kda_chunk_fwd": ([P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, P, SZ, P], I),
             "kda_chunk_fwd_workspace_size": ([I64, I, I, I, I, I, I], SZ),
+            "kda_chunk_fwd_noalloc": ([P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, P], I),
             "kda_decode_step": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, U, I, P], I),
             "kda_segment_summary": ([P, P, P, P, P, I, I64, I, I, I, I, U, I, P, P, P, SZ, P], I),
             "kda_segment_summary_workspace_size": ([I64, I, I, I, I, I, I], SZ),
@@ -166,6 +167,30 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, gate, out, initial_state, final_stat
                            _ptr(out), _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens),
                            n_seq, T, H, dk, dv, chunk, float(scale), int(flags), dt, _ptr(ws),
                            wsb, _stream(stream))
+    _check(lib, st)
+    return out, final_state
+
+
+def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, gate, out, initial_state, final_state,
+                          cu_seqlens, n_seq, scale=1.0, flags=KDA_QK_L2NORM, stream=None,
+                          chunk=CHUNK):
+    """kda_chunk_fwd using the library's fixed device scratch (no workspace).
+
+    For callers that cannot allocate device memory where they run the mixer;
+    the library allocates nothing either. Problems needing more than the fixed
+    scratch raise KdaError(KDA_ERR_WORKSPACE). Calls that overlap on the GPU
+    share the scratch and race."""
+    lib = load()
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    _f32_or_none(initial_state, "initial_state")
+    _f32_or_none(final_state, "final_state")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    st = lib.kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                   _ptr(gate), _ptr(out), _ptr(initial_state), _ptr(final_state),
+                                   _ptr(cu_seqlens), n_seq, T, H, dk, dv, chunk, float(scale),
+                                   int(flags), _dtype_code(k), _stream(stream))
     _check(lib, st)
     return out, final_state
 

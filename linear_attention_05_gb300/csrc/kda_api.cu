@@ -91,6 +91,17 @@ kda_status common_checks(int64_t T_total, int n_seq, int H, int dk, int dv, int 
 
 }  // namespace
 
+namespace kda {
+// Sets this thread's kda_last_error_string() message and returns `st`.
+kda_status api_fail(kda_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+}  // namespace kda
+
 extern "C" {
 
 const char *kda_version(void) { return "libkda 0.1 sm_103a"; }

@@ -90,6 +90,9 @@ cudaError_t launch_scan_combine(const float *X, const float *Z, int n_seg,
                                 int H, int dk, int dv, const float *S_init,
                                 float *E_out, float *S_final, cudaStream_t st);
 
+// Sets the calling thread's kda_last_error_string() message; returns `st`.
+kda_status api_fail(kda_status st, const char *fmt, ...);
+
 // Read-and-clear of each translation unit's device error word.
 cudaError_t chunk_take_error(unsigned *bits);
 cudaError_t decode_take_error(unsigned *bits);
