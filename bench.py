@@ -284,19 +284,31 @@ def run_gpu(args, rank, world, local):
     ms_per_step = total_ms / args.steps
     value = world * TOKENS_PER_STEP / (ms_per_step * 1e-3) / 1e6
 
-    # roofline of the dominant launch (chunk prep or state pass)
-    names = ["kda_chunk_table", "kda_prep_simt", "kda_state_simt"]
+    # roofline of the dominant launch (update cards or state pass)
+    tc = (w.dtype == torch.bfloat16 and d == 128)
+    names = (["kda_chunk_table", "kda_card_tc", "kda_state_tc"] if tc else
+             ["kda_chunk_table", "kda_prep_simt", "kda_state_simt"])
     dom = int(np.argmax(per_launch))
-    alg_bytes = {  # algorithmic bytes per launch of each kernel
+    chunk_heads = (T // 64) * H
+    alg_bytes = {  # algorithmic HBM bytes per launch of each kernel
         0: (n_seq + 1) * 4,
-        1: TOKEN_HEADS * (4 * d * 2 + 2),
-        2: TOKEN_HEADS * (2 * d * 2) + 2 * n_seq * H * STATE_BYTES,
+        1: TOKEN_HEADS * (4 * d * 2 + 2),                                 # q, k, v, log_alpha, beta
+        2: TOKEN_HEADS * (2 * d * 2) + 2 * n_seq * H * STATE_BYTES,       # gate, o, states
     }
     achieved = alg_bytes[dom] / (per_launch[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                 "traffic": None, "peak_source": pk["source"],
-                "launch_ms": [round(t, 4) for t in per_launch]}
+                "launch_ms": dict(zip(names, [round(t, 4) for t in per_launch]))}
+    if tc:
+        # tensor-core work per (chunk, head): card GEMMs 1-4 and the state-pass MMA group
+        card_flop = 2 * (128 * 64 * 128 + 2 * 128 * 64 * 64 + 2 * 128 * 64 * 64 + 2 * 128 * 128 * 64)
+        state_flop = 2 * 128 * 192 * 128
+        t_gemm = (per_launch[1] + per_launch[2]) * 1e-3
+        tf = chunk_heads * (card_flop + state_flop) / t_gemm / 1e12
+        roofline["tensor"] = {"kernels": names[1:], "achieved": round(tf, 2), "unit": "TFLOP/s",
+                              "peak": pk["bf16_tflops"], "frac": round(tf / pk["bf16_tflops"], 4),
+                              "flop_per_chunk_head": card_flop + state_flop}
 
     # end to end through the public API: pinned host inputs -> device -> host
     host = {k: v.to("cpu").pin_memory() for k, v in x.items() if k != "cu_seqlens" and v is not None}

@@ -45,11 +45,15 @@ class KdaError(RuntimeError):
         self.status = status
 
 
-def declared_functions(header: str = HEADER):
-    """Names of the functions include/kda.h declares."""
-    txt = open(header).read()
-    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", txt)))
+def declared_functions(header: str | None = None):
+    """Names of the functions the headers in include/ declare (or one header)."""
+    import glob
+    paths = [header] if header else sorted(glob.glob(os.path.join(os.path.dirname(HEADER), "*.h")))
+    names = set()
+    for p in paths:
+        txt = re.sub(r"/\*.*?\*/", "", open(p).read(), flags=re.S)
+        names |= set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", txt))
+    return sorted(names)
 
 
 def load(path: str = LIB_PATH):
@@ -75,6 +79,7 @@ def load(path: str = LIB_PATH):
             "kda_scan_combine": ([P, P, I, I, I, I, P, P, P, P], I),
             "kda_get_error": ([P], I),
             "kda_trace_events": ([ctypes.POINTER(P), ctypes.POINTER(P), I], I),
+            "kda_selftest_umma": ([P, P, P, I, I, I, I, I, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -259,6 +264,16 @@ def kda_trace_events(begin, end):
     b = arr_t(*[e.cuda_event for e in begin])
     en = arr_t(*[e.cuda_event for e in end])
     _check(lib, lib.kda_trace_events(b, en, n))
+
+
+def kda_selftest_umma(A, B, D, a_mn_major=0, b_mn_major=0, stream=None):
+    """One tcgen05 product D = A @ B through the kernels' shared-memory tile
+    layouts (diagnostic; see include/kda_selftest.h). Returns the status."""
+    lib = load()
+    M, K = A.shape
+    N = B.shape[1]
+    return int(lib.kda_selftest_umma(_ptr(A), _ptr(B), _ptr(D), M, N, K, int(a_mn_major),
+                                     int(b_mn_major), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- conveniences

@@ -112,6 +112,7 @@ size_t kda_chunk_fwd_workspace_size(int64_t T_total, int n_seq, int H, int dk, i
                                     int chunk, kda_dtype dtype) {
   if (common_checks(T_total, n_seq, H, dk, dv, chunk, dtype, (const int32_t *)1) != KDA_OK)
     return 0;
+  if (kda::tc_path(dk, dv, dtype)) return kda::tc_ws_bytes(T_total, n_seq, H);
   return kda::chunk_ws_bytes(T_total, n_seq, H, dk, dv);
 }
 
@@ -144,27 +145,36 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
   KDA_REQUIRE(cu_seqlens == nullptr || ((uintptr_t)cu_seqlens & 3u) == 0, KDA_ERR_INVALID_ARG,
               "cu_seqlens is not 4-byte aligned");
   if (n_seq == 0) return KDA_OK;
-  const size_t need = kda::chunk_ws_bytes(T_total, n_seq, H, dk, dv);
+  const bool tc = kda::tc_path(dk, dv, dtype);
+  const size_t need = tc ? kda::tc_ws_bytes(T_total, n_seq, H)
+                         : kda::chunk_ws_bytes(T_total, n_seq, H, dk, dv);
   KDA_REQUIRE(workspace != nullptr && workspace_bytes >= need, KDA_ERR_WORKSPACE,
               "workspace %zu bytes, need %zu", workspace_bytes, need);
   KDA_REQUIRE(((uintptr_t)workspace & 255u) == 0, KDA_ERR_INVALID_ARG,
               "workspace is not 256-byte aligned");
   cudaStream_t s = (cudaStream_t)stream;
   Tracer tr(s);
-  kda::ChunkWs ws = kda::chunk_ws_carve(workspace, T_total, n_seq, H, dk, dv);
+  kda::ChunkWs ws = tc ? kda::tc_ws_carve(workspace, T_total, n_seq, H)
+                       : kda::chunk_ws_carve(workspace, T_total, n_seq, H, dk, dv);
   st = cuda_status(tr([&] { return kda::launch_chunk_table(cu_seqlens, n_seq, T_total, ws, s); }),
                    "chunk table");
   if (st != KDA_OK) return st;
   st = cuda_status(tr([&] {
-                     return kda::launch_prep(q, k, v, log_alpha, beta, cu_seqlens, n_seq, T_total,
-                                             H, dk, dv, flags, dtype, ws, true, s);
+                     return tc ? kda::launch_card_tc(q, k, v, log_alpha, beta, cu_seqlens, n_seq,
+                                                     T_total, H, flags, ws, s)
+                               : kda::launch_prep(q, k, v, log_alpha, beta, cu_seqlens, n_seq,
+                                                  T_total, H, dk, dv, flags, dtype, ws, true, s);
                    }),
                    "chunk prep");
   if (st != KDA_OK) return st;
   return cuda_status(tr([&] {
-                       return kda::launch_state_pass(0, gate, out, initial_state, final_state,
-                                                     nullptr, nullptr, cu_seqlens, n_seq, T_total,
-                                                     H, dk, dv, scale, dtype, ws, s);
+                       return tc ? kda::launch_state_tc(0, gate, out, initial_state, final_state,
+                                                        nullptr, nullptr, cu_seqlens, n_seq,
+                                                        T_total, H, scale, ws, s)
+                                 : kda::launch_state_pass(0, gate, out, initial_state,
+                                                          final_state, nullptr, nullptr,
+                                                          cu_seqlens, n_seq, T_total, H, dk, dv,
+                                                          scale, dtype, ws, s);
                      }),
                      "state pass");
 }
@@ -222,27 +232,35 @@ kda_status kda_segment_summary(const void *k, const void *v, const void *log_alp
   KDA_REQUIRE(cu_segs == nullptr || ((uintptr_t)cu_segs & 3u) == 0, KDA_ERR_INVALID_ARG,
               "cu_segs is not 4-byte aligned");
   if (n_seg == 0) return KDA_OK;
-  const size_t need = kda::chunk_ws_bytes(T_total, n_seg, H, dk, dv);
+  const bool tc = kda::tc_path(dk, dv, dtype);
+  const size_t need = tc ? kda::tc_ws_bytes(T_total, n_seg, H)
+                         : kda::chunk_ws_bytes(T_total, n_seg, H, dk, dv);
   KDA_REQUIRE(workspace != nullptr && workspace_bytes >= need, KDA_ERR_WORKSPACE,
               "workspace %zu bytes, need %zu", workspace_bytes, need);
   KDA_REQUIRE(((uintptr_t)workspace & 255u) == 0, KDA_ERR_INVALID_ARG,
               "workspace is not 256-byte aligned");
   cudaStream_t s = (cudaStream_t)stream;
   Tracer tr(s);
-  kda::ChunkWs ws = kda::chunk_ws_carve(workspace, T_total, n_seg, H, dk, dv);
+  kda::ChunkWs ws = tc ? kda::tc_ws_carve(workspace, T_total, n_seg, H)
+                       : kda::chunk_ws_carve(workspace, T_total, n_seg, H, dk, dv);
   st = cuda_status(tr([&] { return kda::launch_chunk_table(cu_segs, n_seg, T_total, ws, s); }),
                    "chunk table");
   if (st != KDA_OK) return st;
   st = cuda_status(tr([&] {
-                     return kda::launch_prep(k, k, v, log_alpha, beta, cu_segs, n_seg, T_total, H,
-                                             dk, dv, flags, dtype, ws, false, s);
+                     return tc ? kda::launch_card_tc(k, k, v, log_alpha, beta, cu_segs, n_seg,
+                                                     T_total, H, flags, ws, s)
+                               : kda::launch_prep(k, k, v, log_alpha, beta, cu_segs, n_seg,
+                                                  T_total, H, dk, dv, flags, dtype, ws, false, s);
                    }),
                    "chunk prep");
   if (st != KDA_OK) return st;
   return cuda_status(tr([&] {
-                       return kda::launch_state_pass(1, nullptr, nullptr, nullptr, nullptr, X_out,
-                                                     Z_out, cu_segs, n_seg, T_total, H, dk, dv,
-                                                     1.0f, dtype, ws, s);
+                       return tc ? kda::launch_state_tc(1, nullptr, nullptr, nullptr, nullptr,
+                                                        X_out, Z_out, cu_segs, n_seg, T_total, H,
+                                                        1.0f, ws, s)
+                                 : kda::launch_state_pass(1, nullptr, nullptr, nullptr, nullptr,
+                                                          X_out, Z_out, cu_segs, n_seg, T_total,
+                                                          H, dk, dv, 1.0f, dtype, ws, s);
                      }),
                      "summary state pass");
 }
@@ -285,10 +303,11 @@ kda_status kda_trace_events(void *const *begin, void *const *end, int n) {
 kda_status kda_get_error(kda_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "stream synchronize");
-  unsigned a = 0, b = 0;
+  unsigned a = 0, b = 0, c = 0;
   if ((e = kda::chunk_take_error(&a)) != cudaSuccess) return cuda_status(e, "error word");
   if ((e = kda::decode_take_error(&b)) != cudaSuccess) return cuda_status(e, "error word");
-  const unsigned bits = a | b;
+  if ((e = kda::tc_take_error(&c)) != cudaSuccess) return cuda_status(e, "error word");
+  const unsigned bits = a | b | c;
   if (bits & kda::kErrTimeout) return fail(KDA_ERR_TIMEOUT, "a bounded device wait ran out");
   if (bits & kda::kErrBadSeqlens)
     return fail(KDA_ERR_INVALID_ARG, "malformed cu_seqlens / cu_segs or state_slot on device");

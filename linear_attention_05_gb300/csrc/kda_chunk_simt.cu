@@ -473,7 +473,7 @@ size_t chunk_ws_bytes(int64_t T_total, int n_seq, int H, int dk, int dv) {
 }
 
 ChunkWs chunk_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int dv) {
-  ChunkWs w;
+  ChunkWs w = {};
   const size_t mc = max_chunks_of(T_total, n_seq);
   char *p = (char *)ws;
   w.meta = (ChunkMeta *)p;

@@ -59,7 +59,8 @@ namespace kda {
 struct ChunkWs {
   ChunkMeta *meta;
   int *seq_chunk_off;  // [n_seq + 1]
-  float *W, *U, *Q, *Kd, *P, *D;
+  float *W, *U, *Q, *Kd, *P, *D;  // SIMT path
+  uint8_t *cards;                 // tensor-core path: one update card per (chunk, head)
   int max_chunks;
 };
 
@@ -89,6 +90,19 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v,
 cudaError_t launch_scan_combine(const float *X, const float *Z, int n_seg,
                                 int H, int dk, int dv, const float *S_init,
                                 float *E_out, float *S_final, cudaStream_t st);
+
+// Tensor-core path (bf16, dk = dv = 128): update cards + state pass.
+bool tc_path(int dk, int dv, kda_dtype dt);
+size_t tc_ws_bytes(int64_t T_total, int n_seq, int H);
+ChunkWs tc_ws_carve(void *ws, int64_t T_total, int n_seq, int H);
+cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const void *la,
+                           const void *beta, const int32_t *cu, int n_seq, int64_t T_total,
+                           int H, unsigned flags, const ChunkWs &ws, cudaStream_t st);
+cudaError_t launch_state_tc(int mode, const void *gate, void *out, const float *S0,
+                            float *S_final, float *X_out, float *Z_out, const int32_t *cu,
+                            int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
+                            cudaStream_t st);
+cudaError_t tc_take_error(unsigned *bits);
 
 // Sets the calling thread's kda_last_error_string() message; returns `st`.
 kda_status api_fail(kda_status st, const char *fmt, ...);

@@ -242,8 +242,10 @@ def test_decode_equals_chunk_one_token():
     cu = torch.arange(N + 1, dtype=torch.int32, device=DEV)
     oc, sc = B.chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], S_in, cu,
                          n_seq=N)
-    assert rel_err(np32(o), np32(oc)) <= 1e-2
-    assert rel_err(np32(S), np32(sc)) <= 1e-4
+    # bf16 inputs: both paths within the bf16 tolerance of each other (the chunked
+    # tensor-core path multiplies bf16-rounded state operands)
+    assert rel_err(np32(o), np32(oc)) <= TOL[torch.bfloat16]
+    assert rel_err(np32(S), np32(sc)) <= TOL[torch.bfloat16]
 
 
 def test_decode_bad_slot_reported():
