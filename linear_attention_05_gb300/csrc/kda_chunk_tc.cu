@@ -4,8 +4,8 @@
 // "FlashKDA": per-chunk update cards prepared in parallel; only the state
 // hand-off and read-out run in order):
 //
-// Stage A, kda_card_tc: one CTA per (chunk, head) builds the chunk's update
-// card. With G the inclusive running sum of log_alpha inside the chunk,
+// Stage A, kda_card_tc: one CTA per (chunk, head), two per SM, builds the
+// chunk's update card from TMA-loaded, 128-byte-swizzled input tiles. With G the inclusive running sum of log_alpha inside the chunk,
 // Kt = k e^{G}, Kh = k e^{-G}, Qt = q e^{G}, Kd = k e^{G_C - G} (k, q L2-normalised):
 //   M  = strict_lower(diag(b) Kt Kh^T),   P = lower(Qt Kh^T)              (GEMM 1)
 //   T  = (I + M)^{-1}  (blocked forward substitution), T' = T diag(b)
@@ -20,9 +20,14 @@
 // tensor memory as S^T (lane = value channel). Per chunk the CTA pre-loads
 // Diag(e^{G_C}) S + B_c into tensor memory and issues one group of MMAs,
 // bf16(S^T) x [Phi'^T | Q'^T], accumulating onto it, so the serial path has a
-// single tensor-core round trip per chunk.
+// single tensor-core round trip per chunk; separate warps turn the output
+// accumulators into o while the next chunk's MMAs run.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "kda_common.cuh"
 #include "tc_common.cuh"
@@ -45,17 +50,6 @@ constexpr int CARD_D = 81920;      // e^{G_C}: 128 fp32
 constexpr int CARD_OIT = 82432;    // O_intra^T: [8][128][8] bf16
 constexpr int CARD_BYTES = 98816;
 constexpr int CARD_STAGE = 82432;  // part copied into shared memory (PhiQ, B_c^T, e^{G_C})
-
-// ---- stage A shared memory (offsets from a 1024-aligned base)
-constexpr int A_X1 = 0;         // 32768: [Kt ; Qt] 128-row tile (K-major / MN-major)
-constexpr int A_KH = 32768;     // 16384: Kh 64-row tile; during the solve T (fp32); later W^T 128x64
-constexpr int A_VS = 49152;     // 16384: V 64-row tile; later Ut^T 128x64
-constexpr int A_KD = 65536;     // 16384: Kd 64-row tile
-constexpr int A_STG = 81920;    // 32768: input staging (half chunk); later P, T', M
-constexpr int A_P = A_STG;            // 8192: P 64-row tile
-constexpr int A_TB = A_STG + 8192;    // 8192: T' 64-row tile (and block temporaries during the solve)
-constexpr int A_MS = A_STG + 16384;   // 16384: M fp32 64x64 (column-swizzled)
-constexpr int A_DYN = 114688 + 1024;  // dynamic shared memory request (with alignment slack)
 
 // ---- stage B shared memory
 constexpr int B_STAGE_BYTES = 82944;  // CARD_STAGE rounded up to 1024
@@ -111,21 +105,43 @@ __device__ __forceinline__ void unpack8(uint4 u, float *v) {
 __device__ __forceinline__ int mix(int r, int c) { return r * 64 + (c ^ (r & 31)); }
 
 // ===========================================================================
-// Stage A: update cards. 128 threads; thread t is key/value channel t in the
-// element-wise phase and tensor-memory lane t in the epilogues.
-__global__ void __launch_bounds__(128, 2) kda_card_tc(
-    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-    const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ la,
+// Stage A: update cards. One CTA (256 threads, two per SM) per (chunk, head).
+// The four input tiles arrive by TMA with 128-byte swizzling, i.e. already in
+// the tensor-core operand layout, and the element-wise pass rewrites them in
+// place: k -> Kt, q -> Qt (one 128-row tile [Kt ; Qt]), log_alpha -> Kh -> Kd.
+// Shared memory (offsets from a 1024-aligned base):
+constexpr int A_X1 = 0;          // 32768: [k|Kt ; q|Qt] 128-row tile; later P (64-row) at 0
+constexpr int A_LA = 32768;      // 16384: log_alpha -> Kh -> Kd (64-row tile)
+constexpr int A_V = 49152;       // 16384: V (64-row tile)
+constexpr int A_M = 65536;       // 16384: M (fp32, 64x64); later W^T (128-row x 64)
+constexpr int A_T = 81920;       // 16384: T (fp32, 64x64); later Ut^T (128-row x 64)
+constexpr int A_TB = 98304;      // 8192:  T' = T diag(b) (bf16 64-row tile)
+constexpr int A_XT = 106496;     // 3072:  block temporaries of the solve
+constexpr int A_DYN = 109568 + 1024;  // with alignment slack
+constexpr uint32_t A_TMA_BYTES = 8 * 8192;
+
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(256, 2) kda_card_tc(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+    const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_v,
     const __nv_bfloat16 *__restrict__ beta, const int32_t *__restrict__ cu, int n_seq,
     int64_t fixed_len, int H, unsigned flags, const ChunkMeta *__restrict__ meta,
     const int *__restrict__ off, uint8_t *__restrict__ cards) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_mma;
+  __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_base;
-  __shared__ float s_rk[C], s_rq[C], s_b[C], s_d[DD];
+  __shared__ float s_rk[C], s_rq[C], s_b[C], s_d[DD], s_part[DD];
 
   const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
+  const int warp = tid >> 5, lane = tid & 31, quad = warp & 3, grp = warp >> 2;
   if (meta->invalid || ci >= meta->total_chunks) return;
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(sm);
@@ -135,161 +151,135 @@ __global__ void __launch_bounds__(128, 2) kda_card_tc(
   seq_range(cu, fixed_len, s, &ts, &ls);
   const int64_t t0 = ts + (int64_t)(ci - off[s]) * C;
   const int len = (int)min((int64_t)C, ls - (int64_t)(ci - off[s]) * C);
-  const size_t row_stride = (size_t)H * DD;  // elements between consecutive tokens
   const bool l2 = (flags & KDA_QK_L2NORM) != 0;
   const bool dbg = (flags & KDA_DEBUG_CHECK) != 0;
 
-  if (warp == 0) {
+  if (tid == 0) {
+    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar_tma, A_TMA_BYTES);
+    for (int a = 0; a < 2; ++a) {
+      tma_load_3d(sm + A_X1 + a * 16384, &tm_k, 64 * a, h, (int)t0, &bar_tma);
+      tma_load_3d(sm + A_X1 + a * 16384 + 8192, &tm_q, 64 * a, h, (int)t0, &bar_tma);
+      tma_load_3d(sm + A_LA + a * 8192, &tm_la, 64 * a, h, (int)t0, &bar_tma);
+      tma_load_3d(sm + A_V + a * 8192, &tm_v, 64 * a, h, (int)t0, &bar_tma);
+    }
+  }
+  if (warp == 1) {
     tmem_alloc(&tmem_base, 256);
     tmem_relinquish();
   }
-  if (tid == 0) {
-    mbar_init(&bar_mma, 1);
-    fence_mbar_init();
-  }
   if (tid < C) {
-    float b = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+    const float b = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
     if (dbg && tid < len && !(b >= 0.f && b <= 1.f)) set_err(kErrPrecondition);
     s_b[tid] = b;
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tmem_base;
+  bool ok = mbar_wait(&bar_tma, 0);
 
-  // ---------------- element-wise phase, two halves of 32 rows
-  float G = 0.f;  // running log-decay of channel tid
-  const __nv_bfloat16 *srcs[4] = {k, q, la, v};
-  for (int half = 0; half < 2; ++half) {
-    const int h0 = half * 32;
-    // stage rows [h0, h0 + 32) of k, q, log_alpha, v as raw bf16 rows of 256 bytes
-#pragma unroll 4
-    for (int i = 0; i < 16; ++i) {
-      const int idx = tid + 128 * i;
-      const int tn = idx >> 9, row = (idx >> 4) & 31, ch = idx & 15;
-      uint4 val = make_uint4(0, 0, 0, 0);
-      if (h0 + row < len)
-        val = *reinterpret_cast<const uint4 *>(srcs[tn] + (size_t)(t0 + h0 + row) * row_stride +
-                                               (size_t)h * DD + ch * 8);
-      *reinterpret_cast<uint4 *>(sm + A_STG + tn * 8192 + row * 256 + ch * 16) = val;
-    }
-    __syncthreads();
-    // row norms of k and q: four threads per row, 32 channels each
-    {
-      const int row = tid >> 2, part = tid & 3;
-      float sk = 0.f, sq = 0.f;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float a[8], b[8];
-        unpack8(*reinterpret_cast<const uint4 *>(sm + A_STG + 0 * 8192 + row * 256 +
-                                                 (part * 4 + c4) * 16), a);
-        unpack8(*reinterpret_cast<const uint4 *>(sm + A_STG + 1 * 8192 + row * 256 +
-                                                 (part * 4 + c4) * 16), b);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          sk = fmaf(a[e], a[e], sk);
-          sq = fmaf(b[e], b[e], sq);
-        }
-      }
-      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 2);
-      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-      if (part == 0) {
-        s_rk[h0 + row] = l2 ? rsqrtf(sk + kL2Eps) : 1.f;
-        s_rq[h0 + row] = l2 ? rsqrtf(sq + kL2Eps) : 1.f;
-      }
-    }
-    __syncthreads();
-    // channel-parallel pass: running decay and the decayed operands
-    {
-      const int c = tid;
-      for (int row = 0; row < 32; ++row) {
-        const int r = h0 + row;
-        const float l = bf(sm + A_STG + 2 * 8192, row * 256 + c * 2);
-        if (dbg && r < len && !(l >= kLogAlphaMin && l <= 0.f)) set_err(kErrPrecondition);
-        G += l;
-        const float ep = __expf(G), en = __expf(-G);
-        const float kn = bf(sm + A_STG, row * 256 + c * 2) * s_rk[r];
-        const float qn = bf(sm + A_STG + 8192, row * 256 + c * 2) * s_rq[r];
-        const float vv = bf(sm + A_STG + 3 * 8192, row * 256 + c * 2);
-        put_bf(sm + A_X1, sw128_off(r, c, 128), kn * ep);
-        put_bf(sm + A_X1, sw128_off(64 + r, c, 128), qn * ep);
-        put_bf(sm + A_KH, sw128_off(r, c, 64), kn * en);
-        put_bf(sm + A_VS, sw128_off(r, c, 64), vv);
-      }
-    }
-    __syncthreads();
-  }
-  // Kd = Kh * e^{G_C}
+  // ---------------- row norms of k and q: four threads per row, 32 channels each
   {
-    const int c = tid;
-    const float eC = __expf(G);
-    s_d[c] = eC;
-    for (int r = 0; r < C; ++r) put_bf(sm + A_KD, sw128_off(r, c, 64), bf(sm + A_KH, sw128_off(r, c, 64)) * eC);
+    const int r = tid >> 2, part = tid & 3;
+    float sk = 0.f, sq = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float a[8], b[8];
+      unpack8(*reinterpret_cast<const uint4 *>(sm + A_X1 + sw128_chunk(r, part * 4 + i, 128)), a);
+      unpack8(*reinterpret_cast<const uint4 *>(sm + A_X1 + sw128_chunk(64 + r, part * 4 + i, 128)),
+              b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sk = fmaf(a[e], a[e], sk);
+        sq = fmaf(b[e], b[e], sq);
+      }
+    }
+    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+    sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+    if (part == 0) {
+      // padded rows (r >= len) come back as zero: no contribution anywhere
+      s_rk[r] = r >= len ? 0.f : (l2 ? rsqrtf(sk + kL2Eps) : 1.f);
+      s_rq[r] = r >= len ? 0.f : (l2 ? rsqrtf(sq + kL2Eps) : 1.f);
+    }
+  }
+  // ---------------- running log-decay: thread = (channel c, block of 32 rows)
+  const int c = tid & 127, rb = tid >> 7;
+  {
+    float p = 0.f;
+    for (int r = rb * 32; r < rb * 32 + 32; ++r) {
+      const float l = r < len ? bf(sm + A_LA, sw128_off(r, c, 64)) : 0.f;
+      if (dbg && r < len && !(l >= kLogAlphaMin && l <= 0.f)) set_err(kErrPrecondition);
+      p += l;
+    }
+    if (rb == 0) s_part[c] = p;
+  }
+  __syncthreads();
+  {
+    float G = rb ? s_part[c] : 0.f;
+    for (int r = rb * 32; r < rb * 32 + 32; ++r) {
+      const float l = r < len ? bf(sm + A_LA, sw128_off(r, c, 64)) : 0.f;
+      G += l;
+      const float ep = __expf(G), en = __expf(-G);
+      const float kn = bf(sm + A_X1, sw128_off(r, c, 128)) * s_rk[r];
+      const float qn = bf(sm + A_X1, sw128_off(64 + r, c, 128)) * s_rq[r];
+      put_bf(sm + A_X1, sw128_off(r, c, 128), kn * ep);
+      put_bf(sm + A_X1, sw128_off(64 + r, c, 128), qn * ep);
+      put_bf(sm + A_LA, sw128_off(r, c, 64), kn * en);
+    }
+    if (rb == 1) s_d[c] = __expf(G);  // e^{G_C}
   }
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tb = tmem_base;
   uint32_t phase = 0;
-  bool ok = true;
-
   auto wait_mma = [&]() {
-    if (!mbar_wait(&bar_mma, phase)) {
-      if (lane == 0) set_err(kErrTimeout);
-      ok = false;
-    }
+    if (ok && !mbar_wait(&bar_mma, phase)) ok = false;
     phase ^= 1u;
     tc_fence_after();
   };
 
-  // ---------------- GEMM 1: D1[0,64) = [Kt ; Qt] Kh^T  (M=128, N=64, K=128)
-  if (tid == 0) {
+  // ---------------- GEMM 1: D1[0,64) = [Kt ; Qt] Kh^T   (M=128, N=64, K=128)
+  if (tid == 0 && ok) {
     const uint32_t id = idesc_bf16(128, 64, 0, 0);
     for (int kk = 0; kk < 8; ++kk)
-      mma_bf16(tb + 0, desc_kmajor(sb + A_X1, 128, kk), desc_kmajor(sb + A_KH, 64, kk), id,
-               kk > 0);
+      mma_bf16(tb + 0, desc_kmajor(sb + A_X1, 128, kk), desc_kmajor(sb + A_LA, 64, kk), id, kk > 0);
     mma_commit(&bar_mma);
   }
   wait_mma();
-  // epilogue 1: lanes 0-63 -> M (fp32, strict lower, beta-scaled rows); lanes 64-127 -> P (bf16)
   {
-    const int L = warp * 32 + lane;
-    float a[64];
-    {
-      float t32[32];
-      tmem_ld32(tmem_addr(tb, warp * 32, 0), t32);
+    // lanes 0-63: M = strict_lower(diag(b) Kt Kh^T) -> fp32; group g takes columns [32g, 32g+32)
+    if (quad < 2) {
+      const int r = quad * 32 + lane;
+      float a[32];
+      tmem_ld32(tmem_addr(tb, quad * 32, 32 * grp), a);
       tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) a[i] = t32[i];
-      tmem_ld32(tmem_addr(tb, warp * 32, 32), t32);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) a[32 + i] = t32[i];
-    }
-    float *Ms = reinterpret_cast<float *>(sm + A_MS);
-    if (L < 64) {
-      const int r = L;
+      float *Ms = reinterpret_cast<float *>(sm + A_M);
       const float b = s_b[r];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) Ms[mix(r, i)] = i < r ? b * a[i] : 0.f;
-    } else {
-      const int r = L - 64;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        float e[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) e[u] = (ch * 8 + u <= r) ? a[ch * 8 + u] : 0.f;
-        *reinterpret_cast<uint4 *>(sm + A_P + sw128_chunk(r, ch, 64)) = pack8(e);
+      for (int i = 0; i < 32; ++i) {
+        const int col = 32 * grp + i;
+        Ms[mix(r, col)] = col < r ? b * a[i] : 0.f;
       }
     }
+    // Kh is no longer read by the tensor cores: Kd = Kh * e^{G_C} in place
+    const float eC = s_d[c];
+    for (int r = rb * 32; r < rb * 32 + 32; ++r)
+      put_bf(sm + A_LA, sw128_off(r, c, 64), bf(sm + A_LA, sw128_off(r, c, 64)) * eC);
   }
   tc_fence_before();
   __syncthreads();
 
-  // ---------------- T = (I + M)^{-1}, blocked by 16; T kept in A_KH (fp32, swizzled)
+  // ---------------- T = (I + M)^{-1}, blocked by 16 (fp32)
   {
-    const float *Ms = reinterpret_cast<const float *>(sm + A_MS);
-    float *Ts = reinterpret_cast<float *>(sm + A_KH);
-    float *Xt = reinterpret_cast<float *>(sm + A_TB);  // 3 x 16 x 16 temporaries
+    const float *Ms = reinterpret_cast<const float *>(sm + A_M);
+    float *Ts = reinterpret_cast<float *>(sm + A_T);
+    float *Xt = reinterpret_cast<float *>(sm + A_XT);
     if (tid < 64) {  // diagonal blocks: thread = (block a, column j)
       const int a = tid >> 4, j = tid & 15, o = 16 * a;
       float t[16];
@@ -306,38 +296,38 @@ __global__ void __launch_bounds__(128, 2) kda_card_tc(
     __syncthreads();
     for (int d = 1; d < 4; ++d) {
       const int nb = 4 - d;
-      for (int e = tid; e < nb * 256; e += 128) {
-        const int a = e >> 8, i = (e >> 4) & 15, j = e & 15, rb = a + d;
+      for (int e = tid; e < nb * 256; e += 256) {
+        const int a = e >> 8, i = (e >> 4) & 15, j = e & 15, rbk = a + d;
         float acc = 0.f;
-        for (int kb = a; kb < rb; ++kb)
+        for (int kb = a; kb < rbk; ++kb)
 #pragma unroll
           for (int kx = 0; kx < 16; ++kx)
-            acc = fmaf(Ms[mix(16 * rb + i, 16 * kb + kx)], Ts[mix(16 * kb + kx, 16 * a + j)], acc);
+            acc = fmaf(Ms[mix(16 * rbk + i, 16 * kb + kx)], Ts[mix(16 * kb + kx, 16 * a + j)], acc);
         Xt[e] = acc;
       }
       __syncthreads();
-      for (int e = tid; e < nb * 256; e += 128) {
-        const int a = e >> 8, i = (e >> 4) & 15, j = e & 15, rb = a + d;
+      for (int e = tid; e < nb * 256; e += 256) {
+        const int a = e >> 8, i = (e >> 4) & 15, j = e & 15, rbk = a + d;
         float acc = 0.f;
 #pragma unroll
         for (int kx = 0; kx < 16; ++kx)
-          acc = fmaf(Ts[mix(16 * rb + i, 16 * rb + kx)], Xt[(a << 8) + (kx << 4) + j], acc);
-        Ts[mix(16 * rb + i, 16 * a + j)] = -acc;
+          acc = fmaf(Ts[mix(16 * rbk + i, 16 * rbk + kx)], Xt[(a << 8) + (kx << 4) + j], acc);
+        Ts[mix(16 * rbk + i, 16 * a + j)] = -acc;
       }
       __syncthreads();
     }
-    // T' = T diag(beta) -> bf16 64-row K-major tile (rows r, columns j)
+    // T' = T diag(b) -> bf16 64-row K-major tile (rows r, columns j): 16 columns per thread
     {
-      const int r = tid >> 1, hc = tid & 1;
+      const int r = tid >> 2, qc = tid & 3;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         float e[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const int j = hc * 32 + ch * 8 + u;
+          const int j = qc * 16 + ch * 8 + u;
           e[u] = (j <= r) ? Ts[mix(r, j)] * s_b[j] : 0.f;
         }
-        *reinterpret_cast<uint4 *>(sm + A_TB + sw128_chunk(r, hc * 4 + ch, 64)) = pack8(e);
+        *reinterpret_cast<uint4 *>(sm + A_TB + sw128_chunk(r, qc * 2 + ch, 64)) = pack8(e);
       }
     }
   }
@@ -347,29 +337,42 @@ __global__ void __launch_bounds__(128, 2) kda_card_tc(
   tc_fence_after();
 
   // ---------------- GEMM 2: W^T -> [64,128), Ut^T -> [128,192)   (M=128, N=64, K=64)
-  if (tid == 0) {
+  if (tid == 0 && ok) {
     const uint32_t id = idesc_bf16(128, 64, 1, 0);
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t bd = desc_kmajor(sb + A_TB, 64, kk);
       mma_bf16(tb + 64, sdesc_sw128(sb + A_X1 + kk * 2048, 128 * 128, 1024), bd, id, kk > 0);
-      mma_bf16(tb + 128, sdesc_sw128(sb + A_VS + kk * 2048, 64 * 128, 1024), bd, id, kk > 0);
+      mma_bf16(tb + 128, sdesc_sw128(sb + A_V + kk * 2048, 64 * 128, 1024), bd, id, kk > 0);
     }
     mma_commit(&bar_mma);
   }
   wait_mma();
-  // epilogue 2: W^T and Ut^T rows (lane = channel) -> bf16 128-row K-major tiles
-#pragma unroll 1
-  for (int which = 0; which < 2; ++which) {
-    const int L = warp * 32 + lane;
-    uint8_t *dst = sm + (which == 0 ? A_KH : A_VS);
+  {
+    const int L = quad * 32 + lane;
+    // group 0: W^T rows -> tile at A_M; group 1: Ut^T rows -> tile at A_T (128-row K-major)
+    uint8_t *dst = sm + (grp == 0 ? A_M : A_T);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       float t32[32];
-      tmem_ld32(tmem_addr(tb, warp * 32, 64 + 64 * which + 32 * half), t32);
+      tmem_ld32(tmem_addr(tb, quad * 32, 64 + 64 * grp + 32 * half), t32);
       tmem_wait_ld();
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch)
         *reinterpret_cast<uint4 *>(dst + sw128_chunk(L, half * 4 + ch, 128)) = pack8(t32 + ch * 8);
+    }
+    // lanes 64-127 of D1 hold Qt Kh^T: P = lower(.) -> bf16 64-row tile at A_X1 (Kt is dead)
+    if (quad >= 2) {
+      const int r = L - 64;
+      float a[32];
+      tmem_ld32(tmem_addr(tb, quad * 32, 32 * grp), a);
+      tmem_wait_ld();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        float e[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) e[u] = (32 * grp + ch * 8 + u <= r) ? a[ch * 8 + u] : 0.f;
+        *reinterpret_cast<uint4 *>(sm + A_X1 + sw128_chunk(r, grp * 4 + ch, 64)) = pack8(e);
+      }
     }
   }
   fence_async_smem();
@@ -378,49 +381,40 @@ __global__ void __launch_bounds__(128, 2) kda_card_tc(
   tc_fence_after();
 
   uint8_t *card = cards + ((size_t)ci * H + h) * CARD_BYTES;
+  const int L = quad * 32 + lane;  // tensor-memory lane: key channel (a) / value channel (b)
   // ---------------- GEMMs 3a/4a on W^T: (PW)^T -> [0,64), W^T Kd -> [64,192)
-  if (tid == 0) {
+  if (tid == 0 && ok) {
     const uint32_t id3 = idesc_bf16(128, 64, 0, 0), id4 = idesc_bf16(128, 128, 0, 1);
     for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = desc_kmajor(sb + A_KH, 128, kk);
-      mma_bf16(tb + 0, ad, desc_kmajor(sb + A_P, 64, kk), id3, kk > 0);
-      mma_bf16(tb + 64, ad, desc_mnmajor(sb + A_KD, 64, kk), id4, kk > 0);
+      const uint64_t ad = desc_kmajor(sb + A_M, 128, kk);
+      mma_bf16(tb + 0, ad, desc_kmajor(sb + A_X1, 64, kk), id3, kk > 0);
+      mma_bf16(tb + 64, ad, desc_mnmajor(sb + A_LA, 64, kk), id4, kk > 0);
     }
     mma_commit(&bar_mma);
   }
   wait_mma();
-  {
-    const int c = warp * 32 + lane;  // key channel
-    // Q'^T[c][r] = Qt[r][c] - (PW)^T[c][r]
+  // six 32-column pieces: 0-1 Q'^T = Qt^T - (PW)^T, 2-5 Phi'^T = -(W^T Kd); group g takes 3g..3g+2
+#pragma unroll 1
+  for (int p = 3 * grp; p < 3 * grp + 3; ++p) {
+    float t32[32];
+    tmem_ld32(tmem_addr(tb, quad * 32, 32 * p), t32);
+    tmem_wait_ld();
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float t32[32];
-      tmem_ld32(tmem_addr(tb, warp * 32, 32 * half), t32);
-      tmem_wait_ld();
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        float e[8];
+    for (int ch = 0; ch < 4; ++ch) {
+      float e[8];
+      if (p < 2) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const int r = half * 32 + ch * 8 + u;
-          e[u] = bf(sm + A_X1, sw128_off(64 + r, c, 128)) - t32[ch * 8 + u];
+          const int r = p * 32 + ch * 8 + u;
+          e[u] = bf(sm + A_X1, sw128_off(64 + r, L, 128)) - t32[ch * 8 + u];
         }
-        *reinterpret_cast<uint4 *>(card + CARD_PHIQ + sw128_chunk(c, 16 + half * 4 + ch, 128)) =
+        *reinterpret_cast<uint4 *>(card + CARD_PHIQ + sw128_chunk(L, 16 + p * 4 + ch, 128)) =
             pack8(e);
-      }
-    }
-    // Phi'^T[c][c'] = -(W^T Kd)[c][c']
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      float t32[32];
-      tmem_ld32(tmem_addr(tb, warp * 32, 64 + 32 * q4), t32);
-      tmem_wait_ld();
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        float e[8];
+      } else {
 #pragma unroll
         for (int u = 0; u < 8; ++u) e[u] = -t32[ch * 8 + u];
-        *reinterpret_cast<uint4 *>(card + CARD_PHIQ + sw128_chunk(c, q4 * 4 + ch, 128)) = pack8(e);
+        *reinterpret_cast<uint4 *>(card + CARD_PHIQ + sw128_chunk(L, (p - 2) * 4 + ch, 128)) =
+            pack8(e);
       }
     }
   }
@@ -428,64 +422,65 @@ __global__ void __launch_bounds__(128, 2) kda_card_tc(
   __syncthreads();
   tc_fence_after();
   // ---------------- GEMMs 3b/4b on Ut^T: O_intra^T -> [0,64), B_c^T -> [64,192)
-  if (tid == 0) {
+  if (tid == 0 && ok) {
     const uint32_t id3 = idesc_bf16(128, 64, 0, 0), id4 = idesc_bf16(128, 128, 0, 1);
     for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = desc_kmajor(sb + A_VS, 128, kk);
-      mma_bf16(tb + 0, ad, desc_kmajor(sb + A_P, 64, kk), id3, kk > 0);
-      mma_bf16(tb + 64, ad, desc_mnmajor(sb + A_KD, 64, kk), id4, kk > 0);
+      const uint64_t ad = desc_kmajor(sb + A_T, 128, kk);
+      mma_bf16(tb + 0, ad, desc_kmajor(sb + A_X1, 64, kk), id3, kk > 0);
+      mma_bf16(tb + 64, ad, desc_mnmajor(sb + A_LA, 64, kk), id4, kk > 0);
     }
     mma_commit(&bar_mma);
   }
   wait_mma();
-  {
-    const int j = warp * 32 + lane;  // value channel
+#pragma unroll 1
+  for (int p = 3 * grp; p < 3 * grp + 3; ++p) {
+    float t32[32];
+    tmem_ld32(tmem_addr(tb, quad * 32, 32 * p), t32);
+    tmem_wait_ld();
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float t32[32];
-      tmem_ld32(tmem_addr(tb, warp * 32, 32 * half), t32);
-      tmem_wait_ld();
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-        *reinterpret_cast<uint4 *>(card + CARD_OIT + ((half * 4 + ch) * 128 + j) * 16) =
-            pack8(t32 + ch * 8);
+    for (int ch = 0; ch < 4; ++ch) {
+      const int off8 = p < 2 ? CARD_OIT + ((p * 4 + ch) * 128 + L) * 16
+                             : CARD_BCT + (((p - 2) * 4 + ch) * 128 + L) * 16;
+      *reinterpret_cast<uint4 *>(card + off8) = pack8(t32 + ch * 8);
     }
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      float t32[32];
-      tmem_ld32(tmem_addr(tb, warp * 32, 64 + 32 * q4), t32);
-      tmem_wait_ld();
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-        *reinterpret_cast<uint4 *>(card + CARD_BCT + ((q4 * 4 + ch) * 128 + j) * 16) =
-            pack8(t32 + ch * 8);
-    }
-    reinterpret_cast<float *>(card + CARD_D)[tid] = s_d[tid];
   }
-  (void)ok;
+  if (tid < DD) reinterpret_cast<float *>(card + CARD_D)[tid] = s_d[tid];
+  if (!ok && lane == 0) set_err(kErrTimeout);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tb, 256);
+  if (warp == 1) tmem_dealloc(tb, 256);
 }
 
 // ===========================================================================
-// Stage B: the sequential state pass. 128 threads; thread j owns tensor-memory
-// lane j = value channel j (row j of S^T). mode 0: prefill; mode 1: segment
-// summary on [X | Z] (blockIdx.y = 0: X with entry I; 1: Z with entry 0).
-__global__ void __launch_bounds__(128, 1) kda_state_tc(
+// Stage B: the sequential state pass, one CTA per (sequence, head), 256 threads.
+// Warps 0-3 (state group) carry the serial path: thread j owns tensor-memory
+// lane j = value channel j (row j of S^T). Warps 4-7 (output group) read the
+// chunk outputs from the same lanes, add O_intra, apply scale and gate and store
+// o, off the serial path. mode 0: prefill; mode 1: segment summary on [X | Z]
+// (blockIdx.y = 0: X with entry I; 1: Z with entry 0), no output.
+//
+// Tensor memory: [0,128) the fp32 state S^T; [128,192) and [192,256) the output
+// accumulators of even and odd chunks. mbarriers: bar_full[2] card stages
+// landed; bar_mma chunk MMAs done (state group); bar_ofull[2] output buffer
+// written (output group); bar_ofree[2] output buffer read (MMA issuer).
+__global__ void __launch_bounds__(256, 1) kda_state_tc(
     int mode, const __nv_bfloat16 *__restrict__ gate, __nv_bfloat16 *__restrict__ out,
     const float *__restrict__ S0, float *__restrict__ S_final, float *__restrict__ X_out,
     float *__restrict__ Z_out, const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len,
     int H, float scale, const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
     const uint8_t *__restrict__ cards) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[2], bar_mma;
+  __shared__ uint64_t bar_full[2], bar_mma, bar_ofull[2], bar_ofree[2];
   __shared__ uint32_t tmem_base;
+  __shared__ int s_fail;
   if (meta->invalid) return;
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(sm);
   const int chain = blockIdx.x, s = chain / H, h = chain % H, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31, j = tid;
+  const int warp = tid >> 5, lane = tid & 31;
+  const bool state_grp = tid < 128;
+  const int j = tid & 127;   // tensor-memory lane / value channel
+  const int quad = warp & 3; // lane quadrant of this warp
   const bool xpart = (mode == 1 && blockIdx.y == 0);
   const bool with_bc = !xpart;
   const bool with_o = (mode == 0 && out != nullptr);
@@ -495,7 +490,7 @@ __global__ void __launch_bounds__(128, 1) kda_state_tc(
   const int nchunks = (int)((ls + C - 1) / C);
   const int cbase = nchunks > 0 ? off[s] : 0;
   auto card_of = [&](int n) { return cards + ((size_t)(cbase + n) * H + h) * CARD_BYTES; };
-  // element (c, j) of the entry state, and of the result
+  // element (c, j) of the entry state, and where element (c, j) of the result goes
   auto entry = [&](int c) -> float {
     if (mode == 0) return S0 ? S0[(((size_t)s * H + h) * DD + c) * DD + j] : 0.f;
     return (xpart && c == j) ? 1.f : 0.f;
@@ -506,10 +501,11 @@ __global__ void __launch_bounds__(128, 1) kda_state_tc(
     return Z_out + (((size_t)s * H + h) * DD + c) * DD + j;
   };
   if (nchunks == 0) {
-    for (int c = 0; c < DD; ++c) {
-      float *p = result_ptr(c);
-      if (p) *p = entry(c);
-    }
+    if (state_grp)
+      for (int c = 0; c < DD; ++c) {
+        float *p = result_ptr(c);
+        if (p) *p = entry(c);
+      }
     return;
   }
 
@@ -521,166 +517,194 @@ __global__ void __launch_bounds__(128, 1) kda_state_tc(
     mbar_init(&bar_full[0], 1);
     mbar_init(&bar_full[1], 1);
     mbar_init(&bar_mma, 1);
+    mbar_init(&bar_ofull[0], 1);
+    mbar_init(&bar_ofull[1], 1);
+    mbar_init(&bar_ofree[0], 128);
+    mbar_init(&bar_ofree[1], 128);
     fence_mbar_init();
+    s_fail = 0;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = tmem_base;
-  int loads_issued = 0;
-  auto load_card = [&](int n) {  // by thread 0
-    uint8_t *dst = sm + (n & 1) * B_STAGE_BYTES;
-    const uint8_t *src = card_of(n);
-    mbar_arrive_expect_tx(&bar_full[n & 1], CARD_STAGE);
-    for (int o = 0; o < CARD_STAGE; o += 16384) {
-      const int bytes = min(16384, CARD_STAGE - o);
-      bulk_g2s(dst + o, src + o, bytes, &bar_full[n & 1]);
-    }
-    ++loads_issued;
-  };
-  if (tid == 0) {
-    load_card(0);
-    if (nchunks > 1) load_card(1);
-  }
-  uint32_t full_phase[2] = {0u, 0u}, mma_phase = 0u;
-  int loads_done = 0;
-  bool ok = true;
-
-  // For the MMA of chunk n: tensor memory [0,128) <- Diag(e^{G_C}) S + B_c (fp32) and the
-  // bf16 operand S^T (row j) in shared memory, from one 32-column piece `x` of row j of S^T.
-  auto stage_piece = [&](int n, int q4, const float *x) {
-    const uint8_t *st = sm + (n & 1) * B_STAGE_BYTES;
-    const float *dv = reinterpret_cast<const float *>(st + CARD_D);
-    float init[32];
-#pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-      float bc[8];
-      if (with_bc)
-        unpack8(*reinterpret_cast<const uint4 *>(st + CARD_BCT + ((q4 * 4 + ch) * 128 + j) * 16),
-                bc);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int c = q4 * 32 + ch * 8 + u;
-        init[ch * 8 + u] = dv[c] * x[ch * 8 + u] + (with_bc ? bc[u] : 0.f);
+  if (state_grp) {
+    int loads_issued = 0, loads_done = 0;
+    uint32_t full_phase[2] = {0u, 0u}, mma_phase = 0u;
+    bool ok = true;
+    auto load_card = [&](int n) {  // by thread 0
+      uint8_t *dst = sm + (n & 1) * B_STAGE_BYTES;
+      const uint8_t *src = card_of(n);
+      mbar_arrive_expect_tx(&bar_full[n & 1], CARD_STAGE);
+      for (int o = 0; o < CARD_STAGE; o += 16384) {
+        const int bytes = min(16384, CARD_STAGE - o);
+        bulk_g2s(dst + o, src + o, bytes, &bar_full[n & 1]);
       }
-      *reinterpret_cast<uint4 *>(sm + B_SA + sw128_chunk(j, q4 * 4 + ch, 128)) = pack8(x + ch * 8);
-    }
-    tmem_st32(tmem_addr(tb, warp * 32, 32 * q4), init);
-  };
-  auto finish_stage = [&]() {
-    tmem_wait_st();
-    fence_async_smem();
-    tc_fence_before();
-  };
-  auto issue_mma = [&](int n) {  // by thread 0
-    const uint32_t stg = sb + (n & 1) * B_STAGE_BYTES;
-    const uint32_t idS = idesc_bf16(128, 128, 0, 1), idO = idesc_bf16(128, 64, 0, 1);
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint64_t ad = desc_kmajor(sb + B_SA, 128, kk);
-      const uint64_t bS = sdesc_sw128(stg + CARD_PHIQ + kk * 2048, 128 * 128, 1024);
-      mma_bf16(tb + 0, ad, bS, idS, 1u);
-      if (with_o) {
-        const uint64_t bO = sdesc_sw128(stg + CARD_PHIQ + 2 * 16384 + kk * 2048, 128 * 128, 1024);
-        mma_bf16(tb + 128 + 64 * (n & 1), ad, bO, idO, kk > 0);
-      }
-    }
-    mma_commit(&bar_mma);
-  };
-  auto wait_full = [&](int n) -> bool {
-    const bool r = mbar_wait(&bar_full[n & 1], full_phase[n & 1]);
-    full_phase[n & 1] ^= 1u;
-    if (r) ++loads_done;
-    return r;
-  };
-
-  // chunk 0: entry state from global memory
-  if (!wait_full(0)) ok = false;
-  if (ok) {
-#pragma unroll 1
-    for (int q4 = 0; q4 < 4; ++q4) {
-      float x[32];
+      ++loads_issued;
+    };
+    auto wait_full = [&](int n) -> bool {
+      const bool r = mbar_wait(&bar_full[n & 1], full_phase[n & 1]);
+      full_phase[n & 1] ^= 1u;
+      if (r) ++loads_done;
+      return r;
+    };
+    // Tensor memory [0,128) <- Diag(e^{G_C}) S + B_c of chunk n (fp32) and the bf16
+    // operand S^T (row j) in shared memory, from one 32-column piece `x` of row j.
+    auto stage_piece = [&](int n, int q4, const float *x) {
+      const uint8_t *st = sm + (n & 1) * B_STAGE_BYTES;
+      const float *dv = reinterpret_cast<const float *>(st + CARD_D);
+      float init[32];
 #pragma unroll
-      for (int u = 0; u < 32; ++u) x[u] = entry(q4 * 32 + u);
-      stage_piece(0, q4, x);
-    }
-    finish_stage();
-  }
-  __syncthreads();
-  tc_fence_after();
-  if (tid == 0 && ok) issue_mma(0);
-
-  for (int n = 0; n < nchunks && ok; ++n) {
-    const int64_t t0 = ts + (int64_t)n * C;
-    const int len = (int)min((int64_t)C, ls - (int64_t)n * C);
-    if (!mbar_wait(&bar_mma, mma_phase)) {
-      ok = false;
-      break;
-    }
-    mma_phase ^= 1u;
-    tc_fence_after();
-    // the card of chunk n is consumed: refill its stage with chunk n + 2
-    if (tid == 0 && n + 2 < nchunks) load_card(n + 2);
-    const bool last = (n + 1 == nchunks);
-    if (!last && !wait_full(n + 1)) {
-      ok = false;
-      break;
-    }
-    // state after chunk n: stage it for chunk n + 1, or write it out
-#pragma unroll 1
-    for (int q4 = 0; q4 < 4; ++q4) {
-      float x[32];
-      tmem_ld32(tmem_addr(tb, warp * 32, 32 * q4), x);
-      tmem_wait_ld();
-      if (last) {
+      for (int ch = 0; ch < 4; ++ch) {
+        float bc[8];
+        if (with_bc)
+          unpack8(*reinterpret_cast<const uint4 *>(st + CARD_BCT + ((q4 * 4 + ch) * 128 + j) * 16),
+                  bc);
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          float *p = result_ptr(q4 * 32 + u);
-          if (p) *p = x[u];
+        for (int u = 0; u < 8; ++u) {
+          const int c = q4 * 32 + ch * 8 + u;
+          init[ch * 8 + u] = dv[c] * x[ch * 8 + u] + (with_bc ? bc[u] : 0.f);
         }
-      } else {
-        stage_piece(n + 1, q4, x);
+        *reinterpret_cast<uint4 *>(sm + B_SA + sw128_chunk(j, q4 * 4 + ch, 128)) =
+            pack8(x + ch * 8);
+      }
+      tmem_st32(tmem_addr(tb, quad * 32, 32 * q4), init);
+    };
+    auto finish_stage = [&]() {
+      tmem_wait_st();
+      fence_async_smem();
+      tc_fence_before();
+    };
+    auto issue_mma = [&](int n) -> bool {  // by thread 0
+      // the output buffer of chunk n was last used by chunk n - 2
+      if (with_o && n >= 2 && !mbar_wait(&bar_ofree[n & 1], ((n >> 1) - 1) & 1)) return false;
+      tc_fence_after();
+      const uint32_t stg = sb + (n & 1) * B_STAGE_BYTES;
+      const uint32_t idS = idesc_bf16(128, 128, 0, 1), idO = idesc_bf16(128, 64, 0, 1);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t ad = desc_kmajor(sb + B_SA, 128, kk);
+        const uint64_t bS = sdesc_sw128(stg + CARD_PHIQ + kk * 2048, 128 * 128, 1024);
+        mma_bf16(tb + 0, ad, bS, idS, 1u);
+        if (with_o) {
+          const uint64_t bO =
+              sdesc_sw128(stg + CARD_PHIQ + 2 * 16384 + kk * 2048, 128 * 128, 1024);
+          mma_bf16(tb + 128 + 64 * (n & 1), ad, bO, idO, kk > 0);
+        }
+      }
+      mma_commit(&bar_mma);
+      if (with_o) mma_commit(&bar_ofull[n & 1]);
+      return true;
+    };
+
+    if (tid == 0) {
+      load_card(0);
+      if (nchunks > 1) load_card(1);
+    }
+    // chunk 0: entry state from global memory
+    if (!wait_full(0)) ok = false;
+    if (ok) {
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float x[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) x[u] = entry(q4 * 32 + u);
+        stage_piece(0, q4, x);
+      }
+      finish_stage();
+    }
+    named_bar(1, 128);
+    tc_fence_after();
+    if (tid == 0 && ok && !issue_mma(0)) s_fail = 1;
+
+    for (int n = 0; n < nchunks && ok; ++n) {
+      if (!mbar_wait(&bar_mma, mma_phase)) {
+        ok = false;
+        break;
+      }
+      mma_phase ^= 1u;
+      tc_fence_after();
+      // the card of chunk n is consumed: refill its stage with chunk n + 2
+      if (tid == 0 && n + 2 < nchunks) load_card(n + 2);
+      const bool last = (n + 1 == nchunks);
+      if (!last && !wait_full(n + 1)) {
+        ok = false;
+        break;
+      }
+      // state after chunk n: stage it for chunk n + 1, or write it out
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float x[32];
+        tmem_ld32(tmem_addr(tb, quad * 32, 32 * q4), x);
+        tmem_wait_ld();
+        if (last) {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            float *p = result_ptr(q4 * 32 + u);
+            if (p) *p = x[u];
+          }
+        } else {
+          stage_piece(n + 1, q4, x);
+        }
+      }
+      if (!last) {
+        finish_stage();
+        named_bar(1, 128);
+        tc_fence_after();
+        if (tid == 0 && !issue_mma(n + 1)) s_fail = 1;
       }
     }
-    if (!last) {
-      finish_stage();
-      named_bar(1, 128);
-      tc_fence_after();
-      if (tid == 0) issue_mma(n + 1);
+    if (!ok || s_fail) {
+      if (lane == 0) set_err(kErrTimeout);
+      // let copies still in flight land (bounded) before shared memory is released
+      if (tid == 0)
+        for (int n = loads_done; n < loads_issued; ++n) {
+          if (!mbar_wait(&bar_full[n & 1], full_phase[n & 1], 100000000ull)) break;
+          full_phase[n & 1] ^= 1u;
+        }
     }
-    // output of chunk n (overlaps the MMA of chunk n + 1)
-    if (with_o) {
+  } else if (with_o) {
+    // output group: o = scale * g * (Q' S + O_intra) for chunk n
+    uint32_t ofull_phase[2] = {0u, 0u};
+    for (int n = 0; n < nchunks; ++n) {
+      const int64_t t0 = ts + (int64_t)n * C;
+      const int len = (int)min((int64_t)C, ls - (int64_t)n * C);
+      float gv[C];
+#pragma unroll
+      for (int r = 0; r < C; ++r)
+        gv[r] = (gate && r < len) ? __bfloat162float(gate[((size_t)(t0 + r) * H + h) * DD + j])
+                                  : 1.f;
+      uint4 oi[8];
       const uint8_t *card = card_of(n);
-#pragma unroll 1
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        oi[ch] = *reinterpret_cast<const uint4 *>(card + CARD_OIT + (ch * 128 + j) * 16);
+      if (!mbar_wait(&bar_ofull[n & 1], ofull_phase[n & 1])) {
+        if (lane == 0) set_err(kErrTimeout);
+        break;
+      }
+      ofull_phase[n & 1] ^= 1u;
+      tc_fence_after();
+#pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float t32[32];
-        tmem_ld32(tmem_addr(tb, warp * 32, 128 + 64 * (n & 1) + 32 * hf), t32);
+        tmem_ld32(tmem_addr(tb, quad * 32, 128 + 64 * (n & 1) + 32 * hf), t32);
         tmem_wait_ld();
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          float oi[8];
-          unpack8(*reinterpret_cast<const uint4 *>(card + CARD_OIT + ((hf * 4 + ch) * 128 + j) * 16),
-                  oi);
+          float o8[8];
+          unpack8(oi[hf * 4 + ch], o8);
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int r = hf * 32 + ch * 8 + u;
-            if (r < len) {
-              const size_t g = ((size_t)(t0 + r) * H + h) * DD + j;
-              const float gv = gate ? __bfloat162float(gate[g]) : 1.f;
-              out[g] = __float2bfloat16_rn(scale * gv * (t32[ch * 8 + u] + oi[u]));
-            }
+            if (r < len)
+              out[((size_t)(t0 + r) * H + h) * DD + j] =
+                  __float2bfloat16_rn(scale * gv[r] * (t32[ch * 8 + u] + o8[u]));
           }
         }
       }
       tc_fence_before();
+      mbar_arrive(&bar_ofree[n & 1]);
     }
-  }
-  if (!ok) {
-    if (lane == 0) set_err(kErrTimeout);
-    // let copies still in flight land (bounded) before shared memory is released
-    if (tid == 0)
-      for (int n = loads_done; n < loads_issued; ++n)
-        if (!mbar_wait(&bar_full[n & 1], full_phase[n & 1], 100000000ull)) break;
-        else full_phase[n & 1] ^= 1u;
   }
   tc_fence_before();
   __syncthreads();
@@ -713,17 +737,50 @@ ChunkWs tc_ws_carve(void *ws, int64_t T_total, int n_seq, int H) {
   return w;
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map over a packed [T_total, H, 128] bf16 tensor; box = 64 channels x 1 head x 64 tokens,
+// 128-byte swizzle (the tensor-core tile layout), zero fill past T_total.
+static bool make_token_map(CUtensorMap *m, const void *base, int64_t T_total, int H) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)DD, (cuuint64_t)H, (cuuint64_t)T_total};
+  cuuint64_t strides[2] = {(cuuint64_t)DD * 2, (cuuint64_t)H * DD * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const void *la,
                            const void *beta, const int32_t *cu, int n_seq, int64_t T_total, int H,
                            unsigned flags, const ChunkWs &ws, cudaStream_t st) {
+  if (T_total == 0) return cudaSuccess;  // no chunk has tokens
+  CUtensorMap mk, mq, mla, mv;
+  if (!make_token_map(&mk, k, T_total, H) || !make_token_map(&mq, q, T_total, H) ||
+      !make_token_map(&mla, la, T_total, H) || !make_token_map(&mv, v, T_total, H))
+    return cudaErrorInvalidValue;
   cudaError_t e =
       cudaFuncSetAttribute(kda_card_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, A_DYN);
   if (e != cudaSuccess) return e;
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
-  kda_card_tc<<<dim3(ws.max_chunks, H), 128, A_DYN, st>>>(
-      (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
-      (const __nv_bfloat16 *)la, (const __nv_bfloat16 *)beta, cu, n_seq, fixed_len, H, flags,
-      ws.meta, ws.seq_chunk_off, ws.cards);
+  kda_card_tc<<<dim3(ws.max_chunks, H), 256, A_DYN, st>>>(
+      mk, mq, mla, mv, (const __nv_bfloat16 *)beta, cu, n_seq, fixed_len, H, flags, ws.meta,
+      ws.seq_chunk_off, ws.cards);
   return cudaGetLastError();
 }
 
@@ -735,7 +792,7 @@ cudaError_t launch_state_tc(int mode, const void *gate, void *out, const float *
       cudaFuncSetAttribute(kda_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, B_DYN);
   if (e != cudaSuccess) return e;
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
-  kda_state_tc<<<dim3(n_seq * H, mode == 0 ? 1 : 2), 128, B_DYN, st>>>(
+  kda_state_tc<<<dim3(n_seq * H, mode == 0 ? 1 : 2), 256, B_DYN, st>>>(
       mode, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final, X_out, Z_out, cu,
       n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.cards);
   return cudaGetLastError();
