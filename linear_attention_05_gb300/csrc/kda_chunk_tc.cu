@@ -20,8 +20,8 @@
 // tensor memory as S^T (lane = value channel). Per chunk the CTA pre-loads
 // Diag(e^{G_C}) S + B_c into tensor memory and issues one group of MMAs,
 // bf16(S^T) x [Phi'^T | Q'^T], accumulating onto it, so the serial path has a
-// single tensor-core round trip per chunk; separate warps turn the output
-// accumulators into o while the next chunk's MMAs run.
+// single tensor-core round trip per chunk; two warpgroups stage the state and a
+// third turns the output accumulators into o while the next chunk's MMAs run.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -49,12 +49,14 @@ constexpr int CARD_BCT = 49152;    // B_c^T: [16][128][8] bf16 (8-column chunks,
 constexpr int CARD_D = 81920;      // e^{G_C}: 128 fp32
 constexpr int CARD_OIT = 82432;    // O_intra^T: [8][128][8] bf16
 constexpr int CARD_BYTES = 98816;
-constexpr int CARD_STAGE = 82432;  // part copied into shared memory (PhiQ, B_c^T, e^{G_C})
 
 // ---- stage B shared memory
-constexpr int B_STAGE_BYTES = 82944;  // CARD_STAGE rounded up to 1024
-constexpr int B_SA = 2 * B_STAGE_BYTES;   // S^T bf16 operand, 128 x 128 K-major (32768)
-constexpr int B_DYN = B_SA + 32768 + 1024;
+constexpr int B_NSTAGE = 3;            // card ring depth
+constexpr int B_STAGE_TX = CARD_BCT + 512;  // [Phi'^T | Q'^T] then e^{G_C} (49664 bytes)
+constexpr int B_STAGE_BYTES = 50176;  // B_STAGE_TX rounded up to 1024
+constexpr int B_SA = B_NSTAGE * B_STAGE_BYTES;  // S^T bf16 operand, 128 x 128 K-major (32768)
+constexpr int B_OT = B_SA + 32768;         // output transposes: 4 warps x 32 x 33 fp32
+constexpr int B_DYN = B_OT + 4 * 32 * 33 * 4 + 1024;
 
 __device__ __forceinline__ void set_err(unsigned bits) { atomicOr(&g_tc_err, bits); }
 
@@ -81,9 +83,6 @@ __device__ __forceinline__ void seq_range(const int32_t *cu, int64_t fixed_len, 
 __device__ __forceinline__ float bf(const uint8_t *base, uint32_t off) {
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
 }
-__device__ __forceinline__ void put_bf(uint8_t *base, uint32_t off, float x) {
-  *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
-}
 __device__ __forceinline__ uint4 pack8(const float *v) {
   uint4 u;
   u.x = pack_bf16x2(v[0], v[1]);
@@ -101,8 +100,8 @@ __device__ __forceinline__ void unpack8(uint4 u, float *v) {
   }
 }
 
-// fp32 64x64 matrix in shared memory, column index XOR-swizzled by row.
-__device__ __forceinline__ int mix(int r, int c) { return r * 64 + (c ^ (r & 31)); }
+// fp32 64x64 matrix in shared memory with a padded row pitch.
+__device__ __forceinline__ int mix(int r, int c) { return r * 65 + c; }
 
 // ===========================================================================
 // Stage A: update cards. One CTA (256 threads, two per SM) per (chunk, head).
@@ -113,11 +112,12 @@ __device__ __forceinline__ int mix(int r, int c) { return r * 64 + (c ^ (r & 31)
 constexpr int A_X1 = 0;          // 32768: [k|Kt ; q|Qt] 128-row tile; later P (64-row) at 0
 constexpr int A_LA = 32768;      // 16384: log_alpha -> Kh -> Kd (64-row tile)
 constexpr int A_V = 49152;       // 16384: V (64-row tile)
-constexpr int A_M = 65536;       // 16384: M (fp32, 64x64); later W^T (128-row x 64)
-constexpr int A_T = 81920;       // 16384: T (fp32, 64x64); later Ut^T (128-row x 64)
-constexpr int A_TB = 98304;      // 8192:  T' = T diag(b) (bf16 64-row tile)
-constexpr int A_XT = 106496;     // 3072:  block temporaries of the solve
-constexpr int A_DYN = 109568 + 1024;  // with alignment slack
+constexpr int A_M = 65536;       // 16640: M (fp32, 64 x 65 padded); later W^T (128-row x 64)
+constexpr int A_T = 82176;       // 16640: T (fp32, 64 x 65 padded)
+constexpr int A_TB = 99328;      // 8192:  T' = T diag(b) (bf16 64-row tile); later identity
+constexpr int A_XT = 107520;     // 3072:  block temporaries of the solve
+constexpr int A_DYN = 110592 + 1024;  // with alignment slack
+constexpr int LDM = 65;          // row pitch of M and T (conflict-free rows and columns)
 constexpr uint32_t A_TMA_BYTES = 8 * 8192;
 
 __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, int c0, int c1,
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_base;
-  __shared__ float s_rk[C], s_rq[C], s_b[C], s_d[DD], s_part[DD];
+  __shared__ float s_rk[C], s_rq[C], s_b[C], s_d[DD];
 
   const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31, quad = warp & 3, grp = warp >> 2;
@@ -181,57 +181,87 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
   const uint32_t tb = tmem_base;
   bool ok = mbar_wait(&bar_tma, 0);
 
-  // ---------------- row norms of k and q: four threads per row, 32 channels each
+  // ---------------- element-wise phase: thread = (8-channel chunk cc, rows 4*rg .. 4*rg+3)
+  const int cc = tid & 15, rg = tid >> 4;
+  float* part = reinterpret_cast<float *>(sm + A_M);  // [16 row groups][128 channels], before M
+  float la8[4][8];
   {
-    const int r = tid >> 2, part = tid & 3;
-    float sk = 0.f, sq = 0.f;
+    float ssk[4], ssq[4], tot[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) tot[u] = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float a[8], b[8];
-      unpack8(*reinterpret_cast<const uint4 *>(sm + A_X1 + sw128_chunk(r, part * 4 + i, 128)), a);
-      unpack8(*reinterpret_cast<const uint4 *>(sm + A_X1 + sw128_chunk(64 + r, part * 4 + i, 128)),
-              b);
+      const int r = rg * 4 + i;
+      float kk[8], qq[8];
+      unpack8(*reinterpret_cast<const uint4 *>(sm + A_X1 + sw128_chunk(r, cc, 128)), kk);
+      unpack8(*reinterpret_cast<const uint4 *>(sm + A_X1 + sw128_chunk(64 + r, cc, 128)), qq);
+      unpack8(*reinterpret_cast<const uint4 *>(sm + A_LA + sw128_chunk(r, cc, 64)), la8[i]);
+      ssk[i] = 0.f;
+      ssq[i] = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        sk = fmaf(a[e], a[e], sk);
-        sq = fmaf(b[e], b[e], sq);
+      for (int u = 0; u < 8; ++u) {
+        ssk[i] = fmaf(kk[u], kk[u], ssk[i]);
+        ssq[i] = fmaf(qq[u], qq[u], ssq[i]);
+        if (r >= len) la8[i][u] = 0.f;
+        if (dbg && r < len && !(la8[i][u] >= kLogAlphaMin && la8[i][u] <= 0.f))
+          set_err(kErrPrecondition);
+        tot[u] += la8[i][u];
       }
     }
-    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-    sk += __shfl_xor_sync(0xffffffffu, sk, 2);
-    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-    if (part == 0) {
-      // padded rows (r >= len) come back as zero: no contribution anywhere
-      s_rk[r] = r >= len ? 0.f : (l2 ? rsqrtf(sk + kL2Eps) : 1.f);
-      s_rq[r] = r >= len ? 0.f : (l2 ? rsqrtf(sq + kL2Eps) : 1.f);
-    }
-  }
-  // ---------------- running log-decay: thread = (channel c, block of 32 rows)
-  const int c = tid & 127, rb = tid >> 7;
-  {
-    float p = 0.f;
-    for (int r = rb * 32; r < rb * 32 + 32; ++r) {
-      const float l = r < len ? bf(sm + A_LA, sw128_off(r, c, 64)) : 0.f;
-      if (dbg && r < len && !(l >= kLogAlphaMin && l <= 0.f)) set_err(kErrPrecondition);
-      p += l;
-    }
-    if (rb == 0) s_part[c] = p;
+    // row sums over the 16 threads of a half-warp (same rows, all 128 channels)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) {
+        ssk[i] += __shfl_xor_sync(0xffffffffu, ssk[i], o);
+        ssq[i] += __shfl_xor_sync(0xffffffffu, ssq[i], o);
+      }
+    if (cc == 0)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = rg * 4 + i;
+        // padded rows (r >= len) are scaled to zero: no contribution anywhere
+        s_rk[r] = r >= len ? 0.f : (l2 ? rsqrtf(ssk[i] + kL2Eps) : 1.f);
+        s_rq[r] = r >= len ? 0.f : (l2 ? rsqrtf(ssq[i] + kL2Eps) : 1.f);
+      }
+    *reinterpret_cast<float4 *>(part + rg * 128 + cc * 8) = make_float4(tot[0], tot[1], tot[2], tot[3]);
+    *reinterpret_cast<float4 *>(part + rg * 128 + cc * 8 + 4) = make_float4(tot[4], tot[5], tot[6], tot[7]);
   }
   __syncthreads();
   {
-    float G = rb ? s_part[c] : 0.f;
-    for (int r = rb * 32; r < rb * 32 + 32; ++r) {
-      const float l = r < len ? bf(sm + A_LA, sw128_off(r, c, 64)) : 0.f;
-      G += l;
-      const float ep = __expf(G), en = __expf(-G);
-      const float kn = bf(sm + A_X1, sw128_off(r, c, 128)) * s_rk[r];
-      const float qn = bf(sm + A_X1, sw128_off(64 + r, c, 128)) * s_rq[r];
-      put_bf(sm + A_X1, sw128_off(r, c, 128), kn * ep);
-      put_bf(sm + A_X1, sw128_off(64 + r, c, 128), qn * ep);
-      put_bf(sm + A_LA, sw128_off(r, c, 64), kn * en);
+    // running log-decay G entering this thread's first row: sum over earlier row groups
+    float G[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) G[u] = 0.f;
+    for (int g = 0; g < rg; ++g) {
+      const float4 x0 = *reinterpret_cast<const float4 *>(part + g * 128 + cc * 8);
+      const float4 x1 = *reinterpret_cast<const float4 *>(part + g * 128 + cc * 8 + 4);
+      G[0] += x0.x; G[1] += x0.y; G[2] += x0.z; G[3] += x0.w;
+      G[4] += x1.x; G[5] += x1.y; G[6] += x1.z; G[7] += x1.w;
     }
-    if (rb == 1) s_d[c] = __expf(G);  // e^{G_C}
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = rg * 4 + i;
+      float kk[8], qq[8], kt[8], qt[8], kh[8];
+      unpack8(*reinterpret_cast<const uint4 *>(sm + A_X1 + sw128_chunk(r, cc, 128)), kk);
+      unpack8(*reinterpret_cast<const uint4 *>(sm + A_X1 + sw128_chunk(64 + r, cc, 128)), qq);
+      const float rk = s_rk[r], rq = s_rq[r];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        G[u] += la8[i][u];
+        const float ep = __expf(G[u]), en = __expf(-G[u]);
+        const float kn = kk[u] * rk;
+        kt[u] = kn * ep;
+        kh[u] = kn * en;
+        qt[u] = qq[u] * rq * ep;
+      }
+      *reinterpret_cast<uint4 *>(sm + A_X1 + sw128_chunk(r, cc, 128)) = pack8(kt);
+      *reinterpret_cast<uint4 *>(sm + A_X1 + sw128_chunk(64 + r, cc, 128)) = pack8(qt);
+      *reinterpret_cast<uint4 *>(sm + A_LA + sw128_chunk(r, cc, 64)) = pack8(kh);
+    }
+    if (rg == 15)  // after the last row: G = G_C
+#pragma unroll
+      for (int u = 0; u < 8; ++u) s_d[cc * 8 + u] = __expf(G[u]);
   }
   fence_async_smem();
   tc_fence_before();
@@ -268,9 +298,18 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
       }
     }
     // Kh is no longer read by the tensor cores: Kd = Kh * e^{G_C} in place
-    const float eC = s_d[c];
-    for (int r = rb * 32; r < rb * 32 + 32; ++r)
-      put_bf(sm + A_LA, sw128_off(r, c, 64), bf(sm + A_LA, sw128_off(r, c, 64)) * eC);
+    float eC[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) eC[u] = s_d[cc * 8 + u];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 *p = reinterpret_cast<uint4 *>(sm + A_LA + sw128_chunk(rg * 4 + i, cc, 64));
+      float x[8];
+      unpack8(*p, x);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] *= eC[u];
+      *p = pack8(x);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -280,39 +319,51 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
     const float *Ms = reinterpret_cast<const float *>(sm + A_M);
     float *Ts = reinterpret_cast<float *>(sm + A_T);
     float *Xt = reinterpret_cast<float *>(sm + A_XT);
-    if (tid < 64) {  // diagonal blocks: thread = (block a, column j)
+    if (tid < 64) {  // diagonal blocks: thread = (block a, column j); right-looking
       const int a = tid >> 4, j = tid & 15, o = 16 * a;
-      float t[16];
+      float acc[16], t[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float acc = 0.f;
+      for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll
-        for (int kx = 0; kx < i; ++kx) acc = fmaf(Ms[mix(o + i, o + kx)], t[kx], acc);
-        t[i] = (i == j) ? 1.f : (i < j ? 0.f : -acc);
+      for (int kx = 0; kx < 16; ++kx) {
+        t[kx] = (kx == j) ? 1.f : (kx < j ? 0.f : -acc[kx]);
+#pragma unroll
+        for (int i = kx + 1; i < 16; ++i) acc[i] = fmaf(Ms[mix(o + i, o + kx)], t[kx], acc[i]);
       }
 #pragma unroll
       for (int i = 0; i < 16; ++i) Ts[mix(o + i, o + j)] = t[i];
     }
     __syncthreads();
+#pragma unroll 1
     for (int d = 1; d < 4; ++d) {
-      const int nb = 4 - d;
-      for (int e = tid; e < nb * 256; e += 256) {
-        const int a = e >> 8, i = (e >> 4) & 15, j = e & 15, rbk = a + d;
-        float acc = 0.f;
-        for (int kb = a; kb < rbk; ++kb)
+      const int nb = 4 - d;  // output blocks (a + d, a), a < nb; one element per thread each
 #pragma unroll
-          for (int kx = 0; kx < 16; ++kx)
-            acc = fmaf(Ms[mix(16 * rbk + i, 16 * kb + kx)], Ts[mix(16 * kb + kx, 16 * a + j)], acc);
-        Xt[e] = acc;
+      for (int m = 0; m < 3; ++m) {
+        if (m >= nb) break;
+        const int e = tid + 256 * m, a = e >> 8, i = (e >> 4) & 15, jj = e & 15, rbk = a + d;
+        float p0 = 0.f, p1 = 0.f;
+#pragma unroll 1
+        for (int kb = 0; kb < d; ++kb)
+#pragma unroll
+          for (int kx = 0; kx < 16; kx += 2) {
+            p0 = fmaf(Ms[mix(16 * rbk + i, 16 * (a + kb) + kx)], Ts[mix(16 * (a + kb) + kx, 16 * a + jj)], p0);
+            p1 = fmaf(Ms[mix(16 * rbk + i, 16 * (a + kb) + kx + 1)],
+                      Ts[mix(16 * (a + kb) + kx + 1, 16 * a + jj)], p1);
+          }
+        Xt[e] = p0 + p1;
       }
       __syncthreads();
-      for (int e = tid; e < nb * 256; e += 256) {
-        const int a = e >> 8, i = (e >> 4) & 15, j = e & 15, rbk = a + d;
-        float acc = 0.f;
 #pragma unroll
-        for (int kx = 0; kx < 16; ++kx)
-          acc = fmaf(Ts[mix(16 * rbk + i, 16 * rbk + kx)], Xt[(a << 8) + (kx << 4) + j], acc);
-        Ts[mix(16 * rbk + i, 16 * a + j)] = -acc;
+      for (int m = 0; m < 3; ++m) {
+        if (m >= nb) break;
+        const int e = tid + 256 * m, a = e >> 8, i = (e >> 4) & 15, jj = e & 15, rbk = a + d;
+        float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+        for (int kx = 0; kx < 16; kx += 2) {
+          p0 = fmaf(Ts[mix(16 * rbk + i, 16 * rbk + kx)], Xt[(a << 8) + (kx << 4) + jj], p0);
+          p1 = fmaf(Ts[mix(16 * rbk + i, 16 * rbk + kx + 1)], Xt[(a << 8) + ((kx + 1) << 4) + jj], p1);
+        }
+        Ts[mix(16 * rbk + i, 16 * a + jj)] = -(p0 + p1);
       }
       __syncthreads();
     }
@@ -349,8 +400,9 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
   wait_mma();
   {
     const int L = quad * 32 + lane;
-    // group 0: W^T rows -> tile at A_M; group 1: Ut^T rows -> tile at A_T (128-row K-major)
-    uint8_t *dst = sm + (grp == 0 ? A_M : A_T);
+    // group 0: W^T rows -> tile at A_M; group 1: Ut^T rows -> tile at A_V (128-row K-major;
+    // V is no longer read)
+    uint8_t *dst = sm + (grp == 0 ? A_M : A_V);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       float t32[32];
@@ -359,6 +411,15 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch)
         *reinterpret_cast<uint4 *>(dst + sw128_chunk(L, half * 4 + ch, 128)) = pack8(t32 + ch * 8);
+    }
+    // identity (64 x 64, bf16) in the T' tile, which GEMM 2 has finished reading
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int e = tid * 2 + i, row = e >> 3, ch = e & 7;
+      float v8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v8[u] = (ch * 8 + u == row) ? 1.f : 0.f;
+      *reinterpret_cast<uint4 *>(sm + A_TB + sw128_chunk(row, ch, 64)) = pack8(v8);
     }
     // lanes 64-127 of D1 hold Qt Kh^T: P = lower(.) -> bf16 64-row tile at A_X1 (Kt is dead)
     if (quad >= 2) {
@@ -382,41 +443,34 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
 
   uint8_t *card = cards + ((size_t)ci * H + h) * CARD_BYTES;
   const int L = quad * 32 + lane;  // tensor-memory lane: key channel (a) / value channel (b)
-  // ---------------- GEMMs 3a/4a on W^T: (PW)^T -> [0,64), W^T Kd -> [64,192)
+  // ---------------- GEMMs 3a/4a: Q'^T = Qt^T I - W^T P^T -> [0,64), Phi'^T = -W^T Kd -> [64,192)
+  // (A negated through the instruction descriptor)
   if (tid == 0 && ok) {
-    const uint32_t id3 = idesc_bf16(128, 64, 0, 0), id4 = idesc_bf16(128, 128, 0, 1);
+    const uint32_t idI = idesc_bf16(128, 64, 1, 0);
+    const uint32_t id3 = idesc_bf16(128, 64, 0, 0) | kNegateA;
+    const uint32_t id4 = idesc_bf16(128, 128, 0, 1) | kNegateA;
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16(tb + 0, sdesc_sw128(sb + A_X1 + 8192 + kk * 2048, 128 * 128, 1024),
+               desc_kmajor(sb + A_TB, 64, kk), idI, kk > 0);
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t ad = desc_kmajor(sb + A_M, 128, kk);
-      mma_bf16(tb + 0, ad, desc_kmajor(sb + A_X1, 64, kk), id3, kk > 0);
+      mma_bf16(tb + 0, ad, desc_kmajor(sb + A_X1, 64, kk), id3, 1u);
       mma_bf16(tb + 64, ad, desc_mnmajor(sb + A_LA, 64, kk), id4, kk > 0);
     }
     mma_commit(&bar_mma);
   }
   wait_mma();
-  // six 32-column pieces: 0-1 Q'^T = Qt^T - (PW)^T, 2-5 Phi'^T = -(W^T Kd); group g takes 3g..3g+2
+  // six 32-column pieces: 0-1 Q'^T (card atom column 2), 2-5 Phi'^T; group g takes 3g..3g+2
 #pragma unroll 1
   for (int p = 3 * grp; p < 3 * grp + 3; ++p) {
     float t32[32];
     tmem_ld32(tmem_addr(tb, quad * 32, 32 * p), t32);
     tmem_wait_ld();
+    const int ch0 = p < 2 ? 16 + p * 4 : (p - 2) * 4;
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-      float e[8];
-      if (p < 2) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int r = p * 32 + ch * 8 + u;
-          e[u] = bf(sm + A_X1, sw128_off(64 + r, L, 128)) - t32[ch * 8 + u];
-        }
-        *reinterpret_cast<uint4 *>(card + CARD_PHIQ + sw128_chunk(L, 16 + p * 4 + ch, 128)) =
-            pack8(e);
-      } else {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) e[u] = -t32[ch * 8 + u];
-        *reinterpret_cast<uint4 *>(card + CARD_PHIQ + sw128_chunk(L, (p - 2) * 4 + ch, 128)) =
-            pack8(e);
-      }
-    }
+    for (int ch = 0; ch < 4; ++ch)
+      *reinterpret_cast<uint4 *>(card + CARD_PHIQ + sw128_chunk(L, ch0 + ch, 128)) =
+          pack8(t32 + ch * 8);
   }
   tc_fence_before();
   __syncthreads();
@@ -425,7 +479,7 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
   if (tid == 0 && ok) {
     const uint32_t id3 = idesc_bf16(128, 64, 0, 0), id4 = idesc_bf16(128, 128, 0, 1);
     for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = desc_kmajor(sb + A_T, 128, kk);
+      const uint64_t ad = desc_kmajor(sb + A_V, 128, kk);
       mma_bf16(tb + 0, ad, desc_kmajor(sb + A_X1, 64, kk), id3, kk > 0);
       mma_bf16(tb + 64, ad, desc_mnmajor(sb + A_LA, 64, kk), id4, kk > 0);
     }
@@ -452,25 +506,30 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
 }
 
 // ===========================================================================
-// Stage B: the sequential state pass, one CTA per (sequence, head), 256 threads.
-// Warps 0-3 (state group) carry the serial path: thread j owns tensor-memory
-// lane j = value channel j (row j of S^T). Warps 4-7 (output group) read the
-// chunk outputs from the same lanes, add O_intra, apply scale and gate and store
-// o, off the serial path. mode 0: prefill; mode 1: segment summary on [X | Z]
-// (blockIdx.y = 0: X with entry I; 1: Z with entry 0), no output.
+// Stage B: the sequential state pass, one CTA per (sequence, head), 384 threads.
+// Warps 0-7 (state group) carry the serial path: warp w serves tensor-memory
+// lanes 32*(w%4).. (lane j = value channel j, i.e. row j of S^T) and the key
+// columns [64*(w/4), 64*(w/4) + 64) of that row. Warps 8-11 (output group) read
+// the chunk outputs from the same lanes, add O_intra, apply scale and gate and
+// store o, off the serial path. mode 0: prefill; mode 1: segment summary on
+// [X | Z] (blockIdx.y = 0: X with entry I; 1: Z with entry 0), no output.
 //
-// Tensor memory: [0,128) the fp32 state S^T; [128,192) and [192,256) the output
-// accumulators of even and odd chunks. mbarriers: bar_full[2] card stages
-// landed; bar_mma chunk MMAs done (state group); bar_ofull[2] output buffer
-// written (output group); bar_ofree[2] output buffer read (MMA issuer).
-__global__ void __launch_bounds__(256, 1) kda_state_tc(
+// Tensor memory holds two accumulator sets, chunk n using set n % 2: columns
+// [256b, 256b+128) the fp32 state S^T, [256b+128, 256b+192) the output block.
+// Before the MMAs of chunk n the set is pre-loaded with Diag(e^{G_C}) S + B_c
+// (state group) and zeros (output group), so one N = 192 MMA chain per chunk
+// produces both the next state and the chunk output.
+// mbarriers: bar_full[3] card stages landed; bar_mma chunk MMAs done (state
+// group); bar_ofull[2] output block written (output group); bar_ofree[2]
+// output block read and re-zeroed (MMA issuer).
+__global__ void __launch_bounds__(384, 1) kda_state_tc(
     int mode, const __nv_bfloat16 *__restrict__ gate, __nv_bfloat16 *__restrict__ out,
     const float *__restrict__ S0, float *__restrict__ S_final, float *__restrict__ X_out,
     float *__restrict__ Z_out, const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len,
     int H, float scale, const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
     const uint8_t *__restrict__ cards) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[2], bar_mma, bar_ofull[2], bar_ofree[2];
+  __shared__ uint64_t bar_full[B_NSTAGE], bar_mma, bar_ofull[2], bar_ofree[2];
   __shared__ uint32_t tmem_base;
   __shared__ int s_fail;
   if (meta->invalid) return;
@@ -478,9 +537,10 @@ __global__ void __launch_bounds__(256, 1) kda_state_tc(
   const uint32_t sb = smem_u32(sm);
   const int chain = blockIdx.x, s = chain / H, h = chain % H, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const bool state_grp = tid < 128;
-  const int j = tid & 127;   // tensor-memory lane / value channel
-  const int quad = warp & 3; // lane quadrant of this warp
+  const bool state_grp = warp < 8;
+  const int quad = warp & 3;           // lane quadrant of this warp
+  const int j = quad * 32 + lane;      // tensor-memory lane / value channel
+  const int half = (warp >> 2) & 1;    // state group: which 64 key columns
   const bool xpart = (mode == 1 && blockIdx.y == 0);
   const bool with_bc = !xpart;
   const bool with_o = (mode == 0 && out != nullptr);
@@ -502,7 +562,7 @@ __global__ void __launch_bounds__(256, 1) kda_state_tc(
   };
   if (nchunks == 0) {
     if (state_grp)
-      for (int c = 0; c < DD; ++c) {
+      for (int c = 64 * half; c < 64 * half + 64; ++c) {
         float *p = result_ptr(c);
         if (p) *p = entry(c);
       }
@@ -510,12 +570,11 @@ __global__ void __launch_bounds__(256, 1) kda_state_tc(
   }
 
   if (warp == 0) {
-    tmem_alloc(&tmem_base, 256);
+    tmem_alloc(&tmem_base, 512);
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(&bar_full[0], 1);
-    mbar_init(&bar_full[1], 1);
+    for (int i = 0; i < B_NSTAGE; ++i) mbar_init(&bar_full[i], 1);
     mbar_init(&bar_mma, 1);
     mbar_init(&bar_ofull[0], 1);
     mbar_init(&bar_ofull[1], 1);
@@ -528,38 +587,51 @@ __global__ void __launch_bounds__(256, 1) kda_state_tc(
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = tmem_base;
+  auto set_col = [](int n) { return 256 * (n & 1); };
   if (state_grp) {
     int loads_issued = 0, loads_done = 0;
-    uint32_t full_phase[2] = {0u, 0u}, mma_phase = 0u;
+    uint32_t full_phase[B_NSTAGE] = {}, mma_phase = 0u;
     bool ok = true;
-    auto load_card = [&](int n) {  // by thread 0
-      uint8_t *dst = sm + (n & 1) * B_STAGE_BYTES;
+    const bool loader = (tid == 32);  // issues the card copies, off the MMA issuer's path
+    auto stage_of = [](int n) { return n % B_NSTAGE; };
+    // card n -> stage n % 3: [Phi'^T | Q'^T] and e^{G_C}
+    auto load_card = [&](int n) {
+      const int st = stage_of(n);
+      uint8_t *dst = sm + st * B_STAGE_BYTES;
       const uint8_t *src = card_of(n);
-      mbar_arrive_expect_tx(&bar_full[n & 1], CARD_STAGE);
-      for (int o = 0; o < CARD_STAGE; o += 16384) {
-        const int bytes = min(16384, CARD_STAGE - o);
-        bulk_g2s(dst + o, src + o, bytes, &bar_full[n & 1]);
-      }
+      mbar_arrive_expect_tx(&bar_full[st], B_STAGE_TX);
+      for (int o = 0; o < CARD_BCT; o += 16384) bulk_g2s(dst + o, src + o, 16384, &bar_full[st]);
+      bulk_g2s(dst + CARD_BCT, src + CARD_D, 512, &bar_full[st]);
       ++loads_issued;
     };
     auto wait_full = [&](int n) -> bool {
-      const bool r = mbar_wait(&bar_full[n & 1], full_phase[n & 1]);
-      full_phase[n & 1] ^= 1u;
+      const int st = stage_of(n);
+      const bool r = mbar_wait(&bar_full[st], full_phase[st]);
+      full_phase[st] ^= 1u;
       if (r) ++loads_done;
       return r;
     };
-    // Tensor memory [0,128) <- Diag(e^{G_C}) S + B_c of chunk n (fp32) and the bf16
-    // operand S^T (row j) in shared memory, from one 32-column piece `x` of row j.
-    auto stage_piece = [&](int n, int q4, const float *x) {
-      const uint8_t *st = sm + (n & 1) * B_STAGE_BYTES;
-      const float *dv = reinterpret_cast<const float *>(st + CARD_D);
+    // this thread's 64 columns of B_c^T row j of chunk n, straight from the card in global
+    // memory (lane-interleaved: a warp reads 512 contiguous bytes per 8-column chunk)
+    uint4 bcr[8];
+    auto fetch_bc = [&](int n) {
+      if (!with_bc || n >= nchunks) return;
+      const uint8_t *src = card_of(n) + CARD_BCT;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8)
+        bcr[c8] = *reinterpret_cast<const uint4 *>(src + ((8 * half + c8) * 128 + j) * 16);
+    };
+    // Pre-load for chunk n: tensor memory <- Diag(e^{G_C}) S + B_c (fp32) and the bf16
+    // operand S^T (row j) in shared memory, from the 32 key columns 64*half + 32*qq.
+    auto stage_piece = [&](int n, int qq, const float *x) {
+      const float *dv =
+          reinterpret_cast<const float *>(sm + stage_of(n) * B_STAGE_BYTES + CARD_BCT);
+      const int q4 = 2 * half + qq;
       float init[32];
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         float bc[8];
-        if (with_bc)
-          unpack8(*reinterpret_cast<const uint4 *>(st + CARD_BCT + ((q4 * 4 + ch) * 128 + j) * 16),
-                  bc);
+        if (with_bc) unpack8(bcr[qq * 4 + ch], bc);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const int c = q4 * 32 + ch * 8 + u;
@@ -568,7 +640,7 @@ __global__ void __launch_bounds__(256, 1) kda_state_tc(
         *reinterpret_cast<uint4 *>(sm + B_SA + sw128_chunk(j, q4 * 4 + ch, 128)) =
             pack8(x + ch * 8);
       }
-      tmem_st32(tmem_addr(tb, quad * 32, 32 * q4), init);
+      tmem_st32(tmem_addr(tb, quad * 32, set_col(n) + 32 * q4), init);
     };
     auto finish_stage = [&]() {
       tmem_wait_st();
@@ -576,45 +648,38 @@ __global__ void __launch_bounds__(256, 1) kda_state_tc(
       tc_fence_before();
     };
     auto issue_mma = [&](int n) -> bool {  // by thread 0
-      // the output buffer of chunk n was last used by chunk n - 2
-      if (with_o && n >= 2 && !mbar_wait(&bar_ofree[n & 1], ((n >> 1) - 1) & 1)) return false;
+      // the output block of set n % 2 is read and zeroed (prologue, then chunk n - 2)
+      if (with_o && !mbar_wait(&bar_ofree[n & 1], (n >> 1) & 1)) return false;
       tc_fence_after();
-      const uint32_t stg = sb + (n & 1) * B_STAGE_BYTES;
-      const uint32_t idS = idesc_bf16(128, 128, 0, 1), idO = idesc_bf16(128, 64, 0, 1);
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = desc_kmajor(sb + B_SA, 128, kk);
-        const uint64_t bS = sdesc_sw128(stg + CARD_PHIQ + kk * 2048, 128 * 128, 1024);
-        mma_bf16(tb + 0, ad, bS, idS, 1u);
-        if (with_o) {
-          const uint64_t bO =
-              sdesc_sw128(stg + CARD_PHIQ + 2 * 16384 + kk * 2048, 128 * 128, 1024);
-          mma_bf16(tb + 128 + 64 * (n & 1), ad, bO, idO, kk > 0);
-        }
-      }
+      const uint32_t stg = sb + stage_of(n) * B_STAGE_BYTES;
+      const uint32_t id = idesc_bf16(128, with_o ? 192 : 128, 0, 1);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16(tb + set_col(n), desc_kmajor(sb + B_SA, 128, kk),
+                 sdesc_sw128(stg + CARD_PHIQ + kk * 2048, 128 * 128, 1024), id, 1u);
       mma_commit(&bar_mma);
       if (with_o) mma_commit(&bar_ofull[n & 1]);
       return true;
     };
 
-    if (tid == 0) {
-      load_card(0);
-      if (nchunks > 1) load_card(1);
-    }
+    if (loader)
+      for (int n = 0; n < B_NSTAGE && n < nchunks; ++n) load_card(n);
+    fetch_bc(0);
     // chunk 0: entry state from global memory
     if (!wait_full(0)) ok = false;
     if (ok) {
-#pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
         float x[32];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) x[u] = entry(q4 * 32 + u);
-        stage_piece(0, q4, x);
+        for (int u = 0; u < 32; ++u) x[u] = entry(64 * half + 32 * qq + u);
+        stage_piece(0, qq, x);
       }
       finish_stage();
     }
-    named_bar(1, 128);
+    named_bar(1, 256);
     tc_fence_after();
     if (tid == 0 && ok && !issue_mma(0)) s_fail = 1;
+    fetch_bc(1);
 
     for (int n = 0; n < nchunks && ok; ++n) {
       if (!mbar_wait(&bar_mma, mma_phase)) {
@@ -623,56 +688,78 @@ __global__ void __launch_bounds__(256, 1) kda_state_tc(
       }
       mma_phase ^= 1u;
       tc_fence_after();
-      // the card of chunk n is consumed: refill its stage with chunk n + 2
-      if (tid == 0 && n + 2 < nchunks) load_card(n + 2);
+      // the card of chunk n is consumed: refill its stage with chunk n + 3
+      if (loader && n + B_NSTAGE < nchunks) load_card(n + B_NSTAGE);
       const bool last = (n + 1 == nchunks);
       if (!last && !wait_full(n + 1)) {
         ok = false;
         break;
       }
       // state after chunk n: stage it for chunk n + 1, or write it out
-#pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float x[32];
-        tmem_ld32(tmem_addr(tb, quad * 32, 32 * q4), x);
-        tmem_wait_ld();
-        if (last) {
+      float x0[32], x1[32];
+      tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 64 * half), x0);
+      tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 64 * half + 32), x1);
+      tmem_wait_ld();
+      if (last) {
 #pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            float *p = result_ptr(q4 * 32 + u);
-            if (p) *p = x[u];
-          }
-        } else {
-          stage_piece(n + 1, q4, x);
+        for (int u = 0; u < 32; ++u) {
+          float *p0 = result_ptr(64 * half + u), *p1 = result_ptr(64 * half + 32 + u);
+          if (p0) *p0 = x0[u];
+          if (p1) *p1 = x1[u];
         }
-      }
-      if (!last) {
+      } else {
+        stage_piece(n + 1, 0, x0);
+        stage_piece(n + 1, 1, x1);
         finish_stage();
-        named_bar(1, 128);
+        named_bar(1, 256);
         tc_fence_after();
         if (tid == 0 && !issue_mma(n + 1)) s_fail = 1;
+        fetch_bc(n + 2);
       }
     }
     if (!ok || s_fail) {
       if (lane == 0) set_err(kErrTimeout);
       // let copies still in flight land (bounded) before shared memory is released
-      if (tid == 0)
+      if (loader)
         for (int n = loads_done; n < loads_issued; ++n) {
-          if (!mbar_wait(&bar_full[n & 1], full_phase[n & 1], 100000000ull)) break;
-          full_phase[n & 1] ^= 1u;
+          const int st = stage_of(n);
+          if (!mbar_wait(&bar_full[st], full_phase[st], 100000000ull)) break;
+          full_phase[st] ^= 1u;
         }
     }
   } else if (with_o) {
-    // output group: o = scale * g * (Q' S + O_intra) for chunk n
+    // output group: o = scale * g * (Q' S + O_intra) for chunk n. Each warp owns 32 value
+    // channels (its lane quadrant); it transposes each 32 x 32 (channel x token) block
+    // through shared memory so that gate loads and output stores are 16-byte vectors.
+    float *ot = reinterpret_cast<float *>(sm + B_OT) + quad * 32 * 33;
+    const int jc = quad * 32;  // first channel of this warp
+    float zero[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) zero[u] = 0.f;
+    // both output blocks start at zero
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) tmem_st32(tmem_addr(tb, quad * 32, 256 * b + 128 + 32 * hf), zero);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&bar_ofree[0]);
+    mbar_arrive(&bar_ofree[1]);
     uint32_t ofull_phase[2] = {0u, 0u};
     for (int n = 0; n < nchunks; ++n) {
       const int64_t t0 = ts + (int64_t)n * C;
       const int len = (int)min((int64_t)C, ls - (int64_t)n * C);
-      float gv[C];
+      uint4 gq[2][4];  // gate of token (hf * 32 + lane), channels jc + 8i .. +8
 #pragma unroll
-      for (int r = 0; r < C; ++r)
-        gv[r] = (gate && r < len) ? __bfloat162float(gate[((size_t)(t0 + r) * H + h) * DD + j])
-                                  : 1.f;
+      for (int hf = 0; hf < 2; ++hf) {
+        const int r = hf * 32 + lane;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          gq[hf][i] = (gate && r < len)
+                          ? *reinterpret_cast<const uint4 *>(
+                                gate + ((size_t)(t0 + r) * H + h) * DD + jc + 8 * i)
+                          : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+      }
       uint4 oi[8];
       const uint8_t *card = card_of(n);
 #pragma unroll
@@ -684,31 +771,45 @@ __global__ void __launch_bounds__(256, 1) kda_state_tc(
       }
       ofull_phase[n & 1] ^= 1u;
       tc_fence_after();
+      float t[2][32];
+      tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 128), t[0]);
+      tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 160), t[1]);
+      tmem_wait_ld();
+      // the block is read: zero it for chunk n + 2 and hand it back to the MMA issuer
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+        tmem_st32(tmem_addr(tb, quad * 32, set_col(n) + 128 + 32 * hf), zero);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar_ofree[n & 1]);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        float t32[32];
-        tmem_ld32(tmem_addr(tb, quad * 32, 128 + 64 * (n & 1) + 32 * hf), t32);
-        tmem_wait_ld();
+        __syncwarp();
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           float o8[8];
           unpack8(oi[hf * 4 + ch], o8);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int r = hf * 32 + ch * 8 + u;
-            if (r < len)
-              out[((size_t)(t0 + r) * H + h) * DD + j] =
-                  __float2bfloat16_rn(scale * gv[r] * (t32[ch * 8 + u] + o8[u]));
+          for (int u = 0; u < 8; ++u) ot[lane * 33 + ch * 8 + u] = t[hf][ch * 8 + u] + o8[u];
+        }
+        __syncwarp();
+        const int r = hf * 32 + lane;  // this thread's token now
+        if (r < len) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float g8[8], e[8];
+            unpack8(gq[hf][i], g8);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) e[u] = scale * g8[u] * ot[(8 * i + u) * 33 + lane];
+            *reinterpret_cast<uint4 *>(out + ((size_t)(t0 + r) * H + h) * DD + jc + 8 * i) = pack8(e);
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&bar_ofree[n & 1]);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tb, 256);
+  if (warp == 0) tmem_dealloc(tb, 512);
 }
 
 }  // namespace
@@ -792,7 +893,7 @@ cudaError_t launch_state_tc(int mode, const void *gate, void *out, const float *
       cudaFuncSetAttribute(kda_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, B_DYN);
   if (e != cudaSuccess) return e;
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
-  kda_state_tc<<<dim3(n_seq * H, mode == 0 ? 1 : 2), 256, B_DYN, st>>>(
+  kda_state_tc<<<dim3(n_seq * H, mode == 0 ? 1 : 2), 384, B_DYN, st>>>(
       mode, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final, X_out, Z_out, cu,
       n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.cards);
   return cudaGetLastError();

@@ -157,6 +157,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
          | ((uint32_t)(M >> 4) << 24);     // M / 16
 }
 
+// Instruction-descriptor bit that negates the A operand (kind::f16).
+constexpr uint32_t kNegateA = 1u << 13;
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled tile (sm_100 family
 // layout: start>>4 [0,14), LBO>>4 [16,30), SBO>>4 [32,46), version 1 at 46,
 // swizzle mode 2 = 128B at [61,64)).
