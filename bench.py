@@ -39,6 +39,31 @@ BYTES_PER_TOKEN_HEAD = 5 * 128 * 2 + 2 + 128 * 2
 STATE_BYTES = 128 * 128 * 4
 
 
+PROFILE_OF = {"kda_card_tc": "kda_card_tc_prefill.md", "kda_state_tc": "kda_state_tc_prefill.md",
+              "kda_decode_kernel": "kda_decode_kernel_decode.md",
+              "kda_scan_kernel": "kda_scan_kernel_scan.md"}
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary of `kernel`, or None when
+    there is none or the kernel's source file changed since the counters were taken."""
+    import hashlib
+    import re
+    name = PROFILE_OF.get(kernel)
+    if name is None:
+        return None
+    try:
+        txt = open(os.path.join(ROOT, "profiles", name)).read()
+        mh = re.search(r"source_sha256: ([0-9a-f]+) \(([^)]+)\)", txt)
+        mt = re.search(r"traffic_bytes_per_launch: (\d+)", txt)
+        if not mh or not mt:
+            return None
+        cur = hashlib.sha256(open(os.path.join(ROOT, mh.group(2)), "rb").read()).hexdigest()
+        return int(mt.group(1)) if cur[:16] == mh.group(1) else None
+    except OSError:
+        return None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -298,7 +323,7 @@ def run_gpu(args, rank, world, local):
     achieved = alg_bytes[dom] / (per_launch[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": None, "peak_source": pk["source"],
+                "traffic": profiled_traffic(names[dom]), "peak_source": pk["source"],
                 "launch_ms": dict(zip(names, [round(t, 4) for t in per_launch]))}
     if tc:
         # tensor-core work per (chunk, head): card GEMMs 1-4 and the state-pass MMA group
@@ -362,6 +387,7 @@ def run_gpu(args, rank, world, local):
     if rank == 0 and not args.skip_extra:
         line["decode"] = bench_decode(dev, pk, stream)
         line["segment_scan"] = bench_segment_scan(dev, pk, stream)
+        line["scan_combine"] = bench_scan(dev, pk, stream)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
@@ -411,7 +437,8 @@ def bench_decode(dev, pk, stream, steps=64):
             "kernel_us": round(kern_ms * 1e3, 2),
             "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": round(gbs, 1),
                          "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(gbs / pk["hbm_gbs"], 4),
+                         "traffic": profiled_traffic("kda_decode_kernel"),
                          "bytes_per_launch": bytes_step},
             "gpu_launches": steps}
 
@@ -470,6 +497,43 @@ def bench_segment_scan(dev, pk, stream, reps=2):
             "gpu_launches": 7 * reps}
 
 
+def bench_scan(dev, pk, stream, reps=20):
+    """kda_scan_combine alone on long-context-sized summaries (8 segments x 16 heads)."""
+    import linear_attention_05_gb300 as kda
+
+    n_seg, H, d = 8, 16, 128
+    g = torch.Generator(device=dev).manual_seed(77)
+    X = (torch.randn((n_seg, H, d, d), generator=g, device=dev) / d ** 0.5).contiguous()
+    Z = torch.randn((n_seg, H, d, d), generator=g, device=dev).contiguous()
+    E = torch.empty_like(Z)
+    Sf = torch.empty((H, d, d), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        kda.kda_scan_combine(X, Z, None, E, Sf, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        kda.kda_scan_combine(X, Z, None, E, Sf, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = (2 * n_seg + n_seg + 1) * H * d * d * 4
+    return {"workload": "scan combine, 8 segments x 16 heads, dk=dv=128, fp32", "ms": round(ms, 4),
+            "value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "frac": round(nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+            "traffic": profiled_traffic("kda_scan_kernel"), "gpu_launches": reps}
+
+
+def run_part(args, local):
+    """One part of the path on its own (used for profiling a single kernel)."""
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+    fn = {"decode": bench_decode, "segscan": bench_segment_scan, "scan": bench_scan}[args.only]
+    print(json.dumps({"part": args.only, **fn(dev, pk, stream)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -480,12 +544,17 @@ def main():
                     help="reference arm: tokens per sequence timed per step")
     ap.add_argument("--skip-extra", action="store_true", help="prefill line only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--only", default=None, choices=["decode", "segscan", "scan"],
+                    help="run one part of the path alone and print its numbers (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.only:
+        if rank == 0:
+            run_part(args, local)
     else:
         run_gpu(args, rank, world, local)
     if world > 1:
