@@ -272,3 +272,28 @@ def test_segment_summary_vs_oracle(dtype):
     E, Sf = B.scan_combine(X, Z, S_init)
     rE, rSf = oracle.scan_combine(np32(X), np32(Z), np32(S_init))
     assert rel_err(np32(E), rE) <= 1e-5 and rel_err(np32(Sf), rSf) <= 1e-5
+
+
+def test_context_parallel_driver_one_rank():
+    """cp.context_parallel_forward with the device library on a one-rank NCCL group
+    equals the monolithic chunked pass from the same initial state."""
+    import socket
+
+    import torch.distributed as dist
+
+    from linear_attention_05_gb300 import cp
+    with socket.socket() as sck:
+        sck.bind(("127.0.0.1", 0))
+        port = sck.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        x, _ = make_tokens([300], 4, 128, 128, torch.bfloat16, seed=60)
+        S0 = inputs.state(1, 4, 128, 128, seed=61, device=DEV)
+        out, s_mine, s_last = cp.context_parallel_forward(
+            x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], S0[0].contiguous())
+        ref_o, ref_s = gpu_chunk(x, [0, 300], S0=S0)
+        assert rel_err(np32(out), np32(ref_o)) <= TOL[torch.bfloat16]
+        assert rel_err(np32(s_mine), np32(ref_s[0])) <= TOL[torch.bfloat16]
+        assert rel_err(np32(s_last), np32(ref_s[0])) <= TOL[torch.bfloat16]
+    finally:
+        dist.destroy_process_group()
