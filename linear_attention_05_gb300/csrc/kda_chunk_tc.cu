@@ -676,43 +676,47 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
       }
       finish_stage();
     }
-    named_bar(1, 256);
+    // all state threads agree on `ok`, so none is left waiting at a later barrier
+    ok = named_bar_and(1, 256, ok);
     tc_fence_after();
     if (tid == 0 && ok && !issue_mma(0)) s_fail = 1;
     fetch_bc(1);
 
     for (int n = 0; n < nchunks && ok; ++n) {
-      if (!mbar_wait(&bar_mma, mma_phase)) {
-        ok = false;
-        break;
-      }
+      // a timed-out wait only clears `good`; the group votes on it at the barrier below
+      bool good = mbar_wait(&bar_mma, mma_phase);
       mma_phase ^= 1u;
       tc_fence_after();
       // the card of chunk n is consumed: refill its stage with chunk n + 3
-      if (loader && n + B_NSTAGE < nchunks) load_card(n + B_NSTAGE);
+      if (good && loader && n + B_NSTAGE < nchunks) load_card(n + B_NSTAGE);
       const bool last = (n + 1 == nchunks);
-      if (!last && !wait_full(n + 1)) {
-        ok = false;
-        break;
-      }
+      if (good && !last) good = wait_full(n + 1);
       // state after chunk n: stage it for chunk n + 1, or write it out
       float x0[32], x1[32];
-      tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 64 * half), x0);
-      tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 64 * half + 32), x1);
-      tmem_wait_ld();
+      if (good) {
+        tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 64 * half), x0);
+        tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 64 * half + 32), x1);
+        tmem_wait_ld();
+      }
       if (last) {
+        if (good)
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          float *p0 = result_ptr(64 * half + u), *p1 = result_ptr(64 * half + 32 + u);
-          if (p0) *p0 = x0[u];
-          if (p1) *p1 = x1[u];
-        }
+          for (int u = 0; u < 32; ++u) {
+            float *p0 = result_ptr(64 * half + u), *p1 = result_ptr(64 * half + 32 + u);
+            if (p0) *p0 = x0[u];
+            if (p1) *p1 = x1[u];
+          }
+        else
+          ok = false;
       } else {
-        stage_piece(n + 1, 0, x0);
-        stage_piece(n + 1, 1, x1);
-        finish_stage();
-        named_bar(1, 256);
+        if (good) {
+          stage_piece(n + 1, 0, x0);
+          stage_piece(n + 1, 1, x1);
+          finish_stage();
+        }
+        ok = named_bar_and(1, 256, good);
         tc_fence_after();
+        if (!ok) break;
         if (tid == 0 && !issue_mma(n + 1)) s_fail = 1;
         fetch_bc(n + 2);
       }

@@ -110,5 +110,6 @@ kda_status api_fail(kda_status st, const char *fmt, ...);
 // Read-and-clear of each translation unit's device error word.
 cudaError_t chunk_take_error(unsigned *bits);
 cudaError_t decode_take_error(unsigned *bits);
+cudaError_t scan_take_error(unsigned *bits);
 
 }  // namespace kda
