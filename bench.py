@@ -388,6 +388,7 @@ def run_gpu(args, rank, world, local):
         line["decode"] = bench_decode(dev, pk, stream)
         line["segment_scan"] = bench_segment_scan(dev, pk, stream)
         line["scan_combine"] = bench_scan(dev, pk, stream)
+        line["prefill_checkpoints"] = bench_checkpoints(dev, pk, stream)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
@@ -497,6 +498,50 @@ def bench_segment_scan(dev, pk, stream, reps=2):
             "gpu_launches": 7 * reps}
 
 
+def bench_checkpoints(dev, pk, stream, reps=20, every=1024):
+    """The prefill workload with prefix-cache checkpoints every 1024 tokens
+    (kda_chunk_fwd_checkpoints), timed beside the same call without them."""
+    import linear_attention_05_gb300 as kda
+    from linear_attention_05_gb300 import inputs
+
+    w = inputs.WORKLOADS["prefill"]
+    x = inputs.make(w, device=dev)
+    T, H, d, n_seq = w.T_total, w.H, w.dk, len(w.lengths)
+    per = w.lengths[0] // every
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((n_seq, H, d, d), dtype=torch.float32, device=dev)
+    ck = torch.empty((n_seq, per, H, d, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(kda.kda_chunk_fwd_workspace_size(T, n_seq, H, d, d), dtype=torch.uint8,
+                     device=dev)
+
+    def plain():
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], out,
+                          x["S0"], fs, None, n_seq, workspace=ws, stream=stream)
+
+    def with_ckpt():
+        kda.kda_chunk_fwd_checkpoints(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                      x["gate"], out, x["S0"], fs, ck, every, None, n_seq,
+                                      workspace=ws, stream=stream)
+
+    ms = {}
+    for name, fn in (("plain", plain), ("ckpt", with_ckpt)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms[name] = e0.elapsed_time(e1) / reps
+    return {"workload": "prefill B=4 T=4096 H=16 dk=dv=128 bf16, a checkpoint every 1024 "
+                        "tokens (4 per sequence)",
+            "value": round(T / (ms["ckpt"] * 1e-3) / 1e6, 3), "unit": "Mtok/s",
+            "ms": round(ms["ckpt"], 4), "ms_without": round(ms["plain"], 4),
+            "checkpoint_bytes": ck.numel() * 4, "gpu_launches": 3 * reps}
+
+
 def bench_scan(dev, pk, stream, reps=20):
     """kda_scan_combine alone on long-context-sized summaries (8 segments x 16 heads)."""
     import linear_attention_05_gb300 as kda
@@ -530,7 +575,8 @@ def run_part(args, local):
     torch.cuda.set_device(dev)
     pk = peaks()
     stream = torch.cuda.current_stream()
-    fn = {"decode": bench_decode, "segscan": bench_segment_scan, "scan": bench_scan}[args.only]
+    fn = {"decode": bench_decode, "segscan": bench_segment_scan, "scan": bench_scan,
+          "ckpt": bench_checkpoints}[args.only]
     print(json.dumps({"part": args.only, **fn(dev, pk, stream)}), flush=True)
 
 
@@ -544,7 +590,7 @@ def main():
                     help="reference arm: tokens per sequence timed per step")
     ap.add_argument("--skip-extra", action="store_true", help="prefill line only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", default=None, choices=["decode", "segscan", "scan"],
+    ap.add_argument("--only", default=None, choices=["decode", "segscan", "scan", "ckpt"],
                     help="run one part of the path alone and print its numbers (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -105,6 +105,37 @@ size_t kda_chunk_fwd_workspace_size(int64_t T_total, int n_seq, int H, int dk,
                                     int dv, int chunk, kda_dtype dtype);
 
 /*
+ * kda_chunk_fwd that also saves the state at fixed token boundaries, for a
+ * prefix cache that resumes a sequence from its longest cached prefix.
+ * Source: K3 explainer section 14 "Prefix Cache": a reused prefix must restore
+ * the fixed-size KDA state at the same boundary as the attention KV pages, so
+ * state checkpoints are kept at reusable boundaries.
+ *
+ * Arguments and results of kda_chunk_fwd (same workspace size), plus
+ *  checkpoints         : [n_seq, checkpoints_per_seq, H, dk, dv] fp32. Slot
+ *                        (s, i) receives the state of sequence s after its
+ *                        first (i + 1) * checkpoint_every tokens (the state
+ *                        the sequence's token (i + 1) * checkpoint_every
+ *                        starts from), for every i < checkpoints_per_seq with
+ *                        (i + 1) * checkpoint_every <= len_s. Other slots are
+ *                        not written. A boundary at the end of a sequence
+ *                        equals its final state.
+ *  checkpoint_every    : > 0, a multiple of chunk (64)
+ *  checkpoints_per_seq : >= 0; 0 writes no checkpoint (then checkpoints may
+ *                        be NULL)
+ * Checkpoints are the kernel's fp32 running state, bitwise equal to the
+ * final_state a kda_chunk_fwd call over the prefix returns.
+ */
+kda_status kda_chunk_fwd_checkpoints(
+    const void *q, const void *k, const void *v, const void *log_alpha,
+    const void *beta, const void *gate, void *out, const float *initial_state,
+    float *final_state, float *checkpoints, int64_t checkpoint_every,
+    int checkpoints_per_seq, const int32_t *cu_seqlens, int n_seq,
+    int64_t T_total, int H, int dk, int dv, int chunk, float scale,
+    unsigned flags, kda_dtype dtype, void *workspace, size_t workspace_bytes,
+    kda_stream_t stream);
+
+/*
  * kda_chunk_fwd without a workspace argument, for callers that cannot
  * allocate device memory where they run the mixer: host frameworks that
  * reserve the device heap up front and give a kernel only its inputs and

@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH):
             "kda_last_error_string": ([], ctypes.c_char_p),
             "kda_chunk_fwd": ([P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, P, SZ, P], I),
             "kda_chunk_fwd_workspace_size": ([I64, I, I, I, I, I, I], SZ),
+            "kda_chunk_fwd_checkpoints": ([P, P, P, P, P, P, P, P, P, P, I64, I, P, I, I64, I, I,
+                                           I, I, F, U, I, P, SZ, P], I),
             "kda_chunk_fwd_noalloc": ([P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, P], I),
             "kda_decode_step": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, U, I, P], I),
             "kda_segment_summary": ([P, P, P, P, P, I, I64, I, I, I, I, U, I, P, P, P, SZ, P], I),
@@ -174,6 +176,35 @@ def kda_chunk_fwd(q, k, v, log_alpha, beta, gate, out, initial_state, final_stat
                            wsb, _stream(stream))
     _check(lib, st)
     return out, final_state
+
+
+def kda_chunk_fwd_checkpoints(q, k, v, log_alpha, beta, gate, out, initial_state, final_state,
+                              checkpoints, checkpoint_every, cu_seqlens, n_seq, scale=1.0,
+                              flags=KDA_QK_L2NORM, workspace=None, stream=None, chunk=CHUNK):
+    """kda_chunk_fwd that also writes the state every ``checkpoint_every`` tokens into
+    ``checkpoints`` [n_seq, per_seq, H, dk, dv] fp32 (or None for no checkpoints)."""
+    lib = load()
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(k)
+    _f32_or_none(initial_state, "initial_state")
+    _f32_or_none(final_state, "final_state")
+    _f32_or_none(checkpoints, "checkpoints")
+    per_seq = 0 if checkpoints is None else checkpoints.shape[1]
+    if checkpoints is not None and tuple(checkpoints.shape) != (n_seq, per_seq, H, dk, dv):
+        raise ValueError(f"checkpoints must be [n_seq, per_seq, H, dk, dv], got "
+                         f"{tuple(checkpoints.shape)}")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    need = lib.kda_chunk_fwd_workspace_size(T, n_seq, H, dk, dv, chunk, dt)
+    ws, wsb = _workspace(need, k.device, workspace)
+    st = lib.kda_chunk_fwd_checkpoints(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(gate), _ptr(out),
+        _ptr(initial_state), _ptr(final_state), _ptr(checkpoints), int(checkpoint_every),
+        per_seq, _ptr(cu_seqlens), n_seq, T, H, dk, dv, chunk, float(scale), int(flags), dt,
+        _ptr(ws), wsb, _stream(stream))
+    _check(lib, st)
+    return out, final_state, checkpoints
 
 
 def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, gate, out, initial_state, final_state,
@@ -292,6 +323,36 @@ def chunk_fwd(q, k, v, log_alpha, beta, gate=None, initial_state=None, cu_seqlen
                   scale=scale, flags=KDA_QK_L2NORM if l2norm else 0, workspace=workspace,
                   stream=stream)
     return out, fs
+
+
+def chunk_fwd_checkpoints(q, k, v, log_alpha, beta, gate=None, initial_state=None,
+                          cu_seqlens=None, n_seq=None, checkpoint_every=1024,
+                          checkpoints_per_seq=None, scale=1.0, l2norm=True, workspace=None,
+                          stream=None):
+    """Allocate the outputs and call kda_chunk_fwd_checkpoints.
+
+    Returns (out, final_state, checkpoints); checkpoints[s, i] is the state of sequence s
+    after its first (i + 1) * checkpoint_every tokens. checkpoints_per_seq defaults to the
+    longest sequence's count (reads cu_seqlens on the host)."""
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    if n_seq is None:
+        n_seq = (cu_seqlens.numel() - 1) if cu_seqlens is not None else 1
+    if checkpoints_per_seq is None:
+        if cu_seqlens is not None:
+            longest = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if n_seq > 0 else 0
+        else:
+            longest = T // n_seq if n_seq > 0 else 0
+        checkpoints_per_seq = longest // checkpoint_every
+    out = torch.empty((T, H, dv), dtype=v.dtype, device=v.device)
+    fs = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=v.device)
+    ck = torch.zeros((n_seq, checkpoints_per_seq, H, dk, dv), dtype=torch.float32,
+                     device=v.device)
+    return kda_chunk_fwd_checkpoints(q, k, v, log_alpha, beta, gate, out, initial_state, fs,
+                                     ck if checkpoints_per_seq > 0 else None, checkpoint_every,
+                                     cu_seqlens, n_seq, scale=scale,
+                                     flags=KDA_QK_L2NORM if l2norm else 0, workspace=workspace,
+                                     stream=stream)[:2] + (ck,)
 
 
 def decode_step(q, k, v, log_alpha, beta, gate, state, state_slot=None, scale=1.0, l2norm=True,

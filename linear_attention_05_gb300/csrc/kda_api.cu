@@ -121,12 +121,16 @@ size_t kda_segment_summary_workspace_size(int64_t T_total, int n_seg, int H, int
   return kda_chunk_fwd_workspace_size(T_total, n_seg, H, dk, dv, chunk, dtype);
 }
 
-kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *log_alpha,
-                         const void *beta, const void *gate, void *out,
-                         const float *initial_state, float *final_state,
-                         const int32_t *cu_seqlens, int n_seq, int64_t T_total, int H, int dk,
-                         int dv, int chunk, float scale, unsigned flags, kda_dtype dtype,
-                         void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+}  // extern "C"
+
+// kda_chunk_fwd and kda_chunk_fwd_checkpoints: one path, the checkpoint output optional.
+static kda_status chunk_fwd_impl(const void *q, const void *k, const void *v,
+                                 const void *log_alpha, const void *beta, const void *gate,
+                                 void *out, const float *initial_state, float *final_state,
+                                 kda::CkptOut ck, const int32_t *cu_seqlens, int n_seq,
+                                 int64_t T_total, int H, int dk, int dv, int chunk, float scale,
+                                 unsigned flags, kda_dtype dtype, void *workspace,
+                                 size_t workspace_bytes, kda_stream_t stream) {
   kda_status st = common_checks(T_total, n_seq, H, dk, dv, chunk, dtype, cu_seqlens);
   if (st != KDA_OK) return st;
   KDA_REQUIRE((flags & ~(unsigned)(KDA_QK_L2NORM | KDA_DEBUG_CHECK)) == 0, KDA_ERR_INVALID_ARG,
@@ -170,13 +174,51 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
   return cuda_status(tr([&] {
                        return tc ? kda::launch_state_tc(0, gate, out, initial_state, final_state,
                                                         nullptr, nullptr, cu_seqlens, n_seq,
-                                                        T_total, H, scale, ws, s)
+                                                        T_total, H, scale, ws, s, ck)
                                  : kda::launch_state_pass(0, gate, out, initial_state,
                                                           final_state, nullptr, nullptr,
                                                           cu_seqlens, n_seq, T_total, H, dk, dv,
-                                                          scale, dtype, ws, s);
+                                                          scale, dtype, ws, s, ck);
                      }),
                      "state pass");
+}
+
+extern "C" {
+
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *log_alpha,
+                         const void *beta, const void *gate, void *out,
+                         const float *initial_state, float *final_state,
+                         const int32_t *cu_seqlens, int n_seq, int64_t T_total, int H, int dk,
+                         int dv, int chunk, float scale, unsigned flags, kda_dtype dtype,
+                         void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+  return chunk_fwd_impl(q, k, v, log_alpha, beta, gate, out, initial_state, final_state,
+                        kda::CkptOut(), cu_seqlens, n_seq, T_total, H, dk, dv, chunk, scale,
+                        flags, dtype, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_chunk_fwd_checkpoints(
+    const void *q, const void *k, const void *v, const void *log_alpha, const void *beta,
+    const void *gate, void *out, const float *initial_state, float *final_state,
+    float *checkpoints, int64_t checkpoint_every, int checkpoints_per_seq,
+    const int32_t *cu_seqlens, int n_seq, int64_t T_total, int H, int dk, int dv, int chunk,
+    float scale, unsigned flags, kda_dtype dtype, void *workspace, size_t workspace_bytes,
+    kda_stream_t stream) {
+  KDA_REQUIRE(checkpoint_every > 0 && chunk > 0 && checkpoint_every % chunk == 0 &&
+                  checkpoint_every / chunk <= (int64_t)INT32_MAX,
+              KDA_ERR_INVALID_ARG, "checkpoint_every=%lld: a positive multiple of chunk=%d",
+              (long long)checkpoint_every, chunk);
+  KDA_REQUIRE(checkpoints_per_seq >= 0, KDA_ERR_INVALID_ARG, "checkpoints_per_seq=%d < 0",
+              checkpoints_per_seq);
+  KDA_CHECK_PTR(checkpoints, checkpoints_per_seq > 0);
+  kda::CkptOut ck;
+  if (checkpoints_per_seq > 0) {
+    ck.ptr = checkpoints;
+    ck.every_chunks = (int)(checkpoint_every / chunk);
+    ck.per_seq = checkpoints_per_seq;
+  }
+  return chunk_fwd_impl(q, k, v, log_alpha, beta, gate, out, initial_state, final_state, ck,
+                        cu_seqlens, n_seq, T_total, H, dk, dv, chunk, scale, flags, dtype,
+                        workspace, workspace_bytes, stream);
 }
 
 kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *log_alpha,

@@ -287,7 +287,8 @@ __global__ void __launch_bounds__(256) kda_state_simt(
     float *__restrict__ Z_out, const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len,
     int H, float scale, const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
     const float *__restrict__ Wg, const float *__restrict__ Ug, const float *__restrict__ Qg,
-    const float *__restrict__ Kdg, const float *__restrict__ Pg, const float *__restrict__ Dg) {
+    const float *__restrict__ Kdg, const float *__restrict__ Pg, const float *__restrict__ Dg,
+    CkptOut ck) {
   constexpr int LK = DK + 1, LS = BV + 1, LP = C + 1;
   extern __shared__ float smem[];
   float *sS = smem;            // [DK][LS]
@@ -391,6 +392,10 @@ __global__ void __launch_bounds__(256) kda_state_simt(
     __syncthreads();
 #pragma unroll
     for (int m = 0; m < DK / 8; ++m) sS[(rt + 8 * m) * LS + jt] = ns[m];
+    if (mode == 0)
+      if (float *cp = ckpt_after_chunk(ck, s, jc, ls, H, h, DK, DV))
+#pragma unroll
+        for (int m = 0; m < DK / 8; ++m) cp[(size_t)(rt + 8 * m) * DV + j0 + jt] = ns[m];
     __syncthreads();
   }
 
@@ -438,7 +443,7 @@ template <int DK, int DV, typename Tout>
 cudaError_t launch_state_t(int mode, const void *gate, void *out, const float *S0,
                            float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                            int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
-                           cudaStream_t st) {
+                           cudaStream_t st, CkptOut ck) {
   auto kern = kda_state_simt<DK, DV, Tout>;
   constexpr size_t sm = state_smem<DK>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
@@ -448,7 +453,7 @@ cudaError_t launch_state_t(int mode, const void *gate, void *out, const float *S
   dim3 grid(n_seq * H, ncols / BV);
   kern<<<grid, 256, sm, st>>>(mode, (const Tout *)gate, (Tout *)out, S0, S_final, X_out, Z_out,
                               cu, n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.W,
-                              ws.U, ws.Q, ws.Kd, ws.P, ws.D);
+                              ws.U, ws.Q, ws.Kd, ws.P, ws.D, ck);
   return cudaGetLastError();
 }
 
@@ -521,15 +526,15 @@ cudaError_t launch_prep(const void *q, const void *k, const void *v, const void 
 cudaError_t launch_state_pass(int mode, const void *gate, void *out, const float *S0,
                               float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                               int n_seq, int64_t T_total, int H, int dk, int dv, float scale,
-                              kda_dtype dt, const ChunkWs &ws, cudaStream_t st) {
+                              kda_dtype dt, const ChunkWs &ws, cudaStream_t st, CkptOut ck) {
   if (dt == KDA_DTYPE_BF16) {
     KDA_DISPATCH_DKDV(dk, dv, return launch_state_t<DK, DV, __nv_bfloat16>(
                                   mode, gate, out, S0, S_final, X_out, Z_out, cu, n_seq,
-                                  T_total, H, scale, ws, st));
+                                  T_total, H, scale, ws, st, ck));
   } else {
     KDA_DISPATCH_DKDV(dk, dv, return launch_state_t<DK, DV, float>(
                                   mode, gate, out, S0, S_final, X_out, Z_out, cu, n_seq,
-                                  T_total, H, scale, ws, st));
+                                  T_total, H, scale, ws, st, ck));
   }
 }
 

@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
     const float *__restrict__ S0, float *__restrict__ S_final, float *__restrict__ X_out,
     float *__restrict__ Z_out, const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len,
     int H, float scale, const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
-    const uint8_t *__restrict__ cards) {
+    const uint8_t *__restrict__ cards, CkptOut ck) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[B_NSTAGE], bar_mma, bar_ofull[2], bar_ofree[2];
   __shared__ uint32_t tmem_base;
@@ -559,6 +559,17 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
     if (mode == 0) return S_final ? S_final + (((size_t)s * H + h) * DD + c) * DD + j : nullptr;
     if (xpart) return X_out + (((size_t)s * H + h) * DD + c) * DD + j;
     return Z_out + (((size_t)s * H + h) * DD + c) * DD + j;
+  };
+  // prefix-cache checkpoint after chunk n (mode 0): this thread's 64 rows of column j
+  auto save_ckpt = [&](int n, const float *x0, const float *x1) {
+    if (mode != 0) return;
+    float *cp = ckpt_after_chunk(ck, s, n, ls, H, h, DD, DD);
+    if (cp == nullptr) return;
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      cp[(size_t)(64 * half + u) * DD + j] = x0[u];
+      cp[(size_t)(64 * half + 32 + u) * DD + j] = x1[u];
+    }
   };
   if (nchunks == 0) {
     if (state_grp)
@@ -708,6 +719,7 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
           }
         else
           ok = false;
+        if (good) save_ckpt(n, x0, x1);
       } else {
         if (good) {
           stage_piece(n + 1, 0, x0);
@@ -718,6 +730,7 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
         tc_fence_after();
         if (!ok) break;
         if (tid == 0 && !issue_mma(n + 1)) s_fail = 1;
+        save_ckpt(n, x0, x1);  // off the serial path: the next chunk's MMAs are in flight
         fetch_bc(n + 2);
       }
     }
@@ -892,14 +905,14 @@ cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const vo
 cudaError_t launch_state_tc(int mode, const void *gate, void *out, const float *S0,
                             float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                             int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
-                            cudaStream_t st) {
+                            cudaStream_t st, CkptOut ck) {
   cudaError_t e =
       cudaFuncSetAttribute(kda_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, B_DYN);
   if (e != cudaSuccess) return e;
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
   kda_state_tc<<<dim3(n_seq * H, mode == 0 ? 1 : 2), 384, B_DYN, st>>>(
       mode, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final, X_out, Z_out, cu,
-      n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.cards);
+      n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.cards, ck);
   return cudaGetLastError();
 }
 

@@ -51,6 +51,25 @@ __host__ __device__ constexpr size_t align_up(size_t x, size_t a) {
   return (x + a - 1) / a * a;
 }
 
+// Prefix-cache state checkpoints: [n_seq, per_seq, H, dk, dv] fp32; slot (s, i) holds the
+// state after the first (i + 1) * every_chunks * 64 tokens of sequence s.
+struct CkptOut {
+  float *ptr = nullptr;
+  int every_chunks = 0;  // boundary spacing in chunks (> 0 when ptr is set)
+  int per_seq = 0;       // slots per sequence
+};
+
+// Base of the [dk, dv] checkpoint written after chunk n (0-based) of sequence s, or null when
+// that chunk does not end on a checkpoint boundary inside the sequence.
+__device__ __forceinline__ float *ckpt_after_chunk(const CkptOut &ck, int s, int n, int64_t len,
+                                                   int H, int h, int dk, int dv) {
+  if (ck.ptr == nullptr || (n + 1) % ck.every_chunks != 0) return nullptr;
+  if ((int64_t)(n + 1) * 64 > len) return nullptr;  // boundary past the sequence end
+  const int i = (n + 1) / ck.every_chunks - 1;
+  if (i >= ck.per_seq) return nullptr;
+  return ck.ptr + (((size_t)s * ck.per_seq + i) * H + h) * dk * dv;
+}
+
 }  // namespace kda
 
 // Launchers and error-word accessors defined in the kernel translation units.
@@ -80,7 +99,7 @@ cudaError_t launch_state_pass(int mode, const void *gate, void *out,
                               float *Z_out, const int32_t *cu, int n_seq,
                               int64_t T_total, int H, int dk, int dv,
                               float scale, kda_dtype dt, const ChunkWs &ws,
-                              cudaStream_t st);
+                              cudaStream_t st, CkptOut ck = CkptOut());
 cudaError_t launch_decode(const void *q, const void *k, const void *v,
                           const void *la, const void *beta, const void *gate,
                           void *out, float *state, const int32_t *slot,
@@ -101,7 +120,7 @@ cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const vo
 cudaError_t launch_state_tc(int mode, const void *gate, void *out, const float *S0,
                             float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                             int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
-                            cudaStream_t st);
+                            cudaStream_t st, CkptOut ck = CkptOut());
 cudaError_t tc_take_error(unsigned *bits);
 
 // Sets the calling thread's kda_last_error_string() message; returns `st`.

@@ -69,6 +69,39 @@ def test_chunk_fwd_no_sequences_is_noop(lib):
                  ws=None) == B.KDA_OK
 
 
+def ckpt(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, la=FAKE, beta=FAKE, gate=None, out=FAKE, s0=None, sf=None,
+             cp=FAKE, every=128, per=2, cu=None, n_seq=1, T=256, H=2, dk=64, dv=64, chunk=64,
+             scale=1.0, flags=1, dtype=1, ws=FAKE, wsb=0, stream=None)
+    a.update(kw)
+    return lib.kda_chunk_fwd_checkpoints(
+        a["q"], a["k"], a["v"], a["la"], a["beta"], a["gate"], a["out"], a["s0"], a["sf"],
+        a["cp"], a["every"], a["per"], a["cu"], a["n_seq"], a["T"], a["H"], a["dk"], a["dv"],
+        a["chunk"], a["scale"], a["flags"], a["dtype"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(every=0), B.KDA_ERR_INVALID_ARG),
+    (dict(every=-64), B.KDA_ERR_INVALID_ARG),
+    (dict(every=100), B.KDA_ERR_INVALID_ARG),     # not a multiple of the chunk
+    (dict(every=64 * (2 ** 31)), B.KDA_ERR_INVALID_ARG),  # spacing in chunks overflows int
+    (dict(per=-1), B.KDA_ERR_INVALID_ARG),
+    (dict(cp=None), B.KDA_ERR_INVALID_ARG),       # slots requested, no buffer
+    (dict(cp=ODD), B.KDA_ERR_INVALID_ARG),
+    (dict(dk=96), B.KDA_ERR_UNSUPPORTED),         # then every kda_chunk_fwd check
+    (dict(ws=None), B.KDA_ERR_WORKSPACE),
+])
+def test_chunk_fwd_checkpoints_rejects(lib, kw, status):
+    assert ckpt(lib, **kw) == status
+    assert B.kda_last_error_string() != ""
+
+
+def test_chunk_fwd_checkpoints_no_sequences_is_noop(lib):
+    # zero slots: the buffer may be NULL; no sequences: nothing runs
+    assert ckpt(lib, cp=None, per=0, n_seq=0, T=0, q=None, k=None, v=None, la=None, beta=None,
+                out=None, ws=None) == B.KDA_OK
+
+
 def test_workspace_size(lib):
     s1 = B.kda_chunk_fwd_workspace_size(4096, 1, 16, 128, 128)
     s2 = B.kda_chunk_fwd_workspace_size(8192, 1, 16, 128, 128)
