@@ -13,6 +13,10 @@ Two independent restatements of the same definition live here:
   explicit dk x dk matrix, A_t = (I - b k k^T) Diag(a), in NumPy. Used on tiny
   cases to pin the C code.
 
+``autograd.py`` holds the backward oracle: the recurrence once more in PyTorch
+(fp64, CPU) and its gradients by torch.autograd, pinned to the C forward and to
+finite differences of ``brute.py``.
+
 Definition sources: K3 training overview (zuoshipin.com/article/18261) section
 2 "KDA" (channel-wise forget gate, delta-rule corrective write, full-rank
 output gate) and section 3 "KDA context parallel" (per-segment transition and
