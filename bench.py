@@ -389,6 +389,7 @@ def run_gpu(args, rank, world, local):
         line["segment_scan"] = bench_segment_scan(dev, pk, stream)
         line["scan_combine"] = bench_scan(dev, pk, stream)
         line["prefill_checkpoints"] = bench_checkpoints(dev, pk, stream)
+        line["backward"] = bench_backward(dev, pk, stream)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
@@ -542,6 +543,45 @@ def bench_checkpoints(dev, pk, stream, reps=20, every=1024):
             "checkpoint_bytes": ck.numel() * 4, "gpu_launches": 3 * reps}
 
 
+def bench_backward(dev, pk, stream, reps=5):
+    """kda_chunk_bwd on the prefill workload (bf16 inputs, fp32 arithmetic): gradients of
+    <d_out, o> + <d_final, S_final> for all seven inputs."""
+    import linear_attention_05_gb300 as kda
+    from linear_attention_05_gb300 import inputs
+
+    w = inputs.WORKLOADS["prefill"]
+    x = inputs.make(w, device=dev)
+    T, H, d, n_seq = w.T_total, w.H, w.dk, len(w.lengths)
+    g = torch.Generator(device=dev).manual_seed(99)
+    d_out = torch.randn((T, H, d), generator=g, device=dev).to(torch.bfloat16)
+    d_fin = torch.randn((n_seq, H, d, d), generator=g, device=dev)
+    grads = {n: torch.empty_like(x[n]) for n in ("q", "k", "v", "log_alpha", "beta", "gate")}
+    dS0 = torch.empty((n_seq, H, d, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(kda.kda_chunk_bwd_workspace_size(T, n_seq, H, d, d), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        kda.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], x["S0"],
+                          d_out, d_fin, grads["q"], grads["k"], grads["v"], grads["log_alpha"],
+                          grads["beta"], grads["gate"], dS0, None, n_seq, workspace=ws,
+                          stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    return {"workload": "backward of prefill B=4 T=4096 H=16 dk=dv=128, bf16 in/out, fp32 "
+                        "arithmetic (CUDA cores)",
+            "value": round(T / (ms * 1e-3) / 1e6, 3), "unit": "Mtok/s", "ms": round(ms, 3),
+            "workspace_bytes": ws.numel(), "gpu_launches": 14 * reps}
+
+
 def bench_scan(dev, pk, stream, reps=20):
     """kda_scan_combine alone on long-context-sized summaries (8 segments x 16 heads)."""
     import linear_attention_05_gb300 as kda
@@ -576,7 +616,7 @@ def run_part(args, local):
     pk = peaks()
     stream = torch.cuda.current_stream()
     fn = {"decode": bench_decode, "segscan": bench_segment_scan, "scan": bench_scan,
-          "ckpt": bench_checkpoints}[args.only]
+          "ckpt": bench_checkpoints, "bwd": bench_backward}[args.only]
     print(json.dumps({"part": args.only, **fn(dev, pk, stream)}), flush=True)
 
 
@@ -590,7 +630,7 @@ def main():
                     help="reference arm: tokens per sequence timed per step")
     ap.add_argument("--skip-extra", action="store_true", help="prefill line only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", default=None, choices=["decode", "segscan", "scan", "ckpt"],
+    ap.add_argument("--only", default=None, choices=["decode", "segscan", "scan", "ckpt", "bwd"],
                     help="run one part of the path alone and print its numbers (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:

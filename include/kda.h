@@ -136,6 +136,44 @@ kda_status kda_chunk_fwd_checkpoints(
     kda_stream_t stream);
 
 /*
+ * Chunked backward pass: gradients of
+ *     L = sum_t <d_out_t, o_t> + sum_s <d_final_state_s, final_state_s>
+ * for the forward that kda_chunk_fwd computes with the same arguments.
+ * Source: K3 training overview section 4 "FlashKDA" presents the chunked
+ * kernel as a training kernel; this is its reverse mode. The forward chunk
+ * quantities are recomputed (nothing is kept from a forward call). All steps
+ * run in fp32; the kernels are CUDA-core (SIMT) code.
+ *
+ *  q, k, v, log_alpha, beta, gate, initial_state, cu_seqlens, n_seq, T_total,
+ *  H, dk, dv, chunk, scale, flags, dtype : as for kda_chunk_fwd
+ *  d_out            : [T_total, H, dv] dtype, cotangent of out
+ *  d_final_state    : [n_seq, H, dk, dv] fp32 cotangent of final_state, or NULL (0)
+ *  d_q, d_k, d_log_alpha : [T_total, H, dk] dtype (written); gradients with
+ *                     respect to the raw q and k (through the L2 normalisation
+ *                     when KDA_QK_L2NORM is set) and to log_alpha
+ *  d_v              : [T_total, H, dv] dtype (written)
+ *  d_beta           : [T_total, H] dtype (written)
+ *  d_gate           : [T_total, H, dv] dtype, or NULL (not written); must be
+ *                     NULL when gate is NULL
+ *  d_initial_state  : [n_seq, H, dk, dv] fp32, or NULL (not written)
+ *  workspace        : >= kda_chunk_bwd_workspace_size(...) bytes
+ * Gradients in bf16 are rounded to nearest even from fp32.
+ */
+kda_status kda_chunk_bwd(const void *q, const void *k, const void *v,
+                         const void *log_alpha, const void *beta,
+                         const void *gate, const float *initial_state,
+                         const void *d_out, const float *d_final_state,
+                         void *d_q, void *d_k, void *d_v, void *d_log_alpha,
+                         void *d_beta, void *d_gate, float *d_initial_state,
+                         const int32_t *cu_seqlens, int n_seq, int64_t T_total,
+                         int H, int dk, int dv, int chunk, float scale,
+                         unsigned flags, kda_dtype dtype, void *workspace,
+                         size_t workspace_bytes, kda_stream_t stream);
+
+size_t kda_chunk_bwd_workspace_size(int64_t T_total, int n_seq, int H, int dk,
+                                    int dv, int chunk, kda_dtype dtype);
+
+/*
  * kda_chunk_fwd without a workspace argument, for callers that cannot
  * allocate device memory where they run the mixer: host frameworks that
  * reserve the device heap up front and give a kernel only its inputs and

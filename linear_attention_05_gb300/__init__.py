@@ -5,7 +5,8 @@ The compute lives in ``libkda.so`` (hand-written CUDA behind a C ABI,
 same names. ``inputs`` draws seeded synthetic workloads.
 """
 from .binding import (KDA_DEBUG_CHECK, KDA_DTYPE_BF16, KDA_DTYPE_F32, KDA_QK_L2NORM, KdaError,
-                      chunk_fwd, chunk_fwd_checkpoints, decode_step, kda_chunk_fwd,
+                      chunk_bwd, chunk_fwd, chunk_fwd_checkpoints, decode_step, kda_chunk_bwd,
+                      kda_chunk_bwd_workspace_size, kda_chunk_fwd,
                       kda_chunk_fwd_checkpoints, kda_chunk_fwd_noalloc,
                       kda_chunk_fwd_workspace_size,
                       kda_decode_step, kda_get_error, kda_last_error_string, kda_scan_combine,

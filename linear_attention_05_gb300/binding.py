@@ -72,6 +72,9 @@ def load(path: str = LIB_PATH):
             "kda_last_error_string": ([], ctypes.c_char_p),
             "kda_chunk_fwd": ([P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, P, SZ, P], I),
             "kda_chunk_fwd_workspace_size": ([I64, I, I, I, I, I, I], SZ),
+            "kda_chunk_bwd": ([P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I,
+                               I, F, U, I, P, SZ, P], I),
+            "kda_chunk_bwd_workspace_size": ([I64, I, I, I, I, I, I], SZ),
             "kda_chunk_fwd_checkpoints": ([P, P, P, P, P, P, P, P, P, P, I64, I, P, I, I64, I, I,
                                            I, I, F, U, I, P, SZ, P], I),
             "kda_chunk_fwd_noalloc": ([P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, P], I),
@@ -205,6 +208,33 @@ def kda_chunk_fwd_checkpoints(q, k, v, log_alpha, beta, gate, out, initial_state
         _ptr(ws), wsb, _stream(stream))
     _check(lib, st)
     return out, final_state, checkpoints
+
+
+def kda_chunk_bwd_workspace_size(T_total, n_seq, H, dk, dv, chunk=CHUNK, dtype=KDA_DTYPE_BF16):
+    return int(load().kda_chunk_bwd_workspace_size(T_total, n_seq, H, dk, dv, chunk, dtype))
+
+
+def kda_chunk_bwd(q, k, v, log_alpha, beta, gate, initial_state, d_out, d_final_state, d_q, d_k,
+                  d_v, d_log_alpha, d_beta, d_gate, d_initial_state, cu_seqlens, n_seq,
+                  scale=1.0, flags=KDA_QK_L2NORM, workspace=None, stream=None, chunk=CHUNK):
+    """Chunked backward pass; writes the gradient tensors passed in."""
+    lib = load()
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(k)
+    for t, n in ((initial_state, "initial_state"), (d_final_state, "d_final_state"),
+                 (d_initial_state, "d_initial_state")):
+        _f32_or_none(t, n)
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    need = lib.kda_chunk_bwd_workspace_size(T, n_seq, H, dk, dv, chunk, dt)
+    ws, wsb = _workspace(need, k.device, workspace)
+    st = lib.kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(gate),
+                           _ptr(initial_state), _ptr(d_out), _ptr(d_final_state), _ptr(d_q),
+                           _ptr(d_k), _ptr(d_v), _ptr(d_log_alpha), _ptr(d_beta), _ptr(d_gate),
+                           _ptr(d_initial_state), _ptr(cu_seqlens), n_seq, T, H, dk, dv, chunk,
+                           float(scale), int(flags), dt, _ptr(ws), wsb, _stream(stream))
+    _check(lib, st)
 
 
 def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, gate, out, initial_state, final_state,
@@ -353,6 +383,25 @@ def chunk_fwd_checkpoints(q, k, v, log_alpha, beta, gate=None, initial_state=Non
                                      cu_seqlens, n_seq, scale=scale,
                                      flags=KDA_QK_L2NORM if l2norm else 0, workspace=workspace,
                                      stream=stream)[:2] + (ck,)
+
+
+def chunk_bwd(q, k, v, log_alpha, beta, gate, initial_state, d_out, d_final_state=None,
+              cu_seqlens=None, n_seq=None, scale=1.0, l2norm=True, workspace=None, stream=None):
+    """Allocate the gradients and call kda_chunk_bwd. Returns a dict with dq, dk, dv,
+    dlog_alpha, dbeta, dgate (None without a gate) and dS0 (fp32)."""
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    if n_seq is None:
+        n_seq = (cu_seqlens.numel() - 1) if cu_seqlens is not None else 1
+    g = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+         "dlog_alpha": torch.empty_like(log_alpha), "dbeta": torch.empty_like(beta),
+         "dgate": None if gate is None else torch.empty_like(gate),
+         "dS0": torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=k.device)}
+    kda_chunk_bwd(q, k, v, log_alpha, beta, gate, initial_state, d_out, d_final_state, g["dq"],
+                  g["dk"], g["dv"], g["dlog_alpha"], g["dbeta"], g["dgate"], g["dS0"],
+                  cu_seqlens, n_seq, scale=scale, flags=KDA_QK_L2NORM if l2norm else 0,
+                  workspace=workspace, stream=stream)
+    return g
 
 
 def decode_step(q, k, v, log_alpha, beta, gate, state, state_slot=None, scale=1.0, l2norm=True,

@@ -221,6 +221,64 @@ kda_status kda_chunk_fwd_checkpoints(
                         workspace, workspace_bytes, stream);
 }
 
+size_t kda_chunk_bwd_workspace_size(int64_t T_total, int n_seq, int H, int dk, int dv,
+                                    int chunk, kda_dtype dtype) {
+  if (common_checks(T_total, n_seq, H, dk, dv, chunk, dtype, (const int32_t *)1) != KDA_OK)
+    return 0;
+  return kda::chunk_bwd_ws_bytes(T_total, n_seq, H, dk, dv);
+}
+
+kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void *log_alpha,
+                         const void *beta, const void *gate, const float *initial_state,
+                         const void *d_out, const float *d_final_state, void *d_q, void *d_k,
+                         void *d_v, void *d_log_alpha, void *d_beta, void *d_gate,
+                         float *d_initial_state, const int32_t *cu_seqlens, int n_seq,
+                         int64_t T_total, int H, int dk, int dv, int chunk, float scale,
+                         unsigned flags, kda_dtype dtype, void *workspace,
+                         size_t workspace_bytes, kda_stream_t stream) {
+  kda_status st = common_checks(T_total, n_seq, H, dk, dv, chunk, dtype, cu_seqlens);
+  if (st != KDA_OK) return st;
+  KDA_REQUIRE((flags & ~(unsigned)(KDA_QK_L2NORM | KDA_DEBUG_CHECK)) == 0, KDA_ERR_INVALID_ARG,
+              "unknown flag bits 0x%x", flags);
+  const bool tokens = T_total > 0;
+  KDA_CHECK_PTR(q, tokens);
+  KDA_CHECK_PTR(k, tokens);
+  KDA_CHECK_PTR(v, tokens);
+  KDA_CHECK_PTR(log_alpha, tokens);
+  KDA_REQUIRE(!tokens || beta != nullptr, KDA_ERR_INVALID_ARG, "beta must not be NULL");
+  KDA_CHECK_PTR(gate, false);
+  KDA_CHECK_PTR(initial_state, false);
+  KDA_CHECK_PTR(d_out, tokens);
+  KDA_CHECK_PTR(d_final_state, false);
+  KDA_CHECK_PTR(d_q, tokens);
+  KDA_CHECK_PTR(d_k, tokens);
+  KDA_CHECK_PTR(d_v, tokens);
+  KDA_CHECK_PTR(d_log_alpha, tokens);
+  KDA_REQUIRE(!tokens || d_beta != nullptr, KDA_ERR_INVALID_ARG, "d_beta must not be NULL");
+  KDA_CHECK_PTR(d_gate, false);
+  KDA_REQUIRE(gate != nullptr || d_gate == nullptr, KDA_ERR_INVALID_ARG,
+              "d_gate given without gate");
+  KDA_CHECK_PTR(d_initial_state, false);
+  KDA_REQUIRE(cu_seqlens == nullptr || ((uintptr_t)cu_seqlens & 3u) == 0, KDA_ERR_INVALID_ARG,
+              "cu_seqlens is not 4-byte aligned");
+  if (n_seq == 0) return KDA_OK;
+  const size_t need = kda::chunk_bwd_ws_bytes(T_total, n_seq, H, dk, dv);
+  KDA_REQUIRE(workspace != nullptr && workspace_bytes >= need, KDA_ERR_WORKSPACE,
+              "workspace %zu bytes, need %zu", workspace_bytes, need);
+  KDA_REQUIRE(((uintptr_t)workspace & 255u) == 0, KDA_ERR_INVALID_ARG,
+              "workspace is not 256-byte aligned");
+  cudaStream_t s = (cudaStream_t)stream;
+  Tracer tr(s);
+  return cuda_status(tr([&] {
+                       return kda::launch_chunk_bwd(
+                           q, k, v, log_alpha, beta, gate, initial_state, d_out, d_final_state,
+                           d_q, d_k, d_v, d_log_alpha, d_beta, d_gate, d_initial_state,
+                           cu_seqlens, n_seq, T_total, H, dk, dv, scale, flags, dtype, workspace,
+                           s);
+                     }),
+                     "backward");
+}
+
 kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *log_alpha,
                            const void *beta, const void *gate, void *out, float *state,
                            const int32_t *state_slot, int n_slots, int N, int H, int dk, int dv,

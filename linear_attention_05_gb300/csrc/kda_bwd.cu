@@ -1,0 +1,642 @@
+// Chunked backward pass of KDA (fp32 SIMT).
+//
+// Gradients of L = <dO, o> + <dS_final, S_final> with respect to q, k, v,
+// log_alpha, beta, gate and the initial state. The forward is the chunked form
+// of K3 training overview (zuoshipin.com/article/18261) section 4 "FlashKDA"
+// (per-chunk preparation, then the ordered state hand-off); section 4 presents it
+// as a training kernel, so it needs these gradients. Per chunk, with S the state
+// entering the chunk and S' the state leaving it (operands as in the forward):
+//   U = U~ - W S,  O = Q~ S + P U,  S' = Diag(e^{G_C}) S + K_d^T U,  o = scale g O,
+//   W = T diag(b) K~,  U~ = T diag(b) V,  T = (I + A)^-1,  A = strict_lower(diag(b) K~ K^^T).
+// Reverse mode, given dS' and dO = scale g do:
+//   dU  = P^T dO + K_d dS'                       dS  = Diag(e^{G_C}) dS' + Q~^T dO - W^T dU
+//   dP  = lower(dO U^T)                          dQ~ = dO S^T + dP K^
+//   dK_d = U dS'^T                               dW  = -dU S^T
+//   [dB_k | dB_v] = T^T [dW | dU]                dA  = strict_lower(-dB_k W^T - dB_v U~^T)
+//   dK~ = diag(b) (dA K^ + dB_k)                 dK^ = dP^T Q~ + dA^T diag(b) K~
+//   db  = rowdot(K~, dA K^ + dB_k) + rowdot(V, dB_v),   dv = diag(b) dB_v
+// then through K~ = k e^G, K^ = k e^-G, Q~ = q e^G, K_d = k e^{G_C - G}, e^{G_C}
+// to k, q and the running log-decay G, whose reverse cumulative sum gives
+// dlog_alpha, and through the optional L2 normalisation of q and k.
+//
+// Launch sequence (all on the caller's stream): chunk table; prep (forward
+// operands + K^, diag(b)K~, A); forward state pass saving S, U, O per chunk;
+// dO; reverse state pass (dS' per chunk, dU, dS_0); seven batched 64-row GEMMs;
+// one triangular solve; the finishing kernel.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kda_common.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int C = kChunk;  // 64
+
+__device__ __forceinline__ float bf(float x) { return x; }
+__device__ __forceinline__ float bf(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T>
+__device__ __forceinline__ T to_out(float x);
+template <>
+__device__ __forceinline__ float to_out<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float wsum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// token range of chunk ci (global index) -> (sequence, first token, valid rows)
+__device__ __forceinline__ void chunk_rows(const int32_t *cu, int64_t fixed_len, int n_seq,
+                                           const int *off, int ci, int *s_out, int64_t *t0,
+                                           int *len) {
+  int lo = 0, hi = n_seq - 1;  // last s with off[s] <= ci (skipping empty sequences)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= ci) lo = mid;
+    else hi = mid - 1;
+  }
+  const int s = lo;
+  int64_t ts, ls;
+  if (cu) {
+    ts = cu[s];
+    ls = (int64_t)cu[s + 1] - cu[s];
+  } else {
+    ts = (int64_t)s * fixed_len;
+    ls = fixed_len;
+  }
+  const int j = ci - off[s];
+  *s_out = s;
+  *t0 = ts + (int64_t)j * C;
+  *len = (int)min((int64_t)C, ls - (int64_t)j * C);
+}
+
+// ---------------------------------------------------------------------------
+// dO = scale * g * do in chunk layout [slab][64][dv] (zero on padded rows)
+template <int DV, typename Tin>
+__global__ void __launch_bounds__(256) kda_bwd_dO(const Tin *__restrict__ d_out,
+                                                  const Tin *__restrict__ gate,
+                                                  const int32_t *__restrict__ cu, int n_seq,
+                                                  int64_t fixed_len, int H, float scale,
+                                                  const ChunkMeta *__restrict__ meta,
+                                                  const int *__restrict__ off,
+                                                  float *__restrict__ dO) {
+  const int ci = blockIdx.x, h = blockIdx.y;
+  if (meta->invalid || ci >= meta->total_chunks) return;
+  int s, len;
+  int64_t t0;
+  chunk_rows(cu, fixed_len, n_seq, off, ci, &s, &t0, &len);
+  float *dst = dO + ((size_t)ci * H + h) * C * DV;
+  for (int e = threadIdx.x; e < C * DV; e += 256) {
+    const int r = e / DV, j = e % DV;
+    float x = 0.f;
+    if (r < len) {
+      const size_t g = ((size_t)(t0 + r) * H + h) * DV + j;
+      x = scale * bf(d_out[g]) * (gate ? bf(gate[g]) : 1.f);
+    }
+    dst[e] = x;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Reverse state pass: one block per (sequence, head, 32 value columns), chunks
+// last to first. Writes dS' (the cotangent of the state leaving each chunk) and
+// dU per chunk, and dS_0.
+constexpr int RBV = 32;
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(256) kda_bwd_state(
+    const float *__restrict__ dS_final, float *__restrict__ dS_init,
+    const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len, int H,
+    const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
+    const float *__restrict__ Qg, const float *__restrict__ Wg, const float *__restrict__ Kdg,
+    const float *__restrict__ Pg, const float *__restrict__ Dg, const float *__restrict__ dOg,
+    float *__restrict__ dSb, float *__restrict__ dUg) {
+  constexpr int LK = DK + 1, LS = RBV + 1, LP = C + 1;
+  extern __shared__ float smem[];
+  float *sS = smem;            // [DK][LS]   running dS
+  float *sO = sS + DK * LS;    // [C][LS]    dO slice
+  float *sU = sO + C * LS;     // [C][LS]    dU slice
+  float *sQ = sU + C * LS;     // [C][LK]
+  float *sW = sQ + C * LK;     // [C][LK]
+  float *sKd = sW + C * LK;    // [C][LK]
+  float *sP = sKd + C * LK;    // [C][LP]
+  float *sD = sP + C * LP;     // [DK]
+  if (meta->invalid) return;
+  const int chain = blockIdx.x, s = chain / H, h = chain % H, tid = threadIdx.x;
+  const int j0 = blockIdx.y * RBV, jt = tid & 31, rt = tid >> 5;
+  for (int c = rt; c < DK; c += 8)
+    sS[c * LS + jt] = dS_final ? dS_final[(((size_t)s * H + h) * DK + c) * DV + j0 + jt] : 0.f;
+  int64_t ls;
+  if (cu) ls = (int64_t)cu[s + 1] - cu[s];
+  else ls = fixed_len;
+  const int nchunks = (int)((ls + C - 1) / C);
+  __syncthreads();
+  for (int jc = nchunks - 1; jc >= 0; --jc) {
+    const size_t slab = (size_t)(off[s] + jc) * H + h;
+    for (int c = rt; c < DK; c += 8) dSb[(slab * DK + c) * DV + j0 + jt] = sS[c * LS + jt];
+    for (int e = tid; e < C * DK; e += 256) {
+      const int r = e / DK, c = e % DK;
+      sQ[r * LK + c] = Qg[slab * C * DK + e];
+      sW[r * LK + c] = Wg[slab * C * DK + e];
+      sKd[r * LK + c] = Kdg[slab * C * DK + e];
+    }
+    for (int e = tid; e < C * C; e += 256) sP[(e / C) * LP + e % C] = Pg[slab * C * C + e];
+    for (int e = tid; e < C * RBV; e += 256) {
+      const int r = e / RBV, c = e % RBV;
+      sO[r * LS + c] = dOg[(slab * C + r) * DV + j0 + c];
+    }
+    if (tid < DK) sD[tid] = Dg[slab * DK + tid];
+    __syncthreads();
+    // dU = P^T dO + K_d dS'   (P is lower triangular: P[i][r] = 0 for i < r)
+#pragma unroll 1
+    for (int m = 0; m < C / 8; ++m) {
+      const int r = rt + 8 * m;
+      float acc = 0.f;
+      for (int i = r; i < C; ++i) acc = fmaf(sP[i * LP + r], sO[i * LS + jt], acc);
+      for (int c = 0; c < DK; ++c) acc = fmaf(sKd[r * LK + c], sS[c * LS + jt], acc);
+      sU[r * LS + jt] = acc;
+      dUg[(slab * C + r) * DV + j0 + jt] = acc;
+    }
+    __syncthreads();
+    // dS = Diag(e^{G_C}) dS' + Q~^T dO - W^T dU
+    float ns[DK / 8];
+#pragma unroll
+    for (int m = 0; m < DK / 8; ++m) {
+      const int c = rt + 8 * m;
+      float acc = sD[c] * sS[c * LS + jt];
+      for (int r = 0; r < C; ++r)
+        acc = fmaf(sQ[r * LK + c], sO[r * LS + jt], fmaf(-sW[r * LK + c], sU[r * LS + jt], acc));
+      ns[m] = acc;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < DK / 8; ++m) sS[(rt + 8 * m) * LS + jt] = ns[m];
+    __syncthreads();
+  }
+  if (dS_init)
+    for (int c = rt; c < DK; c += 8)
+      dS_init[(((size_t)s * H + h) * DK + c) * DV + j0 + jt] = sS[c * LS + jt];
+}
+
+template <int DK>
+constexpr size_t bwd_state_smem() {
+  return sizeof(float) * (DK * (RBV + 1) + 2 * C * (RBV + 1) + 3 * C * (DK + 1) + C * (C + 1) + DK);
+}
+
+// ---------------------------------------------------------------------------
+// Batched 64-row GEMM over (chunk, head) slabs:
+//   C = mask( sum_i alpha_i op(A_i) op(B_i) ),  C: [64, N] row-major,
+// op(A)(m, k) = a_t ? A[k * lda + m] : A[m * lda + k],
+// op(B)(k, n) = b_t ? B[n * ldb + k] : B[k * ldb + n].
+// mask 0: none; 1: keep n <= m; 2: keep n < m. 256 threads, 4 x (N/16) outputs each.
+struct GemmTerm {
+  const float *A, *B;
+  size_t sA, sB;  // per-slab strides (floats)
+  int lda, ldb, a_t, b_t, K;
+  float alpha;
+};
+struct GemmArgs {
+  GemmTerm t[2];
+  int nterms;
+  float *Cm;
+  size_t sC;
+  int mask;
+};
+
+constexpr int GKT = 32;  // K tile
+
+template <int N>
+__global__ void __launch_bounds__(256) kda_bwd_gemm(GemmArgs g, int H,
+                                                    const ChunkMeta *__restrict__ meta) {
+  constexpr int PA = C + 1, PB = N + 1, NJ = N / 16;
+  __shared__ float sA[GKT * PA];
+  __shared__ float sB[GKT * PB];
+  const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  if (meta->invalid || ci >= meta->total_chunks) return;
+  const size_t slab = (size_t)ci * H + h;
+  const int ty = tid >> 4, tx = tid & 15;
+  float acc[4][NJ];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) acc[i][jj] = 0.f;
+  for (int ti = 0; ti < g.nterms; ++ti) {
+    const GemmTerm t = g.t[ti];
+    const float *A = t.A + slab * t.sA, *B = t.B + slab * t.sB;
+    for (int k0 = 0; k0 < t.K; k0 += GKT) {
+      __syncthreads();  // previous tile consumed
+      for (int e = tid; e < GKT * C; e += 256) {
+        int m, kk;
+        if (t.a_t) { kk = e / C; m = e % C; }      // coalesced along m
+        else { m = e / GKT; kk = e % GKT; }        // coalesced along k
+        const float x = t.a_t ? A[(size_t)(k0 + kk) * t.lda + m] : A[(size_t)m * t.lda + k0 + kk];
+        sA[kk * PA + m] = t.alpha * x;
+      }
+      for (int e = tid; e < GKT * N; e += 256) {
+        int n, kk;
+        if (t.b_t) { n = e / GKT; kk = e % GKT; }  // coalesced along k
+        else { kk = e / N; n = e % N; }            // coalesced along n
+        sB[kk * PB + n] = t.b_t ? B[(size_t)n * t.ldb + k0 + kk] : B[(size_t)(k0 + kk) * t.ldb + n];
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int kk = 0; kk < GKT; ++kk) {
+        float a[4], b[NJ];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = sA[kk * PA + 4 * ty + i];
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj) b[jj] = sB[kk * PB + tx + 16 * jj];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jj = 0; jj < NJ; ++jj) acc[i][jj] = fmaf(a[i], b[jj], acc[i][jj]);
+      }
+    }
+  }
+  float *Cm = g.Cm + slab * g.sC;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) {
+      const int m = 4 * ty + i, n = tx + 16 * jj;
+      const bool keep = g.mask == 0 || (g.mask == 1 ? n <= m : n < m);
+      Cm[(size_t)m * N + n] = keep ? acc[i][jj] : 0.f;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// [X1 | X2] = T^T [Y1 | Y2] in place, T = (I + A)^-1: back substitution on the
+// unit upper-triangular (I + A)^T, X_r = Y_r - sum_{s > r} A[s][r] X_s.
+// One thread per column (N1 + N2 <= 256), columns staged in shared memory.
+template <int N1, int N2>
+__global__ void __launch_bounds__(256) kda_bwd_solve(const float *__restrict__ Ag,
+                                                     float *__restrict__ Y1,
+                                                     float *__restrict__ Y2, int H,
+                                                     const ChunkMeta *__restrict__ meta) {
+  constexpr int NC = N1 + N2, LA = C + 1, LY = NC + 1;
+  extern __shared__ float smem[];
+  float *sA = smem;          // [C][LA]
+  float *sY = sA + C * LA;   // [C][LY]
+  const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  if (meta->invalid || ci >= meta->total_chunks) return;
+  const size_t slab = (size_t)ci * H + h;
+  float *y1 = Y1 + slab * C * N1, *y2 = Y2 + slab * C * N2;
+  for (int e = tid; e < C * C; e += 256) sA[(e / C) * LA + e % C] = Ag[slab * C * C + e];
+  for (int e = tid; e < C * N1; e += 256) sY[(e / N1) * LY + e % N1] = y1[e];
+  for (int e = tid; e < C * N2; e += 256) sY[(e / N2) * LY + N1 + e % N2] = y2[e];
+  __syncthreads();
+  if (tid < NC) {
+    float *col = sY + tid;
+    for (int r = C - 2; r >= 0; --r) {
+      float acc = col[r * LY];
+      for (int s = r + 1; s < C; ++s) acc = fmaf(-sA[s * LA + r], col[s * LY], acc);
+      col[r * LY] = acc;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < C * N1; e += 256) y1[e] = sY[(e / N1) * LY + e % N1];
+  for (int e = tid; e < C * N2; e += 256) y2[e] = sY[(e / N2) * LY + N1 + e % N2];
+}
+
+// ---------------------------------------------------------------------------
+// Finishing kernel, one block per (chunk, head): from the chunk-level cotangents
+// to the token gradients. Warp w handles token rows w, w + 8, ...; lane l the key
+// channels l + 32 i and value channels l + 32 i.
+template <int DK, int DV, typename Tio>
+__global__ void __launch_bounds__(256) kda_bwd_finish(
+    const Tio *__restrict__ q, const Tio *__restrict__ k, const Tio *__restrict__ v,
+    const Tio *__restrict__ la, const Tio *__restrict__ beta, const Tio *__restrict__ d_out,
+    Tio *__restrict__ dq, Tio *__restrict__ dk, Tio *__restrict__ dv, Tio *__restrict__ dla,
+    Tio *__restrict__ dbeta, Tio *__restrict__ dgate, const int32_t *__restrict__ cu, int n_seq,
+    int64_t fixed_len, int H, float scale, unsigned flags, const ChunkMeta *__restrict__ meta,
+    const int *__restrict__ off, const float *__restrict__ Yg, const float *__restrict__ dBkg,
+    const float *__restrict__ dBvg, const float *__restrict__ dKhg,
+    const float *__restrict__ dQtg, const float *__restrict__ dKdg,
+    const float *__restrict__ Sbg, const float *__restrict__ dSbg, const float *__restrict__ Og) {
+  constexpr int LK = DK + 1, NI = DK / 32, NJ = DV / 32;
+  extern __shared__ float smem[];
+  float *sG = smem;             // [C][LK]  running log-decay G
+  float *sdG = sG + C * LK;     // [C][LK]  dL/dG
+  float *sB = sdG + C * LK;     // [C]      beta
+  float *sDc = sB + C;          // [DK]     e^{G_C}
+  float *sdD = sDc + DK;        // [DK]     dL/d e^{G_C} from the state hand-off
+  float *sGCp = sdD + DK;       // [8][DK]  per-warp partial dL/dG_C
+  const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  if (meta->invalid || ci >= meta->total_chunks) return;
+  int s, len;
+  int64_t t0;
+  chunk_rows(cu, fixed_len, n_seq, off, ci, &s, &t0, &len);
+  const size_t slab = (size_t)ci * H + h;
+  const bool l2 = (flags & KDA_QK_L2NORM) != 0;
+
+  if (tid < C) sB[tid] = tid < len ? bf(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+  if (tid < DK) {
+    const int c = tid;
+    float G = 0.f;
+    for (int r = 0; r < C; ++r) {
+      if (r < len) G += bf(la[((size_t)(t0 + r) * H + h) * DK + c]);
+      sG[r * LK + c] = G;
+    }
+    sDc[c] = expf(G);
+  }
+  // dL/d e^{G_C}[c] = sum_j dS'[c][j] S[c][j]
+  for (int c = warp; c < DK; c += 8) {
+    const float *sb = Sbg + (slab * DK + c) * DV, *dsb = dSbg + (slab * DK + c) * DV;
+    float acc = 0.f;
+    for (int j = lane; j < DV; j += 32) acc = fmaf(dsb[j], sb[j], acc);
+    acc = wsum(acc);
+    if (lane == 0) sdD[c] = acc;
+  }
+  __syncthreads();
+
+  float gcp[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) gcp[i] = 0.f;
+  for (int r = warp; r < C; r += 8) {
+    if (r >= len) {
+#pragma unroll
+      for (int i = 0; i < NI; ++i) sdG[r * LK + lane + 32 * i] = 0.f;
+      continue;
+    }
+    const size_t tok = (size_t)(t0 + r) * H + h;
+    const float b = sB[r];
+    float kn[NI], qn[NI], sk = 0.f, sq = 0.f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      kn[i] = bf(k[tok * DK + lane + 32 * i]);
+      qn[i] = bf(q[tok * DK + lane + 32 * i]);
+      sk = fmaf(kn[i], kn[i], sk);
+      sq = fmaf(qn[i], qn[i], sq);
+    }
+    float rk = 1.f, rq = 1.f;
+    if (l2) {
+      rk = rsqrtf(wsum(sk) + kL2Eps);
+      rq = rsqrtf(wsum(sq) + kL2Eps);
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        kn[i] *= rk;
+        qn[i] *= rq;
+      }
+    }
+    const size_t rowk = (slab * C + r) * DK;
+    float dkn[NI], dqn[NI], dbk = 0.f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int c = lane + 32 * i;
+      const float G = sG[r * LK + c], eP = expf(G), eN = expf(-G), Dc = sDc[c];
+      const float Kt = kn[i] * eP, Kh = kn[i] * eN, Qt = qn[i] * eP, Kd = Kh * Dc;
+      const float y = Yg[rowk + c] + dBkg[rowk + c];
+      const float dKt = b * y, dKh = dKhg[rowk + c], dQt = dQtg[rowk + c], dKd = dKdg[rowk + c];
+      dkn[i] = dKt * eP + dKh * eN + dKd * eN * Dc;
+      dqn[i] = dQt * eP;
+      sdG[r * LK + c] = dKt * Kt - dKh * Kh + dQt * Qt - dKd * Kd;
+      gcp[i] = fmaf(dKd, Kd, gcp[i]);
+      dbk = fmaf(Kt, y, dbk);
+    }
+    if (l2) {  // d(x / |x|) : dx = r (dn - n (n . dn))
+      float pk = 0.f, pq = 0.f;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        pk = fmaf(kn[i], dkn[i], pk);
+        pq = fmaf(qn[i], dqn[i], pq);
+      }
+      pk = wsum(pk);
+      pq = wsum(pq);
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        dkn[i] = rk * (dkn[i] - kn[i] * pk);
+        dqn[i] = rq * (dqn[i] - qn[i] * pq);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      dk[tok * DK + lane + 32 * i] = to_out<Tio>(dkn[i]);
+      dq[tok * DK + lane + 32 * i] = to_out<Tio>(dqn[i]);
+    }
+    const size_t rowv = (slab * C + r) * DV;
+    float dbv = 0.f;
+#pragma unroll
+    for (int i = 0; i < NJ; ++i) {
+      const int j = lane + 32 * i;
+      const float g = dBvg[rowv + j];
+      dbv = fmaf(bf(v[tok * DV + j]), g, dbv);
+      dv[tok * DV + j] = to_out<Tio>(b * g);
+      if (dgate) dgate[tok * DV + j] = to_out<Tio>(scale * bf(d_out[tok * DV + j]) * Og[rowv + j]);
+    }
+    const float db = wsum(dbk) + wsum(dbv);
+    if (lane == 0) dbeta[tok] = to_out<Tio>(db);
+  }
+#pragma unroll
+  for (int i = 0; i < NI; ++i) sGCp[warp * DK + lane + 32 * i] = gcp[i];
+  __syncthreads();
+  if (tid < DK) {
+    const int c = tid;
+    float dGC = sdD[c] * sDc[c];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) dGC += sGCp[w * DK + c];
+    // G_r = sum_{s <= r} log_alpha_s and G_C = G_63: reverse cumulative sum
+    float acc = 0.f;
+    for (int r = C - 1; r >= 0; --r) {
+      acc += sdG[r * LK + c];
+      if (r < len) dla[((size_t)(t0 + r) * H + h) * DK + c] = to_out<Tio>(acc + dGC);
+    }
+  }
+}
+
+template <int DK>
+constexpr size_t bwd_finish_smem() {
+  return sizeof(float) * (2 * C * (DK + 1) + C + 2 * DK + 8 * DK);
+}
+
+// ---------------------------------------------------------------------------
+// workspace: the forward's SIMT chunk workspace, then the backward's buffers
+struct BwdWs {
+  ChunkWs fw;
+  float *Kh, *Bk, *A, *Sb, *dSb, *Ub, *O, *dO, *dU, *dP, *dQt, *dKd, *dW, *dM, *Y, *dKh;
+};
+
+size_t bwd_extra_bytes(int64_t T_total, int n_seq, int H, int dk, int dv) {
+  const size_t per = ((size_t)(T_total / C) + (size_t)n_seq + 1) * H;
+  const size_t mk = align_up(sizeof(float) * per * C * dk, 256);
+  const size_t mv = align_up(sizeof(float) * per * C * dv, 256);
+  const size_t mc = align_up(sizeof(float) * per * C * C, 256);
+  const size_t ms = align_up(sizeof(float) * per * dk * dv, 256);
+  return 7 * mk + 4 * mv + 3 * mc + 2 * ms;
+}
+
+BwdWs bwd_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int dv) {
+  BwdWs w;
+  w.fw = chunk_ws_carve(ws, T_total, n_seq, H, dk, dv);
+  char *p = (char *)ws + chunk_ws_bytes(T_total, n_seq, H, dk, dv);
+  const size_t per = ((size_t)(T_total / C) + (size_t)n_seq + 1) * H;
+  const size_t mk = align_up(sizeof(float) * per * C * dk, 256);
+  const size_t mv = align_up(sizeof(float) * per * C * dv, 256);
+  const size_t mc = align_up(sizeof(float) * per * C * C, 256);
+  const size_t ms = align_up(sizeof(float) * per * dk * dv, 256);
+  auto take = [&](size_t n) {
+    float *r = (float *)p;
+    p += n;
+    return r;
+  };
+  w.Kh = take(mk); w.Bk = take(mk); w.dQt = take(mk); w.dKd = take(mk); w.dW = take(mk);
+  w.Y = take(mk); w.dKh = take(mk);
+  w.Ub = take(mv); w.O = take(mv); w.dO = take(mv); w.dU = take(mv);
+  w.A = take(mc); w.dP = take(mc); w.dM = take(mc);
+  w.Sb = take(ms); w.dSb = take(ms);
+  return w;
+}
+
+GemmTerm term(const float *A, size_t sA, int lda, int a_t, const float *B, size_t sB, int ldb,
+              int b_t, int K, float alpha) {
+  GemmTerm t;
+  t.A = A; t.sA = sA; t.lda = lda; t.a_t = a_t;
+  t.B = B; t.sB = sB; t.ldb = ldb; t.b_t = b_t;
+  t.K = K; t.alpha = alpha;
+  return t;
+}
+
+template <int N>
+cudaError_t gemm(const GemmTerm &t0, const GemmTerm *t1, float *Cm, int mask, int mc, int H,
+                 const ChunkMeta *meta, cudaStream_t st) {
+  GemmArgs g;
+  g.t[0] = t0;
+  g.t[1] = t1 ? *t1 : t0;
+  g.nterms = t1 ? 2 : 1;
+  g.Cm = Cm;
+  g.sC = (size_t)C * N;
+  g.mask = mask;
+  kda_bwd_gemm<N><<<dim3(mc, H), 256, 0, st>>>(g, H, meta);
+  return cudaGetLastError();
+}
+
+template <int DK, int DV, typename Tio>
+cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, const void *beta,
+                  const void *gate, const float *S0, const void *d_out, const float *dSf,
+                  void *dq, void *dk, void *dv, void *dla, void *dbeta, void *dgate, float *dS0,
+                  const int32_t *cu, int n_seq, int64_t T_total, int H, float scale,
+                  unsigned flags, kda_dtype dt, void *ws_raw, cudaStream_t st) {
+  BwdWs w = bwd_ws_carve(ws_raw, T_total, n_seq, H, DK, DV);
+  const ChunkWs &fw = w.fw;
+  const int mc = fw.max_chunks;
+  const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
+  cudaError_t e;
+#define KDA_TRY(x)              \
+  do {                          \
+    e = (x);                    \
+    if (e != cudaSuccess) return e; \
+  } while (0)
+  KDA_TRY(launch_chunk_table(cu, n_seq, T_total, fw, st));
+  PrepSave ps;
+  ps.Kh = w.Kh; ps.Bk = w.Bk; ps.A = w.A;
+  KDA_TRY(launch_prep(q, k, v, la, beta, cu, n_seq, T_total, H, DK, DV, flags, dt, fw, true, st,
+                      ps));
+  StateSave ss;
+  ss.Sb = w.Sb; ss.Ub = w.Ub; ss.O = w.O;
+  KDA_TRY(launch_state_pass(0, nullptr, nullptr, S0, nullptr, nullptr, nullptr, cu, n_seq,
+                            T_total, H, DK, DV, scale, dt, fw, st, CkptOut(), ss));
+  kda_bwd_dO<DV, Tio><<<dim3(mc, H), 256, 0, st>>>((const Tio *)d_out, (const Tio *)gate, cu,
+                                                   n_seq, fixed_len, H, scale, fw.meta,
+                                                   fw.seq_chunk_off, w.dO);
+  KDA_TRY(cudaGetLastError());
+  {
+    auto kern = kda_bwd_state<DK, DV>;
+    constexpr size_t sm = bwd_state_smem<DK>();
+    KDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+    kern<<<dim3(n_seq * H, DV / RBV), 256, sm, st>>>(dSf, dS0, cu, n_seq, fixed_len, H, fw.meta,
+                                                     fw.seq_chunk_off, fw.Q, fw.W, fw.Kd, fw.P,
+                                                     fw.D, w.dO, w.dSb, w.dU);
+    KDA_TRY(cudaGetLastError());
+  }
+  const size_t sk = (size_t)C * DK, sv = (size_t)C * DV, scc = (size_t)C * C,
+               ss2 = (size_t)DK * DV;
+  // dP = lower(dO U^T)
+  KDA_TRY(gemm<C>(term(w.dO, sv, DV, 0, w.Ub, sv, DV, 1, DV, 1.f), nullptr, w.dP, 1, mc, H,
+                  fw.meta, st));
+  // dQ~ = dO S^T + dP K^
+  {
+    GemmTerm t2 = term(w.dP, scc, C, 0, w.Kh, sk, DK, 0, C, 1.f);
+    KDA_TRY(gemm<DK>(term(w.dO, sv, DV, 0, w.Sb, ss2, DV, 1, DV, 1.f), &t2, w.dQt, 0, mc, H,
+                     fw.meta, st));
+  }
+  // dK_d = U dS'^T
+  KDA_TRY(gemm<DK>(term(w.Ub, sv, DV, 0, w.dSb, ss2, DV, 1, DV, 1.f), nullptr, w.dKd, 0, mc, H,
+                   fw.meta, st));
+  // dW = -dU S^T
+  KDA_TRY(gemm<DK>(term(w.dU, sv, DV, 0, w.Sb, ss2, DV, 1, DV, -1.f), nullptr, w.dW, 0, mc, H,
+                   fw.meta, st));
+  // [dB_k | dB_v] = T^T [dW | dU]   (in place)
+  {
+    auto kern = kda_bwd_solve<DK, DV>;
+    constexpr size_t sm = sizeof(float) * (C * (C + 1) + C * (DK + DV + 1));
+    KDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+    kern<<<dim3(mc, H), 256, sm, st>>>(w.A, w.dW, w.dU, H, fw.meta);
+    KDA_TRY(cudaGetLastError());
+  }
+  // dA = strict_lower(-dB_k W^T - dB_v U~^T)
+  {
+    GemmTerm t2 = term(w.dU, sv, DV, 0, fw.U, sv, DV, 1, DV, -1.f);
+    KDA_TRY(gemm<C>(term(w.dW, sk, DK, 0, fw.W, sk, DK, 1, DK, -1.f), &t2, w.dM, 2, mc, H,
+                    fw.meta, st));
+  }
+  // Y = dA K^
+  KDA_TRY(gemm<DK>(term(w.dM, scc, C, 0, w.Kh, sk, DK, 0, C, 1.f), nullptr, w.Y, 0, mc, H,
+                   fw.meta, st));
+  // dK^ = dP^T Q~ + dA^T diag(b) K~
+  {
+    GemmTerm t2 = term(w.dM, scc, C, 1, w.Bk, sk, DK, 0, C, 1.f);
+    KDA_TRY(gemm<DK>(term(w.dP, scc, C, 1, fw.Q, sk, DK, 0, C, 1.f), &t2, w.dKh, 0, mc, H,
+                     fw.meta, st));
+  }
+  {
+    auto kern = kda_bwd_finish<DK, DV, Tio>;
+    constexpr size_t sm = bwd_finish_smem<DK>();
+    KDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+    kern<<<dim3(mc, H), 256, sm, st>>>(
+        (const Tio *)q, (const Tio *)k, (const Tio *)v, (const Tio *)la, (const Tio *)beta,
+        (const Tio *)d_out, (Tio *)dq, (Tio *)dk, (Tio *)dv, (Tio *)dla, (Tio *)dbeta,
+        gate ? (Tio *)dgate : nullptr, cu, n_seq, fixed_len, H, scale, flags, fw.meta,
+        fw.seq_chunk_off, w.Y, w.dW, w.dU, w.dKh, w.dQt, w.dKd, w.Sb, w.dSb, w.O);
+    KDA_TRY(cudaGetLastError());
+  }
+#undef KDA_TRY
+  return cudaSuccess;
+}
+
+}  // namespace
+
+size_t chunk_bwd_ws_bytes(int64_t T_total, int n_seq, int H, int dk, int dv) {
+  return chunk_ws_bytes(T_total, n_seq, H, dk, dv) + bwd_extra_bytes(T_total, n_seq, H, dk, dv);
+}
+
+cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const void *la,
+                             const void *beta, const void *gate, const float *S0,
+                             const void *d_out, const float *dSf, void *dq, void *dk, void *dv,
+                             void *dla, void *dbeta, void *dgate, float *dS0, const int32_t *cu,
+                             int n_seq, int64_t T_total, int H, int dk_, int dv_, float scale,
+                             unsigned flags, kda_dtype dt, void *ws, cudaStream_t st) {
+#define KDA_BWD_ARGS                                                                          \
+  q, k, v, la, beta, gate, S0, d_out, dSf, dq, dk, dv, dla, dbeta, dgate, dS0, cu, n_seq, \
+      T_total, H, scale, flags, dt, ws, st
+  if (dt == KDA_DTYPE_BF16) {
+    if (dk_ == 128 && dv_ == 128) return bwd_t<128, 128, __nv_bfloat16>(KDA_BWD_ARGS);
+    if (dk_ == 64 && dv_ == 64) return bwd_t<64, 64, __nv_bfloat16>(KDA_BWD_ARGS);
+    if (dk_ == 128 && dv_ == 64) return bwd_t<128, 64, __nv_bfloat16>(KDA_BWD_ARGS);
+    if (dk_ == 64 && dv_ == 128) return bwd_t<64, 128, __nv_bfloat16>(KDA_BWD_ARGS);
+  } else {
+    if (dk_ == 128 && dv_ == 128) return bwd_t<128, 128, float>(KDA_BWD_ARGS);
+    if (dk_ == 64 && dv_ == 64) return bwd_t<64, 64, float>(KDA_BWD_ARGS);
+    if (dk_ == 128 && dv_ == 64) return bwd_t<128, 64, float>(KDA_BWD_ARGS);
+    if (dk_ == 64 && dv_ == 128) return bwd_t<64, 128, float>(KDA_BWD_ARGS);
+  }
+#undef KDA_BWD_ARGS
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kda

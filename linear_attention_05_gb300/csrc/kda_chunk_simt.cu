@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(256) kda_prep_simt(
     int n_seq, int64_t fixed_len, int H, unsigned flags, const ChunkMeta *__restrict__ meta,
     const int *__restrict__ off, float *__restrict__ Wg, float *__restrict__ Ug,
     float *__restrict__ Qg, float *__restrict__ Kdg, float *__restrict__ Pg,
-    float *__restrict__ Dg, int need_q) {
+    float *__restrict__ Dg, int need_q, PrepSave save) {
   constexpr int LK = DK + 1, LV = DV + 1, LA = C + 1;
   extern __shared__ float smem[];
   float *sKt = smem;             // [C][LK]  k*e^{G}, then b*Kt, then W
@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(256) kda_prep_simt(
         int r = rb + i, c2 = cb + jj;
         sA[r * LA + c2] = c2 < r ? sB[r] * a[i][jj] : 0.f;
         Pout[r * C + c2] = c2 <= r ? p[i][jj] : 0.f;
+        if (save.A) save.A[slab * C * C + r * C + c2] = sA[r * LA + c2];
       }
   }
   __syncthreads();
@@ -245,11 +246,13 @@ __global__ void __launch_bounds__(256) kda_prep_simt(
     int r = e / DK, c = e % DK;
     if (need_q) Qout[e] = sQt[r * LK + c];
     Kdout[e] = sKh[r * LK + c] * sGC[c];
+    if (save.Kh) save.Kh[slab * C * DK + e] = sKh[r * LK + c];
   }
   if (tid < DK) Dg[slab * DK + tid] = sGC[tid];
   for (int e = tid; e < C * DK; e += 256) {
     int r = e / DK, c = e % DK;
     sKt[r * LK + c] *= sB[r];
+    if (save.Bk) save.Bk[slab * C * DK + e] = sKt[r * LK + c];
   }
   for (int e = tid; e < C * DV; e += 256) {
     int r = e / DV, c = e % DV;
@@ -288,7 +291,7 @@ __global__ void __launch_bounds__(256) kda_state_simt(
     int H, float scale, const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
     const float *__restrict__ Wg, const float *__restrict__ Ug, const float *__restrict__ Qg,
     const float *__restrict__ Kdg, const float *__restrict__ Pg, const float *__restrict__ Dg,
-    CkptOut ck) {
+    CkptOut ck, StateSave save) {
   constexpr int LK = DK + 1, LS = BV + 1, LP = C + 1;
   extern __shared__ float smem[];
   float *sS = smem;            // [DK][LS]
@@ -323,6 +326,7 @@ __global__ void __launch_bounds__(256) kda_state_simt(
   seq_range(cu, fixed_len, s, &ts, &ls);
   const int nchunks = (int)((ls + C - 1) / C);
   const bool write_o = (mode == 0) && out != nullptr;
+  const bool need_o = write_o || (mode == 0 && save.O != nullptr);
   __syncthreads();
 
   for (int jc = 0; jc < nchunks; ++jc) {
@@ -330,17 +334,19 @@ __global__ void __launch_bounds__(256) kda_state_simt(
     const int64_t t0 = ts + (int64_t)jc * C;
     const int len = (int)min((int64_t)C, ls - (int64_t)jc * C);
     const float *W = Wg + slab * C * DK, *Kd = Kdg + slab * C * DK;
+    if (mode == 0 && save.Sb)  // state entering chunk jc
+      for (int c = rt; c < DK; c += 8) save.Sb[(slab * DK + c) * DV + j0 + jt] = sS[c * LS + jt];
     for (int e = tid; e < C * DK; e += 256) {
       int r = e / DK, c = e % DK;
       sW[r * LK + c] = W[e];
       sKd[r * LK + c] = Kd[e];
-      if (write_o) sQ[r * LK + c] = Qg[slab * C * DK + e];
+      if (need_o) sQ[r * LK + c] = Qg[slab * C * DK + e];
     }
     for (int e = tid; e < C * BV; e += 256) {
       int r = e / BV, c = e % BV;
       sU[r * LS + c] = xpart ? 0.f : Ug[slab * C * DV + (size_t)r * DV + vcol0 + c];
     }
-    if (write_o)
+    if (need_o)
       for (int e = tid; e < C * C; e += 256) sP[(e / C) * LP + e % C] = Pg[slab * C * C + e];
     if (tid < DK) sD[tid] = Dg[slab * DK + tid];
     __syncthreads();
@@ -357,9 +363,12 @@ __global__ void __launch_bounds__(256) kda_state_simt(
     __syncthreads();
 #pragma unroll
     for (int m = 0; m < C / 8; ++m) sU[(rt + 8 * m) * LS + jt] = u[m];
+    if (mode == 0 && save.Ub)
+#pragma unroll
+      for (int m = 0; m < C / 8; ++m) save.Ub[(slab * C + rt + 8 * m) * DV + j0 + jt] = u[m];
     __syncthreads();
 
-    if (write_o) {
+    if (need_o) {
       // O = Qt S + P U
       float o[C / 8] = {};
       for (int c = 0; c < DK; ++c) {
@@ -372,7 +381,8 @@ __global__ void __launch_bounds__(256) kda_state_simt(
         const int r = rt + 8 * m;
         float acc = o[m];
         for (int i = 0; i <= r; ++i) acc = fmaf(sP[r * LP + i], sU[i * LS + jt], acc);
-        if (r < len) {
+        if (save.O) save.O[(slab * C + r) * DV + j0 + jt] = acc;
+        if (write_o && r < len) {
           size_t g = ((size_t)(t0 + r) * H + h) * DV + j0 + jt;
           float gv = gate ? to_f32(gate[g]) : 1.f;
           out[g] = from_f32<Tout>(scale * gv * acc);
@@ -425,7 +435,7 @@ template <int DK, int DV, typename Tin>
 cudaError_t launch_prep_t(const void *q, const void *k, const void *v, const void *la,
                           const void *beta, const int32_t *cu, int n_seq, int64_t T_total,
                           int H, unsigned flags, const ChunkWs &ws, bool need_q,
-                          cudaStream_t st) {
+                          cudaStream_t st, PrepSave save) {
   auto kern = kda_prep_simt<DK, DV, Tin>;
   constexpr size_t sm = prep_smem<DK, DV>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
@@ -435,7 +445,7 @@ cudaError_t launch_prep_t(const void *q, const void *k, const void *v, const voi
   kern<<<grid, 256, sm, st>>>((const Tin *)q, (const Tin *)k, (const Tin *)v, (const Tin *)la,
                               (const Tin *)beta, cu, n_seq, fixed_len, H, flags, ws.meta,
                               ws.seq_chunk_off, ws.W, ws.U, ws.Q, ws.Kd, ws.P, ws.D,
-                              need_q ? 1 : 0);
+                              need_q ? 1 : 0, save);
   return cudaGetLastError();
 }
 
@@ -443,7 +453,7 @@ template <int DK, int DV, typename Tout>
 cudaError_t launch_state_t(int mode, const void *gate, void *out, const float *S0,
                            float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                            int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
-                           cudaStream_t st, CkptOut ck) {
+                           cudaStream_t st, CkptOut ck, StateSave save) {
   auto kern = kda_state_simt<DK, DV, Tout>;
   constexpr size_t sm = state_smem<DK>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
@@ -453,7 +463,7 @@ cudaError_t launch_state_t(int mode, const void *gate, void *out, const float *S
   dim3 grid(n_seq * H, ncols / BV);
   kern<<<grid, 256, sm, st>>>(mode, (const Tout *)gate, (Tout *)out, S0, S_final, X_out, Z_out,
                               cu, n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.W,
-                              ws.U, ws.Q, ws.Kd, ws.P, ws.D, ck);
+                              ws.U, ws.Q, ws.Kd, ws.P, ws.D, ck, save);
   return cudaGetLastError();
 }
 
@@ -513,28 +523,31 @@ cudaError_t launch_chunk_table(const int32_t *cu, int n_seq, int64_t T_total, co
 cudaError_t launch_prep(const void *q, const void *k, const void *v, const void *la,
                         const void *beta, const int32_t *cu, int n_seq, int64_t T_total, int H,
                         int dk, int dv, unsigned flags, kda_dtype dt, const ChunkWs &ws,
-                        bool need_q, cudaStream_t st) {
+                        bool need_q, cudaStream_t st, PrepSave save) {
   if (dt == KDA_DTYPE_BF16) {
     KDA_DISPATCH_DKDV(dk, dv, return launch_prep_t<DK, DV, __nv_bfloat16>(
-                                  q, k, v, la, beta, cu, n_seq, T_total, H, flags, ws, need_q, st));
+                                  q, k, v, la, beta, cu, n_seq, T_total, H, flags, ws, need_q, st,
+                                  save));
   } else {
     KDA_DISPATCH_DKDV(dk, dv, return launch_prep_t<DK, DV, float>(
-                                  q, k, v, la, beta, cu, n_seq, T_total, H, flags, ws, need_q, st));
+                                  q, k, v, la, beta, cu, n_seq, T_total, H, flags, ws, need_q, st,
+                                  save));
   }
 }
 
 cudaError_t launch_state_pass(int mode, const void *gate, void *out, const float *S0,
                               float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                               int n_seq, int64_t T_total, int H, int dk, int dv, float scale,
-                              kda_dtype dt, const ChunkWs &ws, cudaStream_t st, CkptOut ck) {
+                              kda_dtype dt, const ChunkWs &ws, cudaStream_t st, CkptOut ck,
+                              StateSave save) {
   if (dt == KDA_DTYPE_BF16) {
     KDA_DISPATCH_DKDV(dk, dv, return launch_state_t<DK, DV, __nv_bfloat16>(
                                   mode, gate, out, S0, S_final, X_out, Z_out, cu, n_seq,
-                                  T_total, H, scale, ws, st, ck));
+                                  T_total, H, scale, ws, st, ck, save));
   } else {
     KDA_DISPATCH_DKDV(dk, dv, return launch_state_t<DK, DV, float>(
                                   mode, gate, out, S0, S_final, X_out, Z_out, cu, n_seq,
-                                  T_total, H, scale, ws, st, ck));
+                                  T_total, H, scale, ws, st, ck, save));
   }
 }
 

@@ -59,6 +59,19 @@ struct CkptOut {
   int per_seq = 0;       // slots per sequence
 };
 
+// Optional exports of the SIMT prep kernel, per (chunk, head) slab, fp32 (used by the
+// backward pass): K^ = k e^{-G} [64, dk], diag(b) K~ [64, dk], A = strict_lower(diag(b) K~ K^T)
+// [64, 64].
+struct PrepSave {
+  float *Kh = nullptr, *Bk = nullptr, *A = nullptr;
+};
+// Optional saves of the SIMT state pass (mode 0), per slab, fp32: the state entering the chunk
+// Sb [dk, dv], the corrected values U = U~ - W S [64, dv] and the chunk output before scale and
+// gate O = Q~ S + P U [64, dv].
+struct StateSave {
+  float *Sb = nullptr, *Ub = nullptr, *O = nullptr;
+};
+
 // Base of the [dk, dv] checkpoint written after chunk n (0-based) of sequence s, or null when
 // that chunk does not end on a checkpoint boundary inside the sequence.
 __device__ __forceinline__ float *ckpt_after_chunk(const CkptOut &ck, int s, int n, int64_t len,
@@ -92,14 +105,15 @@ cudaError_t launch_prep(const void *q, const void *k, const void *v,
                         const void *la, const void *beta, const int32_t *cu,
                         int n_seq, int64_t T_total, int H, int dk, int dv,
                         unsigned flags, kda_dtype dt, const ChunkWs &ws,
-                        bool need_q, cudaStream_t st);
+                        bool need_q, cudaStream_t st, PrepSave save = PrepSave());
 // mode 0: forward (out, final); mode 1: segment summary (X_out, Z_out)
 cudaError_t launch_state_pass(int mode, const void *gate, void *out,
                               const float *S0, float *S_final, float *X_out,
                               float *Z_out, const int32_t *cu, int n_seq,
                               int64_t T_total, int H, int dk, int dv,
                               float scale, kda_dtype dt, const ChunkWs &ws,
-                              cudaStream_t st, CkptOut ck = CkptOut());
+                              cudaStream_t st, CkptOut ck = CkptOut(),
+                              StateSave save = StateSave());
 cudaError_t launch_decode(const void *q, const void *k, const void *v,
                           const void *la, const void *beta, const void *gate,
                           void *out, float *state, const int32_t *slot,
@@ -122,6 +136,15 @@ cudaError_t launch_state_tc(int mode, const void *gate, void *out, const float *
                             int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
                             cudaStream_t st, CkptOut ck = CkptOut());
 cudaError_t tc_take_error(unsigned *bits);
+
+// chunked backward pass (kda_bwd.cu)
+size_t chunk_bwd_ws_bytes(int64_t T_total, int n_seq, int H, int dk, int dv);
+cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const void *la,
+                             const void *beta, const void *gate, const float *S0,
+                             const void *d_out, const float *dSf, void *dq, void *dk, void *dv,
+                             void *dla, void *dbeta, void *dgate, float *dS0, const int32_t *cu,
+                             int n_seq, int64_t T_total, int H, int dk_, int dv_, float scale,
+                             unsigned flags, kda_dtype dt, void *ws, cudaStream_t st);
 
 // Sets the calling thread's kda_last_error_string() message; returns `st`.
 kda_status api_fail(kda_status st, const char *fmt, ...);

@@ -102,6 +102,45 @@ def test_chunk_fwd_checkpoints_no_sequences_is_noop(lib):
                 out=None, ws=None) == B.KDA_OK
 
 
+def bwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, la=FAKE, beta=FAKE, gate=FAKE, s0=None, dout=FAKE,
+             dsf=None, dq=FAKE, dk_=FAKE, dv_=FAKE, dla=FAKE, db=FAKE, dg=FAKE, ds0=None,
+             cu=None, n_seq=1, T=128, H=2, dk=64, dv=64, chunk=64, scale=1.0, flags=1, dtype=1,
+             ws=FAKE, wsb=0, stream=None)
+    a.update(kw)
+    return lib.kda_chunk_bwd(a["q"], a["k"], a["v"], a["la"], a["beta"], a["gate"], a["s0"],
+                             a["dout"], a["dsf"], a["dq"], a["dk_"], a["dv_"], a["dla"], a["db"],
+                             a["dg"], a["ds0"], a["cu"], a["n_seq"], a["T"], a["H"], a["dk"],
+                             a["dv"], a["chunk"], a["scale"], a["flags"], a["dtype"], a["ws"],
+                             a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=32), B.KDA_ERR_UNSUPPORTED),
+    (dict(chunk=128), B.KDA_ERR_UNSUPPORTED),
+    (dict(T=-5), B.KDA_ERR_INVALID_ARG),
+    (dict(dout=None), B.KDA_ERR_INVALID_ARG),
+    (dict(dq=None), B.KDA_ERR_INVALID_ARG),
+    (dict(db=None), B.KDA_ERR_INVALID_ARG),
+    (dict(dla=ODD), B.KDA_ERR_INVALID_ARG),
+    (dict(gate=None), B.KDA_ERR_INVALID_ARG),   # d_gate without a gate
+    (dict(dsf=ODD), B.KDA_ERR_INVALID_ARG),
+    (dict(flags=8), B.KDA_ERR_INVALID_ARG),
+    (dict(ws=None), B.KDA_ERR_WORKSPACE),
+    (dict(wsb=1000), B.KDA_ERR_WORKSPACE),
+])
+def test_chunk_bwd_rejects(lib, kw, status):
+    assert bwd(lib, **kw) == status
+    assert B.kda_last_error_string() != ""
+
+
+def test_chunk_bwd_workspace_size(lib):
+    fw = B.kda_chunk_fwd_workspace_size(4096, 1, 16, 128, 128, dtype=B.KDA_DTYPE_F32)
+    bw = B.kda_chunk_bwd_workspace_size(4096, 1, 16, 128, 128)
+    assert bw > fw > 0
+    assert B.kda_chunk_bwd_workspace_size(4096, 1, 16, 96, 128) == 0
+
+
 def test_workspace_size(lib):
     s1 = B.kda_chunk_fwd_workspace_size(4096, 1, 16, 128, 128)
     s2 = B.kda_chunk_fwd_workspace_size(8192, 1, 16, 128, 128)
