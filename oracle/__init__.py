@@ -15,7 +15,9 @@ Two independent restatements of the same definition live here:
 
 ``autograd.py`` holds the backward oracle: the recurrence once more in PyTorch
 (fp64, CPU) and its gradients by torch.autograd, pinned to the C forward and to
-finite differences of ``brute.py``.
+finite differences of ``brute.py``. ``gates.py`` writes out the gate
+preparation (sigmoid of the beta and output-gate logits, the lower-bounded
+log-retention) used when the kernels take logits.
 
 Definition sources: K3 training overview (zuoshipin.com/article/18261) section
 2 "KDA" (channel-wise forget gate, delta-rule corrective write, full-rank

@@ -18,7 +18,7 @@ training overview (zuoshipin.com/article/18261) section 2 "KDA", K3 explainer
 gradients: section 4 "FlashKDA" of the training overview presents the chunked
 kernel as a training kernel. The derivatives come from torch.autograd; nothing
 here is hand-differentiated. The tests pin the forward to the C oracle and the
-gradients to central finite differences of the C oracle.
+gradients to central finite differences of the fp64 brute-force oracle.
 """
 from __future__ import annotations
 
@@ -59,21 +59,32 @@ def recurrence(q, k, v, log_alpha, beta, gate, S0, cu_seqlens, scale=1.0, l2norm
     return out, torch.stack(finals)
 
 
+def prepare_gates(beta, gate, log_alpha):
+    """Differentiable beta = sigmoid(x), g = sigmoid(y), log_alpha = max(-e^a, log 1/2)
+    (the definitions of oracle/gates.py) on torch tensors."""
+    la = torch.maximum(-torch.exp(log_alpha), torch.tensor(np.log(0.5), dtype=torch.float64))
+    return torch.sigmoid(beta), None if gate is None else torch.sigmoid(gate), la
+
+
 def backward(q, k, v, log_alpha, beta, gate, S0, cu_seqlens, d_out, d_final=None, scale=1.0,
-             l2norm=True):
+             l2norm=True, gate_logits=False):
     """Vector-Jacobian product of the forward with cotangents (d_out, d_final).
 
     Arrays in, float64 numpy arrays out: dict with dq, dk, dv, dlog_alpha, dbeta, dgate
     (None when gate is None) and dS0 (gradient of the initial state; zero-state runs
-    report the gradient at S0 = 0)."""
+    report the gradient at S0 = 0). gate_logits: beta, gate and log_alpha hold logits and
+    the forget gate's pre-activation (prepare_gates), and the gradients are theirs."""
     n_seq = len(cu_seqlens) - 1
     T, H, dk = np.shape(k)
     dv = np.shape(v)[-1]
     xs = {"q": _t(q), "k": _t(k), "v": _t(v), "log_alpha": _t(log_alpha), "beta": _t(beta)}
     xs["gate"] = None if gate is None else _t(gate)
     xs["S0"] = _t(np.zeros((n_seq, H, dk, dv)) if S0 is None else S0)
-    out, Sf = recurrence(xs["q"], xs["k"], xs["v"], xs["log_alpha"], xs["beta"], xs["gate"],
-                         xs["S0"], cu_seqlens, scale=scale, l2norm=l2norm)
+    b, g, la = xs["beta"], xs["gate"], xs["log_alpha"]
+    if gate_logits:
+        b, g, la = prepare_gates(b, g, la)
+    out, Sf = recurrence(xs["q"], xs["k"], xs["v"], la, b, g, xs["S0"], cu_seqlens, scale=scale,
+                         l2norm=l2norm)
     L = (out * torch.as_tensor(np.asarray(d_out, dtype=np.float64))).sum()
     if d_final is not None:
         L = L + (Sf * torch.as_tensor(np.asarray(d_final, dtype=np.float64))).sum()
