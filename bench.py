@@ -390,6 +390,7 @@ def run_gpu(args, rank, world, local):
         line["scan_combine"] = bench_scan(dev, pk, stream)
         line["prefill_checkpoints"] = bench_checkpoints(dev, pk, stream)
         line["backward"] = bench_backward(dev, pk, stream)
+        line["gate_prep"] = bench_gates(dev, pk, stream)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
@@ -582,6 +583,57 @@ def bench_backward(dev, pk, stream, reps=5):
             "workspace_bytes": ws.numel(), "gpu_launches": 14 * reps}
 
 
+def bench_gates(dev, pk, stream, reps=20):
+    """The prefill workload taking gate logits: kda_chunk_fwd with KDA_GATE_LOGITS (the
+    sigmoids and the log-retention bound applied as the kernels load their inputs),
+    timed beside an element-wise pre-pass (torch) followed by the plain call."""
+    import linear_attention_05_gb300 as kda
+    from linear_attention_05_gb300 import inputs
+
+    w = inputs.WORKLOADS["prefill"]
+    x = inputs.make(w, device=dev)
+    T, H, d, n_seq = w.T_total, w.H, w.dk, len(w.lengths)
+    g = torch.Generator(device=dev).manual_seed(5)
+    raw = {"a": (torch.randn((T, H, d), generator=g, device=dev) - 3.0).to(torch.bfloat16),
+           "bx": torch.randn((T, H), generator=g, device=dev).to(torch.bfloat16),
+           "gx": torch.randn((T, H, d), generator=g, device=dev).to(torch.bfloat16)}
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((n_seq, H, d, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(kda.kda_chunk_fwd_workspace_size(T, n_seq, H, d, d), dtype=torch.uint8,
+                     device=dev)
+    half = float(np.log(0.5))
+
+    def fused():
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], raw["a"], raw["bx"], raw["gx"], out, x["S0"],
+                          fs, None, n_seq, flags=kda.KDA_QK_L2NORM | kda.KDA_GATE_LOGITS,
+                          workspace=ws, stream=stream)
+
+    def unfused():
+        la = torch.clamp_min(-torch.exp(raw["a"].float()), half).to(torch.bfloat16)
+        b = torch.sigmoid(raw["bx"].float()).to(torch.bfloat16)
+        gt = torch.sigmoid(raw["gx"].float()).to(torch.bfloat16)
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], la, b, gt, out, x["S0"], fs, None, n_seq,
+                          workspace=ws, stream=stream)
+
+    ms = {}
+    for name, fn in (("fused", fused), ("unfused", unfused)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms[name] = e0.elapsed_time(e1) / reps
+    return {"workload": "prefill B=4 T=4096 H=16 dk=dv=128 bf16 with beta/gate logits and the "
+                        "forget-gate pre-activation",
+            "value": round(T / (ms["fused"] * 1e-3) / 1e6, 3), "unit": "Mtok/s",
+            "ms": round(ms["fused"], 4), "ms_prepass_then_plain": round(ms["unfused"], 4),
+            "gpu_launches": 3 * reps}
+
+
 def bench_scan(dev, pk, stream, reps=20):
     """kda_scan_combine alone on long-context-sized summaries (8 segments x 16 heads)."""
     import linear_attention_05_gb300 as kda
@@ -616,7 +668,7 @@ def run_part(args, local):
     pk = peaks()
     stream = torch.cuda.current_stream()
     fn = {"decode": bench_decode, "segscan": bench_segment_scan, "scan": bench_scan,
-          "ckpt": bench_checkpoints, "bwd": bench_backward}[args.only]
+          "ckpt": bench_checkpoints, "bwd": bench_backward, "gates": bench_gates}[args.only]
     print(json.dumps({"part": args.only, **fn(dev, pk, stream)}), flush=True)
 
 
@@ -630,7 +682,7 @@ def main():
                     help="reference arm: tokens per sequence timed per step")
     ap.add_argument("--skip-extra", action="store_true", help="prefill line only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", default=None, choices=["decode", "segscan", "scan", "ckpt", "bwd"],
+    ap.add_argument("--only", default=None, choices=["decode", "segscan", "scan", "ckpt", "bwd", "gates"],
                     help="run one part of the path alone and print its numbers (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:

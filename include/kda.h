@@ -64,8 +64,18 @@ typedef enum {
 typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 
 enum {
-  KDA_QK_L2NORM = 1u,  /* normalise q and k rows: x / sqrt(sum x^2 + 1e-6) */
-  KDA_DEBUG_CHECK = 2u /* check log_alpha >= -0.6953125 and beta in [0,1] on device */
+  KDA_QK_L2NORM = 1u,   /* normalise q and k rows: x / sqrt(sum x^2 + 1e-6) */
+  KDA_DEBUG_CHECK = 2u, /* check log_alpha >= -0.6953125 and beta in [0,1] on device */
+  /* Gate preparation fused into the kernels (K3 training overview section 2
+   * "KDA": channel-wise forget gate with a lower bound on the per-step
+   * retention, output gate; section 4 "FlashKDA": the forget gate is part of
+   * the per-chunk update card). With this flag, `beta` and `gate` hold logits
+   * and `log_alpha` holds the forget gate's pre-activation a; the kernels use
+   *     beta = sigmoid(beta),  g = sigmoid(gate),
+   *     log_alpha = max(-exp(a), log(1/2))      (so alpha >= 1/2)
+   * as they load them, saving one element-wise pass over those inputs.
+   * kda_chunk_bwd then returns gradients with respect to the logits and a. */
+  KDA_GATE_LOGITS = 4u
 };
 
 /* Library version string, e.g. "libkda 0.1 sm_103a". */

@@ -4,7 +4,8 @@ The compute lives in ``libkda.so`` (hand-written CUDA behind a C ABI,
 ``include/kda.h``); ``binding`` exposes its entry points to Python under the
 same names. ``inputs`` draws seeded synthetic workloads.
 """
-from .binding import (KDA_DEBUG_CHECK, KDA_DTYPE_BF16, KDA_DTYPE_F32, KDA_QK_L2NORM, KdaError,
+from .binding import (KDA_DEBUG_CHECK, KDA_DTYPE_BF16, KDA_DTYPE_F32, KDA_GATE_LOGITS,
+                      KDA_QK_L2NORM, KdaError,
                       chunk_bwd, chunk_fwd, chunk_fwd_checkpoints, decode_step, kda_chunk_bwd,
                       kda_chunk_bwd_workspace_size, kda_chunk_fwd,
                       kda_chunk_fwd_checkpoints, kda_chunk_fwd_noalloc,

@@ -33,6 +33,7 @@ KDA_DTYPE_F32 = 0
 KDA_DTYPE_BF16 = 1
 KDA_QK_L2NORM = 1
 KDA_DEBUG_CHECK = 2
+KDA_GATE_LOGITS = 4
 CHUNK = 64
 
 _lock = threading.Lock()
@@ -338,9 +339,13 @@ def kda_selftest_umma(A, B, D, a_mn_major=0, b_mn_major=0, stream=None):
 
 
 # ----------------------------------------------------------------------------- conveniences
+def _flags(l2norm, gate_logits):
+    return (KDA_QK_L2NORM if l2norm else 0) | (KDA_GATE_LOGITS if gate_logits else 0)
+
+
 def chunk_fwd(q, k, v, log_alpha, beta, gate=None, initial_state=None, cu_seqlens=None,
               n_seq=None, scale=1.0, l2norm=True, output_final_state=True, workspace=None,
-              stream=None):
+              stream=None, gate_logits=False):
     """Allocate the outputs with torch and call kda_chunk_fwd."""
     T, H, dk = k.shape
     dv = v.shape[-1]
@@ -350,7 +355,7 @@ def chunk_fwd(q, k, v, log_alpha, beta, gate=None, initial_state=None, cu_seqlen
     fs = (torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=v.device)
           if output_final_state else None)
     kda_chunk_fwd(q, k, v, log_alpha, beta, gate, out, initial_state, fs, cu_seqlens, n_seq,
-                  scale=scale, flags=KDA_QK_L2NORM if l2norm else 0, workspace=workspace,
+                  scale=scale, flags=_flags(l2norm, gate_logits), workspace=workspace,
                   stream=stream)
     return out, fs
 
@@ -358,7 +363,7 @@ def chunk_fwd(q, k, v, log_alpha, beta, gate=None, initial_state=None, cu_seqlen
 def chunk_fwd_checkpoints(q, k, v, log_alpha, beta, gate=None, initial_state=None,
                           cu_seqlens=None, n_seq=None, checkpoint_every=1024,
                           checkpoints_per_seq=None, scale=1.0, l2norm=True, workspace=None,
-                          stream=None):
+                          stream=None, gate_logits=False):
     """Allocate the outputs and call kda_chunk_fwd_checkpoints.
 
     Returns (out, final_state, checkpoints); checkpoints[s, i] is the state of sequence s
@@ -381,12 +386,13 @@ def chunk_fwd_checkpoints(q, k, v, log_alpha, beta, gate=None, initial_state=Non
     return kda_chunk_fwd_checkpoints(q, k, v, log_alpha, beta, gate, out, initial_state, fs,
                                      ck if checkpoints_per_seq > 0 else None, checkpoint_every,
                                      cu_seqlens, n_seq, scale=scale,
-                                     flags=KDA_QK_L2NORM if l2norm else 0, workspace=workspace,
+                                     flags=_flags(l2norm, gate_logits), workspace=workspace,
                                      stream=stream)[:2] + (ck,)
 
 
 def chunk_bwd(q, k, v, log_alpha, beta, gate, initial_state, d_out, d_final_state=None,
-              cu_seqlens=None, n_seq=None, scale=1.0, l2norm=True, workspace=None, stream=None):
+              cu_seqlens=None, n_seq=None, scale=1.0, l2norm=True, workspace=None, stream=None,
+              gate_logits=False):
     """Allocate the gradients and call kda_chunk_bwd. Returns a dict with dq, dk, dv,
     dlog_alpha, dbeta, dgate (None without a gate) and dS0 (fp32)."""
     T, H, dk = k.shape
@@ -399,26 +405,27 @@ def chunk_bwd(q, k, v, log_alpha, beta, gate, initial_state, d_out, d_final_stat
          "dS0": torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=k.device)}
     kda_chunk_bwd(q, k, v, log_alpha, beta, gate, initial_state, d_out, d_final_state, g["dq"],
                   g["dk"], g["dv"], g["dlog_alpha"], g["dbeta"], g["dgate"], g["dS0"],
-                  cu_seqlens, n_seq, scale=scale, flags=KDA_QK_L2NORM if l2norm else 0,
+                  cu_seqlens, n_seq, scale=scale, flags=_flags(l2norm, gate_logits),
                   workspace=workspace, stream=stream)
     return g
 
 
 def decode_step(q, k, v, log_alpha, beta, gate, state, state_slot=None, scale=1.0, l2norm=True,
-                stream=None):
+                stream=None, gate_logits=False):
     out = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     return kda_decode_step(q, k, v, log_alpha, beta, gate, out, state, state_slot, scale,
-                           KDA_QK_L2NORM if l2norm else 0, stream)
+                           _flags(l2norm, gate_logits), stream)
 
 
-def segment_summary(k, v, log_alpha, beta, cu_segs, l2norm=True, workspace=None, stream=None):
+def segment_summary(k, v, log_alpha, beta, cu_segs, l2norm=True, workspace=None, stream=None,
+                    gate_logits=False):
     n_seg = cu_segs.numel() - 1
     T, H, dk = k.shape
     dv = v.shape[-1]
     X = torch.empty((n_seg, H, dk, dk), dtype=torch.float32, device=k.device)
     Z = torch.empty((n_seg, H, dk, dv), dtype=torch.float32, device=k.device)
     return kda_segment_summary(k, v, log_alpha, beta, cu_segs, n_seg, X, Z,
-                               KDA_QK_L2NORM if l2norm else 0, workspace, stream)
+                               _flags(l2norm, gate_logits), workspace, stream)
 
 
 def scan_combine(X, Z, S_init=None, stream=None):

@@ -102,6 +102,8 @@ kda_status api_fail(kda_status st, const char *fmt, ...) {
 }
 }  // namespace kda
 
+constexpr unsigned kKnownFlags = KDA_QK_L2NORM | KDA_DEBUG_CHECK | KDA_GATE_LOGITS;
+
 extern "C" {
 
 const char *kda_version(void) { return "libkda 0.1 sm_103a"; }
@@ -133,7 +135,7 @@ static kda_status chunk_fwd_impl(const void *q, const void *k, const void *v,
                                  size_t workspace_bytes, kda_stream_t stream) {
   kda_status st = common_checks(T_total, n_seq, H, dk, dv, chunk, dtype, cu_seqlens);
   if (st != KDA_OK) return st;
-  KDA_REQUIRE((flags & ~(unsigned)(KDA_QK_L2NORM | KDA_DEBUG_CHECK)) == 0, KDA_ERR_INVALID_ARG,
+  KDA_REQUIRE((flags & ~kKnownFlags) == 0, KDA_ERR_INVALID_ARG,
               "unknown flag bits 0x%x", flags);
   const bool tokens = T_total > 0;
   KDA_CHECK_PTR(q, tokens);
@@ -172,10 +174,10 @@ static kda_status chunk_fwd_impl(const void *q, const void *k, const void *v,
                    "chunk prep");
   if (st != KDA_OK) return st;
   return cuda_status(tr([&] {
-                       return tc ? kda::launch_state_tc(0, gate, out, initial_state, final_state,
+                       return tc ? kda::launch_state_tc(0, flags, gate, out, initial_state, final_state,
                                                         nullptr, nullptr, cu_seqlens, n_seq,
                                                         T_total, H, scale, ws, s, ck)
-                                 : kda::launch_state_pass(0, gate, out, initial_state,
+                                 : kda::launch_state_pass(0, flags, gate, out, initial_state,
                                                           final_state, nullptr, nullptr,
                                                           cu_seqlens, n_seq, T_total, H, dk, dv,
                                                           scale, dtype, ws, s, ck);
@@ -238,7 +240,7 @@ kda_status kda_chunk_bwd(const void *q, const void *k, const void *v, const void
                          size_t workspace_bytes, kda_stream_t stream) {
   kda_status st = common_checks(T_total, n_seq, H, dk, dv, chunk, dtype, cu_seqlens);
   if (st != KDA_OK) return st;
-  KDA_REQUIRE((flags & ~(unsigned)(KDA_QK_L2NORM | KDA_DEBUG_CHECK)) == 0, KDA_ERR_INVALID_ARG,
+  KDA_REQUIRE((flags & ~kKnownFlags) == 0, KDA_ERR_INVALID_ARG,
               "unknown flag bits 0x%x", flags);
   const bool tokens = T_total > 0;
   KDA_CHECK_PTR(q, tokens);
@@ -288,7 +290,7 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const vo
   KDA_REQUIRE(dtype == KDA_DTYPE_F32 || dtype == KDA_DTYPE_BF16, KDA_ERR_UNSUPPORTED,
               "dtype %d not supported", (int)dtype);
   KDA_REQUIRE(shape_ok(dk, dv), KDA_ERR_UNSUPPORTED, "dk=%d dv=%d: only 64 or 128", dk, dv);
-  KDA_REQUIRE((flags & ~(unsigned)(KDA_QK_L2NORM | KDA_DEBUG_CHECK)) == 0, KDA_ERR_INVALID_ARG,
+  KDA_REQUIRE((flags & ~kKnownFlags) == 0, KDA_ERR_INVALID_ARG,
               "unknown flag bits 0x%x", flags);
   KDA_REQUIRE((int64_t)N * H < (int64_t)INT32_MAX, KDA_ERR_UNSUPPORTED, "N*H too large");
   if (N == 0) return KDA_OK;
@@ -320,7 +322,7 @@ kda_status kda_segment_summary(const void *k, const void *v, const void *log_alp
                                size_t workspace_bytes, kda_stream_t stream) {
   kda_status st = common_checks(T_total, n_seg, H, dk, dv, chunk, dtype, cu_segs);
   if (st != KDA_OK) return st;
-  KDA_REQUIRE((flags & ~(unsigned)(KDA_QK_L2NORM | KDA_DEBUG_CHECK)) == 0, KDA_ERR_INVALID_ARG,
+  KDA_REQUIRE((flags & ~kKnownFlags) == 0, KDA_ERR_INVALID_ARG,
               "unknown flag bits 0x%x", flags);
   const bool tokens = T_total > 0;
   KDA_CHECK_PTR(k, tokens);
@@ -355,10 +357,10 @@ kda_status kda_segment_summary(const void *k, const void *v, const void *log_alp
                    "chunk prep");
   if (st != KDA_OK) return st;
   return cuda_status(tr([&] {
-                       return tc ? kda::launch_state_tc(1, nullptr, nullptr, nullptr, nullptr,
+                       return tc ? kda::launch_state_tc(1, flags, nullptr, nullptr, nullptr, nullptr,
                                                         X_out, Z_out, cu_segs, n_seg, T_total, H,
                                                         1.0f, ws, s)
-                                 : kda::launch_state_pass(1, nullptr, nullptr, nullptr, nullptr,
+                                 : kda::launch_state_pass(1, flags, nullptr, nullptr, nullptr, nullptr,
                                                           X_out, Z_out, cu_segs, n_seg, T_total,
                                                           H, dk, dv, 1.0f, dtype, ws, s);
                      }),

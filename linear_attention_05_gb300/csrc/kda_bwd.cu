@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(256) kda_bwd_dO(const Tin *__restrict__ d_out,
                                                   const Tin *__restrict__ gate,
                                                   const int32_t *__restrict__ cu, int n_seq,
                                                   int64_t fixed_len, int H, float scale,
+                                                  unsigned flags,
                                                   const ChunkMeta *__restrict__ meta,
                                                   const int *__restrict__ off,
                                                   float *__restrict__ dO) {
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(256) kda_bwd_dO(const Tin *__restrict__ d_out,
     float x = 0.f;
     if (r < len) {
       const size_t g = ((size_t)(t0 + r) * H + h) * DV + j;
-      x = scale * bf(d_out[g]) * (gate ? bf(gate[g]) : 1.f);
+      x = scale * bf(d_out[g]) * (gate ? prep_gate(bf(gate[g]), flags) : 1.f);
     }
     dst[e] = x;
   }
@@ -311,8 +312,8 @@ __global__ void __launch_bounds__(256) kda_bwd_solve(const float *__restrict__ A
 template <int DK, int DV, typename Tio>
 __global__ void __launch_bounds__(256) kda_bwd_finish(
     const Tio *__restrict__ q, const Tio *__restrict__ k, const Tio *__restrict__ v,
-    const Tio *__restrict__ la, const Tio *__restrict__ beta, const Tio *__restrict__ d_out,
-    Tio *__restrict__ dq, Tio *__restrict__ dk, Tio *__restrict__ dv, Tio *__restrict__ dla,
+    const Tio *__restrict__ la, const Tio *__restrict__ beta, const Tio *__restrict__ gate,
+    const Tio *__restrict__ d_out, Tio *__restrict__ dq, Tio *__restrict__ dk, Tio *__restrict__ dv, Tio *__restrict__ dla,
     Tio *__restrict__ dbeta, Tio *__restrict__ dgate, const int32_t *__restrict__ cu, int n_seq,
     int64_t fixed_len, int H, float scale, unsigned flags, const ChunkMeta *__restrict__ meta,
     const int *__restrict__ off, const float *__restrict__ Yg, const float *__restrict__ dBkg,
@@ -336,12 +337,13 @@ __global__ void __launch_bounds__(256) kda_bwd_finish(
   const size_t slab = (size_t)ci * H + h;
   const bool l2 = (flags & KDA_QK_L2NORM) != 0;
 
-  if (tid < C) sB[tid] = tid < len ? bf(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+  const bool logits = (flags & KDA_GATE_LOGITS) != 0;
+  if (tid < C) sB[tid] = tid < len ? prep_beta(bf(beta[(size_t)(t0 + tid) * H + h]), flags) : 0.f;
   if (tid < DK) {
     const int c = tid;
     float G = 0.f;
     for (int r = 0; r < C; ++r) {
-      if (r < len) G += bf(la[((size_t)(t0 + r) * H + h) * DK + c]);
+      if (r < len) G += prep_log_alpha(bf(la[((size_t)(t0 + r) * H + h) * DK + c]), flags);
       sG[r * LK + c] = G;
     }
     sDc[c] = expf(G);
@@ -428,9 +430,17 @@ __global__ void __launch_bounds__(256) kda_bwd_finish(
       const float g = dBvg[rowv + j];
       dbv = fmaf(bf(v[tok * DV + j]), g, dbv);
       dv[tok * DV + j] = to_out<Tio>(b * g);
-      if (dgate) dgate[tok * DV + j] = to_out<Tio>(scale * bf(d_out[tok * DV + j]) * Og[rowv + j]);
+      if (dgate) {
+        float dg = scale * bf(d_out[tok * DV + j]) * Og[rowv + j];
+        if (logits) {  // d sigmoid(x) / dx = s (1 - s)
+          const float gs = sigmoid_f(bf(gate[tok * DV + j]));
+          dg *= gs * (1.f - gs);
+        }
+        dgate[tok * DV + j] = to_out<Tio>(dg);
+      }
     }
-    const float db = wsum(dbk) + wsum(dbv);
+    float db = wsum(dbk) + wsum(dbv);
+    if (logits) db *= b * (1.f - b);
     if (lane == 0) dbeta[tok] = to_out<Tio>(db);
   }
 #pragma unroll
@@ -445,7 +455,15 @@ __global__ void __launch_bounds__(256) kda_bwd_finish(
     float acc = 0.f;
     for (int r = C - 1; r >= 0; --r) {
       acc += sdG[r * LK + c];
-      if (r < len) dla[((size_t)(t0 + r) * H + h) * DK + c] = to_out<Tio>(acc + dGC);
+      if (r < len) {
+        const size_t gi = ((size_t)(t0 + r) * H + h) * DK + c;
+        float d = acc + dGC;
+        if (logits) {  // log_alpha = max(-e^a, log 1/2): slope -e^a above the bound, 0 on it
+          const float e = -expf(bf(la[gi]));
+          d = e > kLogHalf ? d * e : 0.f;
+        }
+        dla[gi] = to_out<Tio>(d);
+      }
     }
   }
 }
@@ -539,10 +557,10 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
                       ps));
   StateSave ss;
   ss.Sb = w.Sb; ss.Ub = w.Ub; ss.O = w.O;
-  KDA_TRY(launch_state_pass(0, nullptr, nullptr, S0, nullptr, nullptr, nullptr, cu, n_seq,
+  KDA_TRY(launch_state_pass(0, flags, nullptr, nullptr, S0, nullptr, nullptr, nullptr, cu, n_seq,
                             T_total, H, DK, DV, scale, dt, fw, st, CkptOut(), ss));
   kda_bwd_dO<DV, Tio><<<dim3(mc, H), 256, 0, st>>>((const Tio *)d_out, (const Tio *)gate, cu,
-                                                   n_seq, fixed_len, H, scale, fw.meta,
+                                                   n_seq, fixed_len, H, scale, flags, fw.meta,
                                                    fw.seq_chunk_off, w.dO);
   KDA_TRY(cudaGetLastError());
   {
@@ -600,7 +618,7 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
     KDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
     kern<<<dim3(mc, H), 256, sm, st>>>(
         (const Tio *)q, (const Tio *)k, (const Tio *)v, (const Tio *)la, (const Tio *)beta,
-        (const Tio *)d_out, (Tio *)dq, (Tio *)dk, (Tio *)dv, (Tio *)dla, (Tio *)dbeta,
+        (const Tio *)gate, (const Tio *)d_out, (Tio *)dq, (Tio *)dk, (Tio *)dv, (Tio *)dla, (Tio *)dbeta,
         gate ? (Tio *)dgate : nullptr, cu, n_seq, fixed_len, H, scale, flags, fw.meta,
         fw.seq_chunk_off, w.Y, w.dW, w.dU, w.dKh, w.dQt, w.dKd, w.Sb, w.dSb, w.O);
     KDA_TRY(cudaGetLastError());

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(256) kda_prep_simt(
       size_t g = ((size_t)(t0 + r) * H + h) * DK + c;
       kv = to_f32(k[g]);
       qv = to_f32(q[g]);
-      lv = to_f32(la[g]);
+      lv = prep_log_alpha(to_f32(la[g]), flags);
       if ((flags & KDA_DEBUG_CHECK) && !(lv >= kLogAlphaMin && lv <= 0.f)) set_err(kErrPrecondition);
     }
     sKh[r * LK + c] = kv;
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(256) kda_prep_simt(
     sV[r * LV + c] = r < len ? to_f32(v[((size_t)(t0 + r) * H + h) * DV + c]) : 0.f;
   }
   if (tid < C) {
-    float b = tid < len ? to_f32(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+    float b = tid < len ? prep_beta(to_f32(beta[(size_t)(t0 + tid) * H + h]), flags) : 0.f;
     if ((flags & KDA_DEBUG_CHECK) && tid < len && !(b >= 0.f && b <= 1.f)) set_err(kErrPrecondition);
     sB[tid] = b;
   }
@@ -285,7 +285,7 @@ constexpr int BV = 32;
 
 template <int DK, int DV, typename Tout>
 __global__ void __launch_bounds__(256) kda_state_simt(
-    int mode, const Tout *__restrict__ gate, Tout *__restrict__ out,
+    int mode, unsigned flags, const Tout *__restrict__ gate, Tout *__restrict__ out,
     const float *__restrict__ S0, float *__restrict__ S_final, float *__restrict__ X_out,
     float *__restrict__ Z_out, const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len,
     int H, float scale, const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(256) kda_state_simt(
         if (save.O) save.O[(slab * C + r) * DV + j0 + jt] = acc;
         if (write_o && r < len) {
           size_t g = ((size_t)(t0 + r) * H + h) * DV + j0 + jt;
-          float gv = gate ? to_f32(gate[g]) : 1.f;
+          float gv = gate ? prep_gate(to_f32(gate[g]), flags) : 1.f;
           out[g] = from_f32<Tout>(scale * gv * acc);
         }
       }
@@ -450,7 +450,7 @@ cudaError_t launch_prep_t(const void *q, const void *k, const void *v, const voi
 }
 
 template <int DK, int DV, typename Tout>
-cudaError_t launch_state_t(int mode, const void *gate, void *out, const float *S0,
+cudaError_t launch_state_t(int mode, unsigned flags, const void *gate, void *out, const float *S0,
                            float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                            int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
                            cudaStream_t st, CkptOut ck, StateSave save) {
@@ -461,7 +461,7 @@ cudaError_t launch_state_t(int mode, const void *gate, void *out, const float *S
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
   const int ncols = mode == 0 ? DV : DK + DV;
   dim3 grid(n_seq * H, ncols / BV);
-  kern<<<grid, 256, sm, st>>>(mode, (const Tout *)gate, (Tout *)out, S0, S_final, X_out, Z_out,
+  kern<<<grid, 256, sm, st>>>(mode, flags, (const Tout *)gate, (Tout *)out, S0, S_final, X_out, Z_out,
                               cu, n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.W,
                               ws.U, ws.Q, ws.Kd, ws.P, ws.D, ck, save);
   return cudaGetLastError();
@@ -535,18 +535,18 @@ cudaError_t launch_prep(const void *q, const void *k, const void *v, const void 
   }
 }
 
-cudaError_t launch_state_pass(int mode, const void *gate, void *out, const float *S0,
+cudaError_t launch_state_pass(int mode, unsigned flags, const void *gate, void *out, const float *S0,
                               float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                               int n_seq, int64_t T_total, int H, int dk, int dv, float scale,
                               kda_dtype dt, const ChunkWs &ws, cudaStream_t st, CkptOut ck,
                               StateSave save) {
   if (dt == KDA_DTYPE_BF16) {
     KDA_DISPATCH_DKDV(dk, dv, return launch_state_t<DK, DV, __nv_bfloat16>(
-                                  mode, gate, out, S0, S_final, X_out, Z_out, cu, n_seq,
+                                  mode, flags, gate, out, S0, S_final, X_out, Z_out, cu, n_seq,
                                   T_total, H, scale, ws, st, ck, save));
   } else {
     KDA_DISPATCH_DKDV(dk, dv, return launch_state_t<DK, DV, float>(
-                                  mode, gate, out, S0, S_final, X_out, Z_out, cu, n_seq,
+                                  mode, flags, gate, out, S0, S_final, X_out, Z_out, cu, n_seq,
                                   T_total, H, scale, ws, st, ck, save));
   }
 }

@@ -55,8 +55,8 @@ constexpr int B_NSTAGE = 3;            // card ring depth
 constexpr int B_STAGE_TX = CARD_BCT + 512;  // [Phi'^T | Q'^T] then e^{G_C} (49664 bytes)
 constexpr int B_STAGE_BYTES = 50176;  // B_STAGE_TX rounded up to 1024
 constexpr int B_SA = B_NSTAGE * B_STAGE_BYTES;  // S^T bf16 operand, 128 x 128 K-major (32768)
-constexpr int B_OT = B_SA + 32768;         // output transposes: 4 warps x 32 x 33 fp32
-constexpr int B_DYN = B_OT + 4 * 32 * 33 * 4 + 1024;
+constexpr int B_OT = B_SA + 32768;         // output transposes: 4 warps x 2 x 32 x 33 fp32
+constexpr int B_DYN = B_OT + 4 * 2 * 32 * 33 * 4 + 1024;
 
 __device__ __forceinline__ void set_err(unsigned bits) { atomicOr(&g_tc_err, bits); }
 
@@ -171,7 +171,8 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
     tmem_relinquish();
   }
   if (tid < C) {
-    const float b = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+    float b = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * H + h]) : 0.f;
+    if (tid < len && (flags & KDA_GATE_LOGITS)) b = __frcp_rn(1.f + __expf(-b));  // sigmoid
     if (dbg && tid < len && !(b >= 0.f && b <= 1.f)) set_err(kErrPrecondition);
     s_b[tid] = b;
   }
@@ -202,7 +203,10 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
       for (int u = 0; u < 8; ++u) {
         ssk[i] = fmaf(kk[u], kk[u], ssk[i]);
         ssq[i] = fmaf(qq[u], qq[u], ssq[i]);
-        if (r >= len) la8[i][u] = 0.f;
+        // with gate logits: log(alpha) = max(-e^a, log 1/2)
+        la8[i][u] = r >= len ? 0.f
+                    : (flags & KDA_GATE_LOGITS) ? fmaxf(-__expf(la8[i][u]), kLogHalf)
+                                                : la8[i][u];
         if (dbg && r < len && !(la8[i][u] >= kLogAlphaMin && la8[i][u] <= 0.f))
           set_err(kErrPrecondition);
         tot[u] += la8[i][u];
@@ -523,7 +527,8 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
 // group); bar_ofull[2] output block written (output group); bar_ofree[2]
 // output block read and re-zeroed (MMA issuer).
 __global__ void __launch_bounds__(384, 1) kda_state_tc(
-    int mode, const __nv_bfloat16 *__restrict__ gate, __nv_bfloat16 *__restrict__ out,
+    int mode, unsigned flags, const __nv_bfloat16 *__restrict__ gate,
+    __nv_bfloat16 *__restrict__ out,
     const float *__restrict__ S0, float *__restrict__ S_final, float *__restrict__ X_out,
     float *__restrict__ Z_out, const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len,
     int H, float scale, const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
@@ -746,82 +751,111 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
     }
   } else if (with_o) {
     // output group: o = scale * g * (Q' S + O_intra) for chunk n. Each warp owns 32 value
-    // channels (its lane quadrant); it transposes each 32 x 32 (channel x token) block
-    // through shared memory so that gate loads and output stores are 16-byte vectors.
-    float *ot = reinterpret_cast<float *>(sm + B_OT) + quad * 32 * 33;
+    // channels (its lane quadrant). The output block of chunk n starts as O_intra^T (seeded
+    // two chunks ahead from the card), so the MMA leaves Q' S + O_intra in it. Each 32 x 32
+    // (channel x token) half is transposed through shared memory so that gate loads and output
+    // stores are 16-byte vectors; the gate is prefetched one chunk ahead.
+    float *ot = reinterpret_cast<float *>(sm + B_OT) + quad * 2 * 32 * 33;
     const int jc = quad * 32;  // first channel of this warp
-    float zero[32];
+    const bool logits = gate && (flags & KDA_GATE_LOGITS);
+    // this lane's O_intra^T row (all 64 tokens, bf16) of chunk c, from the card
+    auto load_oi = [&](int c, uint4 *oi) {
+      const uint8_t *card = card_of(c);
 #pragma unroll
-    for (int u = 0; u < 32; ++u) zero[u] = 0.f;
-    // both output blocks start at zero
+      for (int ch = 0; ch < 8; ++ch)
+        oi[ch] = c < nchunks ? *reinterpret_cast<const uint4 *>(card + CARD_OIT + (ch * 128 + j) * 16)
+                             : make_uint4(0u, 0u, 0u, 0u);
+    };
+    auto seed = [&](int c, const uint4 *oi) {
 #pragma unroll
-    for (int b = 0; b < 2; ++b)
+      for (int hf = 0; hf < 2; ++hf) {
+        float x[32];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) tmem_st32(tmem_addr(tb, quad * 32, 256 * b + 128 + 32 * hf), zero);
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(&bar_ofree[0]);
-    mbar_arrive(&bar_ofree[1]);
-    uint32_t ofull_phase[2] = {0u, 0u};
-    for (int n = 0; n < nchunks; ++n) {
-      const int64_t t0 = ts + (int64_t)n * C;
-      const int len = (int)min((int64_t)C, ls - (int64_t)n * C);
-      uint4 gq[2][4];  // gate of token (hf * 32 + lane), channels jc + 8i .. +8
+        for (int ch = 0; ch < 4; ++ch) unpack8(oi[hf * 4 + ch], x + ch * 8);
+        tmem_st32(tmem_addr(tb, quad * 32, set_col(c) + 128 + 32 * hf), x);
+      }
+    };
+    // gate of token (hf * 32 + lane) of chunk c, channels jc + 8i .. +8 (1.0 when absent)
+    auto load_gate = [&](int c, uint4 (*gq)[4]) {
+      const int64_t tc0 = ts + (int64_t)c * C;
+      const int lc = (int)min((int64_t)C, ls - (int64_t)c * C);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int r = hf * 32 + lane;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          gq[hf][i] = (gate && r < len)
+          gq[hf][i] = (gate && c < nchunks && r < lc)
                           ? *reinterpret_cast<const uint4 *>(
-                                gate + ((size_t)(t0 + r) * H + h) * DD + jc + 8 * i)
+                                gate + ((size_t)(tc0 + r) * H + h) * DD + jc + 8 * i)
                           : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
       }
+    };
+    {
       uint4 oi[8];
-      const uint8_t *card = card_of(n);
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        oi[ch] = *reinterpret_cast<const uint4 *>(card + CARD_OIT + (ch * 128 + j) * 16);
+      for (int b = 0; b < 2; ++b) {
+        load_oi(b, oi);
+        seed(b, oi);
+      }
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&bar_ofree[0]);
+    mbar_arrive(&bar_ofree[1]);
+    uint32_t ofull_phase[2] = {0u, 0u};
+    uint4 gcur[2][4], gnext[2][4];
+    load_gate(0, gcur);
+    for (int n = 0; n < nchunks; ++n) {
+      const int64_t t0 = ts + (int64_t)n * C;
+      const int len = (int)min((int64_t)C, ls - (int64_t)n * C);
+      // loads for later chunks first, so that their latency overlaps this chunk's work
+      uint4 oi[8];
+      load_oi(n + 2, oi);
+      load_gate(n + 1, gnext);
       if (!mbar_wait(&bar_ofull[n & 1], ofull_phase[n & 1])) {
         if (lane == 0) set_err(kErrTimeout);
         break;
       }
       ofull_phase[n & 1] ^= 1u;
       tc_fence_after();
-      float t[2][32];
-      tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 128), t[0]);
-      tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 160), t[1]);
-      tmem_wait_ld();
-      // the block is read: zero it for chunk n + 2 and hand it back to the MMA issuer
+      // both halves to shared memory (row = channel, column = token), then the block goes
+      // back to the issuer, seeded with O_intra^T of chunk n + 2
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-        tmem_st32(tmem_addr(tb, quad * 32, set_col(n) + 128 + 32 * hf), zero);
+      for (int hf = 0; hf < 2; ++hf) {
+        float t[32];
+        tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 128 + 32 * hf), t);
+        tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 32; ++u) ot[hf * 32 * 33 + lane * 33 + u] = t[u];
+      }
+      seed(n + 2, oi);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar_ofree[n & 1]);
+      __syncwarp();
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        __syncwarp();
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float o8[8];
-          unpack8(oi[hf * 4 + ch], o8);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) ot[lane * 33 + ch * 8 + u] = t[hf][ch * 8 + u] + o8[u];
-        }
-        __syncwarp();
         const int r = hf * 32 + lane;  // this thread's token now
         if (r < len) {
+          const float *oh = ot + hf * 32 * 33;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float g8[8], e[8];
-            unpack8(gq[hf][i], g8);
+            unpack8(gcur[hf][i], g8);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) e[u] = scale * g8[u] * ot[(8 * i + u) * 33 + lane];
+            for (int u = 0; u < 8; ++u) {
+              const float g = logits ? sigmoid_approx(g8[u]) : g8[u];
+              e[u] = scale * g * oh[(8 * i + u) * 33 + lane];
+            }
             *reinterpret_cast<uint4 *>(out + ((size_t)(t0 + r) * H + h) * DD + jc + 8 * i) = pack8(e);
           }
         }
       }
+      __syncwarp();  // the transposes are read before the next chunk overwrites them
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) gcur[hf][i] = gnext[hf][i];
     }
   }
   tc_fence_before();
@@ -902,7 +936,7 @@ cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const vo
   return cudaGetLastError();
 }
 
-cudaError_t launch_state_tc(int mode, const void *gate, void *out, const float *S0,
+cudaError_t launch_state_tc(int mode, unsigned flags, const void *gate, void *out, const float *S0,
                             float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                             int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
                             cudaStream_t st, CkptOut ck) {
@@ -911,7 +945,7 @@ cudaError_t launch_state_tc(int mode, const void *gate, void *out, const float *
   if (e != cudaSuccess) return e;
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
   kda_state_tc<<<dim3(n_seq * H, mode == 0 ? 1 : 2), 384, B_DYN, st>>>(
-      mode, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final, X_out, Z_out, cu,
+      mode, flags, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final, X_out, Z_out, cu,
       n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.cards, ck);
   return cudaGetLastError();
 }

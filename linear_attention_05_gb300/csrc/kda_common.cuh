@@ -51,6 +51,22 @@ __host__ __device__ constexpr size_t align_up(size_t x, size_t a) {
   return (x + a - 1) / a * a;
 }
 
+// Gate preparation fused into the kernels' loads (flag KDA_GATE_LOGITS): beta and the output
+// gate arrive as logits, log_alpha as the forget gate's pre-activation a.
+constexpr float kLogHalf = -0.69314718055994531f;
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+// log(alpha) = max(-e^a, log 1/2): a negative log-retention with the lower bound alpha >= 1/2
+__device__ __forceinline__ float log_alpha_of(float a) { return fmaxf(-expf(a), kLogHalf); }
+__device__ __forceinline__ float prep_beta(float x, unsigned flags) {
+  return (flags & KDA_GATE_LOGITS) ? sigmoid_f(x) : x;
+}
+__device__ __forceinline__ float prep_gate(float x, unsigned flags) {
+  return (flags & KDA_GATE_LOGITS) ? sigmoid_f(x) : x;
+}
+__device__ __forceinline__ float prep_log_alpha(float x, unsigned flags) {
+  return (flags & KDA_GATE_LOGITS) ? log_alpha_of(x) : x;
+}
+
 // Prefix-cache state checkpoints: [n_seq, per_seq, H, dk, dv] fp32; slot (s, i) holds the
 // state after the first (i + 1) * every_chunks * 64 tokens of sequence s.
 struct CkptOut {
@@ -107,7 +123,7 @@ cudaError_t launch_prep(const void *q, const void *k, const void *v,
                         unsigned flags, kda_dtype dt, const ChunkWs &ws,
                         bool need_q, cudaStream_t st, PrepSave save = PrepSave());
 // mode 0: forward (out, final); mode 1: segment summary (X_out, Z_out)
-cudaError_t launch_state_pass(int mode, const void *gate, void *out,
+cudaError_t launch_state_pass(int mode, unsigned flags, const void *gate, void *out,
                               const float *S0, float *S_final, float *X_out,
                               float *Z_out, const int32_t *cu, int n_seq,
                               int64_t T_total, int H, int dk, int dv,
@@ -131,7 +147,7 @@ ChunkWs tc_ws_carve(void *ws, int64_t T_total, int n_seq, int H);
 cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const void *la,
                            const void *beta, const int32_t *cu, int n_seq, int64_t T_total,
                            int H, unsigned flags, const ChunkWs &ws, cudaStream_t st);
-cudaError_t launch_state_tc(int mode, const void *gate, void *out, const float *S0,
+cudaError_t launch_state_tc(int mode, unsigned flags, const void *gate, void *out, const float *S0,
                             float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                             int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
                             cudaStream_t st, CkptOut ck = CkptOut());

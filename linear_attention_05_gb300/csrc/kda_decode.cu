@@ -55,14 +55,14 @@ __global__ void __launch_bounds__(256) kda_decode_kernel(
 
   const size_t tk = ((size_t)n * H + h) * DK, tv = ((size_t)n * H + h) * DV;
   for (int c = tid; c < DK; c += 256) {
-    float l = to_f32(la[tk + c]);
+    float l = prep_log_alpha(to_f32(la[tk + c]), flags);
     if ((flags & KDA_DEBUG_CHECK) && !(l >= kLogAlphaMin && l <= 0.f))
       atomicOr(&g_decode_err, kErrPrecondition);
     sq[c] = to_f32(q[tk + c]);
     sk[c] = to_f32(k[tk + c]);
     sa[c] = expf(l);
   }
-  const float b = to_f32(beta[(size_t)n * H + h]);
+  const float b = prep_beta(to_f32(beta[(size_t)n * H + h]), flags);
   if ((flags & KDA_DEBUG_CHECK) && tid == 0 && !(b >= 0.f && b <= 1.f))
     atomicOr(&g_decode_err, kErrPrecondition);
   __syncthreads();
@@ -123,10 +123,10 @@ __global__ void __launch_bounds__(256) kda_decode_kernel(
     float o0 = scale * (tq4.x + bkq * u.x), o1 = scale * (tq4.y + bkq * u.y);
     float o2 = scale * (tq4.z + bkq * u.z), o3 = scale * (tq4.w + bkq * u.w);
     if (gate) {
-      o0 *= to_f32(gate[tv + c0 + 0]);
-      o1 *= to_f32(gate[tv + c0 + 1]);
-      o2 *= to_f32(gate[tv + c0 + 2]);
-      o3 *= to_f32(gate[tv + c0 + 3]);
+      o0 *= prep_gate(to_f32(gate[tv + c0 + 0]), flags);
+      o1 *= prep_gate(to_f32(gate[tv + c0 + 1]), flags);
+      o2 *= prep_gate(to_f32(gate[tv + c0 + 2]), flags);
+      o3 *= prep_gate(to_f32(gate[tv + c0 + 3]), flags);
     }
     out[tv + c0 + 0] = from_f32<T>(o0);
     out[tv + c0 + 1] = from_f32<T>(o1);

@@ -18,6 +18,14 @@
 namespace kda {
 namespace tc {
 
+// sigmoid(x) = (1 + tanh(x / 2)) / 2 with the hardware tanh (tanh.approx.f32: one
+// special-function instruction, relative error about 2^-11)
+__device__ __forceinline__ float sigmoid_approx(float x) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+  return fmaf(0.5f, t, 0.5f);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -166,7 +166,7 @@ def dec(lib, **kw):
     (dict(state=ODD), B.KDA_ERR_INVALID_ARG),
     (dict(n_slots=2), B.KDA_ERR_INVALID_ARG),  # fewer slots than sequences, no slot map
     (dict(slot=FAKE + 1), B.KDA_ERR_INVALID_ARG),
-    (dict(flags=4), B.KDA_ERR_INVALID_ARG),
+    (dict(flags=8), B.KDA_ERR_INVALID_ARG),
 ])
 def test_decode_rejects(lib, kw, status):
     assert dec(lib, **kw) == status
