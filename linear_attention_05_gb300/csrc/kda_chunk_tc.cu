@@ -52,6 +52,7 @@ constexpr int CARD_BYTES = 98816;
 
 // ---- stage B shared memory
 constexpr int B_NSTAGE = 3;            // card ring depth
+constexpr int kPrefetch = 3;           // cards prefetched into L2 beyond the ring
 constexpr int B_STAGE_TX = CARD_BCT + 512;  // [Phi'^T | Q'^T] then e^{G_C} (49664 bytes)
 constexpr int B_STAGE_BYTES = 50176;  // B_STAGE_TX rounded up to 1024
 constexpr int B_SA = B_NSTAGE * B_STAGE_BYTES;  // S^T bf16 operand, 128 x 128 K-major (32768)
@@ -677,8 +678,17 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
       return true;
     };
 
-    if (loader)
+    // whole cards into L2 ahead of their bulk copies (which otherwise wait on HBM latency)
+    auto prefetch_card = [&](int n) {
+      if (n >= nchunks) return;
+      const uint8_t *src = card_of(n);
+      for (int o = 0; o < CARD_BYTES; o += 32768)
+        prefetch_l2(src + o, min(32768, CARD_BYTES - o));
+    };
+    if (loader) {
       for (int n = 0; n < B_NSTAGE && n < nchunks; ++n) load_card(n);
+      for (int n = B_NSTAGE; n < B_NSTAGE + kPrefetch; ++n) prefetch_card(n);
+    }
     fetch_bc(0);
     // chunk 0: entry state from global memory
     if (!wait_full(0)) ok = false;
@@ -704,7 +714,10 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
       mma_phase ^= 1u;
       tc_fence_after();
       // the card of chunk n is consumed: refill its stage with chunk n + 3
-      if (good && loader && n + B_NSTAGE < nchunks) load_card(n + B_NSTAGE);
+      if (good && loader && n + B_NSTAGE < nchunks) {
+        load_card(n + B_NSTAGE);
+        prefetch_card(n + B_NSTAGE + kPrefetch);
+      }
       const bool last = (n + 1 == nchunks);
       if (good && !last) good = wait_full(n + 1);
       // state after chunk n: stage it for chunk n + 1, or write it out
