@@ -339,37 +339,56 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
       for (int i = 0; i < 16; ++i) Ts[mix(o + i, o + j)] = t[i];
     }
     __syncthreads();
-#pragma unroll 1
-    for (int d = 1; d < 4; ++d) {
-      const int nb = 4 - d;  // output blocks (a + d, a), a < nb; one element per thread each
+    // Off-diagonal blocks by a two-level recursion (T lower triangular, T_aa known):
+    // (1) inside each 32-row half: T_{a+1,a} = -T_{a+1,a+1} (M_{a+1,a} T_{a,a}), a = 0, 2;
+    // (2) T_21 = -T_22 (M_21 T_11) for the 32 x 32 halves. Y = M_21 T_11 is parked in the
+    // unused upper triangle of T (rows 0-31, columns 32-63).
+    {
+      const int a = 2 * (tid >> 7), j = tid & 15, i0 = ((tid >> 4) & 7) * 2;  // 2 rows each
+      const int ro = 16 * (a + 1), co = 16 * a;
+      float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-      for (int m = 0; m < 3; ++m) {
-        if (m >= nb) break;
-        const int e = tid + 256 * m, a = e >> 8, i = (e >> 4) & 15, jj = e & 15, rbk = a + d;
-        float p0 = 0.f, p1 = 0.f;
-#pragma unroll 1
-        for (int kb = 0; kb < d; ++kb)
-#pragma unroll
-          for (int kx = 0; kx < 16; kx += 2) {
-            p0 = fmaf(Ms[mix(16 * rbk + i, 16 * (a + kb) + kx)], Ts[mix(16 * (a + kb) + kx, 16 * a + jj)], p0);
-            p1 = fmaf(Ms[mix(16 * rbk + i, 16 * (a + kb) + kx + 1)],
-                      Ts[mix(16 * (a + kb) + kx + 1, 16 * a + jj)], p1);
-          }
-        Xt[e] = p0 + p1;
+      for (int k = 0; k < 16; ++k) {  // X = M_{a+1,a} T_aa; T_aa[k][j] = 0 for k < j
+        const float t = k >= j ? Ts[mix(co + k, co + j)] : 0.f;
+        x0 = fmaf(Ms[mix(ro + i0, co + k)], t, x0);
+        x1 = fmaf(Ms[mix(ro + i0 + 1, co + k)], t, x1);
       }
+      Xt[(tid >> 7) * 256 + i0 * 16 + j] = x0;
+      Xt[(tid >> 7) * 256 + (i0 + 1) * 16 + j] = x1;
       __syncthreads();
+      float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-      for (int m = 0; m < 3; ++m) {
-        if (m >= nb) break;
-        const int e = tid + 256 * m, a = e >> 8, i = (e >> 4) & 15, jj = e & 15, rbk = a + d;
-        float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-        for (int kx = 0; kx < 16; kx += 2) {
-          p0 = fmaf(Ts[mix(16 * rbk + i, 16 * rbk + kx)], Xt[(a << 8) + (kx << 4) + jj], p0);
-          p1 = fmaf(Ts[mix(16 * rbk + i, 16 * rbk + kx + 1)], Xt[(a << 8) + ((kx + 1) << 4) + jj], p1);
-        }
-        Ts[mix(16 * rbk + i, 16 * a + jj)] = -(p0 + p1);
+      for (int k = 0; k < 16; ++k) {  // T_{a+1,a} = -T_{a+1,a+1} X; T_bb[i][k] = 0 for k > i
+        const float xk = Xt[(tid >> 7) * 256 + k * 16 + j];
+        if (k <= i0) y0 = fmaf(Ts[mix(ro + i0, ro + k)], xk, y0);
+        if (k <= i0 + 1) y1 = fmaf(Ts[mix(ro + i0 + 1, ro + k)], xk, y1);
       }
+      Ts[mix(ro + i0, co + j)] = -y0;
+      Ts[mix(ro + i0 + 1, co + j)] = -y1;
+      __syncthreads();
+    }
+    {
+      const int j = tid & 31, i0 = (tid >> 5) * 4;  // column j, rows i0..i0+3 of the 32 x 32 block
+      float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int k = j; k < 32; ++k) {  // Y = M_21 T_11 (T_11[k][j] = 0 for k < j)
+        const float t = Ts[mix(k, j)];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) y[u] = fmaf(Ms[mix(32 + i0 + u, k)], t, y[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) Ts[mix(i0 + u, 32 + j)] = y[u];
+      __syncthreads();
+      float z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int k = 0; k < i0 + 4; ++k) {  // T_21 = -T_22 Y (T_22[i][k] = 0 for k > i)
+        const float yk = Ts[mix(k, 32 + j)];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (k <= i0 + u) z[u] = fmaf(Ts[mix(32 + i0 + u, 32 + k)], yk, z[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) Ts[mix(32 + i0 + u, j)] = -z[u];
       __syncthreads();
     }
     // T' = T diag(b) -> bf16 64-row K-major tile (rows r, columns j): 16 columns per thread
@@ -465,17 +484,41 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
     mma_commit(&bar_mma);
   }
   wait_mma();
-  // six 32-column pieces: 0-1 Q'^T (card atom column 2), 2-5 Phi'^T; group g takes 3g..3g+2
-#pragma unroll 1
-  for (int p = 3 * grp; p < 3 * grp + 3; ++p) {
-    float t32[32];
-    tmem_ld32(tmem_addr(tb, quad * 32, 32 * p), t32);
-    tmem_wait_ld();
-    const int ch0 = p < 2 ? 16 + p * 4 : (p - 2) * 4;
+  // [Phi'^T | Q'^T] card tile: six 32-column pieces in tensor memory (0-1 Q'^T = tile atom 2,
+  // 2-3 atom 0, 4-5 atom 1). Each warp stages whole 32-row x 128-byte blocks of the swizzled
+  // tile in shared memory that GEMMs 3b/4b do not read (the dead Q~/K~ rows and W^T, T), and
+  // writes each block with one 4 KB bulk copy: its rows are contiguous in the card, whereas
+  // 16-byte stores from registers would touch 32 rows per instruction.
+  {
+    const int L0 = quad * 32;
+    auto stage_half = [&](uint8_t *blk, int half, const float *t32) {
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch)
-      *reinterpret_cast<uint4 *>(card + CARD_PHIQ + sw128_chunk(L, ch0 + ch, 128)) =
-          pack8(t32 + ch * 8);
+      for (int ch = 0; ch < 4; ++ch)
+        *reinterpret_cast<uint4 *>(blk + lane * 128 + ((((half * 4 + ch) ^ (lane & 7))) << 4)) =
+            pack8(t32 + ch * 8);
+    };
+    uint8_t *blk = sm + 65536 + (grp * 4 + quad) * 4096;  // (quadrant, atom grp)
+    uint8_t *blk2 = sm + 8192 + quad * 4096;               // (quadrant, atom 2), shared by grp 0/1
+    float ta[32], tb2[32];
+    tmem_ld32(tmem_addr(tb, quad * 32, 32 * (2 + 2 * grp)), ta);
+    tmem_ld32(tmem_addr(tb, quad * 32, 32 * (3 + 2 * grp)), tb2);
+    tmem_wait_ld();
+    stage_half(blk, 0, ta);
+    stage_half(blk, 1, tb2);
+    tmem_ld32(tmem_addr(tb, quad * 32, 32 * grp), ta);
+    tmem_wait_ld();
+    stage_half(blk2, grp, ta);
+    fence_async_smem();  // this thread's shared-memory writes -> visible to the bulk copies
+    __syncwarp();
+    if (lane == 0) {
+      bulk_s2g(card + CARD_PHIQ + grp * 16384 + L0 * 128, blk, 4096);
+      bulk_commit();
+    }
+    named_bar(2 + quad, 64);  // both halves of the atom-2 block are staged
+    if (grp == 0 && lane == 0) {
+      bulk_s2g(card + CARD_PHIQ + 2 * 16384 + L0 * 128, blk2, 4096);
+      bulk_commit();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -491,20 +534,29 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
     mma_commit(&bar_mma);
   }
   wait_mma();
-#pragma unroll 1
-  for (int p = 3 * grp; p < 3 * grp + 3; ++p) {
-    float t32[32];
-    tmem_ld32(tmem_addr(tb, quad * 32, 32 * p), t32);
-    tmem_wait_ld();
+  {
+    auto store_ob = [&](int p, const float *t32) {
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-      const int off8 = p < 2 ? CARD_OIT + ((p * 4 + ch) * 128 + L) * 16
-                             : CARD_BCT + (((p - 2) * 4 + ch) * 128 + L) * 16;
-      *reinterpret_cast<uint4 *>(card + off8) = pack8(t32 + ch * 8);
-    }
+      for (int ch = 0; ch < 4; ++ch) {
+        const int off8 = p < 2 ? CARD_OIT + ((p * 4 + ch) * 128 + L) * 16
+                               : CARD_BCT + (((p - 2) * 4 + ch) * 128 + L) * 16;
+        *reinterpret_cast<uint4 *>(card + off8) = pack8(t32 + ch * 8);
+      }
+    };
+    const int p0 = 3 * grp;
+    float ta[32], tb2[32];
+    tmem_ld32(tmem_addr(tb, quad * 32, 32 * p0), ta);
+    tmem_ld32(tmem_addr(tb, quad * 32, 32 * (p0 + 1)), tb2);
+    tmem_wait_ld();
+    store_ob(p0, ta);
+    store_ob(p0 + 1, tb2);
+    tmem_ld32(tmem_addr(tb, quad * 32, 32 * (p0 + 2)), ta);
+    tmem_wait_ld();
+    store_ob(p0 + 2, ta);
   }
   if (tid < DD) reinterpret_cast<float *>(card + CARD_D)[tid] = s_d[tid];
   if (!ok && lane == 0) set_err(kErrTimeout);
+  if (lane == 0) bulk_wait_all();  // the card-tile bulk stores have completed
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tb, 256);
