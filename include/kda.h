@@ -184,6 +184,40 @@ size_t kda_chunk_bwd_workspace_size(int64_t T_total, int n_seq, int H, int dk,
                                     int dv, int chunk, kda_dtype dtype);
 
 /*
+ * One sequence split into n_seg segments, evaluated the context-parallel way
+ * on one GPU: per-segment summaries (as kda_segment_summary), their ordered
+ * scan (as kda_scan_combine, from initial_state), then every segment re-run
+ * from its recovered entry state (as kda_chunk_fwd). The update cards are
+ * computed once and serve both the summaries and the re-run.
+ * Source: K3 training overview section 3 "KDA context parallel" (fixed-size
+ * per-segment summaries merged by a prefix scan recover each segment's exact
+ * entry state) and section 4 "FlashKDA" (update cards).
+ *
+ *  q, k, v, log_alpha, beta, gate, out : as kda_chunk_fwd over the T_total tokens
+ *  initial_state        : [H, dk, dv] fp32 state before segment 0, or NULL (0)
+ *  final_state          : [H, dk, dv] fp32 state after the last segment, or NULL
+ *  segment_entry_states : [n_seg, H, dk, dv] fp32 (written: state entering
+ *                         each segment), or NULL (kept in the workspace)
+ *  cu_segs              : device int32 [n_seg + 1] segment bounds, cu_segs[0] = 0,
+ *                         cu_segs[n_seg] = T_total; NULL = n_seg equal segments
+ *  workspace            : >= kda_segmented_fwd_workspace_size(...) bytes
+ * The output equals kda_chunk_fwd over the whole sequence up to rounding.
+ */
+kda_status kda_segmented_fwd(const void *q, const void *k, const void *v,
+                             const void *log_alpha, const void *beta,
+                             const void *gate, void *out,
+                             const float *initial_state, float *final_state,
+                             float *segment_entry_states,
+                             const int32_t *cu_segs, int n_seg, int64_t T_total,
+                             int H, int dk, int dv, int chunk, float scale,
+                             unsigned flags, kda_dtype dtype, void *workspace,
+                             size_t workspace_bytes, kda_stream_t stream);
+
+size_t kda_segmented_fwd_workspace_size(int64_t T_total, int n_seg, int H,
+                                        int dk, int dv, int chunk,
+                                        kda_dtype dtype);
+
+/*
  * kda_chunk_fwd without a workspace argument, for callers that cannot
  * allocate device memory where they run the mixer: host frameworks that
  * reserve the device heap up front and give a kernel only its inputs and

@@ -11,8 +11,9 @@ from .binding import (KDA_DEBUG_CHECK, KDA_DTYPE_BF16, KDA_DTYPE_F32, KDA_GATE_L
                       kda_chunk_fwd_checkpoints, kda_chunk_fwd_noalloc,
                       kda_chunk_fwd_workspace_size,
                       kda_decode_step, kda_get_error, kda_last_error_string, kda_scan_combine,
-                      kda_segment_summary, kda_segment_summary_workspace_size, kda_trace_events,
+                      kda_segment_summary, kda_segment_summary_workspace_size, kda_segmented_fwd,
+                      kda_segmented_fwd_workspace_size, kda_trace_events,
                       kda_version, load,
-                      scan_combine, segment_summary)
+                      scan_combine, segment_summary, segmented_fwd)
 
 __all__ = [n for n in dir() if not n.startswith("_")]

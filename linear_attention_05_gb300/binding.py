@@ -76,6 +76,9 @@ def load(path: str = LIB_PATH):
             "kda_chunk_bwd": ([P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I,
                                I, F, U, I, P, SZ, P], I),
             "kda_chunk_bwd_workspace_size": ([I64, I, I, I, I, I, I], SZ),
+            "kda_segmented_fwd": ([P, P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, P,
+                                   SZ, P], I),
+            "kda_segmented_fwd_workspace_size": ([I64, I, I, I, I, I, I], SZ),
             "kda_chunk_fwd_checkpoints": ([P, P, P, P, P, P, P, P, P, P, I64, I, P, I, I64, I, I,
                                            I, I, F, U, I, P, SZ, P], I),
             "kda_chunk_fwd_noalloc": ([P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, P], I),
@@ -236,6 +239,35 @@ def kda_chunk_bwd(q, k, v, log_alpha, beta, gate, initial_state, d_out, d_final_
                            _ptr(d_initial_state), _ptr(cu_seqlens), n_seq, T, H, dk, dv, chunk,
                            float(scale), int(flags), dt, _ptr(ws), wsb, _stream(stream))
     _check(lib, st)
+
+
+def kda_segmented_fwd_workspace_size(T_total, n_seg, H, dk, dv, chunk=CHUNK,
+                                     dtype=KDA_DTYPE_BF16):
+    return int(load().kda_segmented_fwd_workspace_size(T_total, n_seg, H, dk, dv, chunk, dtype))
+
+
+def kda_segmented_fwd(q, k, v, log_alpha, beta, gate, out, initial_state, final_state,
+                      segment_entry_states, cu_segs, n_seg, scale=1.0, flags=KDA_QK_L2NORM,
+                      workspace=None, stream=None, chunk=CHUNK):
+    """One sequence in n_seg segments: summaries, ordered scan, segment re-run (one card pass)."""
+    lib = load()
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(k)
+    for t, n in ((initial_state, "initial_state"), (final_state, "final_state"),
+                 (segment_entry_states, "segment_entry_states")):
+        _f32_or_none(t, n)
+    if cu_segs is not None and cu_segs.dtype != torch.int32:
+        raise ValueError("cu_segs must be int32")
+    need = lib.kda_segmented_fwd_workspace_size(T, n_seg, H, dk, dv, chunk, dt)
+    ws, wsb = _workspace(need, k.device, workspace)
+    st = lib.kda_segmented_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                               _ptr(gate), _ptr(out), _ptr(initial_state), _ptr(final_state),
+                               _ptr(segment_entry_states), _ptr(cu_segs), n_seg, T, H, dk, dv,
+                               chunk, float(scale), int(flags), dt, _ptr(ws), wsb,
+                               _stream(stream))
+    _check(lib, st)
+    return out, final_state
 
 
 def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, gate, out, initial_state, final_state,
@@ -408,6 +440,24 @@ def chunk_bwd(q, k, v, log_alpha, beta, gate, initial_state, d_out, d_final_stat
                   cu_seqlens, n_seq, scale=scale, flags=_flags(l2norm, gate_logits),
                   workspace=workspace, stream=stream)
     return g
+
+
+def segmented_fwd(q, k, v, log_alpha, beta, gate=None, initial_state=None, cu_segs=None,
+                  n_seg=None, scale=1.0, l2norm=True, gate_logits=False, workspace=None,
+                  stream=None):
+    """Allocate out, the final state and the segment entry states; call kda_segmented_fwd.
+    Returns (out, final_state [H, dk, dv], entry_states [n_seg, H, dk, dv])."""
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    if n_seg is None:
+        n_seg = cu_segs.numel() - 1
+    out = torch.empty((T, H, dv), dtype=v.dtype, device=v.device)
+    fs = torch.empty((H, dk, dv), dtype=torch.float32, device=v.device)
+    ent = torch.empty((n_seg, H, dk, dv), dtype=torch.float32, device=v.device)
+    kda_segmented_fwd(q, k, v, log_alpha, beta, gate, out, initial_state, fs, ent, cu_segs, n_seg,
+                      scale=scale, flags=_flags(l2norm, gate_logits), workspace=workspace,
+                      stream=stream)
+    return out, fs, ent
 
 
 def decode_step(q, k, v, log_alpha, beta, gate, state, state_slot=None, scale=1.0, l2norm=True,

@@ -367,6 +367,97 @@ kda_status kda_segment_summary(const void *k, const void *v, const void *log_alp
                      "summary state pass");
 }
 
+size_t kda_segmented_fwd_workspace_size(int64_t T_total, int n_seg, int H, int dk, int dv,
+                                        int chunk, kda_dtype dtype) {
+  const size_t base = kda_chunk_fwd_workspace_size(T_total, n_seg, H, dk, dv, chunk, dtype);
+  if (base == 0) return 0;
+  const size_t per = (size_t)n_seg * H;
+  return base + kda::align_up(sizeof(float) * per * dk * dk, 256) +
+         2 * kda::align_up(sizeof(float) * per * dk * dv, 256);
+}
+
+kda_status kda_segmented_fwd(const void *q, const void *k, const void *v, const void *log_alpha,
+                             const void *beta, const void *gate, void *out,
+                             const float *initial_state, float *final_state,
+                             float *segment_entry_states, const int32_t *cu_segs, int n_seg,
+                             int64_t T_total, int H, int dk, int dv, int chunk, float scale,
+                             unsigned flags, kda_dtype dtype, void *workspace,
+                             size_t workspace_bytes, kda_stream_t stream) {
+  kda_status st = common_checks(T_total, n_seg, H, dk, dv, chunk, dtype, cu_segs);
+  if (st != KDA_OK) return st;
+  KDA_REQUIRE(n_seg >= 1, KDA_ERR_INVALID_ARG, "n_seg=%d: at least one segment", n_seg);
+  KDA_REQUIRE((flags & ~kKnownFlags) == 0, KDA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+  const bool tokens = T_total > 0;
+  KDA_CHECK_PTR(q, tokens);
+  KDA_CHECK_PTR(k, tokens);
+  KDA_CHECK_PTR(v, tokens);
+  KDA_CHECK_PTR(log_alpha, tokens);
+  KDA_REQUIRE(!tokens || beta != nullptr, KDA_ERR_INVALID_ARG, "beta must not be NULL");
+  KDA_CHECK_PTR(gate, false);
+  KDA_CHECK_PTR(out, tokens);
+  KDA_CHECK_PTR(initial_state, false);
+  KDA_CHECK_PTR(final_state, false);
+  KDA_CHECK_PTR(segment_entry_states, false);
+  KDA_REQUIRE(cu_segs == nullptr || ((uintptr_t)cu_segs & 3u) == 0, KDA_ERR_INVALID_ARG,
+              "cu_segs is not 4-byte aligned");
+  const size_t need = kda_segmented_fwd_workspace_size(T_total, n_seg, H, dk, dv, chunk, dtype);
+  KDA_REQUIRE(workspace != nullptr && workspace_bytes >= need, KDA_ERR_WORKSPACE,
+              "workspace %zu bytes, need %zu", workspace_bytes, need);
+  KDA_REQUIRE(((uintptr_t)workspace & 255u) == 0, KDA_ERR_INVALID_ARG,
+              "workspace is not 256-byte aligned");
+  cudaStream_t s = (cudaStream_t)stream;
+  Tracer tr(s);
+  const bool tc = kda::tc_path(dk, dv, dtype);
+  const size_t base = tc ? kda::tc_ws_bytes(T_total, n_seg, H)
+                         : kda::chunk_ws_bytes(T_total, n_seg, H, dk, dv);
+  kda::ChunkWs ws = tc ? kda::tc_ws_carve(workspace, T_total, n_seg, H)
+                       : kda::chunk_ws_carve(workspace, T_total, n_seg, H, dk, dv);
+  const size_t per = (size_t)n_seg * H;
+  float *X = (float *)((char *)workspace + kda::align_up(base, 256));
+  float *Z = (float *)((char *)X + kda::align_up(sizeof(float) * per * dk * dk, 256));
+  float *E = segment_entry_states
+                 ? segment_entry_states
+                 : (float *)((char *)Z + kda::align_up(sizeof(float) * per * dk * dv, 256));
+  st = cuda_status(tr([&] { return kda::launch_chunk_table(cu_segs, n_seg, T_total, ws, s); }),
+                   "chunk table");
+  if (st != KDA_OK) return st;
+  // one set of update cards serves both the summaries and the re-run
+  st = cuda_status(tr([&] {
+                     return tc ? kda::launch_card_tc(q, k, v, log_alpha, beta, cu_segs, n_seg,
+                                                     T_total, H, flags, ws, s)
+                               : kda::launch_prep(q, k, v, log_alpha, beta, cu_segs, n_seg,
+                                                  T_total, H, dk, dv, flags, dtype, ws, true, s);
+                   }),
+                   "chunk prep");
+  if (st != KDA_OK) return st;
+  st = cuda_status(tr([&] {
+                     return tc ? kda::launch_state_tc(1, flags, nullptr, nullptr, nullptr, nullptr,
+                                                      X, Z, cu_segs, n_seg, T_total, H, 1.0f, ws,
+                                                      s)
+                               : kda::launch_state_pass(1, flags, nullptr, nullptr, nullptr,
+                                                        nullptr, X, Z, cu_segs, n_seg, T_total,
+                                                        H, dk, dv, 1.0f, dtype, ws, s);
+                   }),
+                   "segment summaries");
+  if (st != KDA_OK) return st;
+  st = cuda_status(tr([&] {
+                     return kda::launch_scan_combine(X, Z, n_seg, H, dk, dv, initial_state, E,
+                                                     final_state, s);
+                   }),
+                   "scan combine");
+  if (st != KDA_OK) return st;
+  return cuda_status(tr([&] {
+                       return tc ? kda::launch_state_tc(0, flags, gate, out, E, nullptr, nullptr,
+                                                        nullptr, cu_segs, n_seg, T_total, H,
+                                                        scale, ws, s)
+                                 : kda::launch_state_pass(0, flags, gate, out, E, nullptr,
+                                                          nullptr, nullptr, cu_segs, n_seg,
+                                                          T_total, H, dk, dv, scale, dtype, ws,
+                                                          s);
+                     }),
+                     "segment re-run");
+}
+
 kda_status kda_scan_combine(const float *X, const float *Z, int n_seg, int H, int dk, int dv,
                             const float *S_init, float *S_entry_out, float *S_final_out,
                             kda_stream_t stream) {

@@ -141,6 +141,20 @@ def test_chunk_bwd_workspace_size(lib):
     assert B.kda_chunk_bwd_workspace_size(4096, 1, 16, 96, 128) == 0
 
 
+def test_segmented_fwd_rejects(lib):
+    args = lambda **kw: [kw.get(n, d) for n, d in (
+        ("q", FAKE), ("k", FAKE), ("v", FAKE), ("la", FAKE), ("beta", FAKE), ("gate", None),
+        ("out", FAKE), ("s0", None), ("sf", None), ("ent", None), ("cu", None), ("n_seg", 2),
+        ("T", 256), ("H", 2), ("dk", 64), ("dv", 64), ("chunk", 64), ("scale", 1.0),
+        ("flags", 1), ("dtype", 1), ("ws", FAKE), ("wsb", 0), ("stream", None))]
+    assert lib.kda_segmented_fwd(*args(n_seg=0, T=0)) == B.KDA_ERR_INVALID_ARG
+    assert lib.kda_segmented_fwd(*args(ent=ODD)) == B.KDA_ERR_INVALID_ARG
+    assert lib.kda_segmented_fwd(*args(dv=32)) == B.KDA_ERR_UNSUPPORTED
+    assert lib.kda_segmented_fwd(*args()) == B.KDA_ERR_WORKSPACE
+    assert (B.kda_segmented_fwd_workspace_size(256, 2, 2, 64, 64)
+            > B.kda_chunk_fwd_workspace_size(256, 2, 2, 64, 64))
+
+
 def test_workspace_size(lib):
     s1 = B.kda_chunk_fwd_workspace_size(4096, 1, 16, 128, 128)
     s2 = B.kda_chunk_fwd_workspace_size(8192, 1, 16, 128, 128)
