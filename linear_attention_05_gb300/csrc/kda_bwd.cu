@@ -107,7 +107,9 @@ __global__ void __launch_bounds__(256) kda_bwd_dO(const Tin *__restrict__ d_out,
 // ---------------------------------------------------------------------------
 // Reverse state pass: one block per (sequence, head, 32 value columns), chunks
 // last to first. Writes dS' (the cotangent of the state leaving each chunk) and
-// dU per chunk, and dS_0.
+// dU per chunk, and dS_0. Register-tiled: thread (rg, cg) = (tid >> 3, tid & 7)
+// owns value columns 4cg..4cg+3 and key rows 4rg..4rg+3 of dS (rows 2rg, 2rg+1 of
+// dU); operands come from shared memory as 16-byte vectors.
 constexpr int RBV = 32;
 
 template <int DK, int DV>
@@ -118,21 +120,29 @@ __global__ void __launch_bounds__(256) kda_bwd_state(
     const float *__restrict__ Qg, const float *__restrict__ Wg, const float *__restrict__ Kdg,
     const float *__restrict__ Pg, const float *__restrict__ Dg, const float *__restrict__ dOg,
     float *__restrict__ dSb, float *__restrict__ dUg) {
-  constexpr int LK = DK + 1, LS = RBV + 1, LP = C + 1;
-  extern __shared__ float smem[];
-  float *sS = smem;            // [DK][LS]   running dS
+  static_assert(DK / 4 <= 32 && C / 2 <= 32, "row groups");
+  constexpr int LK = DK + 4, LS = RBV + 4, LC = C + 4;  // float4-aligned pitches
+  extern __shared__ __align__(16) float smem[];
+  float *sS = smem;            // [DK][LS]   running dS (value-column slice)
   float *sO = sS + DK * LS;    // [C][LS]    dO slice
   float *sU = sO + C * LS;     // [C][LS]    dU slice
-  float *sQ = sU + C * LS;     // [C][LK]
-  float *sW = sQ + C * LK;     // [C][LK]
-  float *sKd = sW + C * LK;    // [C][LK]
-  float *sP = sKd + C * LK;    // [C][LP]
-  float *sD = sP + C * LP;     // [DK]
+  float *sQ = sU + C * LS;     // [C][LK]    Q~
+  float *sW = sQ + C * LK;     // [C][LK]    W
+  float *sKt = sW + C * LK;    // [DK][LC]   K_d^T
+  float *sP = sKt + DK * LC;   // [C][LC]    P (row i, column r)
+  float *sD = sP + C * LC;     // [DK]
   if (meta->invalid) return;
   const int chain = blockIdx.x, s = chain / H, h = chain % H, tid = threadIdx.x;
-  const int j0 = blockIdx.y * RBV, jt = tid & 31, rt = tid >> 5;
-  for (int c = rt; c < DK; c += 8)
-    sS[c * LS + jt] = dS_final ? dS_final[(((size_t)s * H + h) * DK + c) * DV + j0 + jt] : 0.f;
+  const int j0 = blockIdx.y * RBV;
+  const int cg = tid & 7, rg = tid >> 3;
+  const int jl = 4 * cg;                 // local value column of this thread
+  const bool s_rows = rg < DK / 4;       // dS rows 4rg..4rg+3
+  const bool u_rows = rg < C / 2;        // dU rows 2rg, 2rg+1
+  for (int e = tid; e < DK * RBV; e += 256) {
+    const int c = e / RBV, jj = e % RBV;
+    sS[c * LS + jj] =
+        dS_final ? dS_final[(((size_t)s * H + h) * DK + c) * DV + j0 + jj] : 0.f;
+  }
   int64_t ls;
   if (cu) ls = (int64_t)cu[s + 1] - cu[s];
   else ls = fixed_len;
@@ -140,54 +150,129 @@ __global__ void __launch_bounds__(256) kda_bwd_state(
   __syncthreads();
   for (int jc = nchunks - 1; jc >= 0; --jc) {
     const size_t slab = (size_t)(off[s] + jc) * H + h;
-    for (int c = rt; c < DK; c += 8) dSb[(slab * DK + c) * DV + j0 + jt] = sS[c * LS + jt];
-    for (int e = tid; e < C * DK; e += 256) {
-      const int r = e / DK, c = e % DK;
-      sQ[r * LK + c] = Qg[slab * C * DK + e];
-      sW[r * LK + c] = Wg[slab * C * DK + e];
-      sKd[r * LK + c] = Kdg[slab * C * DK + e];
+    for (int e = tid; e < DK * RBV; e += 256) {
+      const int c = e / RBV, jj = e % RBV;
+      dSb[(slab * DK + c) * DV + j0 + jj] = sS[c * LS + jj];
     }
-    for (int e = tid; e < C * C; e += 256) sP[(e / C) * LP + e % C] = Pg[slab * C * C + e];
-    for (int e = tid; e < C * RBV; e += 256) {
-      const int r = e / RBV, c = e % RBV;
-      sO[r * LS + c] = dOg[(slab * C + r) * DV + j0 + c];
+    {  // operands of chunk jc: 16-byte loads, each batch issued before any of its stores
+      constexpr int NK = C * DK / 4 / 256, NP = C * C / 4 / 256, NO = C * RBV / 4 / 256;
+      const float *Q = Qg + slab * C * DK, *W = Wg + slab * C * DK, *Kd = Kdg + slab * C * DK;
+      float4 rq[NK], rw[NK];
+#pragma unroll
+      for (int m = 0; m < NK; ++m) {
+        rq[m] = *reinterpret_cast<const float4 *>(Q + 4 * (tid + 256 * m));
+        rw[m] = *reinterpret_cast<const float4 *>(W + 4 * (tid + 256 * m));
+      }
+#pragma unroll
+      for (int m = 0; m < NK; ++m) {
+        const int e = 4 * (tid + 256 * m), r = e / DK, c = e % DK;
+        *reinterpret_cast<float4 *>(sQ + r * LK + c) = rq[m];
+        *reinterpret_cast<float4 *>(sW + r * LK + c) = rw[m];
+      }
+      float4 rp[NP], ro[NO];
+#pragma unroll
+      for (int m = 0; m < NK; ++m) rq[m] = *reinterpret_cast<const float4 *>(Kd + 4 * (tid + 256 * m));
+#pragma unroll
+      for (int m = 0; m < NP; ++m)
+        rp[m] = *reinterpret_cast<const float4 *>(Pg + slab * C * C + 4 * (tid + 256 * m));
+#pragma unroll
+      for (int m = 0; m < NO; ++m) {
+        const int e = 4 * (tid + 256 * m), r = e / RBV, jj = e % RBV;
+        ro[m] = *reinterpret_cast<const float4 *>(dOg + (slab * C + r) * DV + j0 + jj);
+      }
+#pragma unroll
+      for (int m = 0; m < NK; ++m) {
+        const int e = 4 * (tid + 256 * m), r = e / DK, c = e % DK;
+        sKt[(c + 0) * LC + r] = rq[m].x; sKt[(c + 1) * LC + r] = rq[m].y;
+        sKt[(c + 2) * LC + r] = rq[m].z; sKt[(c + 3) * LC + r] = rq[m].w;
+      }
+#pragma unroll
+      for (int m = 0; m < NP; ++m) {
+        const int e = 4 * (tid + 256 * m), r = e / C, i = e % C;
+        *reinterpret_cast<float4 *>(sP + r * LC + i) = rp[m];
+      }
+#pragma unroll
+      for (int m = 0; m < NO; ++m) {
+        const int e = 4 * (tid + 256 * m), r = e / RBV, jj = e % RBV;
+        *reinterpret_cast<float4 *>(sO + r * LS + jj) = ro[m];
+      }
+      if (tid < DK) sD[tid] = Dg[slab * DK + tid];
     }
-    if (tid < DK) sD[tid] = Dg[slab * DK + tid];
     __syncthreads();
-    // dU = P^T dO + K_d dS'   (P is lower triangular: P[i][r] = 0 for i < r)
-#pragma unroll 1
-    for (int m = 0; m < C / 8; ++m) {
-      const int r = rt + 8 * m;
-      float acc = 0.f;
-      for (int i = r; i < C; ++i) acc = fmaf(sP[i * LP + r], sO[i * LS + jt], acc);
-      for (int c = 0; c < DK; ++c) acc = fmaf(sKd[r * LK + c], sS[c * LS + jt], acc);
-      sU[r * LS + jt] = acc;
-      dUg[(slab * C + r) * DV + j0 + jt] = acc;
+    // dU = P^T dO + K_d dS'  (P[i][r] = 0 for i < r)
+    if (u_rows) {
+      const int r0 = 2 * rg;
+      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int i = r0; i < C; ++i) {
+        const float2 p = *reinterpret_cast<const float2 *>(sP + i * LC + r0);
+        const float4 o = *reinterpret_cast<const float4 *>(sO + i * LS + jl);
+        a0[0] = fmaf(p.x, o.x, a0[0]); a0[1] = fmaf(p.x, o.y, a0[1]);
+        a0[2] = fmaf(p.x, o.z, a0[2]); a0[3] = fmaf(p.x, o.w, a0[3]);
+        a1[0] = fmaf(p.y, o.x, a1[0]); a1[1] = fmaf(p.y, o.y, a1[1]);
+        a1[2] = fmaf(p.y, o.z, a1[2]); a1[3] = fmaf(p.y, o.w, a1[3]);
+      }
+#pragma unroll 4
+      for (int c = 0; c < DK; ++c) {
+        const float2 kd = *reinterpret_cast<const float2 *>(sKt + c * LC + r0);
+        const float4 d = *reinterpret_cast<const float4 *>(sS + c * LS + jl);
+        a0[0] = fmaf(kd.x, d.x, a0[0]); a0[1] = fmaf(kd.x, d.y, a0[1]);
+        a0[2] = fmaf(kd.x, d.z, a0[2]); a0[3] = fmaf(kd.x, d.w, a0[3]);
+        a1[0] = fmaf(kd.y, d.x, a1[0]); a1[1] = fmaf(kd.y, d.y, a1[1]);
+        a1[2] = fmaf(kd.y, d.z, a1[2]); a1[3] = fmaf(kd.y, d.w, a1[3]);
+      }
+      *reinterpret_cast<float4 *>(sU + r0 * LS + jl) = make_float4(a0[0], a0[1], a0[2], a0[3]);
+      *reinterpret_cast<float4 *>(sU + (r0 + 1) * LS + jl) = make_float4(a1[0], a1[1], a1[2], a1[3]);
+      *reinterpret_cast<float4 *>(dUg + (slab * C + r0) * DV + j0 + jl) =
+          make_float4(a0[0], a0[1], a0[2], a0[3]);
+      *reinterpret_cast<float4 *>(dUg + (slab * C + r0 + 1) * DV + j0 + jl) =
+          make_float4(a1[0], a1[1], a1[2], a1[3]);
     }
     __syncthreads();
     // dS = Diag(e^{G_C}) dS' + Q~^T dO - W^T dU
-    float ns[DK / 8];
+    float ns[4][4];
+    if (s_rows) {
+      const int c0 = 4 * rg;
 #pragma unroll
-    for (int m = 0; m < DK / 8; ++m) {
-      const int c = rt + 8 * m;
-      float acc = sD[c] * sS[c * LS + jt];
-      for (int r = 0; r < C; ++r)
-        acc = fmaf(sQ[r * LK + c], sO[r * LS + jt], fmaf(-sW[r * LK + c], sU[r * LS + jt], acc));
-      ns[m] = acc;
+      for (int u = 0; u < 4; ++u) {
+        const float4 d = *reinterpret_cast<const float4 *>(sS + (c0 + u) * LS + jl);
+        const float dc = sD[c0 + u];
+        ns[u][0] = dc * d.x; ns[u][1] = dc * d.y; ns[u][2] = dc * d.z; ns[u][3] = dc * d.w;
+      }
+#pragma unroll 2
+      for (int r = 0; r < C; ++r) {
+        const float4 q = *reinterpret_cast<const float4 *>(sQ + r * LK + c0);
+        const float4 w = *reinterpret_cast<const float4 *>(sW + r * LK + c0);
+        const float4 o = *reinterpret_cast<const float4 *>(sO + r * LS + jl);
+        const float4 du = *reinterpret_cast<const float4 *>(sU + r * LS + jl);
+        const float qa[4] = {q.x, q.y, q.z, q.w}, wa[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          ns[u][0] = fmaf(qa[u], o.x, fmaf(-wa[u], du.x, ns[u][0]));
+          ns[u][1] = fmaf(qa[u], o.y, fmaf(-wa[u], du.y, ns[u][1]));
+          ns[u][2] = fmaf(qa[u], o.z, fmaf(-wa[u], du.z, ns[u][2]));
+          ns[u][3] = fmaf(qa[u], o.w, fmaf(-wa[u], du.w, ns[u][3]));
+        }
+      }
     }
     __syncthreads();
+    if (s_rows)
 #pragma unroll
-    for (int m = 0; m < DK / 8; ++m) sS[(rt + 8 * m) * LS + jt] = ns[m];
+      for (int u = 0; u < 4; ++u)
+        *reinterpret_cast<float4 *>(sS + (4 * rg + u) * LS + jl) =
+            make_float4(ns[u][0], ns[u][1], ns[u][2], ns[u][3]);
     __syncthreads();
   }
   if (dS_init)
-    for (int c = rt; c < DK; c += 8)
-      dS_init[(((size_t)s * H + h) * DK + c) * DV + j0 + jt] = sS[c * LS + jt];
+    for (int e = tid; e < DK * RBV; e += 256) {
+      const int c = e / RBV, jj = e % RBV;
+      dS_init[(((size_t)s * H + h) * DK + c) * DV + j0 + jj] = sS[c * LS + jj];
+    }
 }
 
 template <int DK>
 constexpr size_t bwd_state_smem() {
-  return sizeof(float) * (DK * (RBV + 1) + 2 * C * (RBV + 1) + 3 * C * (DK + 1) + C * (C + 1) + DK);
+  return sizeof(float) * (DK * (RBV + 4) + 2 * C * (RBV + 4) + 2 * C * (DK + 4) +
+                          DK * (C + 4) + C * (C + 4) + DK);
 }
 
 // ---------------------------------------------------------------------------

@@ -292,20 +292,24 @@ __global__ void __launch_bounds__(256) kda_state_simt(
     const float *__restrict__ Wg, const float *__restrict__ Ug, const float *__restrict__ Qg,
     const float *__restrict__ Kdg, const float *__restrict__ Pg, const float *__restrict__ Dg,
     CkptOut ck, StateSave save) {
-  constexpr int LK = DK + 1, LS = BV + 1, LP = C + 1;
-  extern __shared__ float smem[];
-  float *sS = smem;            // [DK][LS]
-  float *sU = sS + DK * LS;    // [C][LS]
-  float *sW = sU + C * LS;     // [C][LK]
-  float *sQ = sW + C * LK;     // [C][LK]
-  float *sKd = sQ + C * LK;    // [C][LK]
-  float *sP = sKd + C * LK;    // [C][LP]
-  float *sD = sP + C * LP;     // [DK]
+  // Register-tiled: thread (rg, cg) = (tid >> 3, tid & 7) owns value columns 4cg..4cg+3 of
+  // this slice, rows 2rg, 2rg+1 of U and O and key rows 4rg..4rg+3 of S. Operands are read
+  // from shared memory as 8- and 16-byte vectors; W, Q~ and P are stored transposed.
+  constexpr int LS = BV + 4, LK = DK + 4, LT = C + 2;
+  extern __shared__ __align__(16) float smem[];
+  float *sS = smem;            // [DK][LS]  state slice
+  float *sU = sS + DK * LS;    // [C][LS]   U~, then U
+  float *sWt = sU + C * LS;    // [DK][LT]  W^T
+  float *sQt = sWt + DK * LT;  // [DK][LT]  Q~^T
+  float *sKd = sQt + DK * LT;  // [C][LK]   K_d
+  float *sPt = sKd + C * LK;   // [C][LT]   P^T
+  float *sD = sPt + C * LT;    // [DK]
 
   if (meta->invalid) return;
   const int chain = blockIdx.x, s = chain / H, h = chain % H, tid = threadIdx.x;
   const int j0 = blockIdx.y * BV;
-  const int jt = tid & 31, rt = tid >> 5;  // column lane, row group (8 groups)
+  const int cg = tid & 7, rg = tid >> 3, jl = 4 * cg, r0 = 2 * rg;
+  const bool s_rows = rg < DK / 4;
   bool xpart = false;
   int vcol0 = j0;  // first value column of this slice (mode 0 / Z part)
   if (mode == 1) {
@@ -313,14 +317,15 @@ __global__ void __launch_bounds__(256) kda_state_simt(
     vcol0 = j0 - DK;
   }
   // entry state
-  for (int c = rt; c < DK; c += 8) {
+  for (int e = tid; e < DK * BV; e += 256) {
+    const int c = e / BV, jj = e % BV;
     float x = 0.f;
     if (mode == 0) {
-      if (S0) x = S0[(((size_t)s * H + h) * DK + c) * DV + j0 + jt];
+      if (S0) x = S0[(((size_t)s * H + h) * DK + c) * DV + j0 + jj];
     } else if (xpart) {
-      x = (c == j0 + jt) ? 1.f : 0.f;
+      x = (c == j0 + jj) ? 1.f : 0.f;
     }
-    sS[c * LS + jt] = x;
+    sS[c * LS + jj] = x;
   }
   int64_t ts, ls;
   seq_range(cu, fixed_len, s, &ts, &ls);
@@ -335,89 +340,173 @@ __global__ void __launch_bounds__(256) kda_state_simt(
     const int len = (int)min((int64_t)C, ls - (int64_t)jc * C);
     const float *W = Wg + slab * C * DK, *Kd = Kdg + slab * C * DK;
     if (mode == 0 && save.Sb)  // state entering chunk jc
-      for (int c = rt; c < DK; c += 8) save.Sb[(slab * DK + c) * DV + j0 + jt] = sS[c * LS + jt];
-    for (int e = tid; e < C * DK; e += 256) {
-      int r = e / DK, c = e % DK;
-      sW[r * LK + c] = W[e];
-      sKd[r * LK + c] = Kd[e];
-      if (need_o) sQ[r * LK + c] = Qg[slab * C * DK + e];
+      for (int e = tid; e < DK * BV; e += 256) {
+        const int c = e / BV, jj = e % BV;
+        save.Sb[(slab * DK + c) * DV + j0 + jj] = sS[c * LS + jj];
+      }
+    // operands of chunk jc: 16-byte loads, each batch issued before any of its stores
+    {
+      constexpr int NK = C * DK / 4 / 256;  // float4 per thread of a [C, DK] matrix
+      float4 rw[NK], rk[NK];
+#pragma unroll
+      for (int m = 0; m < NK; ++m) {
+        rw[m] = *reinterpret_cast<const float4 *>(W + 4 * (tid + 256 * m));
+        rk[m] = *reinterpret_cast<const float4 *>(Kd + 4 * (tid + 256 * m));
+      }
+#pragma unroll
+      for (int m = 0; m < NK; ++m) {
+        const int e = 4 * (tid + 256 * m), r = e / DK, c = e % DK;
+        sWt[(c + 0) * LT + r] = rw[m].x; sWt[(c + 1) * LT + r] = rw[m].y;
+        sWt[(c + 2) * LT + r] = rw[m].z; sWt[(c + 3) * LT + r] = rw[m].w;
+        *reinterpret_cast<float4 *>(sKd + r * LK + c) = rk[m];
+      }
+      if (need_o) {
+        const float *Q = Qg + slab * C * DK, *P = Pg + slab * C * C;
+        constexpr int NP = C * C / 4 / 256;
+        float4 rp[NP];
+#pragma unroll
+        for (int m = 0; m < NK; ++m) rw[m] = *reinterpret_cast<const float4 *>(Q + 4 * (tid + 256 * m));
+#pragma unroll
+        for (int m = 0; m < NP; ++m) rp[m] = *reinterpret_cast<const float4 *>(P + 4 * (tid + 256 * m));
+#pragma unroll
+        for (int m = 0; m < NK; ++m) {
+          const int e = 4 * (tid + 256 * m), r = e / DK, c = e % DK;
+          sQt[(c + 0) * LT + r] = rw[m].x; sQt[(c + 1) * LT + r] = rw[m].y;
+          sQt[(c + 2) * LT + r] = rw[m].z; sQt[(c + 3) * LT + r] = rw[m].w;
+        }
+#pragma unroll
+        for (int m = 0; m < NP; ++m) {
+          const int e = 4 * (tid + 256 * m), r = e / C, i = e % C;
+          sPt[(i + 0) * LT + r] = rp[m].x; sPt[(i + 1) * LT + r] = rp[m].y;
+          sPt[(i + 2) * LT + r] = rp[m].z; sPt[(i + 3) * LT + r] = rp[m].w;
+        }
+      }
+      constexpr int NU = C * BV / 4 / 256;
+#pragma unroll
+      for (int m = 0; m < NU; ++m) {
+        const int e = 4 * (tid + 256 * m), r = e / BV, jj = e % BV;
+        const float4 x = xpart ? make_float4(0.f, 0.f, 0.f, 0.f)
+                               : *reinterpret_cast<const float4 *>(
+                                     Ug + slab * C * DV + (size_t)r * DV + vcol0 + jj);
+        *reinterpret_cast<float4 *>(sU + r * LS + jj) = x;
+      }
+      if (tid < DK) sD[tid] = Dg[slab * DK + tid];
     }
-    for (int e = tid; e < C * BV; e += 256) {
-      int r = e / BV, c = e % BV;
-      sU[r * LS + c] = xpart ? 0.f : Ug[slab * C * DV + (size_t)r * DV + vcol0 + c];
-    }
-    if (need_o)
-      for (int e = tid; e < C * C; e += 256) sP[(e / C) * LP + e % C] = Pg[slab * C * C + e];
-    if (tid < DK) sD[tid] = Dg[slab * DK + tid];
     __syncthreads();
 
-    // U = Ut - W S   (rows rt, rt+8, ...)
-    float u[C / 8];
-#pragma unroll
-    for (int m = 0; m < C / 8; ++m) u[m] = sU[(rt + 8 * m) * LS + jt];
-    for (int c = 0; c < DK; ++c) {
-      float sv = sS[c * LS + jt];
-#pragma unroll
-      for (int m = 0; m < C / 8; ++m) u[m] = fmaf(-sW[(rt + 8 * m) * LK + c], sv, u[m]);
+    // U = U~ - W S   (rows r0, r0 + 1)
+    float u0[4], u1[4];
+    {
+      const float4 a = *reinterpret_cast<const float4 *>(sU + r0 * LS + jl);
+      const float4 b = *reinterpret_cast<const float4 *>(sU + (r0 + 1) * LS + jl);
+      u0[0] = a.x; u0[1] = a.y; u0[2] = a.z; u0[3] = a.w;
+      u1[0] = b.x; u1[1] = b.y; u1[2] = b.z; u1[3] = b.w;
     }
-    __syncthreads();
-#pragma unroll
-    for (int m = 0; m < C / 8; ++m) sU[(rt + 8 * m) * LS + jt] = u[m];
-    if (mode == 0 && save.Ub)
-#pragma unroll
-      for (int m = 0; m < C / 8; ++m) save.Ub[(slab * C + rt + 8 * m) * DV + j0 + jt] = u[m];
+#pragma unroll 4
+    for (int c = 0; c < DK; ++c) {
+      const float2 w = *reinterpret_cast<const float2 *>(sWt + c * LT + r0);
+      const float4 x = *reinterpret_cast<const float4 *>(sS + c * LS + jl);
+      u0[0] = fmaf(-w.x, x.x, u0[0]); u0[1] = fmaf(-w.x, x.y, u0[1]);
+      u0[2] = fmaf(-w.x, x.z, u0[2]); u0[3] = fmaf(-w.x, x.w, u0[3]);
+      u1[0] = fmaf(-w.y, x.x, u1[0]); u1[1] = fmaf(-w.y, x.y, u1[1]);
+      u1[2] = fmaf(-w.y, x.z, u1[2]); u1[3] = fmaf(-w.y, x.w, u1[3]);
+    }
+    __syncthreads();  // every thread has read U~
+    *reinterpret_cast<float4 *>(sU + r0 * LS + jl) = make_float4(u0[0], u0[1], u0[2], u0[3]);
+    *reinterpret_cast<float4 *>(sU + (r0 + 1) * LS + jl) = make_float4(u1[0], u1[1], u1[2], u1[3]);
+    if (mode == 0 && save.Ub) {
+      *reinterpret_cast<float4 *>(save.Ub + (slab * C + r0) * DV + j0 + jl) =
+          make_float4(u0[0], u0[1], u0[2], u0[3]);
+      *reinterpret_cast<float4 *>(save.Ub + (slab * C + r0 + 1) * DV + j0 + jl) =
+          make_float4(u1[0], u1[1], u1[2], u1[3]);
+    }
     __syncthreads();
 
     if (need_o) {
-      // O = Qt S + P U
-      float o[C / 8] = {};
+      // O = Q~ S + P U   (P[r][i] = 0 for i > r)
+      float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
       for (int c = 0; c < DK; ++c) {
-        float sv = sS[c * LS + jt];
-#pragma unroll
-        for (int m = 0; m < C / 8; ++m) o[m] = fmaf(sQ[(rt + 8 * m) * LK + c], sv, o[m]);
+        const float2 q = *reinterpret_cast<const float2 *>(sQt + c * LT + r0);
+        const float4 x = *reinterpret_cast<const float4 *>(sS + c * LS + jl);
+        o0[0] = fmaf(q.x, x.x, o0[0]); o0[1] = fmaf(q.x, x.y, o0[1]);
+        o0[2] = fmaf(q.x, x.z, o0[2]); o0[3] = fmaf(q.x, x.w, o0[3]);
+        o1[0] = fmaf(q.y, x.x, o1[0]); o1[1] = fmaf(q.y, x.y, o1[1]);
+        o1[2] = fmaf(q.y, x.z, o1[2]); o1[3] = fmaf(q.y, x.w, o1[3]);
       }
+      for (int i = 0; i <= r0 + 1; ++i) {
+        const float2 p = *reinterpret_cast<const float2 *>(sPt + i * LT + r0);
+        const float4 x = *reinterpret_cast<const float4 *>(sU + i * LS + jl);
+        o0[0] = fmaf(p.x, x.x, o0[0]); o0[1] = fmaf(p.x, x.y, o0[1]);
+        o0[2] = fmaf(p.x, x.z, o0[2]); o0[3] = fmaf(p.x, x.w, o0[3]);
+        o1[0] = fmaf(p.y, x.x, o1[0]); o1[1] = fmaf(p.y, x.y, o1[1]);
+        o1[2] = fmaf(p.y, x.z, o1[2]); o1[3] = fmaf(p.y, x.w, o1[3]);
+      }
+      const float *orow[2] = {o0, o1};
 #pragma unroll
-      for (int m = 0; m < C / 8; ++m) {
-        const int r = rt + 8 * m;
-        float acc = o[m];
-        for (int i = 0; i <= r; ++i) acc = fmaf(sP[r * LP + i], sU[i * LS + jt], acc);
-        if (save.O) save.O[(slab * C + r) * DV + j0 + jt] = acc;
-        if (write_o && r < len) {
-          size_t g = ((size_t)(t0 + r) * H + h) * DV + j0 + jt;
-          float gv = gate ? prep_gate(to_f32(gate[g]), flags) : 1.f;
-          out[g] = from_f32<Tout>(scale * gv * acc);
-        }
+      for (int v = 0; v < 2; ++v) {
+        const int r = r0 + v;
+        if (save.O)
+          *reinterpret_cast<float4 *>(save.O + (slab * C + r) * DV + j0 + jl) =
+              make_float4(orow[v][0], orow[v][1], orow[v][2], orow[v][3]);
+        if (write_o && r < len)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const size_t g = ((size_t)(t0 + r) * H + h) * DV + j0 + jl + q;
+            const float gv = gate ? prep_gate(to_f32(gate[g]), flags) : 1.f;
+            out[g] = from_f32<Tout>(scale * gv * orow[v][q]);
+          }
       }
     }
 
-    // S = Diag(e^{G_C}) S + Kd^T U
-    float ns[DK / 8];
+    // S = Diag(e^{G_C}) S + K_d^T U   (rows 4rg .. 4rg + 3)
+    float ns[4][4];
+    if (s_rows) {
+      const int c0 = 4 * rg;
 #pragma unroll
-    for (int m = 0; m < DK / 8; ++m) {
-      const int c = rt + 8 * m;
-      float acc = sD[c] * sS[c * LS + jt];
-      for (int i = 0; i < C; ++i) acc = fmaf(sKd[i * LK + c], sU[i * LS + jt], acc);
-      ns[m] = acc;
+      for (int v = 0; v < 4; ++v) {
+        const float4 x = *reinterpret_cast<const float4 *>(sS + (c0 + v) * LS + jl);
+        const float d = sD[c0 + v];
+        ns[v][0] = d * x.x; ns[v][1] = d * x.y; ns[v][2] = d * x.z; ns[v][3] = d * x.w;
+      }
+#pragma unroll 4
+      for (int i = 0; i < C; ++i) {
+        const float4 k4 = *reinterpret_cast<const float4 *>(sKd + i * LK + c0);
+        const float4 x = *reinterpret_cast<const float4 *>(sU + i * LS + jl);
+        const float ka[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          ns[v][0] = fmaf(ka[v], x.x, ns[v][0]); ns[v][1] = fmaf(ka[v], x.y, ns[v][1]);
+          ns[v][2] = fmaf(ka[v], x.z, ns[v][2]); ns[v][3] = fmaf(ka[v], x.w, ns[v][3]);
+        }
+      }
     }
     __syncthreads();
+    if (s_rows) {
 #pragma unroll
-    for (int m = 0; m < DK / 8; ++m) sS[(rt + 8 * m) * LS + jt] = ns[m];
-    if (mode == 0)
-      if (float *cp = ckpt_after_chunk(ck, s, jc, ls, H, h, DK, DV))
+      for (int v = 0; v < 4; ++v)
+        *reinterpret_cast<float4 *>(sS + (4 * rg + v) * LS + jl) =
+            make_float4(ns[v][0], ns[v][1], ns[v][2], ns[v][3]);
+      if (mode == 0)
+        if (float *cp = ckpt_after_chunk(ck, s, jc, ls, H, h, DK, DV))
 #pragma unroll
-        for (int m = 0; m < DK / 8; ++m) cp[(size_t)(rt + 8 * m) * DV + j0 + jt] = ns[m];
+          for (int v = 0; v < 4; ++v)
+            *reinterpret_cast<float4 *>(cp + (size_t)(4 * rg + v) * DV + j0 + jl) =
+                make_float4(ns[v][0], ns[v][1], ns[v][2], ns[v][3]);
+    }
     __syncthreads();
   }
 
   // final state
-  for (int c = rt; c < DK; c += 8) {
-    float x = sS[c * LS + jt];
+  for (int e = tid; e < DK * BV; e += 256) {
+    const int c = e / BV, jj = e % BV;
+    const float x = sS[c * LS + jj];
     if (mode == 0) {
-      if (S_final) S_final[(((size_t)s * H + h) * DK + c) * DV + j0 + jt] = x;
+      if (S_final) S_final[(((size_t)s * H + h) * DK + c) * DV + j0 + jj] = x;
     } else if (xpart) {
-      X_out[(((size_t)s * H + h) * DK + c) * DK + j0 + jt] = x;
+      X_out[(((size_t)s * H + h) * DK + c) * DK + j0 + jj] = x;
     } else {
-      Z_out[(((size_t)s * H + h) * DK + c) * DV + vcol0 + jt] = x;
+      Z_out[(((size_t)s * H + h) * DK + c) * DV + vcol0 + jj] = x;
     }
   }
 }
@@ -428,7 +517,8 @@ constexpr size_t prep_smem() {
 }
 template <int DK>
 constexpr size_t state_smem() {
-  return sizeof(float) * (DK * (BV + 1) + C * (BV + 1) + 3 * C * (DK + 1) + C * (C + 1) + DK);
+  return sizeof(float) * (DK * (BV + 4) + C * (BV + 4) + 2 * DK * (C + 2) + C * (DK + 4) +
+                          C * (C + 2) + DK);
 }
 
 template <int DK, int DV, typename Tin>
