@@ -297,6 +297,71 @@ struct GemmArgs {
 
 constexpr int GKT = 32;  // K tile
 
+// One K tile of op(A) (64 x 32) and op(B) (32 x N) in registers: 16-byte loads along the
+// contiguous axis of each operand (every leading dimension and tile origin is a multiple of 4).
+template <int N>
+struct GemmTile {
+  static constexpr int NA = GKT * C / 4 / 256, NB = GKT * N / 4 / 256;
+  float4 a[NA], b[NB];
+  __device__ __forceinline__ void load(const GemmTerm &t, const float *A, const float *B, int k0,
+                                       int tid) {
+#pragma unroll
+    for (int m = 0; m < NA; ++m) {
+      const int e = tid + 256 * m;
+      if (t.a_t) {  // (k, 4 consecutive m)
+        const int kk = e / (C / 4), m4 = 4 * (e % (C / 4));
+        a[m] = *reinterpret_cast<const float4 *>(A + (size_t)(k0 + kk) * t.lda + m4);
+      } else {      // (m, 4 consecutive k)
+        const int mm = e / (GKT / 4), k4 = 4 * (e % (GKT / 4));
+        a[m] = *reinterpret_cast<const float4 *>(A + (size_t)mm * t.lda + k0 + k4);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < NB; ++m) {
+      const int e = tid + 256 * m;
+      if (t.b_t) {  // (n, 4 consecutive k)
+        const int n = e / (GKT / 4), k4 = 4 * (e % (GKT / 4));
+        b[m] = *reinterpret_cast<const float4 *>(B + (size_t)n * t.ldb + k0 + k4);
+      } else {      // (k, 4 consecutive n)
+        const int kk = e / (N / 4), n4 = 4 * (e % (N / 4));
+        b[m] = *reinterpret_cast<const float4 *>(B + (size_t)(k0 + kk) * t.ldb + n4);
+      }
+    }
+  }
+  // to shared memory as sA[k][m] (pitch C + 1) and sB[k][n] (pitch N + 1), alpha folded into A
+  __device__ __forceinline__ void store(const GemmTerm &t, float *sA, float *sB, int tid) const {
+    constexpr int PA = C + 1, PB = N + 1;
+#pragma unroll
+    for (int m = 0; m < NA; ++m) {
+      const int e = tid + 256 * m;
+      const float v[4] = {t.alpha * a[m].x, t.alpha * a[m].y, t.alpha * a[m].z, t.alpha * a[m].w};
+      if (t.a_t) {
+        const int kk = e / (C / 4), m4 = 4 * (e % (C / 4));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sA[kk * PA + m4 + q] = v[q];
+      } else {
+        const int mm = e / (GKT / 4), k4 = 4 * (e % (GKT / 4));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sA[(k4 + q) * PA + mm] = v[q];
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < NB; ++m) {
+      const int e = tid + 256 * m;
+      const float v[4] = {b[m].x, b[m].y, b[m].z, b[m].w};
+      if (t.b_t) {
+        const int n = e / (GKT / 4), k4 = 4 * (e % (GKT / 4));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sB[(k4 + q) * PB + n] = v[q];
+      } else {
+        const int kk = e / (N / 4), n4 = 4 * (e % (N / 4));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sB[kk * PB + n4 + q] = v[q];
+      }
+    }
+  }
+};
+
 template <int N>
 __global__ void __launch_bounds__(256) kda_bwd_gemm(GemmArgs g, int H,
                                                     const ChunkMeta *__restrict__ meta) {
@@ -312,37 +377,34 @@ __global__ void __launch_bounds__(256) kda_bwd_gemm(GemmArgs g, int H,
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int jj = 0; jj < NJ; ++jj) acc[i][jj] = 0.f;
-  for (int ti = 0; ti < g.nterms; ++ti) {
-    const GemmTerm t = g.t[ti];
-    const float *A = t.A + slab * t.sA, *B = t.B + slab * t.sB;
-    for (int k0 = 0; k0 < t.K; k0 += GKT) {
-      __syncthreads();  // previous tile consumed
-      for (int e = tid; e < GKT * C; e += 256) {
-        int m, kk;
-        if (t.a_t) { kk = e / C; m = e % C; }      // coalesced along m
-        else { m = e / GKT; kk = e % GKT; }        // coalesced along k
-        const float x = t.a_t ? A[(size_t)(k0 + kk) * t.lda + m] : A[(size_t)m * t.lda + k0 + kk];
-        sA[kk * PA + m] = t.alpha * x;
-      }
-      for (int e = tid; e < GKT * N; e += 256) {
-        int n, kk;
-        if (t.b_t) { n = e / GKT; kk = e % GKT; }  // coalesced along k
-        else { kk = e / N; n = e % N; }            // coalesced along n
-        sB[kk * PB + n] = t.b_t ? B[(size_t)n * t.ldb + k0 + kk] : B[(size_t)(k0 + kk) * t.ldb + n];
-      }
-      __syncthreads();
+  // the K tiles of all terms in order; tile i + 1 is loaded while tile i is multiplied
+  const int nt0 = g.t[0].K / GKT, ntiles = nt0 + (g.nterms > 1 ? g.t[1].K / GKT : 0);
+  auto term_of = [&](int i) -> const GemmTerm & { return i < nt0 ? g.t[0] : g.t[1]; };
+  auto k0_of = [&](int i) { return (i < nt0 ? i : i - nt0) * GKT; };
+  GemmTile<N> tile;
+  {
+    const GemmTerm &t = term_of(0);
+    tile.load(t, t.A + slab * t.sA, t.B + slab * t.sB, 0, tid);
+  }
+  for (int i = 0; i < ntiles; ++i) {
+    __syncthreads();  // previous tile consumed
+    tile.store(term_of(i), sA, sB, tid);
+    __syncthreads();
+    if (i + 1 < ntiles) {
+      const GemmTerm &t = term_of(i + 1);
+      tile.load(t, t.A + slab * t.sA, t.B + slab * t.sB, k0_of(i + 1), tid);
+    }
 #pragma unroll 8
-      for (int kk = 0; kk < GKT; ++kk) {
-        float a[4], b[NJ];
+    for (int kk = 0; kk < GKT; ++kk) {
+      float a[4], b[NJ];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = sA[kk * PA + 4 * ty + i];
+      for (int q = 0; q < 4; ++q) a[q] = sA[kk * PA + 4 * ty + q];
 #pragma unroll
-        for (int jj = 0; jj < NJ; ++jj) b[jj] = sB[kk * PB + tx + 16 * jj];
+      for (int jj = 0; jj < NJ; ++jj) b[jj] = sB[kk * PB + tx + 16 * jj];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+      for (int q = 0; q < 4; ++q)
 #pragma unroll
-          for (int jj = 0; jj < NJ; ++jj) acc[i][jj] = fmaf(a[i], b[jj], acc[i][jj]);
-      }
+        for (int jj = 0; jj < NJ; ++jj) acc[q][jj] = fmaf(a[q], b[jj], acc[q][jj]);
     }
   }
   float *Cm = g.Cm + slab * g.sC;
