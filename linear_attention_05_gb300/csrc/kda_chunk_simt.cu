@@ -143,24 +143,56 @@ __global__ void __launch_bounds__(256) kda_prep_simt(
   const int64_t t0 = ts + (int64_t)j * C;
   const int len = (int)min((int64_t)C, ls - (int64_t)j * C);
 
-  // load (rows >= len are zero: no write, no read-out, no decay)
-  for (int e = tid; e < C * DK; e += 256) {
-    int r = e / DK, c = e % DK;
-    float kv = 0.f, qv = 0.f, lv = 0.f;
-    if (r < len) {
-      size_t g = ((size_t)(t0 + r) * H + h) * DK + c;
-      kv = to_f32(k[g]);
-      qv = to_f32(q[g]);
-      lv = prep_log_alpha(to_f32(la[g]), flags);
-      if ((flags & KDA_DEBUG_CHECK) && !(lv >= kLogAlphaMin && lv <= 0.f)) set_err(kErrPrecondition);
+  // load (rows >= len are zero: no write, no read-out, no decay). 8-element vectors, all of a
+  // tensor's loads issued before its shared-memory stores.
+  {
+    constexpr int NVK = C * DK / 8 / 256, NVV = C * DV / 8 / 256;
+    float kv[NVK][8], qv[NVK][8], lv[NVK][8];
+#pragma unroll
+    for (int m = 0; m < NVK; ++m) {
+      const int e = 8 * (tid + 256 * m), r = e / DK, c = e % DK;
+      if (r < len) {
+        const size_t g = ((size_t)(t0 + r) * H + h) * DK + c;
+        load8(k + g, kv[m]);
+        load8(q + g, qv[m]);
+        load8(la + g, lv[m]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) kv[m][u] = qv[m][u] = lv[m][u] = 0.f;
+      }
     }
-    sKh[r * LK + c] = kv;
-    sQt[r * LK + c] = qv;
-    sKt[r * LK + c] = lv;
-  }
-  for (int e = tid; e < C * DV; e += 256) {
-    int r = e / DV, c = e % DV;
-    sV[r * LV + c] = r < len ? to_f32(v[((size_t)(t0 + r) * H + h) * DV + c]) : 0.f;
+#pragma unroll
+    for (int m = 0; m < NVK; ++m) {
+      const int e = 8 * (tid + 256 * m), r = e / DK, c = e % DK;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float l = 0.f;
+        if (r < len) {
+          l = prep_log_alpha(lv[m][u], flags);
+          if ((flags & KDA_DEBUG_CHECK) && !(l >= kLogAlphaMin && l <= 0.f)) set_err(kErrPrecondition);
+        }
+        sKh[r * LK + c + u] = kv[m][u];
+        sQt[r * LK + c + u] = qv[m][u];
+        sKt[r * LK + c + u] = l;
+      }
+    }
+    float vv[NVV][8];
+#pragma unroll
+    for (int m = 0; m < NVV; ++m) {
+      const int e = 8 * (tid + 256 * m), r = e / DV, c = e % DV;
+      if (r < len) {
+        load8(v + ((size_t)(t0 + r) * H + h) * DV + c, vv[m]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) vv[m][u] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < NVV; ++m) {
+      const int e = 8 * (tid + 256 * m), r = e / DV, c = e % DV;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sV[r * LV + c + u] = vv[m][u];
+    }
   }
   if (tid < C) {
     float b = tid < len ? prep_beta(to_f32(beta[(size_t)(t0 + tid) * H + h]), flags) : 0.f;
