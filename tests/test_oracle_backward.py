@@ -1,6 +1,6 @@
 """Pins for the backward oracle (oracle/autograd.py), CPU only.
 
-The autograd oracle is trusted only through checks that do not use it to judge
+The autograd oracle is trusted only through checks that do not use it to check
 itself:
 * its forward equals the (separately pinned) C oracle;
 * every gradient matches central finite differences, along random directions,
