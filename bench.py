@@ -209,6 +209,17 @@ def cpu_baseline(target_s: float = 12.0):
                       f"({ntok} tokens, {ntok * 16} token-heads) in {dt:.2f} s"}
 
 
+METRIC = "KDA prefill Mtok/s & % tensor peak; decode state GB/s vs GB300 HBM peak"
+
+
+def prefill_config(world):
+    return {"workload": "prefill B=4 T=4096 H=16 dk=dv=128 chunk=64, bf16 inputs, "
+                        "fp32 initial/final state",
+            "global_batch": PREFILL["B"] * world, "seq_len": PREFILL["T"],
+            "parallelism": f"independent batch per GPU x{world}",
+            "l2": "inputs (~400 MB) larger than L2; no flush"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -222,12 +233,11 @@ def run_reference(args, rank, world):
     total = sum(steps)
     val = n_tok * len(steps) / total / 1e6
     line = {
-        "impl": "reference", "metric": "KDA prefill Mtok/s", "value": round(val, 6),
+        "impl": "reference", "metric": METRIC, "value": round(val, 6),
         "unit": "Mtok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total / len(steps), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "prefill B=4 T=4096 H=16 dk=dv=128 bf16 inputs, fp32 state",
-                   "sample_tokens_per_sequence": args.ref_tokens},
+        "config": prefill_config(world),
         "cpu_baseline": {"value": round(val, 6), "unit": "Mtok/s", "cores": cores,
                          "kind": "oracle",
                          "sample": f"first {args.ref_tokens} tokens of each of the 4 sequences"
@@ -369,17 +379,13 @@ def run_gpu(args, rank, world, local):
     del host, dev_in
 
     line = {
-        "metric": "KDA prefill Mtok/s & % tensor peak; decode state GB/s vs GB300 HBM peak",
+        "metric": METRIC,
         "value": round(value, 3), "unit": "Mtok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; q,k unit-norm N(0,1), v N(0,1), beta/gate sigmoid(N(0,1)), "
                 "log_alpha max(-exp(N(-3,1)), log 0.5))",
-        "config": {"workload": "prefill B=4 T=4096 H=16 dk=dv=128 chunk=64, bf16 inputs, "
-                               "fp32 initial/final state",
-                   "global_batch": PREFILL["B"] * world, "seq_len": PREFILL["T"],
-                   "parallelism": f"independent batch per GPU x{world}",
-                   "l2": "inputs (~400 MB) larger than L2; no flush"},
+        "config": prefill_config(world),
         "roofline": roofline, "e2e": e2e, "clocks": clocks,
         "gpu_launches": 3 * args.steps,
     }
