@@ -204,9 +204,14 @@ def cpu_baseline(target_s: float = 12.0):
     per_tok = dt / ntok
     n = int(min(PREFILL["T"], max(64, target_s / per_tok / PREFILL["B"])))
     dt, ntok, cores = oracle_prefill_sample(n)
+    # the same oracle on one thread, on a sample a sixteenth as long
+    n1 = max(16, n // 16)
+    dt1, ntok1, _ = oracle_prefill_sample(n1, threads=1)
     return {"value": ntok / dt / 1e6, "unit": "Mtok/s", "cores": cores, "kind": "oracle",
             "sample": f"first {n} tokens of each of the 4 sequences x 16 heads "
-                      f"({ntok} tokens, {ntok * 16} token-heads) in {dt:.2f} s"}
+                      f"({ntok} tokens, {ntok * 16} token-heads) in {dt:.2f} s",
+            "one_thread": {"value": ntok1 / dt1 / 1e6, "unit": "Mtok/s",
+                           "sample": f"first {n1} tokens of each sequence in {dt1:.2f} s"}}
 
 
 METRIC = "KDA prefill Mtok/s & % tensor peak; decode state GB/s vs GB300 HBM peak"
@@ -392,6 +397,7 @@ def run_gpu(args, rank, world, local):
 
     if rank == 0 and not args.skip_extra:
         line["decode"] = bench_decode(dev, pk, stream)
+        line["varlen"] = bench_varlen(dev, pk, stream)
         line["segment_scan"] = bench_segment_scan(dev, pk, stream)
         line["scan_combine"] = bench_scan(dev, pk, stream)
         line["prefill_checkpoints"] = bench_checkpoints(dev, pk, stream)
@@ -524,6 +530,40 @@ def bench_segment_scan(dev, pk, stream, reps=2):
             "scan_gbs": round(scan_bytes / (tot[1] * 1e-3) / 1e9, 1),
             "summary_alg_gbs": round(th * (3 * d * 2 + 2) / (tot[0] * 1e-3) / 1e9, 1),
             "gpu_launches": 12 * reps}
+
+
+def bench_varlen(dev, pk, stream, reps=10):
+    """8 packed sequences (lengths drawn from [1024, 32768], about 112K tokens), 32 heads,
+    dk=dv=128, bf16, zero initial state: kda_chunk_fwd with cu_seqlens."""
+    import linear_attention_05_gb300 as kda
+    from linear_attention_05_gb300 import inputs
+
+    w = inputs.WORKLOADS["varlen"]
+    x = inputs.make(w, device=dev)
+    T, H, d, n_seq = w.T_total, w.H, w.dk, len(w.lengths)
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((n_seq, H, d, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(kda.kda_chunk_fwd_workspace_size(T, n_seq, H, d, d), dtype=torch.uint8,
+                     device=dev)
+
+    def run():
+        kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], out,
+                          None, fs, x["cu_seqlens"], n_seq, workspace=ws, stream=stream)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    return {"workload": f"varlen {n_seq} packed sequences ({T} tokens, longest "
+                        f"{max(w.lengths)}) H=32 dk=dv=128 bf16",
+            "value": round(T / (ms * 1e-3) / 1e6, 3), "unit": "Mtok/s", "ms": round(ms, 3),
+            "gpu_launches": 3 * reps}
 
 
 def bench_checkpoints(dev, pk, stream, reps=20, every=1024):
@@ -694,7 +734,8 @@ def run_part(args, local):
     pk = peaks()
     stream = torch.cuda.current_stream()
     fn = {"decode": bench_decode, "segscan": bench_segment_scan, "scan": bench_scan,
-          "ckpt": bench_checkpoints, "bwd": bench_backward, "gates": bench_gates}[args.only]
+          "ckpt": bench_checkpoints, "bwd": bench_backward, "gates": bench_gates,
+          "varlen": bench_varlen}[args.only]
     print(json.dumps({"part": args.only, **fn(dev, pk, stream)}), flush=True)
 
 
@@ -708,7 +749,7 @@ def main():
                     help="reference arm: tokens per sequence timed per step")
     ap.add_argument("--skip-extra", action="store_true", help="prefill line only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", default=None, choices=["decode", "segscan", "scan", "ckpt", "bwd", "gates"],
+    ap.add_argument("--only", default=None, choices=["decode", "segscan", "scan", "ckpt", "bwd", "gates", "varlen"],
                     help="run one part of the path alone and print its numbers (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
