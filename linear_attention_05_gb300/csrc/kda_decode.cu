@@ -10,7 +10,8 @@
 // once into registers with 16-byte loads, reduces the two dk-long dot products
 // per column across warps through shared memory, and writes the state once.
 // The kernel moves 2 * dk * dv * 4 bytes of state per (sequence, head) and is
-// bound by HBM bandwidth.
+// bound by HBM bandwidth; three blocks per SM (78 registers) keep more state
+// loads in flight than two.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -23,7 +24,7 @@ __device__ unsigned g_decode_err;
 namespace {
 
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(256) kda_decode_kernel(
+__global__ void __launch_bounds__(256, 3) kda_decode_kernel(
     const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
     const T *__restrict__ la, const T *__restrict__ beta, const T *__restrict__ gate,
     T *__restrict__ out, float *__restrict__ state, const int32_t *__restrict__ slot,
