@@ -56,8 +56,8 @@ constexpr int kPrefetch = 3;           // cards prefetched into L2 beyond the ri
 constexpr int B_STAGE_TX = CARD_BCT + 512;  // [Phi'^T | Q'^T] then e^{G_C} (49664 bytes)
 constexpr int B_STAGE_BYTES = 50176;  // B_STAGE_TX rounded up to 1024
 constexpr int B_SA = B_NSTAGE * B_STAGE_BYTES;  // S^T bf16 operand, 128 x 128 K-major (32768)
-constexpr int B_OT = B_SA + 32768;         // output transposes: 4 warps x 2 x 32 x 33 fp32
-constexpr int B_DYN = B_OT + 4 * 2 * 32 * 33 * 4 + 1024;
+constexpr int B_OT = B_SA + 32768;         // output tile: 64 tokens x (128 + 4) fp32
+constexpr int B_DYN = B_OT + 64 * (DD + 4) * 4 + 1024;
 
 __device__ __forceinline__ void set_err(unsigned bits) { atomicOr(&g_tc_err, bits); }
 
@@ -815,13 +815,16 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
         }
     }
   } else if (with_o) {
-    // output group: o = scale * g * (Q' S + O_intra) for chunk n. Each warp owns 32 value
-    // channels (its lane quadrant). The output block of chunk n starts as O_intra^T (seeded
-    // two chunks ahead from the card), so the MMA leaves Q' S + O_intra in it. Each 32 x 32
-    // (channel x token) half is transposed through shared memory so that gate loads and output
-    // stores are 16-byte vectors; the gate is prefetched one chunk ahead.
-    float *ot = reinterpret_cast<float *>(sm + B_OT) + quad * 2 * 32 * 33;
-    const int jc = quad * 32;  // first channel of this warp
+    // output group: o = scale * g * (Q' S + O_intra) for chunk n. The output block of chunk n
+    // starts as O_intra^T (seeded two chunks ahead from the card), so the MMA leaves
+    // Q' S + O_intra in it. The four warps copy their lane quadrants (channels) into one
+    // [64 tokens][128 channels] fp32 tile; then each thread takes 8 tokens x 8 channels, so
+    // that a warp's gate loads and output stores cover two whole 256-byte rows per
+    // instruction. The gate of the next chunk is loaded (same mapping) as this one is used.
+    constexpr int LDT = DD + 4;  // tile row pitch (floats)
+    float *tile = reinterpret_cast<float *>(sm + B_OT);
+    const int ot = tid - 256;                   // output thread 0..127
+    const int c8 = ot & 15, r0 = ot >> 4;       // store phase: channels 8*c8.., tokens r0 + 8m
     const bool logits = gate && (flags & KDA_GATE_LOGITS);
     // this lane's O_intra^T row (all 64 tokens, bf16) of chunk c, from the card
     auto load_oi = [&](int c, uint4 *oi) {
@@ -840,19 +843,16 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
         tmem_st32(tmem_addr(tb, quad * 32, set_col(c) + 128 + 32 * hf), x);
       }
     };
-    // gate of token (hf * 32 + lane) of chunk c, channels jc + 8i .. +8 (1.0 when absent)
-    auto load_gate = [&](int c, uint4 (*gq)[4]) {
+    // gate of tokens r0 + 8m, channels 8*c8 .. 8*c8 + 7 of chunk c (1.0 when absent)
+    auto load_gate = [&](int c, uint4 *gq) {
       const int64_t tc0 = ts + (int64_t)c * C;
       const int lc = (int)min((int64_t)C, ls - (int64_t)c * C);
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int r = hf * 32 + lane;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          gq[hf][i] = (gate && c < nchunks && r < lc)
-                          ? *reinterpret_cast<const uint4 *>(
-                                gate + ((size_t)(tc0 + r) * H + h) * DD + jc + 8 * i)
-                          : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+      for (int m = 0; m < 8; ++m) {
+        const int r = r0 + 8 * m;
+        gq[m] = (gate && c < nchunks && r < lc)
+                    ? *reinterpret_cast<const uint4 *>(gate + ((size_t)(tc0 + r) * H + h) * DD + c8 * 8)
+                    : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
       }
     };
     {
@@ -868,60 +868,52 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
     mbar_arrive(&bar_ofree[0]);
     mbar_arrive(&bar_ofree[1]);
     uint32_t ofull_phase[2] = {0u, 0u};
-    uint4 gcur[2][4], gnext[2][4];
-    load_gate(0, gcur);
+    uint4 gq[8];
+    load_gate(0, gq);
+    bool ok = true;
     for (int n = 0; n < nchunks; ++n) {
       const int64_t t0 = ts + (int64_t)n * C;
       const int len = (int)min((int64_t)C, ls - (int64_t)n * C);
-      // loads for later chunks first, so that their latency overlaps this chunk's work
       uint4 oi[8];
-      load_oi(n + 2, oi);
-      load_gate(n + 1, gnext);
-      if (!mbar_wait(&bar_ofull[n & 1], ofull_phase[n & 1])) {
-        if (lane == 0) set_err(kErrTimeout);
-        break;
-      }
+      load_oi(n + 2, oi);  // its latency overlaps the wait below
+      // every output thread takes the same branch, so a timeout cannot strand the others
+      ok = named_bar_and(2, 128, mbar_wait(&bar_ofull[n & 1], ofull_phase[n & 1]));
+      if (!ok) break;
       ofull_phase[n & 1] ^= 1u;
       tc_fence_after();
-      // both halves to shared memory (row = channel, column = token), then the block goes
-      // back to the issuer, seeded with O_intra^T of chunk n + 2
+      // both halves into the tile (token row, this lane's channel)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float t[32];
         tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 128 + 32 * hf), t);
         tmem_wait_ld();
 #pragma unroll
-        for (int u = 0; u < 32; ++u) ot[hf * 32 * 33 + lane * 33 + u] = t[u];
+        for (int u = 0; u < 32; ++u) tile[(hf * 32 + u) * LDT + j] = t[u];
       }
+      // the block is read: seed it with O_intra^T of chunk n + 2, hand it back to the issuer
       seed(n + 2, oi);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar_ofree[n & 1]);
-      __syncwarp();
+      named_bar(2, 128);  // tile complete
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int r = hf * 32 + lane;  // this thread's token now
-        if (r < len) {
-          const float *oh = ot + hf * 32 * 33;
+      for (int m = 0; m < 8; ++m) {
+        const int r = r0 + 8 * m;
+        const float4 a = *reinterpret_cast<const float4 *>(tile + r * LDT + c8 * 8);
+        const float4 b = *reinterpret_cast<const float4 *>(tile + r * LDT + c8 * 8 + 4);
+        float g8[8], e[8];
+        unpack8(gq[m], g8);
+        const float x8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float g8[8], e[8];
-            unpack8(gcur[hf][i], g8);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float g = logits ? sigmoid_approx(g8[u]) : g8[u];
-              e[u] = scale * g * oh[(8 * i + u) * 33 + lane];
-            }
-            *reinterpret_cast<uint4 *>(out + ((size_t)(t0 + r) * H + h) * DD + jc + 8 * i) = pack8(e);
-          }
-        }
+        for (int u = 0; u < 8; ++u)
+          e[u] = scale * (logits ? sigmoid_approx(g8[u]) : g8[u]) * x8[u];
+        if (r < len)
+          *reinterpret_cast<uint4 *>(out + ((size_t)(t0 + r) * H + h) * DD + c8 * 8) = pack8(e);
       }
-      __syncwarp();  // the transposes are read before the next chunk overwrites them
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) gcur[hf][i] = gnext[hf][i];
+      load_gate(n + 1, gq);  // the next chunk's gate, while its MMAs run
+      named_bar(2, 128);     // tile consumed before the next chunk overwrites it
     }
+    if (!ok && ot == 0) set_err(kErrTimeout);
   }
   tc_fence_before();
   __syncthreads();
