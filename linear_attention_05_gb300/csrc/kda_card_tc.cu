@@ -1,35 +1,26 @@
-// Chunked KDA forward on the sm_103a tensor cores (bf16 inputs, dk = dv = 128).
+// Stage A of the chunked KDA forward on the sm_103a tensor cores (bf16 inputs,
+// dk = dv = 128): the update cards, one CTA per (chunk, head), two per SM.
 //
-// Structure (K3 training overview, zuoshipin.com/article/18261, section 4
-// "FlashKDA": per-chunk update cards prepared in parallel; only the state
-// hand-off and read-out run in order):
-//
-// Stage A, kda_card_tc: one CTA per (chunk, head), two per SM, builds the
-// chunk's update card from TMA-loaded, 128-byte-swizzled input tiles. With G the inclusive running sum of log_alpha inside the chunk,
-// Kt = k e^{G}, Kh = k e^{-G}, Qt = q e^{G}, Kd = k e^{G_C - G} (k, q L2-normalised):
+// K3 training overview (zuoshipin.com/article/18261), section 4 "FlashKDA": the update cards
+// (forget gate, Q/K normalisation, decay, intra-chunk correction matrix) are prepared in
+// parallel across chunks. From TMA-loaded, 128-byte-swizzled input tiles (card layout and
+// the resulting affine step in tc_card_layout.cuh):
 //   M  = strict_lower(diag(b) Kt Kh^T),   P = lower(Qt Kh^T)              (GEMM 1)
-//   T  = (I + M)^{-1}  (blocked forward substitution), T' = T diag(b)
+//   T  = (I + M)^{-1}  (16 x 16 diagonal blocks, two-level recursion), T' = T diag(b)
 //   W^T = Kt^T T'^T,   Ut^T = V^T T'^T                                    (GEMM 2)
 //   Q'  = Qt - P W,    O_intra = P Ut                                     (GEMM 3)
 //   Phi' = -Kd^T W,    B_c = Kd^T Ut                                      (GEMM 4)
-// so that, for the state S entering the chunk,
-//   S_next = Diag(e^{G_C}) S + Phi' S + B_c,   O = Q' S + O_intra,  o = scale g O.
 // (Derivation: U = Ut - W S, O = Qt S + P U, S_next = Diag(e^{G_C}) S + Kd^T U.)
-//
-// Stage B, kda_state_tc: one CTA per (sequence, head). The fp32 state lives in
-// tensor memory as S^T (lane = value channel). Per chunk the CTA pre-loads
-// Diag(e^{G_C}) S + B_c into tensor memory and issues one group of MMAs,
-// bf16(S^T) x [Phi'^T | Q'^T], accumulating onto it, so the serial path has a
-// single tensor-core round trip per chunk; two warpgroups stage the state and a
-// third turns the output accumulators into o while the next chunk's MMAs run.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "kda_common.cuh"
+#include "tc_card_layout.cuh"
 #include "tc_common.cuh"
 
 namespace kda {
@@ -39,69 +30,9 @@ __device__ unsigned g_tc_err;
 namespace {
 
 using namespace tc;
-
-constexpr int C = kChunk;  // 64
-constexpr int DD = 128;    // dk = dv
-
-// ---- update card (per chunk and head), bytes
-constexpr int CARD_PHIQ = 0;       // [Phi'^T | Q'^T]: MN-major tile, 128 rows x 192 cols, 3 atom cols
-constexpr int CARD_BCT = 49152;    // B_c^T: [16][128][8] bf16 (8-column chunks, lane-interleaved)
-constexpr int CARD_D = 81920;      // e^{G_C}: 128 fp32
-constexpr int CARD_OIT = 82432;    // O_intra^T: [8][128][8] bf16
-constexpr int CARD_BYTES = 98816;
-
-// ---- stage B shared memory
-constexpr int B_NSTAGE = 3;            // card ring depth
-constexpr int kPrefetch = 3;           // cards prefetched into L2 beyond the ring
-constexpr int B_STAGE_TX = CARD_BCT + 512;  // [Phi'^T | Q'^T] then e^{G_C} (49664 bytes)
-constexpr int B_STAGE_BYTES = 50176;  // B_STAGE_TX rounded up to 1024
-constexpr int B_SA = B_NSTAGE * B_STAGE_BYTES;  // S^T bf16 operand, 128 x 128 K-major (32768)
-constexpr int B_OT = B_SA + 32768;         // output tile: 64 tokens x (128 + 4) fp32
-constexpr int B_DYN = B_OT + 64 * (DD + 4) * 4 + 1024;
+using namespace tcl;
 
 __device__ __forceinline__ void set_err(unsigned bits) { atomicOr(&g_tc_err, bits); }
-
-__device__ __forceinline__ int find_seq(const int *off, int n_seq, int ci) {
-  int lo = 0, hi = n_seq - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (off[mid] <= ci) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
-__device__ __forceinline__ void seq_range(const int32_t *cu, int64_t fixed_len, int s, int64_t *t0,
-                                          int64_t *len) {
-  if (cu) {
-    *t0 = cu[s];
-    *len = (int64_t)cu[s + 1] - cu[s];
-  } else {
-    *t0 = (int64_t)s * fixed_len;
-    *len = fixed_len;
-  }
-}
-
-__device__ __forceinline__ float bf(const uint8_t *base, uint32_t off) {
-  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
-}
-__device__ __forceinline__ uint4 pack8(const float *v) {
-  uint4 u;
-  u.x = pack_bf16x2(v[0], v[1]);
-  u.y = pack_bf16x2(v[2], v[3]);
-  u.z = pack_bf16x2(v[4], v[5]);
-  u.w = pack_bf16x2(v[6], v[7]);
-  return u;
-}
-__device__ __forceinline__ void unpack8(uint4 u, float *v) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
-
-// fp32 64x64 matrix in shared memory with a padded row pitch.
 __device__ __forceinline__ int mix(int r, int c) { return r * 65 + c; }
 
 // ===========================================================================
@@ -562,363 +493,6 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
   if (warp == 1) tmem_dealloc(tb, 256);
 }
 
-// ===========================================================================
-// Stage B: the sequential state pass, one CTA per (sequence, head), 384 threads.
-// Warps 0-7 (state group) carry the serial path: warp w serves tensor-memory
-// lanes 32*(w%4).. (lane j = value channel j, i.e. row j of S^T) and the key
-// columns [64*(w/4), 64*(w/4) + 64) of that row. Warps 8-11 (output group) read
-// the chunk outputs from the same lanes, add O_intra, apply scale and gate and
-// store o, off the serial path. mode 0: prefill; mode 1: segment summary on
-// [X | Z] (blockIdx.y = 0: X with entry I; 1: Z with entry 0), no output.
-//
-// Tensor memory holds two accumulator sets, chunk n using set n % 2: columns
-// [256b, 256b+128) the fp32 state S^T, [256b+128, 256b+192) the output block.
-// Before the MMAs of chunk n the set is pre-loaded with Diag(e^{G_C}) S + B_c
-// (state group) and zeros (output group), so one N = 192 MMA chain per chunk
-// produces both the next state and the chunk output.
-// mbarriers: bar_full[3] card stages landed; bar_mma chunk MMAs done (state
-// group); bar_ofull[2] output block written (output group); bar_ofree[2]
-// output block read and re-zeroed (MMA issuer).
-__global__ void __launch_bounds__(384, 1) kda_state_tc(
-    int mode, unsigned flags, const __nv_bfloat16 *__restrict__ gate,
-    __nv_bfloat16 *__restrict__ out,
-    const float *__restrict__ S0, float *__restrict__ S_final, float *__restrict__ X_out,
-    float *__restrict__ Z_out, const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len,
-    int H, float scale, const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
-    const uint8_t *__restrict__ cards, CkptOut ck) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[B_NSTAGE], bar_mma, bar_ofull[2], bar_ofree[2];
-  __shared__ uint32_t tmem_base;
-  __shared__ int s_fail;
-  if (meta->invalid) return;
-  uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t sb = smem_u32(sm);
-  const int chain = blockIdx.x, s = chain / H, h = chain % H, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const bool state_grp = warp < 8;
-  const int quad = warp & 3;           // lane quadrant of this warp
-  const int j = quad * 32 + lane;      // tensor-memory lane / value channel
-  const int half = (warp >> 2) & 1;    // state group: which 64 key columns
-  const bool xpart = (mode == 1 && blockIdx.y == 0);
-  const bool with_bc = !xpart;
-  const bool with_o = (mode == 0 && out != nullptr);
-
-  int64_t ts, ls;
-  seq_range(cu, fixed_len, s, &ts, &ls);
-  const int nchunks = (int)((ls + C - 1) / C);
-  const int cbase = nchunks > 0 ? off[s] : 0;
-  auto card_of = [&](int n) { return cards + ((size_t)(cbase + n) * H + h) * CARD_BYTES; };
-  // element (c, j) of the entry state, and where element (c, j) of the result goes
-  auto entry = [&](int c) -> float {
-    if (mode == 0) return S0 ? S0[(((size_t)s * H + h) * DD + c) * DD + j] : 0.f;
-    return (xpart && c == j) ? 1.f : 0.f;
-  };
-  auto result_ptr = [&](int c) -> float * {
-    if (mode == 0) return S_final ? S_final + (((size_t)s * H + h) * DD + c) * DD + j : nullptr;
-    if (xpart) return X_out + (((size_t)s * H + h) * DD + c) * DD + j;
-    return Z_out + (((size_t)s * H + h) * DD + c) * DD + j;
-  };
-  // prefix-cache checkpoint after chunk n (mode 0): this thread's 64 rows of column j
-  auto save_ckpt = [&](int n, const float *x0, const float *x1) {
-    if (mode != 0) return;
-    float *cp = ckpt_after_chunk(ck, s, n, ls, H, h, DD, DD);
-    if (cp == nullptr) return;
-#pragma unroll
-    for (int u = 0; u < 32; ++u) {
-      cp[(size_t)(64 * half + u) * DD + j] = x0[u];
-      cp[(size_t)(64 * half + 32 + u) * DD + j] = x1[u];
-    }
-  };
-  if (nchunks == 0) {
-    if (state_grp)
-      for (int c = 64 * half; c < 64 * half + 64; ++c) {
-        float *p = result_ptr(c);
-        if (p) *p = entry(c);
-      }
-    return;
-  }
-
-  if (warp == 0) {
-    tmem_alloc(&tmem_base, 512);
-    tmem_relinquish();
-  }
-  if (tid == 0) {
-    for (int i = 0; i < B_NSTAGE; ++i) mbar_init(&bar_full[i], 1);
-    mbar_init(&bar_mma, 1);
-    mbar_init(&bar_ofull[0], 1);
-    mbar_init(&bar_ofull[1], 1);
-    mbar_init(&bar_ofree[0], 128);
-    mbar_init(&bar_ofree[1], 128);
-    fence_mbar_init();
-    s_fail = 0;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tb = tmem_base;
-  auto set_col = [](int n) { return 256 * (n & 1); };
-  if (state_grp) {
-    int loads_issued = 0, loads_done = 0;
-    uint32_t full_phase[B_NSTAGE] = {}, mma_phase = 0u;
-    bool ok = true;
-    const bool loader = (tid == 32);  // issues the card copies, off the MMA issuer's path
-    auto stage_of = [](int n) { return n % B_NSTAGE; };
-    // card n -> stage n % 3: [Phi'^T | Q'^T] and e^{G_C}
-    auto load_card = [&](int n) {
-      const int st = stage_of(n);
-      uint8_t *dst = sm + st * B_STAGE_BYTES;
-      const uint8_t *src = card_of(n);
-      mbar_arrive_expect_tx(&bar_full[st], B_STAGE_TX);
-      for (int o = 0; o < CARD_BCT; o += 16384) bulk_g2s(dst + o, src + o, 16384, &bar_full[st]);
-      bulk_g2s(dst + CARD_BCT, src + CARD_D, 512, &bar_full[st]);
-      ++loads_issued;
-    };
-    auto wait_full = [&](int n) -> bool {
-      const int st = stage_of(n);
-      const bool r = mbar_wait(&bar_full[st], full_phase[st]);
-      full_phase[st] ^= 1u;
-      if (r) ++loads_done;
-      return r;
-    };
-    // this thread's 64 columns of B_c^T row j of chunk n, straight from the card in global
-    // memory (lane-interleaved: a warp reads 512 contiguous bytes per 8-column chunk)
-    uint4 bcr[8];
-    auto fetch_bc = [&](int n) {
-      if (!with_bc || n >= nchunks) return;
-      const uint8_t *src = card_of(n) + CARD_BCT;
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        bcr[c8] = *reinterpret_cast<const uint4 *>(src + ((8 * half + c8) * 128 + j) * 16);
-    };
-    // Pre-load for chunk n: tensor memory <- Diag(e^{G_C}) S + B_c (fp32) and the bf16
-    // operand S^T (row j) in shared memory, from the 32 key columns 64*half + 32*qq.
-    auto stage_piece = [&](int n, int qq, const float *x) {
-      const float *dv =
-          reinterpret_cast<const float *>(sm + stage_of(n) * B_STAGE_BYTES + CARD_BCT);
-      const int q4 = 2 * half + qq;
-      float init[32];
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        float bc[8];
-        if (with_bc) unpack8(bcr[qq * 4 + ch], bc);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int c = q4 * 32 + ch * 8 + u;
-          init[ch * 8 + u] = dv[c] * x[ch * 8 + u] + (with_bc ? bc[u] : 0.f);
-        }
-        *reinterpret_cast<uint4 *>(sm + B_SA + sw128_chunk(j, q4 * 4 + ch, 128)) =
-            pack8(x + ch * 8);
-      }
-      tmem_st32(tmem_addr(tb, quad * 32, set_col(n) + 32 * q4), init);
-    };
-    auto finish_stage = [&]() {
-      tmem_wait_st();
-      fence_async_smem();
-      tc_fence_before();
-    };
-    auto issue_mma = [&](int n) -> bool {  // by thread 0
-      // the output block of set n % 2 is read and zeroed (prologue, then chunk n - 2)
-      if (with_o && !mbar_wait(&bar_ofree[n & 1], (n >> 1) & 1)) return false;
-      tc_fence_after();
-      const uint32_t stg = sb + stage_of(n) * B_STAGE_BYTES;
-      const uint32_t id = idesc_bf16(128, with_o ? 192 : 128, 0, 1);
-      for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(tb + set_col(n), desc_kmajor(sb + B_SA, 128, kk),
-                 sdesc_sw128(stg + CARD_PHIQ + kk * 2048, 128 * 128, 1024), id, 1u);
-      mma_commit(&bar_mma);
-      if (with_o) mma_commit(&bar_ofull[n & 1]);
-      return true;
-    };
-
-    // whole cards into L2 ahead of their bulk copies (which otherwise wait on HBM latency)
-    auto prefetch_card = [&](int n) {
-      if (n >= nchunks) return;
-      const uint8_t *src = card_of(n);
-      for (int o = 0; o < CARD_BYTES; o += 32768)
-        prefetch_l2(src + o, min(32768, CARD_BYTES - o));
-    };
-    if (loader) {
-      for (int n = 0; n < B_NSTAGE && n < nchunks; ++n) load_card(n);
-      for (int n = B_NSTAGE; n < B_NSTAGE + kPrefetch; ++n) prefetch_card(n);
-    }
-    fetch_bc(0);
-    // chunk 0: entry state from global memory
-    if (!wait_full(0)) ok = false;
-    if (ok) {
-#pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
-        float x[32];
-#pragma unroll
-        for (int u = 0; u < 32; ++u) x[u] = entry(64 * half + 32 * qq + u);
-        stage_piece(0, qq, x);
-      }
-      finish_stage();
-    }
-    // all state threads agree on `ok`, so none is left waiting at a later barrier
-    ok = named_bar_and(1, 256, ok);
-    tc_fence_after();
-    if (tid == 0 && ok && !issue_mma(0)) s_fail = 1;
-    fetch_bc(1);
-
-    for (int n = 0; n < nchunks && ok; ++n) {
-      // a timed-out wait only clears `good`; the group votes on it at the barrier below
-      bool good = mbar_wait(&bar_mma, mma_phase);
-      mma_phase ^= 1u;
-      tc_fence_after();
-      // the card of chunk n is consumed: refill its stage with chunk n + 3
-      if (good && loader && n + B_NSTAGE < nchunks) {
-        load_card(n + B_NSTAGE);
-        prefetch_card(n + B_NSTAGE + kPrefetch);
-      }
-      const bool last = (n + 1 == nchunks);
-      if (good && !last) good = wait_full(n + 1);
-      // state after chunk n: stage it for chunk n + 1, or write it out
-      float x0[32], x1[32];
-      if (good) {
-        tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 64 * half), x0);
-        tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 64 * half + 32), x1);
-        tmem_wait_ld();
-      }
-      if (last) {
-        if (good)
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            float *p0 = result_ptr(64 * half + u), *p1 = result_ptr(64 * half + 32 + u);
-            if (p0) *p0 = x0[u];
-            if (p1) *p1 = x1[u];
-          }
-        else
-          ok = false;
-        if (good) save_ckpt(n, x0, x1);
-      } else {
-        if (good) {
-          stage_piece(n + 1, 0, x0);
-          stage_piece(n + 1, 1, x1);
-          finish_stage();
-        }
-        ok = named_bar_and(1, 256, good);
-        tc_fence_after();
-        if (!ok) break;
-        if (tid == 0 && !issue_mma(n + 1)) s_fail = 1;
-        save_ckpt(n, x0, x1);  // off the serial path: the next chunk's MMAs are in flight
-        fetch_bc(n + 2);
-      }
-    }
-    if (!ok || s_fail) {
-      if (lane == 0) set_err(kErrTimeout);
-      // let copies still in flight land (bounded) before shared memory is released
-      if (loader)
-        for (int n = loads_done; n < loads_issued; ++n) {
-          const int st = stage_of(n);
-          if (!mbar_wait(&bar_full[st], full_phase[st], 100000000ull)) break;
-          full_phase[st] ^= 1u;
-        }
-    }
-  } else if (with_o) {
-    // output group: o = scale * g * (Q' S + O_intra) for chunk n. The output block of chunk n
-    // starts as O_intra^T (seeded two chunks ahead from the card), so the MMA leaves
-    // Q' S + O_intra in it. The four warps copy their lane quadrants (channels) into one
-    // [64 tokens][128 channels] fp32 tile; then each thread takes 8 tokens x 8 channels, so
-    // that a warp's gate loads and output stores cover two whole 256-byte rows per
-    // instruction. The gate of the next chunk is loaded (same mapping) as this one is used.
-    constexpr int LDT = DD + 4;  // tile row pitch (floats)
-    float *tile = reinterpret_cast<float *>(sm + B_OT);
-    const int ot = tid - 256;                   // output thread 0..127
-    const int c8 = ot & 15, r0 = ot >> 4;       // store phase: channels 8*c8.., tokens r0 + 8m
-    const bool logits = gate && (flags & KDA_GATE_LOGITS);
-    // this lane's O_intra^T row (all 64 tokens, bf16) of chunk c, from the card
-    auto load_oi = [&](int c, uint4 *oi) {
-      const uint8_t *card = card_of(c);
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        oi[ch] = c < nchunks ? *reinterpret_cast<const uint4 *>(card + CARD_OIT + (ch * 128 + j) * 16)
-                             : make_uint4(0u, 0u, 0u, 0u);
-    };
-    auto seed = [&](int c, const uint4 *oi) {
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float x[32];
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) unpack8(oi[hf * 4 + ch], x + ch * 8);
-        tmem_st32(tmem_addr(tb, quad * 32, set_col(c) + 128 + 32 * hf), x);
-      }
-    };
-    // gate of tokens r0 + 8m, channels 8*c8 .. 8*c8 + 7 of chunk c (1.0 when absent)
-    auto load_gate = [&](int c, uint4 *gq) {
-      const int64_t tc0 = ts + (int64_t)c * C;
-      const int lc = (int)min((int64_t)C, ls - (int64_t)c * C);
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int r = r0 + 8 * m;
-        gq[m] = (gate && c < nchunks && r < lc)
-                    ? *reinterpret_cast<const uint4 *>(gate + ((size_t)(tc0 + r) * H + h) * DD + c8 * 8)
-                    : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
-      }
-    };
-    {
-      uint4 oi[8];
-#pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        load_oi(b, oi);
-        seed(b, oi);
-      }
-    }
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(&bar_ofree[0]);
-    mbar_arrive(&bar_ofree[1]);
-    uint32_t ofull_phase[2] = {0u, 0u};
-    uint4 gq[8];
-    load_gate(0, gq);
-    bool ok = true;
-    for (int n = 0; n < nchunks; ++n) {
-      const int64_t t0 = ts + (int64_t)n * C;
-      const int len = (int)min((int64_t)C, ls - (int64_t)n * C);
-      uint4 oi[8];
-      load_oi(n + 2, oi);  // its latency overlaps the wait below
-      // every output thread takes the same branch, so a timeout cannot strand the others
-      ok = named_bar_and(2, 128, mbar_wait(&bar_ofull[n & 1], ofull_phase[n & 1]));
-      if (!ok) break;
-      ofull_phase[n & 1] ^= 1u;
-      tc_fence_after();
-      // both halves into the tile (token row, this lane's channel)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float t[32];
-        tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 128 + 32 * hf), t);
-        tmem_wait_ld();
-#pragma unroll
-        for (int u = 0; u < 32; ++u) tile[(hf * 32 + u) * LDT + j] = t[u];
-      }
-      // the block is read: seed it with O_intra^T of chunk n + 2, hand it back to the issuer
-      seed(n + 2, oi);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bar_ofree[n & 1]);
-      named_bar(2, 128);  // tile complete
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int r = r0 + 8 * m;
-        const float4 a = *reinterpret_cast<const float4 *>(tile + r * LDT + c8 * 8);
-        const float4 b = *reinterpret_cast<const float4 *>(tile + r * LDT + c8 * 8 + 4);
-        float g8[8], e[8];
-        unpack8(gq[m], g8);
-        const float x8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          e[u] = scale * (logits ? sigmoid_approx(g8[u]) : g8[u]) * x8[u];
-        if (r < len)
-          *reinterpret_cast<uint4 *>(out + ((size_t)(t0 + r) * H + h) * DD + c8 * 8) = pack8(e);
-      }
-      load_gate(n + 1, gq);  // the next chunk's gate, while its MMAs run
-      named_bar(2, 128);     // tile consumed before the next chunk overwrites it
-    }
-    if (!ok && ot == 0) set_err(kErrTimeout);
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tb, 512);
-}
 
 }  // namespace
 
@@ -993,26 +567,14 @@ cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const vo
   return cudaGetLastError();
 }
 
-cudaError_t launch_state_tc(int mode, unsigned flags, const void *gate, void *out, const float *S0,
-                            float *S_final, float *X_out, float *Z_out, const int32_t *cu,
-                            int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
-                            cudaStream_t st, CkptOut ck) {
-  cudaError_t e =
-      cudaFuncSetAttribute(kda_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, B_DYN);
-  if (e != cudaSuccess) return e;
-  const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
-  kda_state_tc<<<dim3(n_seq * H, mode == 0 ? 1 : 2), 384, B_DYN, st>>>(
-      mode, flags, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final, X_out, Z_out, cu,
-      n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.cards, ck);
-  return cudaGetLastError();
-}
-
 cudaError_t tc_take_error(unsigned *bits) {
-  unsigned v = 0, z = 0;
+  unsigned v = 0, z = 0, w = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_tc_err, sizeof(unsigned));
   if (e != cudaSuccess) return e;
   e = cudaMemcpyToSymbol(g_tc_err, &z, sizeof(unsigned));
-  *bits = v;
+  if (e != cudaSuccess) return e;
+  e = state_tc_take_error(&w);  // the state pass's word
+  *bits = v | w;
   return e;
 }
 

@@ -165,7 +165,8 @@ cudaError_t launch_state_tc(int mode, unsigned flags, const void *gate, void *ou
                             float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                             int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
                             cudaStream_t st, CkptOut ck = CkptOut());
-cudaError_t tc_take_error(unsigned *bits);
+cudaError_t tc_take_error(unsigned *bits);        // card and state-pass words together
+cudaError_t state_tc_take_error(unsigned *bits);  // the state pass's word alone
 
 // chunked backward pass (kda_bwd.cu)
 size_t chunk_bwd_ws_bytes(int64_t T_total, int n_seq, int H, int dk, int dv);
