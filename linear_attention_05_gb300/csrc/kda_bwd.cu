@@ -20,9 +20,10 @@
 // dlog_alpha, and through the optional L2 normalisation of q and k.
 //
 // Launch sequence (all on the caller's stream): chunk table; prep (forward
-// operands + K^, diag(b)K~, A); forward state pass saving S, U, O per chunk;
-// dO; reverse state pass (dS' per chunk, dU, dS_0); seven batched 64-row GEMMs;
-// one triangular solve; the finishing kernel.
+// operands + K^, diag(b)K~, A); forward state pass saving S and U per chunk;
+// O = Q~ S + P U, V1 = P^T dO and R = Q~^T dO (batched GEMMs); reverse state
+// pass (dS' per chunk, dU, dS_0); seven more batched 64-row GEMMs; one triangular
+// solve; the finishing kernel.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -106,10 +107,14 @@ __global__ void __launch_bounds__(256) kda_bwd_dO(const Tin *__restrict__ d_out,
 
 // ---------------------------------------------------------------------------
 // Reverse state pass: one block per (sequence, head, 32 value columns), chunks
-// last to first. Writes dS' (the cotangent of the state leaving each chunk) and
-// dU per chunk, and dS_0. Register-tiled: thread (rg, cg) = (tid >> 3, tid & 7)
-// owns value columns 4cg..4cg+3 and key rows 4rg..4rg+3 of dS (rows 2rg, 2rg+1 of
-// dU); operands come from shared memory as 16-byte vectors.
+// last to first. With V1 = P^T dO and R = Q~^T dO precomputed per chunk (they do
+// not depend on the state), the serial step is
+//   dU = V1 + K_d dS',   dS = Diag(e^{G_C}) dS' + R - W^T dU.
+// Writes dS' (the cotangent of the state leaving each chunk) and dU per chunk, and
+// dS_0. Register-tiled: thread (rg, cg) = (tid >> 3, tid & 7) owns value columns
+// 4cg..4cg+3 and key rows 4rg..4rg+3 of dS (rows 2rg, 2rg+1 of dU); W and K_d^T
+// come from shared memory as 16- and 8-byte vectors, V1 and R straight from global
+// memory. About 106 KB of shared memory at dk = 128: two blocks per SM.
 constexpr int RBV = 32;
 
 template <int DK, int DV>
@@ -117,20 +122,17 @@ __global__ void __launch_bounds__(256) kda_bwd_state(
     const float *__restrict__ dS_final, float *__restrict__ dS_init,
     const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len, int H,
     const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
-    const float *__restrict__ Qg, const float *__restrict__ Wg, const float *__restrict__ Kdg,
-    const float *__restrict__ Pg, const float *__restrict__ Dg, const float *__restrict__ dOg,
-    float *__restrict__ dSb, float *__restrict__ dUg) {
+    const float *__restrict__ Wg, const float *__restrict__ Kdg, const float *__restrict__ Dg,
+    const float *__restrict__ V1g, const float *__restrict__ Rg, float *__restrict__ dSb,
+    float *__restrict__ dUg) {
   static_assert(DK / 4 <= 32 && C / 2 <= 32, "row groups");
   constexpr int LK = DK + 4, LS = RBV + 4, LC = C + 4;  // float4-aligned pitches
   extern __shared__ __align__(16) float smem[];
   float *sS = smem;            // [DK][LS]   running dS (value-column slice)
-  float *sO = sS + DK * LS;    // [C][LS]    dO slice
-  float *sU = sO + C * LS;     // [C][LS]    dU slice
-  float *sQ = sU + C * LS;     // [C][LK]    Q~
-  float *sW = sQ + C * LK;     // [C][LK]    W
+  float *sU = sS + DK * LS;    // [C][LS]    dU slice
+  float *sW = sU + C * LS;     // [C][LK]    W
   float *sKt = sW + C * LK;    // [DK][LC]   K_d^T
-  float *sP = sKt + DK * LC;   // [C][LC]    P (row i, column r)
-  float *sD = sP + C * LC;     // [DK]
+  float *sD = sKt + DK * LC;   // [DK]
   if (meta->invalid) return;
   const int chain = blockIdx.x, s = chain / H, h = chain % H, tid = threadIdx.x;
   const int j0 = blockIdx.y * RBV;
@@ -154,63 +156,39 @@ __global__ void __launch_bounds__(256) kda_bwd_state(
       const int c = e / RBV, jj = e % RBV;
       dSb[(slab * DK + c) * DV + j0 + jj] = sS[c * LS + jj];
     }
-    {  // operands of chunk jc: 16-byte loads, each batch issued before any of its stores
-      constexpr int NK = C * DK / 4 / 256, NP = C * C / 4 / 256, NO = C * RBV / 4 / 256;
-      const float *Q = Qg + slab * C * DK, *W = Wg + slab * C * DK, *Kd = Kdg + slab * C * DK;
-      float4 rq[NK], rw[NK];
+    // this thread's V1 and R elements (issued early: they are read after the stores below)
+    float4 v1a = make_float4(0.f, 0.f, 0.f, 0.f), v1b = v1a, rr[4];
+    if (u_rows) {
+      v1a = *reinterpret_cast<const float4 *>(V1g + (slab * C + 2 * rg) * DV + j0 + jl);
+      v1b = *reinterpret_cast<const float4 *>(V1g + (slab * C + 2 * rg + 1) * DV + j0 + jl);
+    }
+    if (s_rows)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        rr[u] = *reinterpret_cast<const float4 *>(Rg + (slab * DK + 4 * rg + u) * DV + j0 + jl);
+    {  // W and K_d of chunk jc: 16-byte loads, all issued before their stores
+      constexpr int NK = C * DK / 4 / 256;
+      const float *W = Wg + slab * C * DK, *Kd = Kdg + slab * C * DK;
+      float4 rw[NK], rk[NK];
 #pragma unroll
       for (int m = 0; m < NK; ++m) {
-        rq[m] = *reinterpret_cast<const float4 *>(Q + 4 * (tid + 256 * m));
         rw[m] = *reinterpret_cast<const float4 *>(W + 4 * (tid + 256 * m));
+        rk[m] = *reinterpret_cast<const float4 *>(Kd + 4 * (tid + 256 * m));
       }
 #pragma unroll
       for (int m = 0; m < NK; ++m) {
         const int e = 4 * (tid + 256 * m), r = e / DK, c = e % DK;
-        *reinterpret_cast<float4 *>(sQ + r * LK + c) = rq[m];
         *reinterpret_cast<float4 *>(sW + r * LK + c) = rw[m];
-      }
-      float4 rp[NP], ro[NO];
-#pragma unroll
-      for (int m = 0; m < NK; ++m) rq[m] = *reinterpret_cast<const float4 *>(Kd + 4 * (tid + 256 * m));
-#pragma unroll
-      for (int m = 0; m < NP; ++m)
-        rp[m] = *reinterpret_cast<const float4 *>(Pg + slab * C * C + 4 * (tid + 256 * m));
-#pragma unroll
-      for (int m = 0; m < NO; ++m) {
-        const int e = 4 * (tid + 256 * m), r = e / RBV, jj = e % RBV;
-        ro[m] = *reinterpret_cast<const float4 *>(dOg + (slab * C + r) * DV + j0 + jj);
-      }
-#pragma unroll
-      for (int m = 0; m < NK; ++m) {
-        const int e = 4 * (tid + 256 * m), r = e / DK, c = e % DK;
-        sKt[(c + 0) * LC + r] = rq[m].x; sKt[(c + 1) * LC + r] = rq[m].y;
-        sKt[(c + 2) * LC + r] = rq[m].z; sKt[(c + 3) * LC + r] = rq[m].w;
-      }
-#pragma unroll
-      for (int m = 0; m < NP; ++m) {
-        const int e = 4 * (tid + 256 * m), r = e / C, i = e % C;
-        *reinterpret_cast<float4 *>(sP + r * LC + i) = rp[m];
-      }
-#pragma unroll
-      for (int m = 0; m < NO; ++m) {
-        const int e = 4 * (tid + 256 * m), r = e / RBV, jj = e % RBV;
-        *reinterpret_cast<float4 *>(sO + r * LS + jj) = ro[m];
+        sKt[(c + 0) * LC + r] = rk[m].x; sKt[(c + 1) * LC + r] = rk[m].y;
+        sKt[(c + 2) * LC + r] = rk[m].z; sKt[(c + 3) * LC + r] = rk[m].w;
       }
       if (tid < DK) sD[tid] = Dg[slab * DK + tid];
     }
     __syncthreads();
-    // dU = P^T dO + K_d dS'  (P[i][r] = 0 for i < r)
+    // dU = V1 + K_d dS'
     if (u_rows) {
       const int r0 = 2 * rg;
-      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int i = r0; i < C; ++i) {
-        const float2 p = *reinterpret_cast<const float2 *>(sP + i * LC + r0);
-        const float4 o = *reinterpret_cast<const float4 *>(sO + i * LS + jl);
-        a0[0] = fmaf(p.x, o.x, a0[0]); a0[1] = fmaf(p.x, o.y, a0[1]);
-        a0[2] = fmaf(p.x, o.z, a0[2]); a0[3] = fmaf(p.x, o.w, a0[3]);
-        a1[0] = fmaf(p.y, o.x, a1[0]); a1[1] = fmaf(p.y, o.y, a1[1]);
-        a1[2] = fmaf(p.y, o.z, a1[2]); a1[3] = fmaf(p.y, o.w, a1[3]);
-      }
+      float a0[4] = {v1a.x, v1a.y, v1a.z, v1a.w}, a1[4] = {v1b.x, v1b.y, v1b.z, v1b.w};
 #pragma unroll 4
       for (int c = 0; c < DK; ++c) {
         const float2 kd = *reinterpret_cast<const float2 *>(sKt + c * LC + r0);
@@ -228,7 +206,7 @@ __global__ void __launch_bounds__(256) kda_bwd_state(
           make_float4(a1[0], a1[1], a1[2], a1[3]);
     }
     __syncthreads();
-    // dS = Diag(e^{G_C}) dS' + Q~^T dO - W^T dU
+    // dS = Diag(e^{G_C}) dS' + R - W^T dU
     float ns[4][4];
     if (s_rows) {
       const int c0 = 4 * rg;
@@ -236,21 +214,18 @@ __global__ void __launch_bounds__(256) kda_bwd_state(
       for (int u = 0; u < 4; ++u) {
         const float4 d = *reinterpret_cast<const float4 *>(sS + (c0 + u) * LS + jl);
         const float dc = sD[c0 + u];
-        ns[u][0] = dc * d.x; ns[u][1] = dc * d.y; ns[u][2] = dc * d.z; ns[u][3] = dc * d.w;
+        ns[u][0] = fmaf(dc, d.x, rr[u].x); ns[u][1] = fmaf(dc, d.y, rr[u].y);
+        ns[u][2] = fmaf(dc, d.z, rr[u].z); ns[u][3] = fmaf(dc, d.w, rr[u].w);
       }
 #pragma unroll 2
       for (int r = 0; r < C; ++r) {
-        const float4 q = *reinterpret_cast<const float4 *>(sQ + r * LK + c0);
         const float4 w = *reinterpret_cast<const float4 *>(sW + r * LK + c0);
-        const float4 o = *reinterpret_cast<const float4 *>(sO + r * LS + jl);
         const float4 du = *reinterpret_cast<const float4 *>(sU + r * LS + jl);
-        const float qa[4] = {q.x, q.y, q.z, q.w}, wa[4] = {w.x, w.y, w.z, w.w};
+        const float wa[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          ns[u][0] = fmaf(qa[u], o.x, fmaf(-wa[u], du.x, ns[u][0]));
-          ns[u][1] = fmaf(qa[u], o.y, fmaf(-wa[u], du.y, ns[u][1]));
-          ns[u][2] = fmaf(qa[u], o.z, fmaf(-wa[u], du.z, ns[u][2]));
-          ns[u][3] = fmaf(qa[u], o.w, fmaf(-wa[u], du.w, ns[u][3]));
+          ns[u][0] = fmaf(-wa[u], du.x, ns[u][0]); ns[u][1] = fmaf(-wa[u], du.y, ns[u][1]);
+          ns[u][2] = fmaf(-wa[u], du.z, ns[u][2]); ns[u][3] = fmaf(-wa[u], du.w, ns[u][3]);
         }
       }
     }
@@ -271,8 +246,7 @@ __global__ void __launch_bounds__(256) kda_bwd_state(
 
 template <int DK>
 constexpr size_t bwd_state_smem() {
-  return sizeof(float) * (DK * (RBV + 4) + 2 * C * (RBV + 4) + 2 * C * (DK + 4) +
-                          DK * (C + 4) + C * (C + 4) + DK);
+  return sizeof(float) * (DK * (RBV + 4) + C * (RBV + 4) + C * (DK + 4) + DK * (C + 4) + DK);
 }
 
 // ---------------------------------------------------------------------------
@@ -624,7 +598,7 @@ constexpr size_t bwd_finish_smem() {
 // workspace: the forward's SIMT chunk workspace, then the backward's buffers
 struct BwdWs {
   ChunkWs fw;
-  float *Kh, *Bk, *A, *Sb, *dSb, *Ub, *O, *dO, *dU, *dP, *dQt, *dKd, *dW, *dM, *Y, *dKh;
+  float *Kh, *Bk, *A, *Sb, *dSb, *R, *Ub, *O, *dO, *dU, *V1, *dP, *dQt, *dKd, *dW, *dM, *Y, *dKh;
 };
 
 size_t bwd_extra_bytes(int64_t T_total, int n_seq, int H, int dk, int dv) {
@@ -633,7 +607,7 @@ size_t bwd_extra_bytes(int64_t T_total, int n_seq, int H, int dk, int dv) {
   const size_t mv = align_up(sizeof(float) * per * C * dv, 256);
   const size_t mc = align_up(sizeof(float) * per * C * C, 256);
   const size_t ms = align_up(sizeof(float) * per * dk * dv, 256);
-  return 7 * mk + 4 * mv + 3 * mc + 2 * ms;
+  return 7 * mk + 5 * mv + 3 * mc + 3 * ms;
 }
 
 BwdWs bwd_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int dv) {
@@ -652,9 +626,9 @@ BwdWs bwd_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int dv) 
   };
   w.Kh = take(mk); w.Bk = take(mk); w.dQt = take(mk); w.dKd = take(mk); w.dW = take(mk);
   w.Y = take(mk); w.dKh = take(mk);
-  w.Ub = take(mv); w.O = take(mv); w.dO = take(mv); w.dU = take(mv);
+  w.Ub = take(mv); w.O = take(mv); w.dO = take(mv); w.dU = take(mv); w.V1 = take(mv);
   w.A = take(mc); w.dP = take(mc); w.dM = take(mc);
-  w.Sb = take(ms); w.dSb = take(ms);
+  w.Sb = take(ms); w.dSb = take(ms); w.R = take(ms);
   return w;
 }
 
@@ -669,13 +643,13 @@ GemmTerm term(const float *A, size_t sA, int lda, int a_t, const float *B, size_
 
 template <int N>
 cudaError_t gemm(const GemmTerm &t0, const GemmTerm *t1, float *Cm, int mask, int mc, int H,
-                 const ChunkMeta *meta, cudaStream_t st) {
+                 const ChunkMeta *meta, cudaStream_t st, size_t sC = 0) {
   GemmArgs g;
   g.t[0] = t0;
   g.t[1] = t1 ? *t1 : t0;
   g.nterms = t1 ? 2 : 1;
   g.Cm = Cm;
-  g.sC = (size_t)C * N;
+  g.sC = sC ? sC : (size_t)C * N;
   g.mask = mask;
   kda_bwd_gemm<N><<<dim3(mc, H), 256, 0, st>>>(g, H, meta);
   return cudaGetLastError();
@@ -702,25 +676,38 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
   ps.Kh = w.Kh; ps.Bk = w.Bk; ps.A = w.A;
   KDA_TRY(launch_prep(q, k, v, la, beta, cu, n_seq, T_total, H, DK, DV, flags, dt, fw, true, st,
                       ps));
-  StateSave ss;
-  ss.Sb = w.Sb; ss.Ub = w.Ub; ss.O = w.O;
+  StateSave ss;  // the replay saves S and U only; O comes from a batched GEMM below
+  ss.Sb = w.Sb; ss.Ub = w.Ub;
   KDA_TRY(launch_state_pass(0, flags, nullptr, nullptr, S0, nullptr, nullptr, nullptr, cu, n_seq,
                             T_total, H, DK, DV, scale, dt, fw, st, CkptOut(), ss));
   kda_bwd_dO<DV, Tio><<<dim3(mc, H), 256, 0, st>>>((const Tio *)d_out, (const Tio *)gate, cu,
                                                    n_seq, fixed_len, H, scale, flags, fw.meta,
                                                    fw.seq_chunk_off, w.dO);
   KDA_TRY(cudaGetLastError());
+  const size_t sk = (size_t)C * DK, sv = (size_t)C * DV, scc = (size_t)C * C,
+               ss2 = (size_t)DK * DV;
+  // O = Q~ S + P U (pre-gate chunk output, for dg)
+  {
+    GemmTerm t2 = term(fw.P, scc, C, 0, w.Ub, sv, DV, 0, C, 1.f);
+    KDA_TRY(gemm<DV>(term(fw.Q, sk, DK, 0, w.Sb, ss2, DV, 0, DK, 1.f), &t2, w.O, 0, mc, H,
+                     fw.meta, st));
+  }
+  // the state-independent parts of the reverse step: V1 = P^T dO, R = Q~^T dO (dk rows,
+  // computed in 64-row halves)
+  KDA_TRY(gemm<DV>(term(fw.P, scc, C, 1, w.dO, sv, DV, 0, C, 1.f), nullptr, w.V1, 0, mc, H,
+                   fw.meta, st));
+  for (int r0 = 0; r0 < DK; r0 += C)
+    KDA_TRY(gemm<DV>(term(fw.Q + r0, sk, DK, 1, w.dO, sv, DV, 0, C, 1.f), nullptr,
+                     w.R + (size_t)r0 * DV, 0, mc, H, fw.meta, st, ss2));
   {
     auto kern = kda_bwd_state<DK, DV>;
     constexpr size_t sm = bwd_state_smem<DK>();
     KDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
     kern<<<dim3(n_seq * H, DV / RBV), 256, sm, st>>>(dSf, dS0, cu, n_seq, fixed_len, H, fw.meta,
-                                                     fw.seq_chunk_off, fw.Q, fw.W, fw.Kd, fw.P,
-                                                     fw.D, w.dO, w.dSb, w.dU);
+                                                     fw.seq_chunk_off, fw.W, fw.Kd, fw.D, w.V1,
+                                                     w.R, w.dSb, w.dU);
     KDA_TRY(cudaGetLastError());
   }
-  const size_t sk = (size_t)C * DK, sv = (size_t)C * DV, scc = (size_t)C * C,
-               ss2 = (size_t)DK * DV;
   // dP = lower(dO U^T)
   KDA_TRY(gemm<C>(term(w.dO, sv, DV, 0, w.Ub, sv, DV, 1, DV, 1.f), nullptr, w.dP, 1, mc, H,
                   fw.meta, st));

@@ -329,13 +329,14 @@ __global__ void __launch_bounds__(256) kda_state_simt(
   // from shared memory as 8- and 16-byte vectors; W, Q~ and P are stored transposed.
   constexpr int LS = BV + 4, LK = DK + 4, LT = C + 2;
   extern __shared__ __align__(16) float smem[];
+  // Q~^T and P^T come last: without an output they are not allocated (two blocks per SM)
   float *sS = smem;            // [DK][LS]  state slice
   float *sU = sS + DK * LS;    // [C][LS]   U~, then U
   float *sWt = sU + C * LS;    // [DK][LT]  W^T
-  float *sQt = sWt + DK * LT;  // [DK][LT]  Q~^T
-  float *sKd = sQt + DK * LT;  // [C][LK]   K_d
-  float *sPt = sKd + C * LK;   // [C][LT]   P^T
-  float *sD = sPt + C * LT;    // [DK]
+  float *sKd = sWt + DK * LT;  // [C][LK]   K_d
+  float *sD = sKd + C * LK;    // [DK]
+  float *sQt = sD + DK;        // [DK][LT]  Q~^T   (with an output only)
+  float *sPt = sQt + DK * LT;  // [C][LT]   P^T    (with an output only)
 
   if (meta->invalid) return;
   const int chain = blockIdx.x, s = chain / H, h = chain % H, tid = threadIdx.x;
@@ -547,10 +548,12 @@ template <int DK, int DV>
 constexpr size_t prep_smem() {
   return sizeof(float) * (3 * C * (DK + 1) + C * (DV + 1) + C * (C + 1) + C + DK);
 }
+// shared memory of the state pass: without an output (segment summaries, the backward's
+// forward replay) the Q~^T and P^T buffers are left out
 template <int DK>
-constexpr size_t state_smem() {
-  return sizeof(float) * (DK * (BV + 4) + C * (BV + 4) + 2 * DK * (C + 2) + C * (DK + 4) +
-                          C * (C + 2) + DK);
+constexpr size_t state_smem(bool with_o) {
+  return sizeof(float) * (DK * (BV + 4) + C * (BV + 4) + DK * (C + 2) + C * (DK + 4) + DK +
+                          (with_o ? DK * (C + 2) + C * (C + 2) : 0));
 }
 
 template <int DK, int DV, typename Tin>
@@ -577,8 +580,10 @@ cudaError_t launch_state_t(int mode, unsigned flags, const void *gate, void *out
                            int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
                            cudaStream_t st, CkptOut ck, StateSave save) {
   auto kern = kda_state_simt<DK, DV, Tout>;
-  constexpr size_t sm = state_smem<DK>();
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  const bool with_o = mode == 0 && (out != nullptr || save.O != nullptr);
+  const size_t sm = state_smem<DK>(with_o);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)state_smem<DK>(true));
   if (e != cudaSuccess) return e;
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
   const int ncols = mode == 0 ? DV : DK + DV;
