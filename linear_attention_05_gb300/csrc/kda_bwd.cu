@@ -409,9 +409,35 @@ __global__ void __launch_bounds__(256) kda_bwd_solve(const float *__restrict__ A
   if (meta->invalid || ci >= meta->total_chunks) return;
   const size_t slab = (size_t)ci * H + h;
   float *y1 = Y1 + slab * C * N1, *y2 = Y2 + slab * C * N2;
-  for (int e = tid; e < C * C; e += 256) sA[(e / C) * LA + e % C] = Ag[slab * C * C + e];
-  for (int e = tid; e < C * N1; e += 256) sY[(e / N1) * LY + e % N1] = y1[e];
-  for (int e = tid; e < C * N2; e += 256) sY[(e / N2) * LY + N1 + e % N2] = y2[e];
+  {  // 16-byte loads, all issued before their stores
+    constexpr int NA = C * C / 4 / 256, NY1 = C * N1 / 4 / 256, NY2 = C * N2 / 4 / 256;
+    float4 ra[NA], r1[NY1], r2[NY2];
+#pragma unroll
+    for (int m = 0; m < NA; ++m)
+      ra[m] = *reinterpret_cast<const float4 *>(Ag + slab * C * C + 4 * (tid + 256 * m));
+#pragma unroll
+    for (int m = 0; m < NY1; ++m) r1[m] = *reinterpret_cast<const float4 *>(y1 + 4 * (tid + 256 * m));
+#pragma unroll
+    for (int m = 0; m < NY2; ++m) r2[m] = *reinterpret_cast<const float4 *>(y2 + 4 * (tid + 256 * m));
+#pragma unroll
+    for (int m = 0; m < NA; ++m) {
+      const int e = 4 * (tid + 256 * m), r = e / C, c = e % C;
+      sA[r * LA + c] = ra[m].x; sA[r * LA + c + 1] = ra[m].y;
+      sA[r * LA + c + 2] = ra[m].z; sA[r * LA + c + 3] = ra[m].w;
+    }
+#pragma unroll
+    for (int m = 0; m < NY1; ++m) {
+      const int e = 4 * (tid + 256 * m), r = e / N1, c = e % N1;
+      sY[r * LY + c] = r1[m].x; sY[r * LY + c + 1] = r1[m].y;
+      sY[r * LY + c + 2] = r1[m].z; sY[r * LY + c + 3] = r1[m].w;
+    }
+#pragma unroll
+    for (int m = 0; m < NY2; ++m) {
+      const int e = 4 * (tid + 256 * m), r = e / N2, c = e % N2;
+      sY[r * LY + N1 + c] = r2[m].x; sY[r * LY + N1 + c + 1] = r2[m].y;
+      sY[r * LY + N1 + c + 2] = r2[m].z; sY[r * LY + N1 + c + 3] = r2[m].w;
+    }
+  }
   __syncthreads();
   if (tid < NC) {
     float *col = sY + tid;
@@ -422,8 +448,19 @@ __global__ void __launch_bounds__(256) kda_bwd_solve(const float *__restrict__ A
     }
   }
   __syncthreads();
-  for (int e = tid; e < C * N1; e += 256) y1[e] = sY[(e / N1) * LY + e % N1];
-  for (int e = tid; e < C * N2; e += 256) y2[e] = sY[(e / N2) * LY + N1 + e % N2];
+#pragma unroll 4
+  for (int e = 4 * tid; e < C * N1; e += 1024) {
+    const int r = e / N1, c = e % N1;
+    *reinterpret_cast<float4 *>(y1 + e) = make_float4(sY[r * LY + c], sY[r * LY + c + 1],
+                                                     sY[r * LY + c + 2], sY[r * LY + c + 3]);
+  }
+#pragma unroll 4
+  for (int e = 4 * tid; e < C * N2; e += 1024) {
+    const int r = e / N2, c = e % N2;
+    *reinterpret_cast<float4 *>(y2 + e) =
+        make_float4(sY[r * LY + N1 + c], sY[r * LY + N1 + c + 1], sY[r * LY + N1 + c + 2],
+                    sY[r * LY + N1 + c + 3]);
+  }
 }
 
 // ---------------------------------------------------------------------------
