@@ -7,8 +7,9 @@
 //   E_0 = S_init,  E_s = X_{s-1} E_{s-1} + Z_{s-1},  S_final = X_{n-1} E_{n-1} + Z_{n-1}.
 // Value columns of E are independent, so each block owns (head, 16 value
 // columns) and runs the n_seg dependent dk x dk by dk x 16 products in order
-// with its slice of E in shared memory, 256 threads x (8 rows, 1 column) each. X_s arrives by bulk copies (one per
-// row, into a padded double buffer) while step s - 1 computes.
+// with its slice of E in shared memory, 256 threads x (8 rows, 1 column) each. X_{s+1} arrives
+// by 16-byte asynchronous copies of all threads (into a padded double buffer) while step s
+// computes.
 #include <cuda_runtime.h>
 
 #include "kda_common.cuh"
@@ -35,32 +36,30 @@ __global__ void __launch_bounds__(256) kda_scan_kernel(const float *__restrict__
   extern __shared__ __align__(16) float smem[];
   float *sX = smem;                 // [2][DK][XP]
   float *sE = smem + 2 * DK * XP;   // [DK][BV]
-  __shared__ uint64_t bar[2];
   const int h = blockIdx.x, j0 = blockIdx.y * BV, tid = threadIdx.x;
   const int jj = tid & 15, rg = tid >> 4;  // column, row group (rows rg + 16 m)
-  if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    fence_mbar_init();
-  }
   for (int e = tid; e < DK * BV; e += 256) {
     const int c = e / BV, j = e % BV;
     sE[e] = S_init ? S_init[((size_t)h * DK + c) * DV + j0 + j] : 0.f;
   }
   __syncthreads();
-  auto load_x = [&](int s) {  // warp 0: one bulk copy per row of X_s
-    const int b = s & 1;
-    if (tid == 0) mbar_arrive_expect_tx(&bar[b], DK * DK * 4);
-    __syncwarp();
-    const float *src = X + ((size_t)s * H + h) * DK * DK;
-    for (int c = tid; c < DK; c += 32) bulk_g2s(sX + (b * DK + c) * XP, src + (size_t)c * DK, DK * 4, &bar[b]);
+  // X_s into buffer s % 2: 16-byte asynchronous copies spread over all threads (the load path;
+  // one commit group per step, also when there is no such step)
+  auto load_x = [&](int s) {
+    if (s < n_seg) {
+      const float *src = X + ((size_t)s * H + h) * DK * DK;
+      const uint32_t dst = smem_u32(sX + (s & 1) * DK * XP);
+      for (int e = tid; e < DK * DK / 4; e += 256) {
+        const int c = e / (DK / 4), q4 = e % (DK / 4);
+        cp_async16(dst + (c * XP + 4 * q4) * 4, src + (size_t)c * DK + 4 * q4);
+      }
+    }
+    cp_async_commit();
   };
-  if (tid < 32 && n_seg > 0) load_x(0);
-  uint32_t phase[2] = {0u, 0u};
-  bool ok = true;
-  for (int s = 0; s < n_seg && ok; ++s) {
+  load_x(0);
+  for (int s = 0; s < n_seg; ++s) {
     const int b = s & 1;
-    if (tid < 32 && s + 1 < n_seg) load_x(s + 1);  // the other buffer was read in step s - 1
+    load_x(s + 1);  // the other buffer was read in step s - 1
     const float *Zs = Z + ((size_t)s * H + h) * DK * DV;
     float acc[RPT];
 #pragma unroll
@@ -69,12 +68,8 @@ __global__ void __launch_bounds__(256) kda_scan_kernel(const float *__restrict__
 #pragma unroll
       for (int m = 0; m < RPT; ++m)
         E_out[(((size_t)s * H + h) * DK + rg + 16 * m) * DV + j0 + jj] = sE[(rg + 16 * m) * BV + jj];
-    // every thread takes the same branch, so a timeout cannot strand others at a barrier
-    if (!__syncthreads_and(mbar_wait(&bar[b], phase[b]))) {
-      ok = false;
-      break;
-    }
-    phase[b] ^= 1u;
+    cp_async_wait_group<1>();  // X_s has landed (only X_{s+1} may be pending)
+    __syncthreads();           // ... for every thread's part of it
     const float *xb = sX + b * DK * XP;
     for (int l = 0; l < DK; l += 4) {
       const float e0 = sE[(l + 0) * BV + jj], e1 = sE[(l + 1) * BV + jj];
@@ -90,14 +85,7 @@ __global__ void __launch_bounds__(256) kda_scan_kernel(const float *__restrict__
     for (int m = 0; m < RPT; ++m) sE[(rg + 16 * m) * BV + jj] = acc[m];
     __syncthreads();
   }
-  if (!ok) {
-    if (tid == 0) {
-      atomicOr(&g_scan_err, kErrTimeout);
-      // let a copy still in flight land (bounded) before shared memory is released
-      for (int b = 0; b < 2; ++b) mbar_wait(&bar[b], phase[b], 100000000ull);
-    }
-    return;
-  }
+  cp_async_wait_group<0>();  // nothing left in flight
   if (S_final)
 #pragma unroll
     for (int m = 0; m < RPT; ++m)

@@ -88,6 +88,18 @@ __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint3
       : "memory");
 }
 // Prefetch `bytes` (multiple of 16) of global memory into L2, asynchronously.
+// 16-byte asynchronous global -> shared copy through the load/store path (not the TMA unit)
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void *gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// all but the newest `n` committed groups of this thread have landed
+template <int n>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
+}
 __device__ __forceinline__ void prefetch_l2(const void *g, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(g), "r"(bytes) : "memory");
 }
