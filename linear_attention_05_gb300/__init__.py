@@ -16,4 +16,6 @@ from .binding import (KDA_DEBUG_CHECK, KDA_DTYPE_BF16, KDA_DTYPE_F32, KDA_GATE_L
                       kda_version, load,
                       scan_combine, segment_summary, segmented_fwd)
 
+from .pipeline import HostPipeline  # noqa: E402
+
 __all__ = [n for n in dir() if not n.startswith("_")]

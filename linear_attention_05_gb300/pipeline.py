@@ -1,0 +1,81 @@
+"""kda_chunk_fwd on host-resident inputs, with the transfers overlapped.
+
+For a batch of equal-length sequences held in pinned host memory, ``HostPipeline.run``
+moves the batch in groups of sequences over three CUDA streams: the inputs of group
+i + 1 are copied in while group i is computed and group i - 1 is copied out. Every
+step of the computation is the library's kda_chunk_fwd on the group's sequences
+(they are independent, so the results are bitwise those of one call on the whole
+batch); this module only orders copies and calls.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding
+
+_TOKEN = ("q", "k", "v", "log_alpha", "beta", "gate")
+
+
+class HostPipeline:
+    """Device buffers, workspace and streams for batches of ``n_seq`` sequences of
+    ``seq_len`` tokens (``H`` heads, ``dk``/``dv``), processed in ``groups`` groups."""
+
+    def __init__(self, n_seq, seq_len, H, dk, dv, dtype=torch.bfloat16, device="cuda",
+                 groups=None, with_gate=True):
+        self.n_seq, self.L, self.H, self.dk, self.dv = n_seq, seq_len, H, dk, dv
+        self.groups = groups or n_seq
+        if n_seq % self.groups:
+            raise ValueError("n_seq must be a multiple of groups")
+        self.spg = n_seq // self.groups  # sequences per group
+        T = n_seq * seq_len
+        dev = torch.device(device)
+        shapes = {"q": (T, H, dk), "k": (T, H, dk), "v": (T, H, dv), "log_alpha": (T, H, dk),
+                  "beta": (T, H), "gate": (T, H, dv)}
+        self.dev_in = {n: torch.empty(s, dtype=dtype, device=dev) for n, s in shapes.items()
+                       if with_gate or n != "gate"}
+        self.dev_s0 = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev)
+        self.dev_out = torch.empty((T, H, dv), dtype=dtype, device=dev)
+        self.dev_fs = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev)
+        tg = self.spg * seq_len
+        nbytes = binding.kda_chunk_fwd_workspace_size(
+            tg, self.spg, H, dk, dv, dtype=binding._dtype_code(self.dev_out))
+        self.ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+        self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(dev), torch.cuda.Stream(dev),
+                                              torch.cuda.Stream(dev))
+
+    def run(self, host, out_host, final_state_host=None, scale=1.0, flags=binding.KDA_QK_L2NORM):
+        """host: dict of pinned tensors q, k, v, log_alpha, beta, gate (optional) and S0
+        (optional, [n_seq, H, dk, dv] fp32). Writes out_host (pinned [T, H, dv]) and, if given,
+        final_state_host. Work is ordered after the current stream; the current stream waits
+        for the last copy out."""
+        cur = torch.cuda.current_stream()
+        self.s_in.wait_stream(cur)
+        self.s_comp.wait_stream(cur)
+        self.s_out.wait_stream(cur)
+        tg = self.spg * self.L
+        has_gate = host.get("gate") is not None
+        has_s0 = host.get("S0") is not None
+        for g in range(self.groups):
+            t0, t1 = g * tg, (g + 1) * tg
+            s0, s1 = g * self.spg, (g + 1) * self.spg
+            with torch.cuda.stream(self.s_in):
+                for n in _TOKEN:
+                    if n == "gate" and not has_gate:
+                        continue
+                    self.dev_in[n][t0:t1].copy_(host[n][t0:t1], non_blocking=True)
+                if has_s0:
+                    self.dev_s0[s0:s1].copy_(host["S0"][s0:s1], non_blocking=True)
+            self.s_comp.wait_stream(self.s_in)
+            binding.kda_chunk_fwd(
+                self.dev_in["q"][t0:t1], self.dev_in["k"][t0:t1], self.dev_in["v"][t0:t1],
+                self.dev_in["log_alpha"][t0:t1], self.dev_in["beta"][t0:t1],
+                self.dev_in["gate"][t0:t1] if has_gate else None, self.dev_out[t0:t1],
+                self.dev_s0[s0:s1] if has_s0 else None, self.dev_fs[s0:s1], None, self.spg,
+                scale=scale, flags=flags, workspace=self.ws, stream=self.s_comp)
+            self.s_out.wait_stream(self.s_comp)
+            with torch.cuda.stream(self.s_out):
+                out_host[t0:t1].copy_(self.dev_out[t0:t1], non_blocking=True)
+                if final_state_host is not None:
+                    final_state_host[s0:s1].copy_(self.dev_fs[s0:s1], non_blocking=True)
+        cur.wait_stream(self.s_out)
+        return out_host, final_state_host
