@@ -273,15 +273,19 @@ constexpr int GKT = 32;  // K tile
 
 // One K tile of op(A) (64 x 32) and op(B) (32 x N) in registers: 16-byte loads along the
 // contiguous axis of each operand (every leading dimension and tile origin is a multiple of 4).
+constexpr int GTHREADS = 128;
+constexpr int GPA = C + 4;  // sA row pitch (floats): 16-byte aligned rows
+
 template <int N>
 struct GemmTile {
-  static constexpr int NA = GKT * C / 4 / 256, NB = GKT * N / 4 / 256;
+  static constexpr int NA = GKT * C / 4 / GTHREADS, NB = GKT * N / 4 / GTHREADS;
+  static constexpr int PB = N + 4;
   float4 a[NA], b[NB];
   __device__ __forceinline__ void load(const GemmTerm &t, const float *A, const float *B, int k0,
                                        int tid) {
 #pragma unroll
     for (int m = 0; m < NA; ++m) {
-      const int e = tid + 256 * m;
+      const int e = tid + GTHREADS * m;
       if (t.a_t) {  // (k, 4 consecutive m)
         const int kk = e / (C / 4), m4 = 4 * (e % (C / 4));
         a[m] = *reinterpret_cast<const float4 *>(A + (size_t)(k0 + kk) * t.lda + m4);
@@ -292,7 +296,7 @@ struct GemmTile {
     }
 #pragma unroll
     for (int m = 0; m < NB; ++m) {
-      const int e = tid + 256 * m;
+      const int e = tid + GTHREADS * m;
       if (t.b_t) {  // (n, 4 consecutive k)
         const int n = e / (GKT / 4), k4 = 4 * (e % (GKT / 4));
         b[m] = *reinterpret_cast<const float4 *>(B + (size_t)n * t.ldb + k0 + k4);
@@ -302,53 +306,52 @@ struct GemmTile {
       }
     }
   }
-  // to shared memory as sA[k][m] (pitch C + 1) and sB[k][n] (pitch N + 1), alpha folded into A
+  // to shared memory as sA[k][m] and sB[k][n] (16-byte aligned rows), alpha folded into A
   __device__ __forceinline__ void store(const GemmTerm &t, float *sA, float *sB, int tid) const {
-    constexpr int PA = C + 1, PB = N + 1;
 #pragma unroll
     for (int m = 0; m < NA; ++m) {
-      const int e = tid + 256 * m;
-      const float v[4] = {t.alpha * a[m].x, t.alpha * a[m].y, t.alpha * a[m].z, t.alpha * a[m].w};
+      const int e = tid + GTHREADS * m;
+      const float4 v = make_float4(t.alpha * a[m].x, t.alpha * a[m].y, t.alpha * a[m].z,
+                                   t.alpha * a[m].w);
       if (t.a_t) {
         const int kk = e / (C / 4), m4 = 4 * (e % (C / 4));
-#pragma unroll
-        for (int q = 0; q < 4; ++q) sA[kk * PA + m4 + q] = v[q];
+        *reinterpret_cast<float4 *>(sA + kk * GPA + m4) = v;
       } else {
         const int mm = e / (GKT / 4), k4 = 4 * (e % (GKT / 4));
-#pragma unroll
-        for (int q = 0; q < 4; ++q) sA[(k4 + q) * PA + mm] = v[q];
+        sA[(k4 + 0) * GPA + mm] = v.x; sA[(k4 + 1) * GPA + mm] = v.y;
+        sA[(k4 + 2) * GPA + mm] = v.z; sA[(k4 + 3) * GPA + mm] = v.w;
       }
     }
 #pragma unroll
     for (int m = 0; m < NB; ++m) {
-      const int e = tid + 256 * m;
-      const float v[4] = {b[m].x, b[m].y, b[m].z, b[m].w};
+      const int e = tid + GTHREADS * m;
       if (t.b_t) {
         const int n = e / (GKT / 4), k4 = 4 * (e % (GKT / 4));
-#pragma unroll
-        for (int q = 0; q < 4; ++q) sB[(k4 + q) * PB + n] = v[q];
+        sB[(k4 + 0) * PB + n] = b[m].x; sB[(k4 + 1) * PB + n] = b[m].y;
+        sB[(k4 + 2) * PB + n] = b[m].z; sB[(k4 + 3) * PB + n] = b[m].w;
       } else {
         const int kk = e / (N / 4), n4 = 4 * (e % (N / 4));
-#pragma unroll
-        for (int q = 0; q < 4; ++q) sB[kk * PB + n4 + q] = v[q];
+        *reinterpret_cast<float4 *>(sB + kk * PB + n4) = b[m];
       }
     }
   }
 };
 
+// 128 threads; thread (ty, tx) = (tid >> 4, tid & 15) owns rows 8ty..8ty+7 and columns
+// tx * (N/16) .. + N/16 of C, read from shared memory as 16-byte vectors.
 template <int N>
-__global__ void __launch_bounds__(256) kda_bwd_gemm(GemmArgs g, int H,
-                                                    const ChunkMeta *__restrict__ meta) {
-  constexpr int PA = C + 1, PB = N + 1, NJ = N / 16;
-  __shared__ float sA[GKT * PA];
-  __shared__ float sB[GKT * PB];
+__global__ void __launch_bounds__(GTHREADS) kda_bwd_gemm(GemmArgs g, int H,
+                                                         const ChunkMeta *__restrict__ meta) {
+  constexpr int PB = N + 4, NJ = N / 16;
+  __shared__ __align__(16) float sA[GKT * GPA];
+  __shared__ __align__(16) float sB[GKT * PB];
   const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   if (meta->invalid || ci >= meta->total_chunks) return;
   const size_t slab = (size_t)ci * H + h;
   const int ty = tid >> 4, tx = tid & 15;
-  float acc[4][NJ];
+  float acc[8][NJ];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int jj = 0; jj < NJ; ++jj) acc[i][jj] = 0.f;
   // the K tiles of all terms in order; tile i + 1 is loaded while tile i is multiplied
@@ -368,28 +371,39 @@ __global__ void __launch_bounds__(256) kda_bwd_gemm(GemmArgs g, int H,
       const GemmTerm &t = term_of(i + 1);
       tile.load(t, t.A + slab * t.sA, t.B + slab * t.sB, k0_of(i + 1), tid);
     }
-#pragma unroll 8
+#pragma unroll 4
     for (int kk = 0; kk < GKT; ++kk) {
-      float a[4], b[NJ];
+      const float4 a0 = *reinterpret_cast<const float4 *>(sA + kk * GPA + 8 * ty);
+      const float4 a1 = *reinterpret_cast<const float4 *>(sA + kk * GPA + 8 * ty + 4);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      float bv[NJ];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) a[q] = sA[kk * PA + 4 * ty + q];
+      for (int q = 0; q < NJ; q += 4) {
+        const float4 b4 = *reinterpret_cast<const float4 *>(sB + kk * PB + tx * NJ + q);
+        bv[q] = b4.x; bv[q + 1] = b4.y; bv[q + 2] = b4.z; bv[q + 3] = b4.w;
+      }
 #pragma unroll
-      for (int jj = 0; jj < NJ; ++jj) b[jj] = sB[kk * PB + tx + 16 * jj];
+      for (int r = 0; r < 8; ++r)
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int jj = 0; jj < NJ; ++jj) acc[q][jj] = fmaf(a[q], b[jj], acc[q][jj]);
+        for (int jj = 0; jj < NJ; ++jj) acc[r][jj] = fmaf(av[r], bv[jj], acc[r][jj]);
     }
   }
   float *Cm = g.Cm + slab * g.sC;
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int r = 0; r < 8; ++r) {
+    const int m = 8 * ty + r;
 #pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) {
-      const int m = 4 * ty + i, n = tx + 16 * jj;
-      const bool keep = g.mask == 0 || (g.mask == 1 ? n <= m : n < m);
-      Cm[(size_t)m * N + n] = keep ? acc[i][jj] : 0.f;
+    for (int q = 0; q < NJ; q += 4) {
+      const int n = tx * NJ + q;
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool keep = g.mask == 0 || (g.mask == 1 ? n + u <= m : n + u < m);
+        v[u] = keep ? acc[r][q + u] : 0.f;
+      }
+      *reinterpret_cast<float4 *>(Cm + (size_t)m * N + n) = make_float4(v[0], v[1], v[2], v[3]);
     }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -688,7 +702,7 @@ cudaError_t gemm(const GemmTerm &t0, const GemmTerm *t1, float *Cm, int mask, in
   g.Cm = Cm;
   g.sC = sC ? sC : (size_t)C * N;
   g.mask = mask;
-  kda_bwd_gemm<N><<<dim3(mc, H), 256, 0, st>>>(g, H, meta);
+  kda_bwd_gemm<N><<<dim3(mc, H), GTHREADS, 0, st>>>(g, H, meta);
   return cudaGetLastError();
 }
 
