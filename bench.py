@@ -315,7 +315,10 @@ def run_gpu(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.monotonic()
-    total_ms, per_launch = time_kernels(step, args.steps, stream, 3)
+    # 3 launches (chunk table, cards, state pass), or 5 for a split prefill (table, leading
+    # cards, leading state pass, trailing cards beside it, trailing state pass)
+    n_launch = kda.kda_chunk_fwd_launches(T, n_seq, H, d, d)
+    total_ms, per_launch = time_kernels(step, args.steps, stream, n_launch)
     t_wall1 = time.monotonic()
     barrier(world)
     sampler.stop()
@@ -324,31 +327,46 @@ def run_gpu(args, rank, world, local):
     ms_per_step = total_ms / args.steps
     value = world * TOKENS_PER_STEP / (ms_per_step * 1e-3) / 1e6
 
-    # roofline of the dominant launch (update cards or state pass)
+    # roofline of the dominant kernel (update cards or state pass), over its launches per step
     tc = (w.dtype == torch.bfloat16 and d == 128)
     names = (["kda_chunk_table", "kda_card_tc", "kda_state_tc"] if tc else
              ["kda_chunk_table", "kda_prep_simt", "kda_state_simt"])
-    dom = int(np.argmax(per_launch))
+    launches_of = [[0], [1, 3], [2, 4]] if n_launch == 5 else [[0], [1], [2]]
+    kernel_ms = [sum(per_launch[i] for i in ix) for ix in launches_of]  # per step
+    dom = int(np.argmax(kernel_ms))
     chunk_heads = (T // 64) * H
-    alg_bytes = {  # algorithmic HBM bytes per launch of each kernel
+    alg_bytes = {  # algorithmic HBM bytes per step of each kernel
         0: (n_seq + 1) * 4,
         1: TOKEN_HEADS * (4 * d * 2 + 2),                                 # q, k, v, log_alpha, beta
         2: TOKEN_HEADS * (2 * d * 2) + 2 * n_seq * H * STATE_BYTES,       # gate, o, states
     }
-    achieved = alg_bytes[dom] / (per_launch[dom] * 1e-3) / 1e9
+    n_dom = len(launches_of[dom])
+    achieved = alg_bytes[dom] / (kernel_ms[dom] * 1e-3) / 1e9  # = per-launch bytes / mean duration
+    traffic = profiled_traffic(names[dom])
     roofline = {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": profiled_traffic(names[dom]), "peak_source": pk["source"],
-                "launch_ms": dict(zip(names, [round(t, 4) for t in per_launch]))}
+                "traffic": traffic, "peak_source": pk["source"],
+                "launches_per_step": n_dom,
+                "alg_bytes_per_launch": alg_bytes[dom] // n_dom,
+                "launch_ms": {"per_step": dict(zip(names, [round(t, 4) for t in kernel_ms])),
+                              "in_order": [round(t, 4) for t in per_launch]}}
+    # the whole step against HBM: the path's algorithmic bytes over the step time
+    step_bytes = sum(alg_bytes.values())
+    roofline["step"] = {"alg_bytes": step_bytes,
+                        "achieved": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
+                        "frac": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+    if n_launch == 5:
+        roofline["schedule"] = ("split prefill: trailing 5/16 of each sequence's cards built "
+                                "beside the state pass over the leading 11/16")
     if tc:
-        # tensor-core work per (chunk, head): card GEMMs 1-4 and the state-pass MMA group
+        # tensor-core work per (chunk, head): card GEMMs 1-4 and the state-pass MMA group,
+        # over the whole step (the launches overlap, so their durations do not add up)
         card_flop = 2 * (128 * 64 * 128 + 2 * 128 * 64 * 64 + 2 * 128 * 64 * 64 + 2 * 128 * 128 * 64)
         state_flop = 2 * 128 * 192 * 128
-        t_gemm = (per_launch[1] + per_launch[2]) * 1e-3
-        tf = chunk_heads * (card_flop + state_flop) / t_gemm / 1e12
+        tf = chunk_heads * (card_flop + state_flop) / (ms_per_step * 1e-3) / 1e12
         roofline["tensor"] = {"kernels": names[1:], "achieved": round(tf, 2), "unit": "TFLOP/s",
                               "peak": pk["bf16_tflops"], "frac": round(tf / pk["bf16_tflops"], 4),
-                              "flop_per_chunk_head": card_flop + state_flop}
+                              "flop_per_chunk_head": card_flop + state_flop, "over": "step"}
 
     # end to end through the public API: pinned host inputs -> device -> host. HostPipeline
     # copies each sequence in, computes it and copies it out on three streams, so the transfers
@@ -390,7 +408,7 @@ def run_gpu(args, rank, world, local):
                 "log_alpha max(-exp(N(-3,1)), log 0.5))",
         "config": prefill_config(world),
         "roofline": roofline, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": n_launch * args.steps,
     }
 
     if rank == 0 and not args.skip_extra:
@@ -561,7 +579,7 @@ def bench_varlen(dev, pk, stream, reps=10):
     return {"workload": f"varlen {n_seq} packed sequences ({T} tokens, longest "
                         f"{max(w.lengths)}) H=32 dk=dv=128 bf16",
             "value": round(T / (ms * 1e-3) / 1e6, 3), "unit": "Mtok/s", "ms": round(ms, 3),
-            "gpu_launches": 3 * reps}
+            "gpu_launches": kda.kda_chunk_fwd_launches(T, n_seq, H, d, d) * reps}
 
 
 def bench_checkpoints(dev, pk, stream, reps=20, every=1024):
@@ -605,7 +623,8 @@ def bench_checkpoints(dev, pk, stream, reps=20, every=1024):
                         "tokens (4 per sequence)",
             "value": round(T / (ms["ckpt"] * 1e-3) / 1e6, 3), "unit": "Mtok/s",
             "ms": round(ms["ckpt"], 4), "ms_without": round(ms["plain"], 4),
-            "checkpoint_bytes": ck.numel() * 4, "gpu_launches": 3 * reps}
+            "checkpoint_bytes": ck.numel() * 4,
+            "gpu_launches": kda.kda_chunk_fwd_launches(T, n_seq, H, 128, 128) * reps}
 
 
 def bench_backward(dev, pk, stream, reps=5):
@@ -695,7 +714,7 @@ def bench_gates(dev, pk, stream, reps=20):
                         "forget-gate pre-activation",
             "value": round(T / (ms["fused"] * 1e-3) / 1e6, 3), "unit": "Mtok/s",
             "ms": round(ms["fused"], 4), "ms_prepass_then_plain": round(ms["unfused"], 4),
-            "gpu_launches": 3 * reps}
+            "gpu_launches": kda.kda_chunk_fwd_launches(T, n_seq, H, 128, 128) * reps}
 
 
 def bench_scan(dev, pk, stream, reps=20):

@@ -101,6 +101,15 @@ const char *kda_version(void);
  *  workspace       : >= kda_chunk_fwd_workspace_size(...) bytes
  * Malformed cu_seqlens found on the device set KDA_ERR_INVALID_ARG in the
  * error word and the call writes nothing.
+ *
+ * Scheduling (bf16, dk = dv = 128, at most 112 (sequence, head) pairs and
+ * >= 16 chunks per sequence on average): the call splits every sequence after
+ * floor(n_chunks * 11 / 16) chunks (environment variable KDA_PREFILL_SPLIT =
+ * sixteenths, 0 = no split, read once per process). The state pass of the
+ * leading parts then runs on `stream` beside the card launch of the trailing
+ * parts on a library-owned stream; events fork that stream off `stream` and
+ * join it back before the call returns, so all work stays ordered on
+ * `stream`. Results are bitwise those of the unsplit schedule.
  */
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                          const void *log_alpha, const void *beta,
@@ -113,6 +122,16 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
 
 size_t kda_chunk_fwd_workspace_size(int64_t T_total, int n_seq, int H, int dk,
                                     int dv, int chunk, kda_dtype dtype);
+
+/*
+ * Kernel launches kda_chunk_fwd (and kda_chunk_fwd_checkpoints) make for this
+ * problem: 3 (chunk table, chunk prep, state pass), 5 for a split prefill
+ * (chunk table, prep of the leading parts, state pass of the leading parts,
+ * prep of the trailing parts, state pass of the trailing parts), 0 for an
+ * empty or invalid problem. Host only.
+ */
+int kda_chunk_fwd_launches(int64_t T_total, int n_seq, int H, int dk, int dv,
+                           int chunk, kda_dtype dtype);
 
 /*
  * kda_chunk_fwd that also saves the state at fixed token boundaries, for a
@@ -323,7 +342,9 @@ kda_status kda_get_error(kda_stream_t stream);
  * handles, created and owned by the caller) on its stream around its i-th
  * kernel launch, i < n; launches past n are not traced. kda_chunk_fwd and
  * kda_segment_summary launch, in order: 0 chunk table, 1 chunk prep,
- * 2 state pass. n = 0 turns tracing off. Records nothing else and allocates
+ * 2 state pass (a split kda_chunk_fwd: the five launches that
+ * kda_chunk_fwd_launches lists, the trailing cards' events on the library's
+ * card stream). n = 0 turns tracing off. Records nothing else and allocates
  * nothing; the caller reads the elapsed times with cudaEventElapsedTime.
  */
 kda_status kda_trace_events(void *const *begin, void *const *end, int n);

@@ -73,6 +73,7 @@ def load(path: str = LIB_PATH):
             "kda_last_error_string": ([], ctypes.c_char_p),
             "kda_chunk_fwd": ([P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, P, SZ, P], I),
             "kda_chunk_fwd_workspace_size": ([I64, I, I, I, I, I, I], SZ),
+            "kda_chunk_fwd_launches": ([I64, I, I, I, I, I, I], I),
             "kda_chunk_bwd": ([P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I,
                                I, F, U, I, P, SZ, P], I),
             "kda_chunk_bwd_workspace_size": ([I64, I, I, I, I, I, I], SZ),
@@ -149,6 +150,11 @@ def kda_last_error_string() -> str:
 
 def kda_chunk_fwd_workspace_size(T_total, n_seq, H, dk, dv, chunk=CHUNK, dtype=KDA_DTYPE_BF16):
     return int(load().kda_chunk_fwd_workspace_size(T_total, n_seq, H, dk, dv, chunk, dtype))
+
+
+def kda_chunk_fwd_launches(T_total, n_seq, H, dk, dv, chunk=CHUNK, dtype=KDA_DTYPE_BF16):
+    """Kernel launches of kda_chunk_fwd for this problem: 3, 5 (split prefill) or 0."""
+    return int(load().kda_chunk_fwd_launches(T_total, n_seq, H, dk, dv, chunk, dtype))
 
 
 def kda_segment_summary_workspace_size(T_total, n_seg, H, dk, dv, chunk=CHUNK, dtype=KDA_DTYPE_BF16):

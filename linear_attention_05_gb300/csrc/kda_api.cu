@@ -2,6 +2,8 @@
 // Every check here runs before any launch, so a rejected call has no effect.
 #include <cuda_runtime.h>
 #include <stdarg.h>
+
+#include <mutex>
 #include <stdint.h>
 #include <stdio.h>
 
@@ -24,14 +26,39 @@ struct Tracer {
   explicit Tracer(cudaStream_t s) : st(s) {}
   template <typename F>
   cudaError_t operator()(F &&launch) {
+    return at(st, launch);
+  }
+  // a launch on another stream than the entry point's: its events go on that stream
+  template <typename F>
+  cudaError_t at(cudaStream_t on_stream, F &&launch) {
     const int i = idx++;
     const bool on = i < g_tr_n;
-    if (on) cudaEventRecord(g_tr_begin[i], st);
+    if (on) cudaEventRecord(g_tr_begin[i], on_stream);
     cudaError_t e = launch();
-    if (on) cudaEventRecord(g_tr_end[i], st);
+    if (on) cudaEventRecord(g_tr_end[i], on_stream);
     return e;
   }
 };
+
+// Library-owned stream (one per device) that carries the trailing cards of a split prefill.
+cudaError_t split_card_stream(cudaStream_t *out) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static cudaStream_t streams[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (streams[dev] == nullptr) {
+    cudaStream_t s = nullptr;
+    e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return e;
+    streams[dev] = s;
+  }
+  *out = streams[dev];
+  return cudaSuccess;
+}
 
 kda_status fail(kda_status st, const char *fmt, ...) {
   va_list ap;
@@ -118,12 +145,76 @@ size_t kda_chunk_fwd_workspace_size(int64_t T_total, int n_seq, int H, int dk, i
   return kda::chunk_ws_bytes(T_total, n_seq, H, dk, dv);
 }
 
+int kda_chunk_fwd_launches(int64_t T_total, int n_seq, int H, int dk, int dv, int chunk,
+                           kda_dtype dtype) {
+  if (common_checks(T_total, n_seq, H, dk, dv, chunk, dtype, (const int32_t *)1) != KDA_OK)
+    return 0;
+  if (n_seq == 0) return 0;
+  return (kda::tc_path(dk, dv, dtype) && kda::tc_split16(T_total, n_seq, H) > 0) ? 5 : 3;
+}
+
 size_t kda_segment_summary_workspace_size(int64_t T_total, int n_seg, int H, int dk, int dv,
                                           int chunk, kda_dtype dtype) {
   return kda_chunk_fwd_workspace_size(T_total, n_seg, H, dk, dv, chunk, dtype);
 }
 
 }  // extern "C"
+
+// Tensor-core prefill split in two parts per sequence (ws.split16 > 0), after the chunk table:
+//   stream s:     leading cards -> state pass over the leading parts -> state pass, trailing
+//   card stream:                   trailing cards (beside the first state pass)
+// The first state pass follows the leading cards in s, so its CTAs are placed on the idle GPU
+// before those of the trailing cards (which reach the GPU through an event); the trailing
+// cards then take the SMs it leaves free. Events fork the card stream off s and join it back,
+// so the call stays ordered on s (and can be captured).
+static kda_status split_prefill(const void *q, const void *k, const void *v,
+                                const void *log_alpha, const void *beta, const void *gate,
+                                void *out, const float *initial_state, float *final_state,
+                                kda::CkptOut ck, const int32_t *cu_seqlens, int n_seq,
+                                int64_t T_total, int H, float scale, unsigned flags,
+                                const kda::ChunkWs &ws, cudaStream_t s, Tracer &tr) {
+  cudaStream_t side = nullptr;
+  kda_status st = cuda_status(split_card_stream(&side), "card stream");
+  if (st != KDA_OK) return st;
+  cudaEvent_t ev[2] = {nullptr, nullptr};
+  for (cudaEvent_t &e : ev) {
+    st = cuda_status(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "event");
+    if (st != KDA_OK) break;
+  }
+  auto cards = [&](int part, cudaStream_t on) {
+    return cuda_status(tr.at(on, [&] {
+                         return kda::launch_card_tc(q, k, v, log_alpha, beta, cu_seqlens, n_seq,
+                                                    T_total, H, flags, ws, on, part);
+                       }),
+                       "chunk prep");
+  };
+  auto state = [&](int part) {
+    return cuda_status(tr([&] {
+                         return kda::launch_state_tc(0, flags, gate, out, initial_state,
+                                                     final_state, nullptr, nullptr, cu_seqlens,
+                                                     n_seq, T_total, H, scale, ws, s, ck, part);
+                       }),
+                       "state pass");
+  };
+  bool forked = false;
+  if (st == KDA_OK) st = cards(0, s);
+  if (st == KDA_OK) st = cuda_status(cudaEventRecord(ev[0], s), "event record");
+  if (st == KDA_OK) st = state(0);
+  if (st == KDA_OK) st = cuda_status(cudaStreamWaitEvent(side, ev[0], 0), "stream wait");
+  if (st == KDA_OK) {
+    forked = true;
+    st = cards(1, side);
+  }
+  if (forked) {  // join the card stream back into s, also after a failed launch
+    kda_status j = cuda_status(cudaEventRecord(ev[1], side), "event record");
+    if (j == KDA_OK) j = cuda_status(cudaStreamWaitEvent(s, ev[1], 0), "stream wait");
+    if (st == KDA_OK) st = j;
+  }
+  if (st == KDA_OK) st = state(1);
+  for (cudaEvent_t e : ev)
+    if (e) cudaEventDestroy(e);
+  return st;
+}
 
 // kda_chunk_fwd and kda_chunk_fwd_checkpoints: one path, the checkpoint output optional.
 static kda_status chunk_fwd_impl(const void *q, const void *k, const void *v,
@@ -165,6 +256,9 @@ static kda_status chunk_fwd_impl(const void *q, const void *k, const void *v,
   st = cuda_status(tr([&] { return kda::launch_chunk_table(cu_seqlens, n_seq, T_total, ws, s); }),
                    "chunk table");
   if (st != KDA_OK) return st;
+  if (tc && ws.split16 > 0)
+    return split_prefill(q, k, v, log_alpha, beta, gate, out, initial_state, final_state, ck,
+                         cu_seqlens, n_seq, T_total, H, scale, flags, ws, s, tr);
   st = cuda_status(tr([&] {
                      return tc ? kda::launch_card_tc(q, k, v, log_alpha, beta, cu_seqlens, n_seq,
                                                      T_total, H, flags, ws, s)

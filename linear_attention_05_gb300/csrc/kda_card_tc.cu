@@ -16,6 +16,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -66,15 +68,34 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
     const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_v,
     const __nv_bfloat16 *__restrict__ beta, const int32_t *__restrict__ cu, int n_seq,
     int64_t fixed_len, int H, unsigned flags, const ChunkMeta *__restrict__ meta,
-    const int *__restrict__ off, uint8_t *__restrict__ cards) {
+    const int *__restrict__ off, const int *__restrict__ off_lo, int chunk_part,
+    uint8_t *__restrict__ cards) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_base;
   __shared__ float s_rk[C], s_rq[C], s_b[C], s_d[DD];
 
-  const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int h = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31, quad = warp & 3, grp = warp >> 2;
-  if (meta->invalid || ci >= meta->total_chunks) return;
+  if (meta->invalid) return;
+  // global chunk of this CTA: all chunks (chunk_part < 0), or the x-th chunk of the leading
+  // (chunk_part 0) or trailing (chunk_part 1) parts of the sequences, in sequence order
+  int ci = blockIdx.x;
+  if (chunk_part == 0) {
+    if (ci >= meta->lo_chunks) return;
+    const int s0 = find_seq(off_lo, n_seq, ci);
+    ci = off[s0] + (ci - off_lo[s0]);
+  } else if (chunk_part == 1) {
+    if (ci >= meta->total_chunks - meta->lo_chunks) return;
+    int lo = 0, hi = n_seq - 1;  // largest s whose trailing part starts at or before ci
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (off[mid] - off_lo[mid] <= ci) lo = mid; else hi = mid - 1;
+    }
+    ci = off[lo] + (off_lo[lo + 1] - off_lo[lo]) + (ci - (off[lo] - off_lo[lo]));
+  } else if (ci >= meta->total_chunks) {
+    return;
+  }
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(sm);
 
@@ -500,10 +521,27 @@ bool tc_path(int dk, int dv, kda_dtype dt) {
   return dt == KDA_DTYPE_BF16 && dk == DD && dv == DD;
 }
 
+// The state pass runs one CTA per (sequence, head). With at most 112 of them (three
+// quarters of a 152-SM GPU's SMs) and at least 16 chunks per sequence on average, the cards
+// of each sequence's last 5/16 are built on the idle SMs while the state pass walks the first
+// 11/16. KDA_PREFILL_SPLIT (0..15 sixteenths, read once) overrides the fraction; 0 turns the
+// split off.
+int tc_split16(int64_t T_total, int n_seq, int H) {
+  static const int frac = [] {
+    const char *e = getenv("KDA_PREFILL_SPLIT");
+    const int v = e ? atoi(e) : 11;
+    return (v >= 0 && v <= 15) ? v : 11;
+  }();
+  if (n_seq <= 0 || (int64_t)n_seq * H > 112 || T_total < (int64_t)16 * C * n_seq) return 0;
+  return frac;
+}
+
 size_t tc_ws_bytes(int64_t T_total, int n_seq, int H) {
   const size_t mc = (size_t)(T_total / C) + (size_t)n_seq + 1;
   size_t b = align_up(sizeof(ChunkMeta), 256);
-  b += align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
+  b += 2 * align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
+  if (tc_split16(T_total, n_seq, H) > 0)
+    b += align_up(sizeof(float) * (size_t)n_seq * H * DD * DD, 256);
   b += (size_t)mc * H * CARD_BYTES;
   return b;
 }
@@ -515,6 +553,15 @@ ChunkWs tc_ws_carve(void *ws, int64_t T_total, int n_seq, int H) {
   p += align_up(sizeof(ChunkMeta), 256);
   w.seq_chunk_off = (int *)p;
   p += align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
+  w.split16 = tc_split16(T_total, n_seq, H);
+  if (w.split16 > 0) {
+    w.seq_chunk_lo = (int *)p;
+    p += align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
+    w.mid = (float *)p;
+    p += align_up(sizeof(float) * (size_t)n_seq * H * DD * DD, 256);
+  } else {
+    p += align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
+  }
   w.cards = (uint8_t *)p;
   w.max_chunks = (int)((size_t)(T_total / C) + (size_t)n_seq + 1);
   return w;
@@ -551,7 +598,7 @@ static bool make_token_map(CUtensorMap *m, const void *base, int64_t T_total, in
 
 cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const void *la,
                            const void *beta, const int32_t *cu, int n_seq, int64_t T_total, int H,
-                           unsigned flags, const ChunkWs &ws, cudaStream_t st) {
+                           unsigned flags, const ChunkWs &ws, cudaStream_t st, int part) {
   if (T_total == 0) return cudaSuccess;  // no chunk has tokens
   CUtensorMap mk, mq, mla, mv;
   if (!make_token_map(&mk, k, T_total, H) || !make_token_map(&mq, q, T_total, H) ||
@@ -561,9 +608,16 @@ cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const vo
       cudaFuncSetAttribute(kda_card_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, A_DYN);
   if (e != cudaSuccess) return e;
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
-  kda_card_tc<<<dim3(ws.max_chunks, H), 256, A_DYN, st>>>(
+  // CTAs beyond a part's chunk count (known on the device only) return at once. Leading parts
+  // hold at most split16/16 of all chunks; trailing parts at most the rest plus one per sequence.
+  int grid = ws.max_chunks;
+  if (part == 0) grid = (int)((int64_t)ws.max_chunks * ws.split16 / 16) + 1;
+  if (part == 1)
+    grid = (int)std::min<int64_t>(ws.max_chunks,
+                                  (int64_t)ws.max_chunks * (16 - ws.split16) / 16 + n_seq + 1);
+  kda_card_tc<<<dim3(grid, H), 256, A_DYN, st>>>(
       mk, mq, mla, mv, (const __nv_bfloat16 *)beta, cu, n_seq, fixed_len, H, flags, ws.meta,
-      ws.seq_chunk_off, ws.cards);
+      ws.seq_chunk_off, ws.seq_chunk_lo, part, ws.cards);
   return cudaGetLastError();
 }
 

@@ -51,39 +51,16 @@ __device__ __forceinline__ void seq_range(const int32_t *cu, int64_t fixed_len, 
   }
 }
 
-// One block: validate cu_seqlens and build per-sequence chunk offsets.
-__global__ void __launch_bounds__(1024) kda_chunk_table(const int32_t *cu, int n_seq,
-                                                        int64_t T_total, ChunkMeta *meta,
-                                                        int *off) {
-  __shared__ int warp_tot[32];
-  __shared__ int bad;
-  const int tid = threadIdx.x, nt = blockDim.x;
-  if (tid == 0) bad = 0;
-  __syncthreads();
-  const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
-  // contiguous range of sequences per thread
-  const int per = (n_seq + nt - 1) / nt;
-  const int s_lo = min(n_seq, tid * per), s_hi = min(n_seq, s_lo + per);
-  int local = 0;
-  for (int s = s_lo; s < s_hi; ++s) {
-    int64_t len;
-    if (cu) {
-      len = (int64_t)cu[s + 1] - cu[s];
-      if (len < 0) bad = 1;
-    } else {
-      len = fixed_len;
-    }
-    local += (int)((len + C - 1) / C);
-  }
-  if (cu && tid == 0 && (cu[0] != 0 || (int64_t)cu[n_seq] != T_total)) bad = 1;
-  // block exclusive scan of `local`
-  const int lane = tid & 31, w = tid >> 5;
+// Exclusive prefix sum of `local` over the block (1024 threads), in thread order.
+__device__ int block_exclusive_scan(int local, int *warp_tot) {
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
   int incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     int y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
+  __syncthreads();  // warp_tot may still be read from a previous scan
   if (lane == 31) warp_tot[w] = incl;
   __syncthreads();
   if (w == 0) {
@@ -97,19 +74,56 @@ __global__ void __launch_bounds__(1024) kda_chunk_table(const int32_t *cu, int n
     warp_tot[lane] = xi - x;  // exclusive
   }
   __syncthreads();
-  int run = warp_tot[w] + incl - local;
+  return warp_tot[w] + incl - local;
+}
+
+// One block: validate cu_seqlens and build per-sequence chunk offsets. With off_lo given,
+// also the offsets of the leading parts (floor(n_s * split16 / 16) chunks of sequence s)
+// that a split prefill processes first.
+__global__ void __launch_bounds__(1024) kda_chunk_table(const int32_t *cu, int n_seq,
+                                                        int64_t T_total, ChunkMeta *meta,
+                                                        int *off, int split16, int *off_lo) {
+  __shared__ int warp_tot[32];
+  __shared__ int bad;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+  const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
+  // contiguous range of sequences per thread
+  const int per = (n_seq + nt - 1) / nt;
+  const int s_lo = min(n_seq, tid * per), s_hi = min(n_seq, s_lo + per);
+  auto chunks_of = [&](int s) -> int {
+    const int64_t len = cu ? (int64_t)cu[s + 1] - cu[s] : fixed_len;
+    return len < 0 ? 0 : (int)((len + C - 1) / C);
+  };
+  int local = 0, local_lo = 0;
+  for (int s = s_lo; s < s_hi; ++s) {
+    if (cu && (int64_t)cu[s + 1] - cu[s] < 0) bad = 1;
+    local += chunks_of(s);
+    local_lo += chunks_of(s) * split16 / 16;
+  }
+  if (cu && tid == 0 && (cu[0] != 0 || (int64_t)cu[n_seq] != T_total)) bad = 1;
+  int run = block_exclusive_scan(local, warp_tot);
   for (int s = s_lo; s < s_hi; ++s) {
     off[s] = run;
-    int64_t len = cu ? (int64_t)cu[s + 1] - cu[s] : fixed_len;
-    run += (int)((len + C - 1) / C);
+    run += chunks_of(s);
   }
-  __syncthreads();
   if (s_hi == n_seq && s_lo < s_hi) off[n_seq] = run;
+  if (off_lo) {
+    int run_lo = block_exclusive_scan(local_lo, warp_tot);
+    for (int s = s_lo; s < s_hi; ++s) {
+      off_lo[s] = run_lo;
+      run_lo += chunks_of(s) * split16 / 16;
+    }
+    if (s_hi == n_seq && s_lo < s_hi) off_lo[n_seq] = run_lo;
+    if (n_seq == 0 && tid == 0) off_lo[0] = 0;
+  }
   if (n_seq == 0 && tid == 0) off[0] = 0;
   __syncthreads();
   if (tid == 0) {
     meta->invalid = bad;
     meta->total_chunks = bad ? 0 : off[n_seq];
+    meta->lo_chunks = (bad || !off_lo) ? 0 : off_lo[n_seq];
     if (bad) set_err(kErrBadSeqlens);
   }
 }
@@ -635,7 +649,8 @@ ChunkWs chunk_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int 
 
 cudaError_t launch_chunk_table(const int32_t *cu, int n_seq, int64_t T_total, const ChunkWs &ws,
                                cudaStream_t st) {
-  kda_chunk_table<<<1, 1024, 0, st>>>(cu, n_seq, T_total, ws.meta, ws.seq_chunk_off);
+  kda_chunk_table<<<1, 1024, 0, st>>>(cu, n_seq, T_total, ws.meta, ws.seq_chunk_off,
+                                      ws.split16, ws.seq_chunk_lo);
   return cudaGetLastError();
 }
 

@@ -58,7 +58,8 @@ __device__ __forceinline__ float warp_sum(float x) {
 struct ChunkMeta {
   int total_chunks;  // sum over sequences of ceil(len / 64)
   int invalid;       // non-zero: cu_seqlens rejected; every kernel exits
-  int pad[62];
+  int lo_chunks;     // split prefill: chunks in the leading parts of all sequences
+  int pad[61];
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) {
@@ -124,6 +125,12 @@ struct ChunkWs {
   float *W, *U, *Q, *Kd, *P, *D;  // SIMT path
   uint8_t *cards;                 // tensor-core path: one update card per (chunk, head)
   int max_chunks;
+  // Split prefill (tensor-core path): each sequence's first floor(n_s * split16 / 16) chunks
+  // form its leading part. seq_chunk_lo [n_seq + 1] holds the leading parts' offsets and mid
+  // [n_seq, H, 128, 128] the state between the parts. split16 = 0: no split.
+  int split16;
+  int *seq_chunk_lo;
+  float *mid;
 };
 
 size_t chunk_ws_bytes(int64_t T_total, int n_seq, int H, int dk, int dv);
@@ -156,15 +163,21 @@ cudaError_t launch_scan_combine(const float *X, const float *Z, int n_seg,
 
 // Tensor-core path (bf16, dk = dv = 128): update cards + state pass.
 bool tc_path(int dk, int dv, kda_dtype dt);
+// Split prefill: sixteenths of each sequence's chunks in its leading part, or 0 when the
+// state pass would leave too few SMs idle for the trailing cards to use.
+int tc_split16(int64_t T_total, int n_seq, int H);
 size_t tc_ws_bytes(int64_t T_total, int n_seq, int H);
 ChunkWs tc_ws_carve(void *ws, int64_t T_total, int n_seq, int H);
+// part -1: every chunk; 0 / 1: the leading / trailing parts of a split prefill (ws.split16 > 0).
+// The state pass of part 0 leaves its state in ws.mid, where part 1 starts.
 cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const void *la,
                            const void *beta, const int32_t *cu, int n_seq, int64_t T_total,
-                           int H, unsigned flags, const ChunkWs &ws, cudaStream_t st);
+                           int H, unsigned flags, const ChunkWs &ws, cudaStream_t st,
+                           int part = -1);
 cudaError_t launch_state_tc(int mode, unsigned flags, const void *gate, void *out, const float *S0,
                             float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                             int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
-                            cudaStream_t st, CkptOut ck = CkptOut());
+                            cudaStream_t st, CkptOut ck = CkptOut(), int part = -1);
 cudaError_t tc_take_error(unsigned *bits);        // card and state-pass words together
 cudaError_t state_tc_take_error(unsigned *bits);  // the state pass's word alone
 

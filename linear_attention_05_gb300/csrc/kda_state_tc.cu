@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
     const float *__restrict__ S0, float *__restrict__ S_final, float *__restrict__ X_out,
     float *__restrict__ Z_out, const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len,
     int H, float scale, const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
-    const uint8_t *__restrict__ cards, CkptOut ck) {
+    const uint8_t *__restrict__ cards, CkptOut ck, int part, int split16, float *__restrict__ mid) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[B_NSTAGE], bar_mma, bar_ofull[2], bar_ofree[2];
   __shared__ uint32_t tmem_base;
@@ -79,23 +79,41 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
 
   int64_t ts, ls;
   seq_range(cu, fixed_len, s, &ts, &ls);
-  const int nchunks = (int)((ls + C - 1) / C);
-  const int cbase = nchunks > 0 ? off[s] : 0;
+  const int64_t ls_seq = ls;
+  int nchunks = (int)((ls + C - 1) / C);
+  // a split prefill walks the first nchunks * split16 / 16 chunks (part 0), handing its
+  // state over in `mid`, then the rest (part 1); chunk n below is chunk n_lo + n of the sequence
+  int n_lo = 0;
+  if (part >= 0) {
+    const int m = nchunks * split16 / 16;
+    if (part == 0) {
+      nchunks = m;
+      ls = (int64_t)m * C;
+    } else {
+      n_lo = m;
+      nchunks -= m;
+      ts += (int64_t)m * C;
+      ls -= (int64_t)m * C;
+    }
+  }
+  const int cbase = nchunks > 0 ? off[s] + n_lo : 0;
   auto card_of = [&](int n) { return cards + ((size_t)(cbase + n) * H + h) * CARD_BYTES; };
+  const float *S_entry = part == 1 ? mid : S0;
+  float *S_exit = part == 0 ? mid : S_final;
   // element (c, j) of the entry state, and where element (c, j) of the result goes
   auto entry = [&](int c) -> float {
-    if (mode == 0) return S0 ? S0[(((size_t)s * H + h) * DD + c) * DD + j] : 0.f;
+    if (mode == 0) return S_entry ? S_entry[(((size_t)s * H + h) * DD + c) * DD + j] : 0.f;
     return (xpart && c == j) ? 1.f : 0.f;
   };
   auto result_ptr = [&](int c) -> float * {
-    if (mode == 0) return S_final ? S_final + (((size_t)s * H + h) * DD + c) * DD + j : nullptr;
+    if (mode == 0) return S_exit ? S_exit + (((size_t)s * H + h) * DD + c) * DD + j : nullptr;
     if (xpart) return X_out + (((size_t)s * H + h) * DD + c) * DD + j;
     return Z_out + (((size_t)s * H + h) * DD + c) * DD + j;
   };
   // prefix-cache checkpoint after chunk n (mode 0): this thread's 64 rows of column j
   auto save_ckpt = [&](int n, const float *x0, const float *x1) {
     if (mode != 0) return;
-    float *cp = ckpt_after_chunk(ck, s, n, ls, H, h, DD, DD);
+    float *cp = ckpt_after_chunk(ck, s, n_lo + n, ls_seq, H, h, DD, DD);
     if (cp == nullptr) return;
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
@@ -400,14 +418,15 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
 cudaError_t launch_state_tc(int mode, unsigned flags, const void *gate, void *out, const float *S0,
                             float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                             int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
-                            cudaStream_t st, CkptOut ck) {
+                            cudaStream_t st, CkptOut ck, int part) {
   cudaError_t e =
       cudaFuncSetAttribute(kda_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, B_DYN);
   if (e != cudaSuccess) return e;
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
   kda_state_tc<<<dim3(n_seq * H, mode == 0 ? 1 : 2), 384, B_DYN, st>>>(
       mode, flags, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final, X_out, Z_out, cu,
-      n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.cards, ck);
+      n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.cards, ck, part, ws.split16,
+      ws.mid);
   return cudaGetLastError();
 }
 

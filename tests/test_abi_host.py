@@ -163,6 +163,25 @@ def test_workspace_size(lib):
     assert B.kda_segment_summary_workspace_size(4096, 2, 16, 128, 128) > 0
 
 
+def test_chunk_fwd_launches(lib):
+    """Prefills with few (sequence, head) pairs and long sequences are split (5 launches);
+    the rest, and every other shape or dtype, take 3."""
+    bf, f32 = B.KDA_DTYPE_BF16, B.KDA_DTYPE_F32
+    assert B.kda_chunk_fwd_launches(4 * 4096, 4, 16, 128, 128, dtype=bf) == 5
+    assert B.kda_chunk_fwd_launches(16 * 1024, 7, 16, 128, 128, dtype=bf) == 5     # 112 pairs
+    assert B.kda_chunk_fwd_launches(16 * 1024, 8, 16, 128, 128, dtype=bf) == 3     # 128 pairs
+    assert B.kda_chunk_fwd_launches(4 * 512, 4, 16, 128, 128, dtype=bf) == 3       # 8 chunks/seq
+    assert B.kda_chunk_fwd_launches(4 * 1024, 4, 16, 128, 128, dtype=bf) == 5      # 16 chunks/seq
+    assert B.kda_chunk_fwd_launches(4 * 4096, 4, 16, 128, 128, dtype=f32) == 3
+    assert B.kda_chunk_fwd_launches(4 * 4096, 4, 16, 64, 64, dtype=bf) == 3
+    assert B.kda_chunk_fwd_launches(0, 0, 16, 128, 128, dtype=bf) == 0
+    assert B.kda_chunk_fwd_launches(4096, 1, 16, 96, 128, dtype=bf) == 0
+    # a split prefill's workspace holds the hand-over state between the parts
+    split = B.kda_chunk_fwd_workspace_size(4 * 1024, 4, 16, 128, 128)
+    whole = B.kda_chunk_fwd_workspace_size(4 * 1024 - 64, 4, 16, 128, 128)
+    assert split - whole >= 4 * 16 * 128 * 128 * 4
+
+
 def dec(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, la=FAKE, beta=FAKE, gate=None, out=FAKE, state=FAKE,
              slot=None, n_slots=4, N=4, H=2, dk=128, dv=128, scale=1.0, flags=1, dtype=1,
