@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
   }
   if (tid < DD) reinterpret_cast<float *>(card + CARD_D)[tid] = s_d[tid];
   if (!ok && lane == 0) set_err(kErrTimeout);
-  if (lane == 0) bulk_wait_all();  // the card-tile bulk stores have completed
+  if (lane == 0) bulk_wait_read_all();  // shared memory read by the card-tile bulk stores
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tb, 256);
@@ -539,7 +539,7 @@ int tc_split16(int64_t T_total, int n_seq, int H) {
 size_t tc_ws_bytes(int64_t T_total, int n_seq, int H) {
   const size_t mc = (size_t)(T_total / C) + (size_t)n_seq + 1;
   size_t b = align_up(sizeof(ChunkMeta), 256);
-  b += 2 * align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
+  b += 3 * align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
   if (tc_split16(T_total, n_seq, H) > 0)
     b += align_up(sizeof(float) * (size_t)n_seq * H * DD * DD, 256);
   b += (size_t)mc * H * CARD_BYTES;
@@ -552,6 +552,8 @@ ChunkWs tc_ws_carve(void *ws, int64_t T_total, int n_seq, int H) {
   w.meta = (ChunkMeta *)p;
   p += align_up(sizeof(ChunkMeta), 256);
   w.seq_chunk_off = (int *)p;
+  p += align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
+  w.seq_order = (int *)p;
   p += align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
   w.split16 = tc_split16(T_total, n_seq, H);
   if (w.split16 > 0) {

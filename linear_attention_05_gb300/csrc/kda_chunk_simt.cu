@@ -82,9 +82,11 @@ __device__ int block_exclusive_scan(int local, int *warp_tot) {
 // that a split prefill processes first.
 __global__ void __launch_bounds__(1024) kda_chunk_table(const int32_t *cu, int n_seq,
                                                         int64_t T_total, ChunkMeta *meta,
-                                                        int *off, int split16, int *off_lo) {
+                                                        int *off, int split16, int *off_lo,
+                                                        int *order) {
   __shared__ int warp_tot[32];
   __shared__ int bad;
+  __shared__ int s_chunks[kOrderMax];
   const int tid = threadIdx.x, nt = blockDim.x;
   if (tid == 0) bad = 0;
   __syncthreads();
@@ -119,6 +121,21 @@ __global__ void __launch_bounds__(1024) kda_chunk_table(const int32_t *cu, int n
     if (n_seq == 0 && tid == 0) off_lo[0] = 0;
   }
   if (n_seq == 0 && tid == 0) off[0] = 0;
+  if (order) {
+    // longest first: rank = sequences with more chunks, or as many and a lower index
+    if (n_seq <= kOrderMax) {
+      for (int s = tid; s < n_seq; s += nt) s_chunks[s] = chunks_of(s);
+      __syncthreads();
+      for (int s = tid; s < n_seq; s += nt) {
+        const int c = s_chunks[s];
+        int r = 0;
+        for (int t = 0; t < n_seq; ++t) r += (s_chunks[t] > c) || (s_chunks[t] == c && t < s);
+        order[r] = s;
+      }
+    } else {
+      for (int s = tid; s < n_seq; s += nt) order[s] = s;
+    }
+  }
   __syncthreads();
   if (tid == 0) {
     meta->invalid = bad;
@@ -650,7 +667,7 @@ ChunkWs chunk_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int 
 cudaError_t launch_chunk_table(const int32_t *cu, int n_seq, int64_t T_total, const ChunkWs &ws,
                                cudaStream_t st) {
   kda_chunk_table<<<1, 1024, 0, st>>>(cu, n_seq, T_total, ws.meta, ws.seq_chunk_off,
-                                      ws.split16, ws.seq_chunk_lo);
+                                      ws.split16, ws.seq_chunk_lo, ws.seq_order);
   return cudaGetLastError();
 }
 

@@ -131,7 +131,12 @@ struct ChunkWs {
   int split16;
   int *seq_chunk_lo;
   float *mid;
+  // tensor-core path: sequences by decreasing chunk count (ties by index) when there are at
+  // most kOrderMax of them, else in index order. The state pass takes its chains in this
+  // order, so the longest chains start in the first wave of CTAs.
+  int *seq_order;
 };
+constexpr int kOrderMax = 256;
 
 size_t chunk_ws_bytes(int64_t T_total, int n_seq, int H, int dk, int dv);
 ChunkWs chunk_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int dv);

@@ -27,7 +27,6 @@ using namespace tcl;
 
 // ---- stage B shared memory
 constexpr int B_NSTAGE = 3;            // card ring depth
-constexpr int kPrefetch = 3;           // cards prefetched into L2 beyond the ring
 constexpr int B_STAGE_TX = CARD_BCT + 512;  // [Phi'^T | Q'^T] then e^{G_C} (49664 bytes)
 constexpr int B_STAGE_BYTES = 50176;  // B_STAGE_TX rounded up to 1024
 constexpr int B_SA = B_NSTAGE * B_STAGE_BYTES;  // S^T bf16 operand, 128 x 128 K-major (32768)
@@ -59,7 +58,8 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
     const float *__restrict__ S0, float *__restrict__ S_final, float *__restrict__ X_out,
     float *__restrict__ Z_out, const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len,
     int H, float scale, const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
-    const uint8_t *__restrict__ cards, CkptOut ck, int part, int split16, float *__restrict__ mid) {
+    const uint8_t *__restrict__ cards, CkptOut ck, int part, int split16, float *__restrict__ mid,
+    const int *__restrict__ seq_order) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[B_NSTAGE], bar_mma, bar_ofull[2], bar_ofree[2];
   __shared__ uint32_t tmem_base;
@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
   if (meta->invalid) return;
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(sm);
-  const int chain = blockIdx.x, s = chain / H, h = chain % H, tid = threadIdx.x;
+  // CTAs take the sequences longest first (the order the chunk table computed)
+  const int chain = blockIdx.x, s = seq_order[chain / H], h = chain % H, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const bool state_grp = warp < 8;
   const int quad = warp & 3;           // lane quadrant of this warp
@@ -222,17 +223,20 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
       return true;
     };
 
-    // whole cards into L2 ahead of their bulk copies (which otherwise wait on HBM latency)
+    // card n into L2 as its [Phi'^T | Q'^T] part is bulk-copied: the plain loads of its B_c^T
+    // and O_intra^T come two chunks later. (Prefetching 1, 2, 3 or 6 chunks further ahead was
+    // measured slower: 0.189, 0.190, 0.192 and 0.216 ms per pass against 0.1885.)
     auto prefetch_card = [&](int n) {
       if (n >= nchunks) return;
       const uint8_t *src = card_of(n);
       for (int o = 0; o < CARD_BYTES; o += 32768)
         prefetch_l2(src + o, min(32768, CARD_BYTES - o));
     };
-    if (loader) {
-      for (int n = 0; n < B_NSTAGE && n < nchunks; ++n) load_card(n);
-      for (int n = B_NSTAGE; n < B_NSTAGE + kPrefetch; ++n) prefetch_card(n);
-    }
+    if (loader)
+      for (int n = 0; n < B_NSTAGE && n < nchunks; ++n) {
+        load_card(n);
+        prefetch_card(n);
+      }
     fetch_bc(0);
     // chunk 0: entry state from global memory
     if (!wait_full(0)) ok = false;
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
       // the card of chunk n is consumed: refill its stage with chunk n + 3
       if (good && loader && n + B_NSTAGE < nchunks) {
         load_card(n + B_NSTAGE);
-        prefetch_card(n + B_NSTAGE + kPrefetch);
+        prefetch_card(n + B_NSTAGE);
       }
       const bool last = (n + 1 == nchunks);
       if (good && !last) good = wait_full(n + 1);
@@ -426,7 +430,7 @@ cudaError_t launch_state_tc(int mode, unsigned flags, const void *gate, void *ou
   kda_state_tc<<<dim3(n_seq * H, mode == 0 ? 1 : 2), 384, B_DYN, st>>>(
       mode, flags, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final, X_out, Z_out, cu,
       n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.cards, ck, part, ws.split16,
-      ws.mid);
+      ws.mid, ws.seq_order);
   return cudaGetLastError();
 }
 
