@@ -356,8 +356,8 @@ def run_gpu(args, rank, world, local):
                         "achieved": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
                         "frac": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
     if n_launch == 5:
-        roofline["schedule"] = ("split prefill: trailing 5/16 of each sequence's cards built "
-                                "beside the state pass over the leading 11/16")
+        roofline["schedule"] = ("split prefill: the cards of each sequence's trailing chunks are "
+                                "built beside the state pass over its leading chunks")
     if tc:
         # tensor-core work per (chunk, head): card GEMMs 1-4 and the state-pass MMA group,
         # over the whole step (the launches overlap, so their durations do not add up)

@@ -27,6 +27,11 @@ using namespace tcl;
 
 // ---- stage B shared memory
 constexpr int B_NSTAGE = 3;            // card ring depth
+// 8 state warps + 8 output warps; launched at 128 registers a thread, split by setmaxnreg
+constexpr int kThreads = 512;
+constexpr int kStateRegs = 160, kOutRegs = 96;
+static_assert(2 * 128 * kStateRegs + 2 * 128 * kOutRegs <= kThreads * 128,
+              "the register split must fit the launch's allocation");
 constexpr int B_STAGE_TX = CARD_BCT + 512;  // [Phi'^T | Q'^T] then e^{G_C} (49664 bytes)
 constexpr int B_STAGE_BYTES = 50176;  // B_STAGE_TX rounded up to 1024
 constexpr int B_SA = B_NSTAGE * B_STAGE_BYTES;  // S^T bf16 operand, 128 x 128 K-major (32768)
@@ -36,13 +41,13 @@ constexpr int B_DYN = B_OT + 64 * (DD + 4) * 4 + 1024;
 __device__ __forceinline__ void set_err(unsigned bits) { atomicOr(&g_state_tc_err, bits); }
 
 // ===========================================================================
-// Stage B: the sequential state pass, one CTA per (sequence, head), 384 threads.
-// Warps 0-7 (state group) carry the serial path: warp w serves tensor-memory
-// lanes 32*(w%4).. (lane j = value channel j, i.e. row j of S^T) and the key
-// columns [64*(w/4), 64*(w/4) + 64) of that row. Warps 8-11 (output group) read
-// the chunk outputs from the same lanes, apply scale and gate and store o, off
-// the serial path. mode 0: prefill; mode 1: segment summary on
-// [X | Z] (blockIdx.y = 0: X with entry I; 1: Z with entry 0), no output.
+// Stage B: the sequential state pass, one CTA per (sequence, head), 512 threads.
+// Warps 0-7 (state group, 168 registers a thread) carry the serial path: warp w serves
+// tensor-memory lanes 32*(w%4).. (lane j = value channel j, i.e. row j of S^T) and the key
+// columns [64*(w/4), 64*(w/4) + 64) of that row. Warps 8-15 (two output warpgroups, 88
+// registers a thread, one per 32-token half of the chunk) read the chunk outputs from the same
+// lanes, apply scale and gate and store o, off the serial path. mode 0: prefill; mode 1:
+// segment summary on [X | Z] (blockIdx.y = 0: X with entry I; 1: Z with entry 0), no output.
 //
 // Tensor memory holds two accumulator sets, chunk n using set n % 2: columns
 // [256b, 256b+128) the fp32 state S^T, [256b+128, 256b+192) the output block.
@@ -52,7 +57,7 @@ __device__ __forceinline__ void set_err(unsigned bits) { atomicOr(&g_state_tc_er
 // mbarriers: bar_full[3] card stages landed; bar_mma chunk MMAs done (state
 // group); bar_ofull[2] output block written (output group); bar_ofree[2]
 // output block read and re-seeded (MMA issuer).
-__global__ void __launch_bounds__(384, 1) kda_state_tc(
+__global__ void __launch_bounds__(kThreads, 1) kda_state_tc(
     int mode, unsigned flags, const __nv_bfloat16 *__restrict__ gate,
     __nv_bfloat16 *__restrict__ out,
     const float *__restrict__ S0, float *__restrict__ S_final, float *__restrict__ X_out,
@@ -140,8 +145,8 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
     mbar_init(&bar_mma, 1);
     mbar_init(&bar_ofull[0], 1);
     mbar_init(&bar_ofull[1], 1);
-    mbar_init(&bar_ofree[0], 128);
-    mbar_init(&bar_ofree[1], 128);
+    mbar_init(&bar_ofree[0], 256);
+    mbar_init(&bar_ofree[1], 256);
     fence_mbar_init();
     s_fail = 0;
   }
@@ -150,6 +155,10 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
   tc_fence_after();
   const uint32_t tb = tmem_base;
   auto set_col = [](int n) { return 256 * (n & 1); };
+  // register split of the launch's kThreads x 128: the two state warpgroups take 168 per
+  // thread, the two output warpgroups 88 (2 x 128 x 168 + 2 x 128 x 88 = 512 x 128)
+  if (state_grp) setmaxnreg_inc<kStateRegs>();
+  else setmaxnreg_dec<kOutRegs>();
   if (state_grp) {
     int loads_issued = 0, loads_done = 0;
     uint32_t full_phase[B_NSTAGE] = {}, mma_phase = 0u;
@@ -311,48 +320,49 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
         }
     }
   } else if (with_o) {
-    // output group: o = scale * g * (Q' S + O_intra) for chunk n. The output block of chunk n
-    // starts as O_intra^T (seeded two chunks ahead from the card), so the MMA leaves
-    // Q' S + O_intra in it. The four warps copy their lane quadrants (channels) into one
-    // [64 tokens][128 channels] fp32 tile; then each thread takes 8 tokens x 8 channels, so
-    // that a warp's gate loads and output stores cover two whole 256-byte rows per
-    // instruction. The gate of the next chunk is loaded (same mapping) as this one is used.
+    // output warpgroups: o = scale * g * (Q' S + O_intra) for chunk n; warpgroup og takes tokens
+    // [32 og, 32 og + 32). The output block of chunk n starts as O_intra^T (seeded two chunks
+    // ahead from the card), so the MMA leaves Q' S + O_intra in it. The warps copy their lane
+    // quadrants (channels) into a [32 tokens][128 channels] fp32 half-tile; then each thread
+    // takes 4 tokens x 8 channels, so that a warp's gate loads and output stores cover two
+    // whole 256-byte rows per instruction. The gate of the next chunk is loaded (same mapping)
+    // as this one is used.
     constexpr int LDT = DD + 4;  // tile row pitch (floats)
-    float *tile = reinterpret_cast<float *>(sm + B_OT);
-    const int ot = tid - 256;                   // output thread 0..127
+    const int og = (warp - 8) >> 2;             // output warpgroup: token half
+    const int bar_id = 2 + og;                  // its named barrier (128 threads)
+    float *tile = reinterpret_cast<float *>(sm + B_OT) + og * 32 * LDT;
+    const int ot = tid - 256 - 128 * og;        // thread of the warpgroup, 0..127
     const int c8 = ot & 15, r0 = ot >> 4;       // store phase: channels 8*c8.., tokens r0 + 8m
     const bool logits = gate && (flags & KDA_GATE_LOGITS);
-    // this lane's O_intra^T row (all 64 tokens, bf16) of chunk c, from the card
+    // this lane's O_intra^T row (this half's 32 tokens, bf16) of chunk c, from the card
     auto load_oi = [&](int c, uint4 *oi) {
       const uint8_t *card = card_of(c);
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        oi[ch] = c < nchunks ? *reinterpret_cast<const uint4 *>(card + CARD_OIT + (ch * 128 + j) * 16)
-                             : make_uint4(0u, 0u, 0u, 0u);
+      for (int ch = 0; ch < 4; ++ch)
+        oi[ch] = c < nchunks
+                     ? *reinterpret_cast<const uint4 *>(card + CARD_OIT + ((4 * og + ch) * 128 + j) * 16)
+                     : make_uint4(0u, 0u, 0u, 0u);
     };
     auto seed = [&](int c, const uint4 *oi) {
+      float x[32];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float x[32];
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) unpack8(oi[hf * 4 + ch], x + ch * 8);
-        tmem_st32(tmem_addr(tb, quad * 32, set_col(c) + 128 + 32 * hf), x);
-      }
+      for (int ch = 0; ch < 4; ++ch) unpack8(oi[ch], x + ch * 8);
+      tmem_st32(tmem_addr(tb, quad * 32, set_col(c) + 128 + 32 * og), x);
     };
-    // gate of tokens r0 + 8m, channels 8*c8 .. 8*c8 + 7 of chunk c (1.0 when absent)
+    // gate of tokens 32 og + r0 + 8m, channels 8*c8 .. 8*c8 + 7 of chunk c (1.0 when absent)
     auto load_gate = [&](int c, uint4 *gq) {
       const int64_t tc0 = ts + (int64_t)c * C;
       const int lc = (int)min((int64_t)C, ls - (int64_t)c * C);
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int r = r0 + 8 * m;
+      for (int m = 0; m < 4; ++m) {
+        const int r = 32 * og + r0 + 8 * m;
         gq[m] = (gate && c < nchunks && r < lc)
                     ? *reinterpret_cast<const uint4 *>(gate + ((size_t)(tc0 + r) * H + h) * DD + c8 * 8)
                     : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
       }
     };
     {
-      uint4 oi[8];
+      uint4 oi[4];
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
         load_oi(b, oi);
@@ -364,39 +374,40 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
     mbar_arrive(&bar_ofree[0]);
     mbar_arrive(&bar_ofree[1]);
     uint32_t ofull_phase[2] = {0u, 0u};
-    uint4 gq[8];
+    uint4 gq[4];
     load_gate(0, gq);
     bool ok = true;
     for (int n = 0; n < nchunks; ++n) {
       const int64_t t0 = ts + (int64_t)n * C;
       const int len = (int)min((int64_t)C, ls - (int64_t)n * C);
-      uint4 oi[8];
+      uint4 oi[4];
       load_oi(n + 2, oi);  // its latency overlaps the wait below
-      // every output thread takes the same branch, so a timeout cannot strand the others
-      ok = named_bar_and(2, 128, mbar_wait(&bar_ofull[n & 1], ofull_phase[n & 1]));
+      // every thread of the warpgroup takes the same branch, so a timeout strands none of them
+      ok = named_bar_and(bar_id, 128, mbar_wait(&bar_ofull[n & 1], ofull_phase[n & 1]));
       if (!ok) break;
       ofull_phase[n & 1] ^= 1u;
       tc_fence_after();
-      // both halves into the tile (token row, this lane's channel)
+      // this half into the half-tile (token row, this lane's channel), 16 tokens at a time
+      // (the registers of the 88-register budget that oi and gq leave)
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float t[32];
-        tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 128 + 32 * hf), t);
+      for (int q = 0; q < 2; ++q) {
+        float t[16];
+        tmem_ld16(tmem_addr(tb, quad * 32, set_col(n) + 128 + 32 * og + 16 * q), t);
         tmem_wait_ld();
 #pragma unroll
-        for (int u = 0; u < 32; ++u) tile[(hf * 32 + u) * LDT + j] = t[u];
+        for (int u = 0; u < 16; ++u) tile[(16 * q + u) * LDT + j] = t[u];
       }
-      // the block is read: seed it with O_intra^T of chunk n + 2, hand it back to the issuer
+      // the half is read: seed it with O_intra^T of chunk n + 2, hand it back to the issuer
       seed(n + 2, oi);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar_ofree[n & 1]);
-      named_bar(2, 128);  // tile complete
+      named_bar(bar_id, 128);  // half-tile complete
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int r = r0 + 8 * m;
-        const float4 a = *reinterpret_cast<const float4 *>(tile + r * LDT + c8 * 8);
-        const float4 b = *reinterpret_cast<const float4 *>(tile + r * LDT + c8 * 8 + 4);
+      for (int m = 0; m < 4; ++m) {
+        const int rr = r0 + 8 * m, r = 32 * og + rr;
+        const float4 a = *reinterpret_cast<const float4 *>(tile + rr * LDT + c8 * 8);
+        const float4 b = *reinterpret_cast<const float4 *>(tile + rr * LDT + c8 * 8 + 4);
         float g8[8], e[8];
         unpack8(gq[m], g8);
         const float x8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -407,7 +418,7 @@ __global__ void __launch_bounds__(384, 1) kda_state_tc(
           *reinterpret_cast<uint4 *>(out + ((size_t)(t0 + r) * H + h) * DD + c8 * 8) = pack8(e);
       }
       load_gate(n + 1, gq);  // the next chunk's gate, while its MMAs run
-      named_bar(2, 128);     // tile consumed before the next chunk overwrites it
+      named_bar(bar_id, 128);  // half-tile consumed before the next chunk overwrites it
     }
     if (!ok && ot == 0) set_err(kErrTimeout);
   }
@@ -427,7 +438,7 @@ cudaError_t launch_state_tc(int mode, unsigned flags, const void *gate, void *ou
       cudaFuncSetAttribute(kda_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, B_DYN);
   if (e != cudaSuccess) return e;
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
-  kda_state_tc<<<dim3(n_seq * H, mode == 0 ? 1 : 2), 384, B_DYN, st>>>(
+  kda_state_tc<<<dim3(n_seq * H, mode == 0 ? 1 : 2), kThreads, B_DYN, st>>>(
       mode, flags, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final, X_out, Z_out, cu,
       n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.cards, ck, part, ws.split16,
       ws.mid, ws.seq_order);

@@ -1,7 +1,7 @@
 """Split prefill (tensor-core path) against the oracle and the unsplit schedule (needs a GPU).
 
 With few (sequence, head) pairs and long sequences, kda_chunk_fwd builds the cards of each
-sequence's leading 11/16 of chunks, runs the state pass over them on a second stream while
+sequence's leading 12/16 of chunks, runs the state pass over them while
 the cards of the trailing chunks are built, and finishes with a state pass over the trailing
 chunks. The chunked algebra is unchanged (K3 training overview, section 4 "FlashKDA": the
 cards are independent per chunk, only the state hand-off is ordered), so the results must
