@@ -26,17 +26,24 @@ using namespace tc;
 using namespace tcl;
 
 // ---- stage B shared memory
-constexpr int B_NSTAGE = 3;            // card ring depth
 // 8 state warps + 8 output warps; launched at 128 registers a thread, split by setmaxnreg
 constexpr int kThreads = 512;
 constexpr int kStateRegs = 160, kOutRegs = 96;
 static_assert(2 * 128 * kStateRegs + 2 * 128 * kOutRegs <= kThreads * 128,
               "the register split must fit the launch's allocation");
-constexpr int B_STAGE_TX = CARD_BCT + 512;  // [Phi'^T | Q'^T] then e^{G_C} (49664 bytes)
-constexpr int B_STAGE_BYTES = 50176;  // B_STAGE_TX rounded up to 1024
-constexpr int B_SA = B_NSTAGE * B_STAGE_BYTES;  // S^T bf16 operand, 128 x 128 K-major (32768)
-constexpr int B_OT = B_SA + 32768;         // output tile: 64 tokens x (128 + 4) fp32
-constexpr int B_DYN = B_OT + 64 * (DD + 4) * 4 + 1024;
+// Card ring geometry. The prefill pass copies [Phi'^T | Q'^T] and e^{G_C} into each stage,
+// three stages deep; the summary pass needs no Q'^T, so its stages are a third smaller and
+// four fit (no output tile either).
+template <bool SUMMARY>
+struct Geo {
+  static constexpr int NST = SUMMARY ? 4 : 3;             // card ring depth
+  static constexpr int PHIQ = SUMMARY ? 32768 : CARD_BCT;  // card bytes of the MMA's B operand
+  static constexpr int TX = PHIQ + 512;                    // then e^{G_C}
+  static constexpr int STAGE = (TX + 1023) / 1024 * 1024;
+  static constexpr int SA = NST * STAGE;  // S^T bf16 operand, 128 x 128 K-major (32768)
+  static constexpr int OT = SA + 32768;   // output tile: 64 tokens x (128 + 4) fp32
+  static constexpr int DYN = OT + (SUMMARY ? 0 : 64 * (DD + 4) * 4) + 1024;
+};
 
 __device__ __forceinline__ void set_err(unsigned bits) { atomicOr(&g_state_tc_err, bits); }
 
@@ -57,6 +64,7 @@ __device__ __forceinline__ void set_err(unsigned bits) { atomicOr(&g_state_tc_er
 // mbarriers: bar_full[3] card stages landed; bar_mma chunk MMAs done (state
 // group); bar_ofull[2] output block written (output group); bar_ofree[2]
 // output block read and re-seeded (MMA issuer).
+template <bool SUMMARY>
 __global__ void __launch_bounds__(kThreads, 1) kda_state_tc(
     int mode, unsigned flags, const __nv_bfloat16 *__restrict__ gate,
     __nv_bfloat16 *__restrict__ out,
@@ -65,6 +73,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_tc(
     int H, float scale, const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
     const uint8_t *__restrict__ cards, CkptOut ck, int part, int split16, float *__restrict__ mid,
     const int *__restrict__ seq_order) {
+  using G = Geo<SUMMARY>;
+  constexpr int B_NSTAGE = G::NST;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_full[B_NSTAGE], bar_mma, bar_ofull[2], bar_ofree[2];
   __shared__ uint32_t tmem_base;
@@ -168,11 +178,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_tc(
     // card n -> stage n % 3: [Phi'^T | Q'^T] and e^{G_C}
     auto load_card = [&](int n) {
       const int st = stage_of(n);
-      uint8_t *dst = sm + st * B_STAGE_BYTES;
+      uint8_t *dst = sm + st * G::STAGE;
       const uint8_t *src = card_of(n);
-      mbar_arrive_expect_tx(&bar_full[st], B_STAGE_TX);
-      for (int o = 0; o < CARD_BCT; o += 16384) bulk_g2s(dst + o, src + o, 16384, &bar_full[st]);
-      bulk_g2s(dst + CARD_BCT, src + CARD_D, 512, &bar_full[st]);
+      mbar_arrive_expect_tx(&bar_full[st], G::TX);
+      for (int o = 0; o < G::PHIQ; o += 16384) bulk_g2s(dst + o, src + o, 16384, &bar_full[st]);
+      bulk_g2s(dst + G::PHIQ, src + CARD_D, 512, &bar_full[st]);
       ++loads_issued;
     };
     auto wait_full = [&](int n) -> bool {
@@ -196,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_tc(
     // operand S^T (row j) in shared memory, from the 32 key columns 64*half + 32*qq.
     auto stage_piece = [&](int n, int qq, const float *x) {
       const float *dv =
-          reinterpret_cast<const float *>(sm + stage_of(n) * B_STAGE_BYTES + CARD_BCT);
+          reinterpret_cast<const float *>(sm + stage_of(n) * G::STAGE + G::PHIQ);
       const int q4 = 2 * half + qq;
       float init[32];
 #pragma unroll
@@ -208,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_tc(
           const int c = q4 * 32 + ch * 8 + u;
           init[ch * 8 + u] = dv[c] * x[ch * 8 + u] + (with_bc ? bc[u] : 0.f);
         }
-        *reinterpret_cast<uint4 *>(sm + B_SA + sw128_chunk(j, q4 * 4 + ch, 128)) =
+        *reinterpret_cast<uint4 *>(sm + G::SA + sw128_chunk(j, q4 * 4 + ch, 128)) =
             pack8(x + ch * 8);
       }
       tmem_st32(tmem_addr(tb, quad * 32, set_col(n) + 32 * q4), init);
@@ -222,10 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_tc(
       // the output block of set n % 2 is read and zeroed (prologue, then chunk n - 2)
       if (with_o && !mbar_wait(&bar_ofree[n & 1], (n >> 1) & 1)) return false;
       tc_fence_after();
-      const uint32_t stg = sb + stage_of(n) * B_STAGE_BYTES;
+      const uint32_t stg = sb + stage_of(n) * G::STAGE;
       const uint32_t id = idesc_bf16(128, with_o ? 192 : 128, 0, 1);
       for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(tb + set_col(n), desc_kmajor(sb + B_SA, 128, kk),
+        mma_bf16(tb + set_col(n), desc_kmajor(sb + G::SA, 128, kk),
                  sdesc_sw128(stg + CARD_PHIQ + kk * 2048, 128 * 128, 1024), id, 1u);
       mma_commit(&bar_mma);
       if (with_o) mma_commit(&bar_ofull[n & 1]);
@@ -330,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_tc(
     constexpr int LDT = DD + 4;  // tile row pitch (floats)
     const int og = (warp - 8) >> 2;             // output warpgroup: token half
     const int bar_id = 2 + og;                  // its named barrier (128 threads)
-    float *tile = reinterpret_cast<float *>(sm + B_OT) + og * 32 * LDT;
+    float *tile = reinterpret_cast<float *>(sm + G::OT) + og * 32 * LDT;
     const int ot = tid - 256 - 128 * og;        // thread of the warpgroup, 0..127
     const int c8 = ot & 15, r0 = ot >> 4;       // store phase: channels 8*c8.., tokens r0 + 8m
     const bool logits = gate && (flags & KDA_GATE_LOGITS);
@@ -434,14 +444,19 @@ cudaError_t launch_state_tc(int mode, unsigned flags, const void *gate, void *ou
                             float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                             int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
                             cudaStream_t st, CkptOut ck, int part) {
-  cudaError_t e =
-      cudaFuncSetAttribute(kda_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, B_DYN);
-  if (e != cudaSuccess) return e;
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
-  kda_state_tc<<<dim3(n_seq * H, mode == 0 ? 1 : 2), kThreads, B_DYN, st>>>(
-      mode, flags, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final, X_out, Z_out, cu,
-      n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.cards, ck, part, ws.split16,
-      ws.mid, ws.seq_order);
+  auto launch = [&](auto kernel, int dyn) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    if (e != cudaSuccess) return e;
+    kernel<<<dim3(n_seq * H, mode == 0 ? 1 : 2), kThreads, dyn, st>>>(
+        mode, flags, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final, X_out, Z_out,
+        cu, n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off, ws.cards, ck, part, ws.split16,
+        ws.mid, ws.seq_order);
+    return cudaSuccess;
+  };
+  cudaError_t e = mode == 0 ? launch(kda_state_tc<false>, Geo<false>::DYN)
+                            : launch(kda_state_tc<true>, Geo<true>::DYN);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
