@@ -666,8 +666,10 @@ ChunkWs chunk_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int 
 
 cudaError_t launch_chunk_table(const int32_t *cu, int n_seq, int64_t T_total, const ChunkWs &ws,
                                cudaStream_t st) {
-  kda_chunk_table<<<1, 1024, 0, st>>>(cu, n_seq, T_total, ws.meta, ws.seq_chunk_off,
-                                      ws.split16, ws.seq_chunk_lo, ws.seq_order);
+  // one thread per sequence up to 1024 (a warp at least): few sequences, few barrier members
+  const int threads = n_seq >= 1024 ? 1024 : ((n_seq + 31) / 32) * 32 + (n_seq == 0 ? 32 : 0);
+  kda_chunk_table<<<1, threads, 0, st>>>(cu, n_seq, T_total, ws.meta, ws.seq_chunk_off,
+                                         ws.split16, ws.seq_chunk_lo, ws.seq_order);
   return cudaGetLastError();
 }
 
