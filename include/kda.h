@@ -109,7 +109,10 @@ const char *kda_version(void);
  * leading parts then runs on `stream` beside the card launch of the trailing
  * parts on a library-owned stream; events fork that stream off `stream` and
  * join it back before the call returns, so all work stays ordered on
- * `stream`. Results are bitwise those of the unsplit schedule.
+ * `stream` (and the call can be captured in a CUDA graph). The library
+ * stream is one per device for the process's lifetime; concurrent calls
+ * from several host threads share it, so their trailing card launches run
+ * one after another. Results are bitwise those of the unsplit schedule.
  */
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                          const void *log_alpha, const void *beta,
