@@ -49,9 +49,9 @@ __device__ __forceinline__ void set_err(unsigned bits) { atomicOr(&g_state_tc_er
 
 // ===========================================================================
 // Stage B: the sequential state pass, one CTA per (sequence, head), 512 threads.
-// Warps 0-7 (state group, 168 registers a thread) carry the serial path: warp w serves
+// Warps 0-7 (state group, kStateRegs registers a thread) carry the serial path: warp w serves
 // tensor-memory lanes 32*(w%4).. (lane j = value channel j, i.e. row j of S^T) and the key
-// columns [64*(w/4), 64*(w/4) + 64) of that row. Warps 8-15 (two output warpgroups, 88
+// columns [64*(w/4), 64*(w/4) + 64) of that row. Warps 8-15 (two output warpgroups, kOutRegs
 // registers a thread, one per 32-token half of the chunk) read the chunk outputs from the same
 // lanes, apply scale and gate and store o, off the serial path. mode 0: prefill; mode 1:
 // segment summary on [X | Z] (blockIdx.y = 0: X with entry I; 1: Z with entry 0), no output.
@@ -61,7 +61,7 @@ __device__ __forceinline__ void set_err(unsigned bits) { atomicOr(&g_state_tc_er
 // Before the MMAs of chunk n the set is pre-loaded with Diag(e^{G_C}) S + B_c
 // (state group) and O_intra^T (output group), so one N = 192 MMA chain per chunk
 // produces both the next state and the chunk output.
-// mbarriers: bar_full[3] card stages landed; bar_mma chunk MMAs done (state
+// mbarriers: bar_full[G::NST] card stages landed; bar_mma chunk MMAs done (state
 // group); bar_ofull[2] output block written (output group); bar_ofree[2]
 // output block read and re-seeded (MMA issuer).
 template <bool SUMMARY>
