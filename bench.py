@@ -315,9 +315,10 @@ def run_gpu(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.monotonic()
-    # 3 launches (chunk table, cards, state pass), or 5 for a split prefill (table, leading
-    # cards, leading state pass, trailing cards beside it, trailing state pass)
-    n_launch = kda.kda_chunk_fwd_launches(T, n_seq, H, d, d)
+    # [chunk table,] cards, state pass; or for a split prefill [table,] leading cards, leading
+    # state pass, trailing cards beside it, trailing state pass. The tensor-core path skips the
+    # table for fixed-length batches (this workload passes no cu_seqlens).
+    n_launch = kda.kda_chunk_fwd_launches(T, n_seq, H, d, d, varlen=False)
     total_ms, per_launch = time_kernels(step, args.steps, stream, n_launch)
     t_wall1 = time.monotonic()
     barrier(world)
@@ -331,12 +332,17 @@ def run_gpu(args, rank, world, local):
     tc = (w.dtype == torch.bfloat16 and d == 128)
     names = (["kda_chunk_table", "kda_card_tc", "kda_state_tc"] if tc else
              ["kda_chunk_table", "kda_prep_simt", "kda_state_simt"])
-    launches_of = [[0], [1, 3], [2, 4]] if n_launch == 5 else [[0], [1], [2]]
+    has_table = n_launch in (3, 5)
+    k0 = 1 if has_table else 0
+    split = (n_launch - k0) == 4
+    launches_of = [[0] if has_table else [],
+                   [k0, k0 + 2] if split else [k0],
+                   [k0 + 1, k0 + 3] if split else [k0 + 1]]
     kernel_ms = [sum(per_launch[i] for i in ix) for ix in launches_of]  # per step
     dom = int(np.argmax(kernel_ms))
     chunk_heads = (T // 64) * H
     alg_bytes = {  # algorithmic HBM bytes per step of each kernel
-        0: (n_seq + 1) * 4,
+        0: (n_seq + 1) * 4 if has_table else 0,
         1: TOKEN_HEADS * (4 * d * 2 + 2),                                 # q, k, v, log_alpha, beta
         2: TOKEN_HEADS * (2 * d * 2) + 2 * n_seq * H * STATE_BYTES,       # gate, o, states
     }
@@ -355,7 +361,7 @@ def run_gpu(args, rank, world, local):
     roofline["step"] = {"alg_bytes": step_bytes,
                         "achieved": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
                         "frac": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
-    if n_launch == 5:
+    if split:
         roofline["schedule"] = ("split prefill: the cards of each sequence's trailing chunks are "
                                 "built beside the state pass over its leading chunks")
     if tc:
@@ -579,7 +585,7 @@ def bench_varlen(dev, pk, stream, reps=10):
     return {"workload": f"varlen {n_seq} packed sequences ({T} tokens, longest "
                         f"{max(w.lengths)}) H=32 dk=dv=128 bf16",
             "value": round(T / (ms * 1e-3) / 1e6, 3), "unit": "Mtok/s", "ms": round(ms, 3),
-            "gpu_launches": kda.kda_chunk_fwd_launches(T, n_seq, H, d, d) * reps}
+            "gpu_launches": kda.kda_chunk_fwd_launches(T, n_seq, H, d, d, varlen=True) * reps}
 
 
 def bench_checkpoints(dev, pk, stream, reps=20, every=1024):
@@ -624,7 +630,7 @@ def bench_checkpoints(dev, pk, stream, reps=20, every=1024):
             "value": round(T / (ms["ckpt"] * 1e-3) / 1e6, 3), "unit": "Mtok/s",
             "ms": round(ms["ckpt"], 4), "ms_without": round(ms["plain"], 4),
             "checkpoint_bytes": ck.numel() * 4,
-            "gpu_launches": kda.kda_chunk_fwd_launches(T, n_seq, H, 128, 128) * reps}
+            "gpu_launches": kda.kda_chunk_fwd_launches(T, n_seq, H, 128, 128, varlen=False) * reps}
 
 
 def bench_backward(dev, pk, stream, reps=5):
@@ -714,7 +720,7 @@ def bench_gates(dev, pk, stream, reps=20):
                         "forget-gate pre-activation",
             "value": round(T / (ms["fused"] * 1e-3) / 1e6, 3), "unit": "Mtok/s",
             "ms": round(ms["fused"], 4), "ms_prepass_then_plain": round(ms["unfused"], 4),
-            "gpu_launches": kda.kda_chunk_fwd_launches(T, n_seq, H, 128, 128) * reps}
+            "gpu_launches": kda.kda_chunk_fwd_launches(T, n_seq, H, 128, 128, varlen=False) * reps}
 
 
 def bench_scan(dev, pk, stream, reps=20):

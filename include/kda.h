@@ -128,13 +128,16 @@ size_t kda_chunk_fwd_workspace_size(int64_t T_total, int n_seq, int H, int dk,
 
 /*
  * Kernel launches kda_chunk_fwd (and kda_chunk_fwd_checkpoints) make for this
- * problem: 3 (chunk table, chunk prep, state pass), 5 for a split prefill
- * (chunk table, prep of the leading parts, state pass of the leading parts,
- * prep of the trailing parts, state pass of the trailing parts), 0 for an
- * empty or invalid problem. Host only.
+ * problem; varlen != 0 when the call passes cu_seqlens. In order: the chunk
+ * table (skipped on the tensor-core path, bf16 with dk = dv = 128, when
+ * cu_seqlens is NULL: its kernels then index the fixed-length sequences
+ * directly), then either chunk prep and state pass, or for a split prefill
+ * the prep of the leading parts, the state pass of the leading parts, the
+ * prep of the trailing parts and the state pass of the trailing parts.
+ * So 2 to 5; 0 for an empty or invalid problem. Host only.
  */
 int kda_chunk_fwd_launches(int64_t T_total, int n_seq, int H, int dk, int dv,
-                           int chunk, kda_dtype dtype);
+                           int chunk, kda_dtype dtype, int varlen);
 
 /*
  * kda_chunk_fwd that also saves the state at fixed token boundaries, for a
@@ -343,11 +346,11 @@ kda_status kda_get_error(kda_stream_t stream);
  * Tracing. After kda_trace_events(begin, end, n) with n > 0, every entry point
  * called from this host thread records begin[i] and end[i] (cudaEvent_t
  * handles, created and owned by the caller) on its stream around its i-th
- * kernel launch, i < n; launches past n are not traced. kda_chunk_fwd and
- * kda_segment_summary launch, in order: 0 chunk table, 1 chunk prep,
- * 2 state pass (a split kda_chunk_fwd: the five launches that
- * kda_chunk_fwd_launches lists, the trailing cards' events on the library's
- * card stream). n = 0 turns tracing off. Records nothing else and allocates
+ * kernel launch, i < n; launches past n are not traced. kda_segment_summary
+ * launches, in order: 0 chunk table, 1 chunk prep, 2 state pass;
+ * kda_chunk_fwd the launches that kda_chunk_fwd_launches lists, in its
+ * order (the trailing cards' events of a split call on the library's card
+ * stream). n = 0 turns tracing off. Records nothing else and allocates
  * nothing; the caller reads the elapsed times with cudaEventElapsedTime.
  */
 kda_status kda_trace_events(void *const *begin, void *const *end, int n);

@@ -73,7 +73,7 @@ def load(path: str = LIB_PATH):
             "kda_last_error_string": ([], ctypes.c_char_p),
             "kda_chunk_fwd": ([P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, P, SZ, P], I),
             "kda_chunk_fwd_workspace_size": ([I64, I, I, I, I, I, I], SZ),
-            "kda_chunk_fwd_launches": ([I64, I, I, I, I, I, I], I),
+            "kda_chunk_fwd_launches": ([I64, I, I, I, I, I, I, I], I),
             "kda_chunk_bwd": ([P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I,
                                I, F, U, I, P, SZ, P], I),
             "kda_chunk_bwd_workspace_size": ([I64, I, I, I, I, I, I], SZ),
@@ -152,9 +152,12 @@ def kda_chunk_fwd_workspace_size(T_total, n_seq, H, dk, dv, chunk=CHUNK, dtype=K
     return int(load().kda_chunk_fwd_workspace_size(T_total, n_seq, H, dk, dv, chunk, dtype))
 
 
-def kda_chunk_fwd_launches(T_total, n_seq, H, dk, dv, chunk=CHUNK, dtype=KDA_DTYPE_BF16):
-    """Kernel launches of kda_chunk_fwd for this problem: 3, 5 (split prefill) or 0."""
-    return int(load().kda_chunk_fwd_launches(T_total, n_seq, H, dk, dv, chunk, dtype))
+def kda_chunk_fwd_launches(T_total, n_seq, H, dk, dv, chunk=CHUNK, dtype=KDA_DTYPE_BF16,
+                           varlen=False):
+    """Kernel launches of kda_chunk_fwd for this problem (varlen: cu_seqlens given): 2 to 5,
+    or 0 for an empty or invalid problem."""
+    return int(load().kda_chunk_fwd_launches(T_total, n_seq, H, dk, dv, chunk, dtype,
+                                             int(bool(varlen))))
 
 
 def kda_segment_summary_workspace_size(T_total, n_seg, H, dk, dv, chunk=CHUNK, dtype=KDA_DTYPE_BF16):

@@ -146,11 +146,13 @@ size_t kda_chunk_fwd_workspace_size(int64_t T_total, int n_seq, int H, int dk, i
 }
 
 int kda_chunk_fwd_launches(int64_t T_total, int n_seq, int H, int dk, int dv, int chunk,
-                           kda_dtype dtype) {
+                           kda_dtype dtype, int varlen) {
   if (common_checks(T_total, n_seq, H, dk, dv, chunk, dtype, (const int32_t *)1) != KDA_OK)
     return 0;
   if (n_seq == 0) return 0;
-  return (kda::tc_path(dk, dv, dtype) && kda::tc_split16(T_total, n_seq, H) > 0) ? 5 : 3;
+  const bool tc = kda::tc_path(dk, dv, dtype);
+  const int table = (!tc || varlen) ? 1 : 0;
+  return table + ((tc && kda::tc_split16(T_total, n_seq, H) > 0) ? 4 : 2);
 }
 
 size_t kda_segment_summary_workspace_size(int64_t T_total, int n_seg, int H, int dk, int dv,
@@ -253,9 +255,13 @@ static kda_status chunk_fwd_impl(const void *q, const void *k, const void *v,
   Tracer tr(s);
   kda::ChunkWs ws = tc ? kda::tc_ws_carve(workspace, T_total, n_seq, H)
                        : kda::chunk_ws_carve(workspace, T_total, n_seq, H, dk, dv);
-  st = cuda_status(tr([&] { return kda::launch_chunk_table(cu_seqlens, n_seq, T_total, ws, s); }),
-                   "chunk table");
-  if (st != KDA_OK) return st;
+  // the tensor-core kernels index fixed-length batches (no cu_seqlens) without the chunk table
+  if (!tc || cu_seqlens != nullptr) {
+    st = cuda_status(
+        tr([&] { return kda::launch_chunk_table(cu_seqlens, n_seq, T_total, ws, s); }),
+        "chunk table");
+    if (st != KDA_OK) return st;
+  }
   if (tc && ws.split16 > 0)
     return split_prefill(q, k, v, log_alpha, beta, gate, out, initial_state, final_state, ck,
                          cu_seqlens, n_seq, T_total, H, scale, flags, ws, s, tr);

@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
     const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_v,
     const __nv_bfloat16 *__restrict__ beta, const int32_t *__restrict__ cu, int n_seq,
     int64_t fixed_len, int H, unsigned flags, const ChunkMeta *__restrict__ meta,
-    const int *__restrict__ off, const int *__restrict__ off_lo, int chunk_part,
+    const int *__restrict__ off, const int *__restrict__ off_lo, int chunk_part, int split16,
     uint8_t *__restrict__ cards) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_tma, bar_mma;
@@ -77,33 +77,45 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
 
   const int h = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31, quad = warp & 3, grp = warp >> 2;
-  if (meta->invalid) return;
-  // global chunk of this CTA: all chunks (chunk_part < 0), or the x-th chunk of the leading
-  // (chunk_part 0) or trailing (chunk_part 1) parts of the sequences, in sequence order
-  int ci = blockIdx.x;
-  if (chunk_part == 0) {
-    if (ci >= meta->lo_chunks) return;
-    const int s0 = find_seq(off_lo, n_seq, ci);
-    ci = off[s0] + (ci - off_lo[s0]);
-  } else if (chunk_part == 1) {
-    if (ci >= meta->total_chunks - meta->lo_chunks) return;
-    int lo = 0, hi = n_seq - 1;  // largest s whose trailing part starts at or before ci
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (off[mid] - off_lo[mid] <= ci) lo = mid; else hi = mid - 1;
+  // global chunk ci of this CTA, its sequence s and its chunk jc within s: all chunks
+  // (chunk_part < 0), or the x-th chunk of the leading (chunk_part 0) or trailing (chunk_part 1)
+  // parts of the sequences, in sequence order. Without cu_seqlens every sequence has n chunks
+  // and the chunk table is not used.
+  int ci = blockIdx.x, s, jc;
+  if (cu == nullptr) {
+    const int n = (int)((fixed_len + C - 1) / C), m = n * split16 / 16;
+    const int per = chunk_part == 0 ? m : (chunk_part == 1 ? n - m : n);
+    if (per == 0 || ci >= n_seq * per) return;
+    s = ci / per;
+    jc = ci - s * per + (chunk_part == 1 ? m : 0);
+    ci = s * n + jc;
+  } else {
+    if (meta->invalid) return;
+    if (chunk_part == 0) {
+      if (ci >= meta->lo_chunks) return;
+      const int s0 = find_seq(off_lo, n_seq, ci);
+      ci = off[s0] + (ci - off_lo[s0]);
+    } else if (chunk_part == 1) {
+      if (ci >= meta->total_chunks - meta->lo_chunks) return;
+      int lo = 0, hi = n_seq - 1;  // largest s whose trailing part starts at or before ci
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] - off_lo[mid] <= ci) lo = mid; else hi = mid - 1;
+      }
+      ci = off[lo] + (off_lo[lo + 1] - off_lo[lo]) + (ci - (off[lo] - off_lo[lo]));
+    } else if (ci >= meta->total_chunks) {
+      return;
     }
-    ci = off[lo] + (off_lo[lo + 1] - off_lo[lo]) + (ci - (off[lo] - off_lo[lo]));
-  } else if (ci >= meta->total_chunks) {
-    return;
+    s = find_seq(off, n_seq, ci);
+    jc = ci - off[s];
   }
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(sm);
 
-  const int s = find_seq(off, n_seq, ci);
   int64_t ts, ls;
   seq_range(cu, fixed_len, s, &ts, &ls);
-  const int64_t t0 = ts + (int64_t)(ci - off[s]) * C;
-  const int len = (int)min((int64_t)C, ls - (int64_t)(ci - off[s]) * C);
+  const int64_t t0 = ts + (int64_t)jc * C;
+  const int len = (int)min((int64_t)C, ls - (int64_t)jc * C);
   const bool l2 = (flags & KDA_QK_L2NORM) != 0;
   const bool dbg = (flags & KDA_DEBUG_CHECK) != 0;
 
@@ -619,7 +631,7 @@ cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const vo
                                   (int64_t)ws.max_chunks * (16 - ws.split16) / 16 + n_seq + 1);
   kda_card_tc<<<dim3(grid, H), 256, A_DYN, st>>>(
       mk, mq, mla, mv, (const __nv_bfloat16 *)beta, cu, n_seq, fixed_len, H, flags, ws.meta,
-      ws.seq_chunk_off, ws.seq_chunk_lo, part, ws.cards);
+      ws.seq_chunk_off, ws.seq_chunk_lo, part, ws.split16, ws.cards);
   return cudaGetLastError();
 }
 

@@ -79,11 +79,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_tc(
   __shared__ uint64_t bar_full[B_NSTAGE], bar_mma, bar_ofull[2], bar_ofree[2];
   __shared__ uint32_t tmem_base;
   __shared__ int s_fail;
-  if (meta->invalid) return;
+  // without cu_seqlens the chunk table is not used: chains in index order, n chunks a sequence
+  if (cu != nullptr && meta->invalid) return;
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(sm);
   // CTAs take the sequences longest first (the order the chunk table computed)
-  const int chain = blockIdx.x, s = seq_order[chain / H], h = chain % H, tid = threadIdx.x;
+  const int chain = blockIdx.x, h = chain % H, tid = threadIdx.x;
+  const int s = cu ? seq_order[chain / H] : chain / H;
   const int warp = tid >> 5, lane = tid & 31;
   const bool state_grp = warp < 8;
   const int quad = warp & 3;           // lane quadrant of this warp
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_tc(
   seq_range(cu, fixed_len, s, &ts, &ls);
   const int64_t ls_seq = ls;
   int nchunks = (int)((ls + C - 1) / C);
+  const int seq_off = cu ? off[s] : s * nchunks;  // first global chunk of the sequence
   // a split prefill walks the first nchunks * split16 / 16 chunks (part 0), handing its
   // state over in `mid`, then the rest (part 1); chunk n below is chunk n_lo + n of the sequence
   int n_lo = 0;
@@ -112,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_tc(
       ls -= (int64_t)m * C;
     }
   }
-  const int cbase = nchunks > 0 ? off[s] + n_lo : 0;
+  const int cbase = nchunks > 0 ? seq_off + n_lo : 0;
   auto card_of = [&](int n) { return cards + ((size_t)(cbase + n) * H + h) * CARD_BYTES; };
   const float *S_entry = part == 1 ? mid : S0;
   float *S_exit = part == 0 ? mid : S_final;

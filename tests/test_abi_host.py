@@ -164,16 +164,21 @@ def test_workspace_size(lib):
 
 
 def test_chunk_fwd_launches(lib):
-    """Prefills with few (sequence, head) pairs and long sequences are split (5 launches);
-    the rest, and every other shape or dtype, take 3."""
+    """Prefills with few (sequence, head) pairs and long sequences are split (two card and two
+    state launches instead of one each); the tensor-core path (bf16, d = 128) skips the chunk
+    table without cu_seqlens; every other shape or dtype takes table, prep and state pass."""
     bf, f32 = B.KDA_DTYPE_BF16, B.KDA_DTYPE_F32
-    assert B.kda_chunk_fwd_launches(4 * 4096, 4, 16, 128, 128, dtype=bf) == 5
-    assert B.kda_chunk_fwd_launches(16 * 1024, 7, 16, 128, 128, dtype=bf) == 5     # 112 pairs
-    assert B.kda_chunk_fwd_launches(16 * 1024, 8, 16, 128, 128, dtype=bf) == 3     # 128 pairs
-    assert B.kda_chunk_fwd_launches(4 * 512, 4, 16, 128, 128, dtype=bf) == 3       # 8 chunks/seq
-    assert B.kda_chunk_fwd_launches(4 * 1024, 4, 16, 128, 128, dtype=bf) == 5      # 16 chunks/seq
-    assert B.kda_chunk_fwd_launches(4 * 4096, 4, 16, 128, 128, dtype=f32) == 3
-    assert B.kda_chunk_fwd_launches(4 * 4096, 4, 16, 64, 64, dtype=bf) == 3
+    L = B.kda_chunk_fwd_launches
+    assert L(4 * 4096, 4, 16, 128, 128, dtype=bf) == 4
+    assert L(4 * 4096, 4, 16, 128, 128, dtype=bf, varlen=True) == 5
+    assert L(16 * 1024, 7, 16, 128, 128, dtype=bf, varlen=True) == 5     # 112 pairs
+    assert L(16 * 1024, 8, 16, 128, 128, dtype=bf, varlen=True) == 3     # 128 pairs
+    assert L(16 * 1024, 8, 16, 128, 128, dtype=bf) == 2
+    assert L(4 * 512, 4, 16, 128, 128, dtype=bf, varlen=True) == 3       # 8 chunks/seq
+    assert L(4 * 1024, 4, 16, 128, 128, dtype=bf) == 4                   # 16 chunks/seq
+    assert L(4 * 4096, 4, 16, 128, 128, dtype=f32) == 3
+    assert L(4 * 4096, 4, 16, 128, 128, dtype=f32, varlen=True) == 3
+    assert L(4 * 4096, 4, 16, 64, 64, dtype=bf) == 3
     assert B.kda_chunk_fwd_launches(0, 0, 16, 128, 128, dtype=bf) == 0
     assert B.kda_chunk_fwd_launches(4096, 1, 16, 96, 128, dtype=bf) == 0
     # a split prefill's workspace holds the hand-over state between the parts

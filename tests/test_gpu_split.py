@@ -60,8 +60,8 @@ def _padded(S0, cu, extra):
 
 def test_schedules_are_as_intended():
     T, n = sum(LENGTHS), len(LENGTHS)
-    assert B.kda_chunk_fwd_launches(T, n, H, D, D) == 5
-    assert B.kda_chunk_fwd_launches(T, n + 2, H, D, D) == 3
+    assert B.kda_chunk_fwd_launches(T, n, H, D, D, varlen=True) == 5
+    assert B.kda_chunk_fwd_launches(T, n + 2, H, D, D, varlen=True) == 3
 
 
 def test_split_vs_oracle():
@@ -109,7 +109,7 @@ def test_split_prefill_workload_bitwise_and_sampled():
     x = inputs.make(w, device=DEV)
     n_seq, L, Hw = len(w.lengths), w.lengths[0], w.H
     T = n_seq * L
-    assert B.kda_chunk_fwd_launches(T, n_seq, Hw, D, D) == 5
+    assert B.kda_chunk_fwd_launches(T, n_seq, Hw, D, D) == 4  # fixed lengths: no chunk table
     out = torch.empty((T, Hw, D), dtype=torch.bfloat16, device=DEV)
     fs = torch.empty((n_seq, Hw, D, D), dtype=torch.float32, device=DEV)
     B.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], out, x["S0"],
@@ -118,7 +118,7 @@ def test_split_prefill_workload_bitwise_and_sampled():
     assert B.kda_get_error() == B.KDA_OK
     # unsplit: the same four sequences plus four empty ones (8 x 16 pairs > 112)
     cu = [s * L for s in range(n_seq + 1)] + [T] * 4
-    assert B.kda_chunk_fwd_launches(T, n_seq + 4, Hw, D, D) == 3
+    assert B.kda_chunk_fwd_launches(T, n_seq + 4, Hw, D, D, varlen=True) == 3
     out_u = torch.empty_like(out)
     fs_u = torch.empty((n_seq + 4, Hw, D, D), dtype=torch.float32, device=DEV)
     S0p = torch.cat([x["S0"], torch.zeros((4, Hw, D, D), dtype=torch.float32, device=DEV)])
