@@ -136,3 +136,34 @@ def test_split_prefill_workload_bitwise_and_sampled():
                                 np32(x["S0"][s:s + 1, h:h + 1]).astype(np.float64), [0, L])
         assert rel_err(np32(out[rows, h:h + 1]), ro) <= TOL[torch.bfloat16]
         assert rel_err(np32(fs[s:s + 1, h:h + 1]), rs) <= TOL[torch.bfloat16]
+
+
+def test_fixed_length_split_checkpoints_equal_prefix_calls():
+    """The bench workload (no cu_seqlens: closed-form indexing, split after chunk 48) with a
+    checkpoint every 1024 tokens. Each slot equals, bit for bit, the final state of a call over
+    just that prefix of every sequence (the slots after chunk 63 of the trailing part and after
+    chunks 15, 31, 47 of the leading one)."""
+    w = inputs.WORKLOADS["prefill"]
+    x = inputs.make(w, device=DEV)
+    n_seq, L, Hw = len(w.lengths), w.lengths[0], w.H
+    T, every, per = n_seq * L, 1024, L // 1024
+    out = torch.empty((T, Hw, D), dtype=torch.bfloat16, device=DEV)
+    fs = torch.empty((n_seq, Hw, D, D), dtype=torch.float32, device=DEV)
+    ck = torch.full((n_seq, per, Hw, D, D), -7.0, dtype=torch.float32, device=DEV)
+    B.kda_chunk_fwd_checkpoints(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"],
+                                out, x["S0"], fs, ck, every, None, n_seq)
+    torch.cuda.synchronize()
+    assert B.kda_get_error() == B.KDA_OK
+    assert torch.equal(ck[:, per - 1], fs)
+    for i in range(per - 1):
+        P = every * (i + 1)
+        xp = {n: x[n].view(n_seq, L, *x[n].shape[1:])[:, :P].reshape(n_seq * P, *x[n].shape[1:])
+              for n in ("q", "k", "v", "log_alpha", "beta", "gate")}
+        fp = torch.empty_like(fs)
+        op = torch.empty((n_seq * P, Hw, D), dtype=torch.bfloat16, device=DEV)
+        B.kda_chunk_fwd(xp["q"], xp["k"], xp["v"], xp["log_alpha"], xp["beta"], xp["gate"], op,
+                        x["S0"], fp, None, n_seq)
+        torch.cuda.synchronize()
+        assert B.kda_get_error() == B.KDA_OK
+        assert torch.equal(ck[:, i], fp), i
+        assert torch.equal(op.view(n_seq, P, Hw, D), out.view(n_seq, L, Hw, D)[:, :P]), i
