@@ -453,13 +453,22 @@ __global__ void __launch_bounds__(256) kda_bwd_solve(const float *__restrict__ A
     }
   }
   __syncthreads();
+  // (I + A)^T X = Y, back substitution: one thread per column, the column in registers
+  // (indices fixed at compile time), each row's dot product in four partial sums
   if (tid < NC) {
     float *col = sY + tid;
+    float x[C];
+#pragma unroll
+    for (int r = 0; r < C; ++r) x[r] = col[r * LY];
+#pragma unroll
     for (int r = C - 2; r >= 0; --r) {
-      float acc = col[r * LY];
-      for (int s = r + 1; s < C; ++s) acc = fmaf(-sA[s * LA + r], col[s * LY], acc);
-      col[r * LY] = acc;
+      float p[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = r + 1; s < C; ++s) p[s & 3] = fmaf(sA[s * LA + r], x[s], p[s & 3]);
+      x[r] -= (p[0] + p[1]) + (p[2] + p[3]);
     }
+#pragma unroll
+    for (int r = 0; r < C - 1; ++r) col[r * LY] = x[r];
   }
   __syncthreads();
 #pragma unroll 4
@@ -511,11 +520,34 @@ __global__ void __launch_bounds__(256) kda_bwd_finish(
 
   const bool logits = (flags & KDA_GATE_LOGITS) != 0;
   if (tid < C) sB[tid] = tid < len ? prep_beta(bf(beta[(size_t)(t0 + tid) * H + h]), flags) : 0.f;
+  // log_alpha of the chunk into sG by 8-element vector loads of all threads (0 on padded rows),
+  // so that the serial running sum below reads shared memory only
+  {
+    constexpr int NV = C * DK / 8 / 256;
+    float lv[NV][8];
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+      const int e = 8 * (tid + 256 * m), r = e / DK, c = e % DK;
+      if (r < len) {
+        load8(la + ((size_t)(t0 + r) * H + h) * DK + c, lv[m]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) lv[m][u] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+      const int e = 8 * (tid + 256 * m), r = e / DK, c = e % DK;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sG[r * LK + c + u] = r < len ? prep_log_alpha(lv[m][u], flags) : 0.f;
+    }
+  }
+  __syncthreads();
   if (tid < DK) {
     const int c = tid;
     float G = 0.f;
     for (int r = 0; r < C; ++r) {
-      if (r < len) G += prep_log_alpha(bf(la[((size_t)(t0 + r) * H + h) * DK + c]), flags);
+      G += sG[r * LK + c];
       sG[r * LK + c] = G;
     }
     sDc[c] = expf(G);

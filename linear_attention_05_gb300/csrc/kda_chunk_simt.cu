@@ -323,15 +323,24 @@ __global__ void __launch_bounds__(256) kda_prep_simt(
   }
   __syncthreads();
 
-  // (I + A) X = [b Kt | b V], forward substitution: one thread per column
+  // (I + A) X = [b Kt | b V], forward substitution: one thread per column, the column in
+  // registers (indices fixed at compile time), each row's dot product in four partial sums
   if (tid < DK + DV) {
     float *col = tid < DK ? sKt + tid : sV + (tid - DK);
     const int ld = tid < DK ? LK : LV;
+    float x[C];
+#pragma unroll
+    for (int r = 0; r < C; ++r) x[r] = col[r * ld];
+#pragma unroll
     for (int r = 1; r < C; ++r) {
-      float acc = col[r * ld];
-      for (int i = 0; i < r; ++i) acc = fmaf(-sA[r * LA + i], col[i * ld], acc);
-      col[r * ld] = acc;
+      const float *Ar = sA + r * LA;
+      float p[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < r; ++i) p[i & 3] = fmaf(Ar[i], x[i], p[i & 3]);
+      x[r] -= (p[0] + p[1]) + (p[2] + p[3]);
     }
+#pragma unroll
+    for (int r = 1; r < C; ++r) col[r * ld] = x[r];
   }
   __syncthreads();
   float *Wout = Wg + slab * C * DK, *Uout = Ug + slab * C * DV;
