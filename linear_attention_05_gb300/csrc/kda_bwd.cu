@@ -152,6 +152,13 @@ __global__ void __launch_bounds__(256) kda_bwd_state(
   __syncthreads();
   for (int jc = nchunks - 1; jc >= 0; --jc) {
     const size_t slab = (size_t)(off[s] + jc) * H + h;
+    if (tid == 0 && blockIdx.y == 0 && jc > 0) {  // the next chunk's operands into L2
+      const size_t sp = slab - H;                  // chunk jc - 1 of this sequence and head
+      prefetch_l2_bulk(Wg + sp * C * DK, C * DK * 4);
+      prefetch_l2_bulk(Kdg + sp * C * DK, C * DK * 4);
+      prefetch_l2_bulk(V1g + sp * C * DV, C * DV * 4);
+      prefetch_l2_bulk(Rg + sp * DK * DV, DK * DV * 4);
+    }
     for (int e = tid; e < DK * RBV; e += 256) {
       const int c = e / RBV, jj = e % RBV;
       dSb[(slab * DK + c) * DV + j0 + jj] = sS[c * LS + jj];

@@ -409,6 +409,16 @@ __global__ void __launch_bounds__(256) kda_state_simt(
 
   for (int jc = 0; jc < nchunks; ++jc) {
     const size_t slab = (size_t)(off[s] + jc) * H + h;
+    if (tid == 0 && blockIdx.y == 0 && jc + 1 < nchunks) {  // the next chunk's operands into L2
+      const size_t sn = slab + H;                             // chunk jc + 1, same head
+      prefetch_l2_bulk(Wg + sn * C * DK, C * DK * 4);
+      prefetch_l2_bulk(Kdg + sn * C * DK, C * DK * 4);
+      prefetch_l2_bulk(Ug + sn * C * DV, C * DV * 4);
+      if (need_o) {
+        prefetch_l2_bulk(Qg + sn * C * DK, C * DK * 4);
+        prefetch_l2_bulk(Pg + sn * C * C, C * C * 4);
+      }
+    }
     const int64_t t0 = ts + (int64_t)jc * C;
     const int len = (int)min((int64_t)C, ls - (int64_t)jc * C);
     const float *W = Wg + slab * C * DK, *Kd = Kdg + slab * C * DK;

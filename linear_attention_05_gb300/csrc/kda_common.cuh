@@ -39,6 +39,11 @@ __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float *o) {
   }
 }
 
+// `bytes` (a multiple of 16, from a 16-byte-aligned address) into L2, asynchronously
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 template <typename T>
 __device__ __forceinline__ T from_f32(float x);
 template <>
