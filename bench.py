@@ -376,7 +376,8 @@ def run_gpu(args, rank, world, local):
 
     # end to end through the public API: pinned host inputs -> device -> host. HostPipeline
     # copies each sequence in, computes it and copies it out on three streams, so the transfers
-    # of one sequence overlap the work on its neighbours.
+    # of one sequence overlap the work on its neighbours. (Time slices of each sequence,
+    # parts > 1, cost more host enqueue time than they save here.)
     from linear_attention_05_gb300.pipeline import HostPipeline
     host = {k: v.to("cpu").pin_memory() for k, v in x.items() if k != "cu_seqlens" and v is not None}
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()

@@ -1,5 +1,6 @@
-"""HostPipeline (copy in / compute / copy out per sequence group on three streams) gives
-bitwise the results of one kda_chunk_fwd call on the device-resident batch (needs a GPU)."""
+"""HostPipeline (copy in / compute / copy out per sequence group on three streams, optionally
+per time slice of each sequence) gives bitwise the results of one kda_chunk_fwd call on the
+device-resident batch (needs a GPU)."""
 import pytest
 import torch
 
@@ -10,8 +11,8 @@ from linear_attention_05_gb300.pipeline import HostPipeline
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("groups", [4, 2])
-def test_pipeline_equals_device_call(groups):
+@pytest.mark.parametrize("groups,parts", [(4, 1), (2, 1), (4, 4), (4, 2)])
+def test_pipeline_equals_device_call(groups, parts):
     w = inputs.WORKLOADS["prefill"]
     x = inputs.make(w, device="cuda")
     n_seq, L, H, d = len(w.lengths), w.lengths[0], w.H, w.dk
@@ -20,7 +21,8 @@ def test_pipeline_equals_device_call(groups):
     host = {k: v.cpu().pin_memory() for k, v in x.items() if k != "cu_seqlens" and v is not None}
     out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
     fs_h = torch.empty(fs_d.shape, dtype=fs_d.dtype).pin_memory()
-    pl = HostPipeline(n_seq, L, H, d, d, dtype=torch.bfloat16, device="cuda", groups=groups)
+    pl = HostPipeline(n_seq, L, H, d, d, dtype=torch.bfloat16, device="cuda", groups=groups,
+                      parts=parts)
     pl.run(host, out_h, fs_h)
     torch.cuda.synchronize()
     assert B.kda_get_error() == B.KDA_OK
