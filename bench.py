@@ -75,37 +75,101 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+    """SM clock and clock-event reasons sampled in a background thread every 2 ms through
+    NVML (libnvidia-ml, read-only queries), so that even a timed region of a few
+    milliseconds holds several samples. Falls back to `nvidia-smi -lms 20` when NVML cannot
+    be loaded."""
 
+    # clock-event reason bits of NVML (nvmlClocksEventReason*)
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
-        self.samples = []
+    def __init__(self, device: torch.device):
+        self.device = device
+        self.samples = []  # (monotonic time, sm MHz, max sm MHz, set of reason names)
         self.proc = None
         self.thread = None
+        self.stop_flag = threading.Event()
+        self.source = None
+
+    def _nvml_handle(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        uuid = getattr(torch.cuda.get_device_properties(self.device), "uuid", None)
+        ok = False
+        if uuid is not None:
+            txt = str(uuid)
+            txt = txt if txt.startswith("GPU-") else "GPU-" + txt
+            ok = nv.nvmlDeviceGetHandleByUUID(txt.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            idx = self.device.index or 0
+            if "CUDA_VISIBLE_DEVICES" in os.environ:
+                idx = int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[idx])
+            if nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+        return nv, h
 
     def start(self):
         try:
+            import ctypes
+            nv, h = self._nvml_handle()
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+
+            def poll():
+                clk, bits = ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self.stop_flag.is_set():
+                    if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                            reasons_fn(h, ctypes.byref(bits)) == 0:
+                        names = {n for b, n in self.REASONS.items() if bits.value & b}
+                        self.samples.append((time.monotonic(), float(clk.value),
+                                             float(mx.value), names))
+                    time.sleep(0.002)
+
+            self.thread = threading.Thread(target=poll, daemon=True)
+            self.source = "nvml 2 ms"
+            self.thread.start()
+            return
+        except (OSError, AttributeError):
+            pass
+        try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", str(self.device.index or 0), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi 20 ms"
+        self.thread = threading.Thread(target=self._read_smi, daemon=True)
         self.thread.start()
 
-    def _read(self):
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
         for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 8:
-                self.samples.append((time.monotonic(), parts))
+            p = [x.strip() for x in line.split(",")]
+            if len(p) >= 8 and num(p[0]) is not None:
+                self.samples.append((time.monotonic(), num(p[0]), num(p[1]),
+                                     {names[i] for i in range(4)
+                                      if p[4 + i].lower().startswith("active")}))
 
     def stop(self):
+        self.stop_flag.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -118,29 +182,23 @@ class ClockSampler:
     def summary(self, t0: float, t1: float):
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
         note = []
-        if not inside:  # window shorter than the sampling period: nearest samples
-            inside = [min(self.samples, key=lambda s: abs(s[0] - 0.5 * (t0 + t1)))[1]]
+        if not inside:  # window shorter than the sampling period: nearest sample
+            inside = [min(self.samples, key=lambda x: abs(x[0] - 0.5 * (t0 + t1)))]
             note = ["window_shorter_than_sampling"]
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-
-        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
-        mx = [num(p[1]) for p in inside if num(p[1]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for p in inside for i in range(4)
-                          if p[4 + i].lower().startswith("active")})
+        sm = [x[1] for x in inside if x[1] is not None]
+        mx = [x[2] for x in inside if x[2] is not None]
+        reasons = sorted(set().union(*[x[3] for x in inside]))
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons + note,
-                "samples": len(inside)}
+                "samples": len(inside), "source": self.source,
+                "window_ms": round((t1 - t0) * 1e3, 2)}
 
 
 def dist_setup(n_gpus):
+    """Rank, world size and local rank from the torchrun environment (WORLD_SIZE must equal
+    n_gpus; main() checks it or launches the ranks itself)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -309,7 +367,7 @@ def run_gpu(args, rank, world, local):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler = ClockSampler(dev)
     sampler.start()
     time.sleep(0.3)
     barrier(world)
@@ -778,6 +836,25 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # launch the N ranks ourselves (one process per GPU, the same torchrun command a
+        # multi-GPU driver uses) and pass their exit status on
+        if args.impl != "reference" and torch.cuda.device_count() < args.gpus:
+            print(f"bench.py: --gpus {args.gpus} but {torch.cuda.device_count()} visible GPUs",
+                  file=sys.stderr)
+            sys.exit(2)
+        import socket
+        with socket.socket() as sck:
+            sck.bind(("127.0.0.1", 0))
+            port = sck.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+               "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+        sys.exit(subprocess.call(cmd))
+    world_env = int(os.environ.get("WORLD_SIZE", "1"))
+    if world_env != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world_env}", file=sys.stderr)
+        sys.exit(2)
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -24,6 +24,19 @@ extern "C" {
 int kda_selftest_umma(const void *A, const void *B, float *D, int M, int N, int K,
                       int a_mn_major, int b_mn_major, kda_stream_t stream);
 
+/*
+ * Exercises the library's bounded device waits without a fault: one CTA of 128
+ * threads waits on an mbarrier that nothing ever arrives on (no copy and no
+ * tensor-core operation is issued against it) for at most `limit_us`
+ * microseconds, votes on the outcome across its threads as the state pass does,
+ * records KDA_ERR_TIMEOUT in the device error word and returns. Asynchronous on
+ * `stream`: the next kda_get_error(stream) returns KDA_ERR_TIMEOUT (and clears
+ * the word, so the call after it returns KDA_OK). limit_us in 1..1000000, else
+ * KDA_ERR_INVALID_ARG; launch failures return KDA_ERR_CUDA. A check of the
+ * library itself; the K3 pages have no counterpart.
+ */
+int kda_selftest_wait_timeout(unsigned limit_us, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -90,6 +90,7 @@ def load(path: str = LIB_PATH):
             "kda_get_error": ([P], I),
             "kda_trace_events": ([ctypes.POINTER(P), ctypes.POINTER(P), I], I),
             "kda_selftest_umma": ([P, P, P, I, I, I, I, I, P], I),
+            "kda_selftest_wait_timeout": ([U, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -377,6 +378,13 @@ def kda_selftest_umma(A, B, D, a_mn_major=0, b_mn_major=0, stream=None):
     N = B.shape[1]
     return int(lib.kda_selftest_umma(_ptr(A), _ptr(B), _ptr(D), M, N, K, int(a_mn_major),
                                      int(b_mn_major), _stream(stream)))
+
+
+def kda_selftest_wait_timeout(limit_us, stream=None):
+    """Launch the bounded-wait self-test (diagnostic; see include/kda_selftest.h): a wait that
+    nothing completes runs out after ``limit_us`` and is reported by the next kda_get_error()."""
+    lib = load()
+    return int(lib.kda_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- conveniences

@@ -53,12 +53,15 @@ def context_parallel_forward(q, k, v, log_alpha, beta, gate=None, initial_state=
     world = dist.get_world_size(group)
     rank = dist.get_rank(group)
     X, Z = summary(k, v, log_alpha, beta, l2norm)  # [1, H, dk, dk], [1, H, dk, dv]
-    X = X.contiguous()
-    Z = Z.contiguous()
+    # gloo exchanges host tensors: the summaries cross over host memory and come back
+    home = X.device
+    via = torch.device("cpu") if dist.get_backend(group) == "gloo" else home
+    X = X.to(via).contiguous()
+    Z = Z.to(via).contiguous()
     xs = [torch.empty_like(X) for _ in range(world)]
     zs = [torch.empty_like(Z) for _ in range(world)]
     dist.all_gather(xs, X, group=group)
     dist.all_gather(zs, Z, group=group)
-    E, S_last = scan(torch.cat(xs, 0), torch.cat(zs, 0), initial_state)
+    E, S_last = scan(torch.cat(xs, 0).to(home), torch.cat(zs, 0).to(home), initial_state)
     out, S_mine = forward(q, k, v, log_alpha, beta, gate, E[rank], scale, l2norm)
     return out, S_mine, S_last

@@ -536,16 +536,11 @@ bool tc_path(int dk, int dv, kda_dtype dt) {
 // The state pass runs one CTA per (sequence, head). With at most 112 of them (three
 // quarters of a 152-SM GPU's SMs) and at least 16 chunks per sequence on average, the cards
 // of each sequence's last 4/16 are built on the idle SMs while the state pass walks the first
-// 12/16. KDA_PREFILL_SPLIT (0..15 sixteenths, read once) overrides the fraction; 0 turns the
-// split off.
+// 12/16 (the fraction measured best on the prefill workload).
 int tc_split16(int64_t T_total, int n_seq, int H) {
-  static const int frac = [] {
-    const char *e = getenv("KDA_PREFILL_SPLIT");
-    const int v = e ? atoi(e) : 12;
-    return (v >= 0 && v <= 15) ? v : 12;
-  }();
+  constexpr int kLeadingSixteenths = 12;
   if (n_seq <= 0 || (int64_t)n_seq * H > 112 || T_total < (int64_t)16 * C * n_seq) return 0;
-  return frac;
+  return kLeadingSixteenths;
 }
 
 size_t tc_ws_bytes(int64_t T_total, int n_seq, int H) {

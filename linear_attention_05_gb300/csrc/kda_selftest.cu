@@ -17,6 +17,8 @@ namespace {
 using namespace kda::tc;
 
 __device__ unsigned g_selftest_err;
+// error word of the bounded-wait self-test, read and cleared by kda_get_error()
+__device__ unsigned g_wait_test_err;
 
 // A: [M x K] row-major bf16; B: [K x N] row-major bf16; D: [M x N] fp32.
 __global__ void __launch_bounds__(128) umma_selftest_kernel(const __nv_bfloat16 *A,
@@ -84,7 +86,41 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(const __nv_bfloat16 
   if (warp == 0) tmem_dealloc(tb, 256);
 }
 
+// Bounded-wait self-test: one CTA of 128 threads waits on an mbarrier that nothing will ever
+// arrive on (no bulk copy and no MMA is issued against it), for at most limit_ns on every
+// thread, exactly as the chunked kernels wait on their copies and MMAs. The threads then vote
+// with a barrier that ANDs their results, as the state pass does, so that every warp leaves
+// by the same branch; on a timeout one thread records it in the error word, and the kernel
+// returns normally.
+__global__ void __launch_bounds__(128) wait_timeout_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = named_bar_and(1, 128, mbar_wait(&bar, 0, limit_ns));
+  if (!ok && threadIdx.x == 0) atomicOr(&g_wait_test_err, kda::kErrTimeout);
+}
+
 }  // namespace
+
+namespace kda {
+cudaError_t selftest_take_error(unsigned *bits) {
+  unsigned v = 0, z = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_wait_test_err, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbol(g_wait_test_err, &z, sizeof(unsigned));
+  *bits = v;
+  return e;
+}
+}  // namespace kda
+
+extern "C" int kda_selftest_wait_timeout(unsigned limit_us, kda_stream_t stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return KDA_ERR_INVALID_ARG;
+  wait_timeout_kernel<<<1, 128, 0, (cudaStream_t)stream>>>((uint64_t)limit_us * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
 
 extern "C" int kda_selftest_umma(const void *A, const void *B, float *D, int M, int N, int K,
                                  int a_mn_major, int b_mn_major, kda_stream_t stream) {

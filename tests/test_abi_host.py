@@ -230,3 +230,9 @@ def test_scan_combine_rejects(lib):
         B.KDA_ERR_UNSUPPORTED
     # nothing requested: a no-op
     assert lib.kda_scan_combine(FAKE, FAKE, 2, 2, 64, 64, None, None, None, None) == B.KDA_OK
+
+
+def test_selftest_wait_timeout_rejects_bad_limit(lib):
+    # checked before any launch: no GPU needed
+    assert lib.kda_selftest_wait_timeout(0, None) == B.KDA_ERR_INVALID_ARG
+    assert lib.kda_selftest_wait_timeout(2_000_000, None) == B.KDA_ERR_INVALID_ARG

@@ -23,3 +23,13 @@ def rel_err(got, ref):
 # Tolerances (max|err| / max|ref| per output tensor): fp32 inputs 1e-4,
 # bf16 inputs with fp32 state 2e-2.
 TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+
+
+def check(name, got, ref, tol):
+    """Assert rel_err(got, ref) <= tol and print the margin as one greppable line
+    ("PARITY <name> err=<e> tol=<t> margin=<tol/e>")."""
+    e = rel_err(got, ref)
+    margin = float("inf") if e == 0.0 else tol / e
+    print(f"PARITY {name} err={e:.3e} tol={tol:.0e} margin={margin:.1f}x", flush=True)
+    assert e <= tol, (name, e, tol)
+    return e
