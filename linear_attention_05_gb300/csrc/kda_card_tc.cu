@@ -10,6 +10,10 @@
 //   W^T = Kt^T T'^T,   Ut^T = V^T T'^T                                    (GEMM 2)
 //   Q'  = Qt - P W,    O_intra = P Ut                                     (GEMM 3)
 //   Phi' = -Kd^T W,    B_c = Kd^T Ut                                      (GEMM 4)
+// Ut enters GEMMs 3b/4b as two bf16 terms, Ut = hi + lo (hi = bf16(Ut), lo = bf16(Ut - hi)):
+// when one key is re-written by many tokens of a chunk, Ut holds differences of successive
+// values that the product with Kd sums back up (a telescoping sum), and a single bf16
+// rounding of each term would add up to a few 1e-2 of the state.
 // (Derivation: U = Ut - W S, O = Qt S + P U, S_next = Diag(e^{G_C}) S + Kd^T U.)
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -50,6 +54,8 @@ constexpr int A_M = 65536;       // 16640: M (fp32, 64 x 65 padded); later W^T (
 constexpr int A_T = 82176;       // 16640: T (fp32, 64 x 65 padded)
 constexpr int A_TB = 99328;      // 8192:  T' = T diag(b) (bf16 64-row tile); later identity
 constexpr int A_XT = 107520;     // 3072:  block temporaries of the solve
+constexpr int A_UL = 82944;      // 16384: after GEMM 2, the low bf16 part of Ut^T (128-row
+                                 // K-major tile) in the dead T (and the gap after it)
 constexpr int A_DYN = 110592 + 1024;  // with alignment slack
 constexpr int LDM = 65;          // row pitch of M and T (conflict-free rows and columns)
 constexpr uint32_t A_TMA_BYTES = 8 * 8192;
@@ -397,8 +403,17 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
       tmem_ld32(tmem_addr(tb, quad * 32, 64 + 64 * grp + 32 * half), t32);
       tmem_wait_ld();
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-        *reinterpret_cast<uint4 *>(dst + sw128_chunk(L, half * 4 + ch, 128)) = pack8(t32 + ch * 8);
+      for (int ch = 0; ch < 4; ++ch) {
+        const uint4 hi = pack8(t32 + ch * 8);
+        *reinterpret_cast<uint4 *>(dst + sw128_chunk(L, half * 4 + ch, 128)) = hi;
+        if (grp == 1) {  // Ut^T: the rounding residue as a second bf16 tile
+          float h8[8], lo[8];
+          unpack8(hi, h8);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) lo[u] = t32[ch * 8 + u] - h8[u];
+          *reinterpret_cast<uint4 *>(sm + A_UL + sw128_chunk(L, half * 4 + ch, 128)) = pack8(lo);
+        }
+      }
     }
     // identity (64 x 64, bf16) in the T' tile, which GEMM 2 has finished reading
 #pragma unroll
@@ -461,8 +476,14 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
         *reinterpret_cast<uint4 *>(blk + lane * 128 + ((((half * 4 + ch) ^ (lane & 7))) << 4)) =
             pack8(t32 + ch * 8);
     };
-    uint8_t *blk = sm + 65536 + (grp * 4 + quad) * 4096;  // (quadrant, atom grp)
-    uint8_t *blk2 = sm + 8192 + quad * 4096;               // (quadrant, atom 2), shared by grp 0/1
+    // twelve 4 KB staging blocks in regions dead by now: the Qt rows and Kt's second atom
+    // column [8192, 32768), W^T [65536, 81920) and the identity [99328, 107520); P, Kd and
+    // both Ut^T tiles stay intact for GEMMs 3b/4b
+    auto stage_block = [&](int i) -> uint8_t * {
+      return sm + (i < 6 ? 8192 + i * 4096 : (i < 10 ? 65536 + (i - 6) * 4096 : 99328 + (i - 10) * 4096));
+    };
+    uint8_t *blk = stage_block(grp * 4 + quad);  // (quadrant, atom grp)
+    uint8_t *blk2 = stage_block(8 + quad);       // (quadrant, atom 2), shared by grp 0/1
     float ta[32], tb2[32];
     tmem_ld32(tmem_addr(tb, quad * 32, 32 * (2 + 2 * grp)), ta);
     tmem_ld32(tmem_addr(tb, quad * 32, 32 * (3 + 2 * grp)), tb2);
@@ -490,11 +511,13 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
   // ---------------- GEMMs 3b/4b on Ut^T: O_intra^T -> [0,64), B_c^T -> [64,192)
   if (tid == 0 && ok) {
     const uint32_t id3 = idesc_bf16(128, 64, 0, 0), id4 = idesc_bf16(128, 128, 0, 1);
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t ad = desc_kmajor(sb + A_V, 128, kk);
-      mma_bf16(tb + 0, ad, desc_kmajor(sb + A_X1, 64, kk), id3, kk > 0);
-      mma_bf16(tb + 64, ad, desc_mnmajor(sb + A_LA, 64, kk), id4, kk > 0);
-    }
+    for (int part2 = 0; part2 < 2; ++part2)  // Ut^T = hi + lo
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ad = desc_kmajor(sb + (part2 ? A_UL : A_V), 128, kk);
+        const uint32_t acc = (part2 | kk) > 0;
+        mma_bf16(tb + 0, ad, desc_kmajor(sb + A_X1, 64, kk), id3, acc);
+        mma_bf16(tb + 64, ad, desc_mnmajor(sb + A_LA, 64, kk), id4, acc);
+      }
     mma_commit(&bar_mma);
   }
   wait_mma();

@@ -55,9 +55,10 @@ def test_two_ranks_library_kernels_match_oracle(tmp_path):
     import oracle
     from linear_attention_05_gb300 import inputs
     from util import TOL, check
-    x = inputs.tokens(sum(SEG), H, D, D, torch.bfloat16, seed=SEED, device="cpu")
-    f = {n: a.float().numpy() for n, a in x.items()}
-    S0 = inputs.state(1, H, D, D, seed=SEED + 1, device="cpu").double().numpy()
+    # the same device generator as the ranks (CPU and CUDA generators draw different values)
+    x = inputs.tokens(sum(SEG), H, D, D, torch.bfloat16, seed=SEED, device="cuda")
+    f = {n: a.float().cpu().numpy() for n, a in x.items()}
+    S0 = inputs.state(1, H, D, D, seed=SEED + 1, device="cuda").double().cpu().numpy()
     T = sum(SEG)
     ref_out, ref_S = oracle.forward(f["q"], f["k"], f["v"], f["log_alpha"], f["beta"], f["gate"],
                                     S0, [0, T], scale=0.9)
