@@ -203,16 +203,29 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
     *reinterpret_cast<float4 *>(part + rg * 128 + cc * 8 + 4) = make_float4(tot[4], tot[5], tot[6], tot[7]);
   }
   __syncthreads();
+  // exclusive prefix of the row-group partial sums, in place: one thread per channel walks the
+  // 16 groups once (a thread per (channel group, row group) re-reading every earlier group
+  // made this the second-slowest step of the card)
+  if (tid < DD) {
+    float x[16];
+#pragma unroll
+    for (int g = 0; g < 16; ++g) x[g] = part[g * 128 + tid];
+    float run = 0.f;
+#pragma unroll
+    for (int g = 0; g < 16; ++g) {
+      part[g * 128 + tid] = run;
+      run += x[g];
+    }
+  }
+  __syncthreads();
   {
     // running log-decay G entering this thread's first row: sum over earlier row groups
     float G[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) G[u] = 0.f;
-    for (int g = 0; g < rg; ++g) {
-      const float4 x0 = *reinterpret_cast<const float4 *>(part + g * 128 + cc * 8);
-      const float4 x1 = *reinterpret_cast<const float4 *>(part + g * 128 + cc * 8 + 4);
-      G[0] += x0.x; G[1] += x0.y; G[2] += x0.z; G[3] += x0.w;
-      G[4] += x1.x; G[5] += x1.y; G[6] += x1.z; G[7] += x1.w;
+    {
+      const float4 x0 = *reinterpret_cast<const float4 *>(part + rg * 128 + cc * 8);
+      const float4 x1 = *reinterpret_cast<const float4 *>(part + rg * 128 + cc * 8 + 4);
+      G[0] = x0.x; G[1] = x0.y; G[2] = x0.z; G[3] = x0.w;
+      G[4] = x1.x; G[5] = x1.y; G[6] = x1.z; G[7] = x1.w;
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -340,9 +353,11 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
     {
       const int j = tid & 31, i0 = (tid >> 5) * 4;  // column j, rows i0..i0+3 of the 32 x 32 block
       float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int k = j; k < 32; ++k) {  // Y = M_21 T_11 (T_11[k][j] = 0 for k < j)
-        const float t = Ts[mix(k, j)];
+      // Y = M_21 T_11, T_11[k][j] = 0 for k < j (not stored there: masked). The loop runs
+      // over all k in every lane: a lane-dependent start made the warps diverge.
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float t = k >= j ? Ts[mix(k, j)] : 0.f;
 #pragma unroll
         for (int u = 0; u < 4; ++u) y[u] = fmaf(Ms[mix(32 + i0 + u, k)], t, y[u]);
       }
@@ -350,12 +365,16 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
       for (int u = 0; u < 4; ++u) Ts[mix(i0 + u, 32 + j)] = y[u];
       __syncthreads();
       float z[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int k = 0; k < i0 + 4; ++k) {  // T_21 = -T_22 Y (T_22[i][k] = 0 for k > i)
+      // T_21 = -T_22 Y, T_22[i][k] = 0 for k > i (masked): every warp runs all 32 steps, so
+      // the warps with the lower rows no longer hold the barrier for those with the higher
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
         const float yk = Ts[mix(k, 32 + j)];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (k <= i0 + u) z[u] = fmaf(Ts[mix(32 + i0 + u, 32 + k)], yk, z[u]);
+        for (int u = 0; u < 4; ++u) {
+          const float t = k <= i0 + u ? Ts[mix(32 + i0 + u, 32 + k)] : 0.f;
+          z[u] = fmaf(t, yk, z[u]);
+        }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) Ts[mix(32 + i0 + u, j)] = -z[u];
