@@ -40,6 +40,7 @@ STATE_BYTES = 128 * 128 * 4
 
 
 PROFILE_OF = {"kda_card_tc": "kda_card_tc_prefill.md", "kda_state_tc": "kda_state_tc_prefill.md",
+              "kda_prefill_fused": "kda_prefill_fused_prefill.md",
               "kda_decode_kernel": "kda_decode_kernel_decode.md",
               "kda_scan_kernel": "kda_scan_kernel_scan.md"}
 
@@ -386,24 +387,33 @@ def run_gpu(args, rank, world, local):
     ms_per_step = total_ms / args.steps
     value = world * TOKENS_PER_STEP / (ms_per_step * 1e-3) / 1e6
 
-    # roofline of the dominant kernel (update cards or state pass), over its launches per step
+    # roofline of the dominant kernel, over its launches per step: the persistent prefill (one
+    # launch: cards and state pass together), or the update cards / state pass of the
+    # two-kernel schedule
     tc = (w.dtype == torch.bfloat16 and d == 128)
-    names = (["kda_chunk_table", "kda_card_tc", "kda_state_tc"] if tc else
-             ["kda_chunk_table", "kda_prep_simt", "kda_state_simt"])
-    has_table = n_launch in (3, 5)
-    k0 = 1 if has_table else 0
-    split = (n_launch - k0) == 4
-    launches_of = [[0] if has_table else [],
-                   [k0, k0 + 2] if split else [k0],
-                   [k0 + 1, k0 + 3] if split else [k0 + 1]]
+    chunk_heads = (T // 64) * H
+    fused = n_launch == 1
+    if fused:
+        names = ["kda_prefill_fused"]
+        launches_of = [[0]]
+        alg_bytes = {0: TOKEN_HEADS * BYTES_PER_TOKEN_HEAD + 2 * n_seq * H * STATE_BYTES}
+        split = False
+    else:
+        names = (["kda_chunk_table", "kda_card_tc", "kda_state_tc"] if tc else
+                 ["kda_chunk_table", "kda_prep_simt", "kda_state_simt"])
+        has_table = n_launch in (3, 5)
+        k0 = 1 if has_table else 0
+        split = (n_launch - k0) == 4
+        launches_of = [[0] if has_table else [],
+                       [k0, k0 + 2] if split else [k0],
+                       [k0 + 1, k0 + 3] if split else [k0 + 1]]
+        alg_bytes = {  # algorithmic HBM bytes per step of each kernel
+            0: (n_seq + 1) * 4 if has_table else 0,
+            1: TOKEN_HEADS * (4 * d * 2 + 2),                                 # q, k, v, log_alpha, beta
+            2: TOKEN_HEADS * (2 * d * 2) + 2 * n_seq * H * STATE_BYTES,       # gate, o, states
+        }
     kernel_ms = [sum(per_launch[i] for i in ix) for ix in launches_of]  # per step
     dom = int(np.argmax(kernel_ms))
-    chunk_heads = (T // 64) * H
-    alg_bytes = {  # algorithmic HBM bytes per step of each kernel
-        0: (n_seq + 1) * 4 if has_table else 0,
-        1: TOKEN_HEADS * (4 * d * 2 + 2),                                 # q, k, v, log_alpha, beta
-        2: TOKEN_HEADS * (2 * d * 2) + 2 * n_seq * H * STATE_BYTES,       # gate, o, states
-    }
     n_dom = len(launches_of[dom])
     achieved = alg_bytes[dom] / (kernel_ms[dom] * 1e-3) / 1e9  # = per-launch bytes / mean duration
     traffic = profiled_traffic(names[dom])
@@ -422,13 +432,17 @@ def run_gpu(args, rank, world, local):
     if split:
         roofline["schedule"] = ("split prefill: the cards of each sequence's trailing chunks are "
                                 "built beside the state pass over its leading chunks")
+    if fused:
+        roofline["schedule"] = ("persistent prefill: one cooperative launch; all SMs build update "
+                                "cards chunk-major, then one CTA per chain walks its chain while "
+                                "the others build the remaining cards")
     if tc:
         # tensor-core work per (chunk, head): card GEMMs 1-4 and the state-pass MMA group,
         # over the whole step (the launches overlap, so their durations do not add up)
         card_flop = 2 * (128 * 64 * 128 + 2 * 128 * 64 * 64 + 2 * 128 * 64 * 64 + 2 * 128 * 128 * 64)
         state_flop = 2 * 128 * 192 * 128
         tf = chunk_heads * (card_flop + state_flop) / (ms_per_step * 1e-3) / 1e12
-        roofline["tensor"] = {"kernels": names[1:], "achieved": round(tf, 2), "unit": "TFLOP/s",
+        roofline["tensor"] = {"kernels": names if fused else names[1:], "achieved": round(tf, 2), "unit": "TFLOP/s",
                               "peak": pk["bf16_tflops"], "frac": round(tf / pk["bf16_tflops"], 4),
                               "flop_per_chunk_head": card_flop + state_flop, "over": "step"}
 

@@ -151,6 +151,8 @@ int kda_chunk_fwd_launches(int64_t T_total, int n_seq, int H, int dk, int dv, in
     return 0;
   if (n_seq == 0) return 0;
   const bool tc = kda::tc_path(dk, dv, dtype);
+  if (tc && !varlen && kda::fused_shape(T_total, n_seq, H) && kda::fused_ctas(n_seq, H) > 0)
+    return 1;  // the persistent prefill
   const int table = (!tc || varlen) ? 1 : 0;
   return table + ((tc && kda::tc_split16(T_total, n_seq, H) > 0) ? 4 : 2);
 }
@@ -255,6 +257,22 @@ static kda_status chunk_fwd_impl(const void *q, const void *k, const void *v,
   Tracer tr(s);
   kda::ChunkWs ws = tc ? kda::tc_ws_carve(workspace, T_total, n_seq, H)
                        : kda::chunk_ws_carve(workspace, T_total, n_seq, H, dk, dv);
+  // fixed lengths, few chains: cards and state pass in one persistent launch; if the device
+  // cannot run it (too few SMs, no cooperative launch), the split schedule below
+  if (tc && cu_seqlens == nullptr && kda::fused_shape(T_total, n_seq, H)) {
+    const int grid = kda::fused_ctas(n_seq, H);
+    if (grid > 0) {
+      cudaError_t e = tr([&] {
+        return kda::launch_prefill_fused(q, k, v, log_alpha, beta, gate, out, initial_state,
+                                         final_state, n_seq, T_total, H, scale, flags, ws, ck,
+                                         grid, s);
+      });
+      if (e == cudaSuccess) return KDA_OK;
+      if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_status(e, "persistent prefill");
+      cudaGetLastError();  // not resident at once on this device: take the split schedule
+      tr.idx = 0;
+    }
+  }
   // the tensor-core kernels index fixed-length batches (no cu_seqlens) without the chunk table
   if (!tc || cu_seqlens != nullptr) {
     st = cuda_status(
@@ -596,13 +614,14 @@ kda_status kda_trace_events(void *const *begin, void *const *end, int n) {
 kda_status kda_get_error(kda_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "stream synchronize");
-  unsigned a = 0, b = 0, c = 0, d = 0, f = 0;
+  unsigned a = 0, b = 0, c = 0, d = 0, f = 0, g = 0;
   if ((e = kda::chunk_take_error(&a)) != cudaSuccess) return cuda_status(e, "error word");
   if ((e = kda::decode_take_error(&b)) != cudaSuccess) return cuda_status(e, "error word");
   if ((e = kda::tc_take_error(&c)) != cudaSuccess) return cuda_status(e, "error word");
   if ((e = kda::scan_take_error(&d)) != cudaSuccess) return cuda_status(e, "error word");
   if ((e = kda::selftest_take_error(&f)) != cudaSuccess) return cuda_status(e, "error word");
-  const unsigned bits = a | b | c | d | f;
+  if ((e = kda::fused_take_error(&g)) != cudaSuccess) return cuda_status(e, "error word");
+  const unsigned bits = a | b | c | d | f | g;
   if (bits & kda::kErrTimeout) return fail(KDA_ERR_TIMEOUT, "a bounded device wait ran out");
   if (bits & kda::kErrBadSeqlens)
     return fail(KDA_ERR_INVALID_ARG, "malformed cu_seqlens / cu_segs or state_slot on device");

@@ -140,8 +140,30 @@ struct ChunkWs {
   // most kOrderMax of them, else in index order. The state pass takes its chains in this
   // order, so the longest chains start in the first wave of CTAs.
   int *seq_order;
+  // persistent prefill (fixed lengths, few chains): one ready flag per (chunk, head) card and the
+  // card counter, both cleared at the start of each call
+  unsigned *ready;
+  int *next;
 };
 constexpr int kOrderMax = 256;
+
+// Persistent prefill (kda_prefill_fused.cu): eligible shapes have at least kFusedMinChunks
+// chunks per sequence and at most kFusedMaxChains (sequence, head) chains, and the device must
+// leave at least kFusedMinBuilders SMs to build cards beside the chain owners. Measured on the
+// GB300 against the two-kernel schedule: 16 chains x 256 chunks 0.731 vs 0.858 ms, 32 x 128
+// 0.410 vs 0.565 ms, 8 x 128 0.384 vs 0.425 ms, 64 x 64 equal (0.39 ms); hence at most 48.
+// The chain owners start their chains once the cards of the leading fraction of the chunks
+// are claimed, the fraction from the rates kFusedCardUs (one card, one group of the persistent
+// kernel) and kFusedStepUs (one chunk step of a chain) -- see fused_switch_chunks.
+constexpr int kFusedMinChunks = 16;
+constexpr int kFusedMaxChains = 48;
+constexpr int kFusedMinBuilders = 48;
+constexpr double kFusedCardUs = 20.0;
+constexpr double kFusedStepUs = 2.85;
+inline size_t fused_flag_bytes(int64_t T_total, int n_seq, int H) {
+  const int64_t n_chunks = n_seq > 0 ? (T_total / n_seq + kChunk - 1) / kChunk : 0;
+  return align_up(sizeof(unsigned) * (size_t)(n_seq * n_chunks * H), 256) + 256;
+}
 
 size_t chunk_ws_bytes(int64_t T_total, int n_seq, int H, int dk, int dv);
 ChunkWs chunk_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int dv);
@@ -188,6 +210,17 @@ cudaError_t launch_state_tc(int mode, unsigned flags, const void *gate, void *ou
                             float *S_final, float *X_out, float *Z_out, const int32_t *cu,
                             int n_seq, int64_t T_total, int H, float scale, const ChunkWs &ws,
                             cudaStream_t st, CkptOut ck = CkptOut(), int part = -1);
+// Persistent prefill: shape eligibility (no device query), the grid for the current device (0:
+// not possible there), the launch (clears the flags first) and its error word.
+bool fused_shape(int64_t T_total, int n_seq, int H);
+int fused_ctas(int n_seq, int H);
+int fused_switch_chunks(int n_chunks, int n_chains, int grid);
+cudaError_t launch_prefill_fused(const void *q, const void *k, const void *v, const void *la,
+                                 const void *beta, const void *gate, void *out, const float *S0,
+                                 float *S_final, int n_seq, int64_t T_total, int H, float scale,
+                                 unsigned flags, const ChunkWs &ws, CkptOut ck, int grid,
+                                 cudaStream_t st);
+cudaError_t fused_take_error(unsigned *bits);
 cudaError_t tc_take_error(unsigned *bits);        // card and state-pass words together
 cudaError_t state_tc_take_error(unsigned *bits);  // the state pass's word alone
 

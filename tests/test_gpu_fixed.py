@@ -4,7 +4,8 @@ Without cu_seqlens the card and state kernels index the sequences in closed form
 table is launched. The same batch passed with cu_seqlens goes through the table; the two must
 agree bit for bit (every chain is computed the same way), and both with the oracle (the plain
 recurrence, K3 training overview section 2) on sampled chains. The lengths leave a ragged
-last chunk, with and without the split schedule.
+last chunk, through the persistent prefill (few chains: one launch) and the two-kernel
+schedule.
 """
 import numpy as np
 import pytest
@@ -20,14 +21,14 @@ DEV = "cuda"
 D = 128
 
 
-@pytest.mark.parametrize("n_seq,L,H,split", [
-    (2, 1100, 4, True),    # 18 chunks, the last of 12 tokens; split after chunk 13
-    (8, 700, 16, False),   # 128 (sequence, head) pairs: no split; 11 chunks, the last of 60
-    (3, 50, 2, False),     # one partial chunk per sequence
+@pytest.mark.parametrize("n_seq,L,H,launches", [
+    (2, 1100, 4, 1),     # 18 chunks, the last of 12 tokens: the persistent prefill
+    (8, 700, 16, 2),     # 128 (sequence, head) pairs: cards, then the state pass
+    (3, 50, 2, 2),       # one partial chunk per sequence
 ])
-def test_fixed_length_equals_varlen_and_oracle(n_seq, L, H, split):
+def test_fixed_length_equals_varlen_and_oracle(n_seq, L, H, launches):
     T = n_seq * L
-    assert B.kda_chunk_fwd_launches(T, n_seq, H, D, D) == (4 if split else 2)
+    assert B.kda_chunk_fwd_launches(T, n_seq, H, D, D) == launches
     x = inputs.tokens(T, H, D, D, torch.bfloat16, seed=91 + L, device=DEV)
     s0 = inputs.state(n_seq, H, D, D, seed=92 + L, device=DEV)
     outs = []

@@ -1,7 +1,9 @@
 """kda_chunk_fwd captured in a CUDA graph (needs a GPU).
 
 A split prefill forks its trailing card launch onto a library stream and joins it back with
-events, all ordered on the caller's stream, so the whole call can be captured and replayed.
+events, all ordered on the caller's stream; the persistent prefill clears its flags with a
+memset on the caller's stream and makes one cooperative launch. Either call can be captured
+and replayed.
 A replay must give the eager call's bits, and, after the inputs are overwritten in place,
 the new inputs' results.
 """
@@ -22,9 +24,13 @@ def _make(seed):
     return x, s0
 
 
-def test_split_prefill_graph_replay_is_bitwise_eager():
+@pytest.mark.parametrize("varlen", [True, False])
+def test_split_prefill_graph_replay_is_bitwise_eager(varlen):
+    """varlen: the split schedule (chunk table, then cards and state passes on two streams);
+    fixed lengths: the persistent prefill (a flag reset and one cooperative launch)."""
     T = N_SEQ * L
-    assert B.kda_chunk_fwd_launches(T, N_SEQ, H, D, D) == 4  # no chunk table: fixed lengths
+    cu = torch.arange(0, T + 1, L, dtype=torch.int32, device=DEV) if varlen else None
+    assert B.kda_chunk_fwd_launches(T, N_SEQ, H, D, D, varlen=varlen) == (5 if varlen else 1)
     x, s0 = _make(81)
     ws = torch.empty(B.kda_chunk_fwd_workspace_size(T, N_SEQ, H, D, D), dtype=torch.uint8,
                      device=DEV)
@@ -33,7 +39,7 @@ def test_split_prefill_graph_replay_is_bitwise_eager():
 
     def call():
         B.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], out, s0, fs,
-                        None, N_SEQ, workspace=ws)
+                        cu, N_SEQ, workspace=ws)
 
     call()
     torch.cuda.synchronize()
