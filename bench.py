@@ -59,7 +59,10 @@ def profiled_traffic(kernel: str):
         mt = re.search(r"traffic_bytes_per_launch: (\d+)", txt)
         if not mh or not mt:
             return None
-        cur = hashlib.sha256(open(os.path.join(ROOT, mh.group(2)), "rb").read()).hexdigest()
+        h = hashlib.sha256()
+        for f in mh.group(2).split(", "):  # the sources the kernel is built from, in order
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        cur = h.hexdigest()
         return int(mt.group(1)) if cur[:16] == mh.group(1) else None
     except OSError:
         return None
@@ -496,6 +499,7 @@ def run_gpu(args, rank, world, local):
         line["segment_scan"] = bench_segment_scan(dev, pk, stream)
         line["scan_combine"] = bench_scan(dev, pk, stream)
         line["prefill_checkpoints"] = bench_checkpoints(dev, pk, stream)
+        line["persistent_prefill"] = bench_persistent(dev, pk, stream)
         line["backward"] = bench_backward(dev, pk, stream)
         line["gate_prep"] = bench_gates(dev, pk, stream)
     if rank == 0 and not args.no_cpu:
@@ -796,6 +800,50 @@ def bench_gates(dev, pk, stream, reps=20):
             "gpu_launches": kda.kda_chunk_fwd_launches(T, n_seq, H, 128, 128, varlen=False) * reps}
 
 
+def bench_persistent(dev, pk, stream, reps=20):
+    """Fixed-length prefill with few chains (2 x 8192 tokens, 16 heads: 32 chains of 128
+    chunks), where kda_chunk_fwd takes the persistent prefill (one cooperative launch), timed
+    beside the same problem through the two-kernel schedule (the lengths passed as cu_seqlens)."""
+    import linear_attention_05_gb300 as kda
+    from linear_attention_05_gb300 import inputs
+
+    n_seq, L, H, d = 2, 8192, 16, 128
+    T = n_seq * L
+    x = inputs.tokens(T, H, d, d, torch.bfloat16, seed=11, device=dev)
+    S0 = inputs.state(n_seq, H, d, d, seed=12, device=dev)
+    out = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((n_seq, H, d, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(kda.kda_chunk_fwd_workspace_size(T, n_seq, H, d, d), dtype=torch.uint8,
+                     device=dev)
+    cu = torch.arange(0, T + 1, L, dtype=torch.int32, device=dev)
+    ms = {}
+    for name, c in (("persistent", None), ("two_kernel", cu)):
+        def fn():
+            kda.kda_chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], out,
+                              S0, fs, c, n_seq, workspace=ws, stream=stream)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms[name] = e0.elapsed_time(e1) / reps
+    alg = T * H * BYTES_PER_TOKEN_HEAD + 2 * n_seq * H * STATE_BYTES
+    return {"workload": "prefill 2 x 8192 tokens, H=16 (32 chains), dk=dv=128 bf16",
+            "value": round(T / (ms["persistent"] * 1e-3) / 1e6, 3), "unit": "Mtok/s",
+            "ms": round(ms["persistent"], 4), "ms_two_kernel": round(ms["two_kernel"], 4),
+            "roofline": {"bound": "hbm", "kernel": "kda_prefill_fused",
+                         "achieved": round(alg / (ms["persistent"] * 1e-3) / 1e9, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(alg / (ms["persistent"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                         "traffic": profiled_traffic("kda_prefill_fused")},
+            "gpu_launches": reps * (kda.kda_chunk_fwd_launches(T, n_seq, H, d, d) +
+                                    kda.kda_chunk_fwd_launches(T, n_seq, H, d, d, varlen=True))}
+
+
 def bench_scan(dev, pk, stream, reps=20):
     """kda_scan_combine alone on long-context-sized summaries (8 segments x 16 heads)."""
     import linear_attention_05_gb300 as kda
@@ -831,7 +879,7 @@ def run_part(args, local):
     stream = torch.cuda.current_stream()
     fn = {"decode": bench_decode, "segscan": bench_segment_scan, "scan": bench_scan,
           "ckpt": bench_checkpoints, "bwd": bench_backward, "gates": bench_gates,
-          "varlen": bench_varlen}[args.only]
+          "varlen": bench_varlen, "persistent": bench_persistent}[args.only]
     print(json.dumps({"part": args.only, **fn(dev, pk, stream)}), flush=True)
 
 
@@ -845,7 +893,8 @@ def main():
                     help="reference arm: tokens per sequence timed per step")
     ap.add_argument("--skip-extra", action="store_true", help="prefill line only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", default=None, choices=["decode", "segscan", "scan", "ckpt", "bwd", "gates", "varlen"],
+    ap.add_argument("--only", default=None, choices=["decode", "segscan", "scan", "ckpt", "bwd", "gates", "varlen",
+                                                     "persistent"],
                     help="run one part of the path alone and print its numbers (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
