@@ -40,7 +40,7 @@ STATE_BYTES = 128 * 128 * 4
 
 
 PROFILE_OF = {"kda_card_tc": "kda_card_tc_prefill.md", "kda_state_tc": "kda_state_tc_prefill.md",
-              "kda_prefill_fused": "kda_prefill_fused_prefill.md",
+              "kda_prefill_fused": "kda_prefill_fused_persistent.md",
               "kda_decode_kernel": "kda_decode_kernel_decode.md",
               "kda_scan_kernel": "kda_scan_kernel_scan.md"}
 
