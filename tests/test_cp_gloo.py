@@ -118,3 +118,32 @@ def test_bench_max_over_ranks(tmp_path):
     mp.spawn(_bench_worker, args=(2, _free_port(), str(tmp_path)), nprocs=2, join=True)
     for r in range(2):
         assert float(np.load(os.path.join(tmp_path, f"max{r}.npy"))[0]) == 2.5
+
+
+def test_bench_launches_its_own_ranks():
+    """bench.py --gpus 2 outside torchrun starts the two ranks itself (the reference arm runs on
+    the host cores, so this needs no GPU): rank 0 prints one JSON line with n_gpus 2, the other
+    rank exits 0 without work."""
+    import json
+    import subprocess
+    env = dict(os.environ)
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl",
+                        "reference", "--steps", "1", "--warmup", "3", "--ref-tokens", "16"],
+                       capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+
+
+def test_bench_rejects_gpus_that_differ_from_world_size():
+    import subprocess
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl",
+                        "reference", "--steps", "1"], capture_output=True, text=True,
+                       timeout=300, env=env, cwd=ROOT)
+    assert r.returncode == 2
+    assert "WORLD_SIZE=1" in r.stderr
