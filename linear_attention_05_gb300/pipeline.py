@@ -11,7 +11,9 @@ With ``parts`` > 1 (one sequence per group), each sequence is also cut in time i
 ``parts`` slices of a multiple of 64 tokens; slice p starts from the state slice p - 1
 left, so the results are still bitwise those of one call (the chunks are the same and the
 fp32 state hand-over is exact), and the pipeline's tail after the last copy in is one
-slice's compute and copy out instead of a whole sequence's.
+slice's compute and copy out instead of a whole sequence's. ``tail_parts`` cuts only the last
+group that way: the tail shrinks while the other groups keep one call each (every call costs
+host time to issue).
 """
 from __future__ import annotations
 
@@ -28,16 +30,18 @@ class HostPipeline:
     sequence in ``parts`` time slices (``parts`` > 1 needs one sequence per group)."""
 
     def __init__(self, n_seq, seq_len, H, dk, dv, dtype=torch.bfloat16, device="cuda",
-                 groups=None, with_gate=True, parts=1):
+                 groups=None, with_gate=True, parts=1, tail_parts=None):
         self.n_seq, self.L, self.H, self.dk, self.dv = n_seq, seq_len, H, dk, dv
         self.groups = groups or n_seq
         if n_seq % self.groups:
             raise ValueError("n_seq must be a multiple of groups")
         self.spg = n_seq // self.groups  # sequences per group
         self.parts = parts
-        if parts > 1 and (self.spg != 1 or seq_len % parts or (seq_len // parts) % binding.CHUNK):
-            raise ValueError("parts > 1 needs one sequence per group and slices of a multiple of "
-                             "64 tokens")
+        self.tail_parts = tail_parts or parts
+        for pp in (parts, self.tail_parts):
+            if pp > 1 and (self.spg != 1 or seq_len % pp or (seq_len // pp) % binding.CHUNK):
+                raise ValueError("parts > 1 needs one sequence per group and slices of a multiple "
+                                 "of 64 tokens")
         T = n_seq * seq_len
         dev = torch.device(device)
         shapes = {"q": (T, H, dk), "k": (T, H, dk), "v": (T, H, dv), "log_alpha": (T, H, dk),
@@ -49,8 +53,8 @@ class HostPipeline:
         self.dev_fs = torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev)
         # states handed between time slices, used alternately
         self.dev_mid = ([torch.empty((n_seq, H, dk, dv), dtype=torch.float32, device=dev)
-                         for _ in range(2)] if parts > 1 else [])
-        tg = self.spg * seq_len // parts  # tokens of one call
+                         for _ in range(2)] if max(parts, self.tail_parts) > 1 else [])
+        tg = self.spg * seq_len // min(parts, self.tail_parts)  # tokens of the largest call
         nbytes = binding.kda_chunk_fwd_workspace_size(
             tg, self.spg, H, dk, dv, dtype=binding._dtype_code(self.dev_out))
         self.ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
@@ -66,7 +70,6 @@ class HostPipeline:
         self.s_in.wait_stream(cur)
         self.s_comp.wait_stream(cur)
         self.s_out.wait_stream(cur)
-        tp = self.spg * self.L // self.parts  # tokens of one call
         has_gate = host.get("gate") is not None
         has_s0 = host.get("S0") is not None
         for g in range(self.groups):
@@ -74,7 +77,9 @@ class HostPipeline:
             if has_s0:
                 with torch.cuda.stream(self.s_in):
                     self.dev_s0[s0:s1].copy_(host["S0"][s0:s1], non_blocking=True)
-            for p in range(self.parts):
+            parts = self.tail_parts if g == self.groups - 1 else self.parts
+            tp = self.spg * self.L // parts  # tokens of one call
+            for p in range(parts):
                 t0 = g * self.spg * self.L + p * tp
                 t1 = t0 + tp
                 with torch.cuda.stream(self.s_in):
@@ -87,7 +92,7 @@ class HostPipeline:
                     entry = self.dev_s0[s0:s1] if has_s0 else None
                 else:
                     entry = self.dev_mid[(p - 1) % 2][s0:s1]
-                last = p == self.parts - 1
+                last = p == parts - 1
                 exit_ = self.dev_fs[s0:s1] if last else self.dev_mid[p % 2][s0:s1]
                 binding.kda_chunk_fwd(
                     self.dev_in["q"][t0:t1], self.dev_in["k"][t0:t1], self.dev_in["v"][t0:t1],
