@@ -20,7 +20,8 @@ using namespace tc;
 using namespace tcl;
 using namespace tsb;
 
-// One CTA per (sequence, head) chain (blockIdx.y: the X / Z part of a summary pass).
+// One CTA per (sequence, head) chain (the prefill pass; a grid y index of 1 would select the X /
+// Z part of a summary pass, which kda_summary_tc now walks in one CTA).
 template <bool SUMMARY>
 __global__ void __launch_bounds__(kThreads, 1) kda_state_tc(const __grid_constant__ StateIn p) {
   extern __shared__ uint8_t smem_raw[];
@@ -30,6 +31,17 @@ __global__ void __launch_bounds__(kThreads, 1) kda_state_tc(const __grid_constan
   const StateShared sh{(uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023), bar_full,
                        &bar_mma, bar_ofull, bar_ofree, &tmem_base, &s_fail, &g_state_tc_err};
   state_body<SUMMARY>(p, sh, blockIdx.x, blockIdx.y, threadIdx.x, true, nullptr);
+}
+
+// Segment summaries: one CTA per (segment, head) walks X and Z together.
+__global__ void __launch_bounds__(kThreads, 1) kda_summary_tc(const __grid_constant__ StateIn p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_full[kSumNst], bar_mma;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_fail;
+  const SummaryShared sh{(uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023), bar_full,
+                         &bar_mma, &tmem_base, &s_fail, &g_state_tc_err};
+  summary_body(p, sh, blockIdx.x, threadIdx.x);
 }
 
 }  // namespace
@@ -45,11 +57,12 @@ cudaError_t launch_state_tc(int mode, unsigned flags, const void *gate, void *ou
     const StateIn p{mode, flags, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final,
                     X_out, Z_out, cu, n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off,
                     ws.cards, ck, part, ws.split16, ws.mid, ws.seq_order};
-    kernel<<<dim3(n_seq * H, mode == 0 ? 1 : 2), kThreads, dyn, st>>>(p);
+    kernel<<<dim3(n_seq * H, 1), kThreads, dyn, st>>>(p);
     return cudaSuccess;
   };
+  // mode 1 (segment summaries): X and Z of a chain in one CTA
   cudaError_t e = mode == 0 ? launch(kda_state_tc<false>, Geo<false>::DYN)
-                            : launch(kda_state_tc<true>, Geo<true>::DYN);
+                            : launch(kda_summary_tc, kSumDyn);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

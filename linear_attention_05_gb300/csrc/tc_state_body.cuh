@@ -522,5 +522,199 @@ __device__ __forceinline__ void state_body(const StateIn &p, const StateShared &
   if (own_tmem && warp == 0) tmem_dealloc(tb, 512);
 }
 
+// ===========================================================================
+// Segment summary of one (segment, head) chain: the transition X (entry I, no B_c) and the
+// zero-entry state Z (entry 0) walked by one CTA, so that a summary needs one CTA instead of
+// two and shares each card copy between them. Warps 0-7 carry X, warps 8-15 Z; each group is
+// laid out as the state warps of state_body (lane quadrant = warp % 4, 64 key columns per
+// warpgroup half) and works 32 key columns at a time to stay within 128 registers. Tensor
+// memory: per accumulator set b (chunk n uses b = n % 2) X^T at [256b, 256b + 128) and Z^T at
+// [256b + 128, 256b + 256). Per chunk, thread 0 issues the two chains' MMA groups (eight
+// M = 128, N = 128, K = 16 steps each, the same card operand) once both groups have staged;
+// every step is the one state_body's summary pass takes for its chain, so the results are the
+// same bits.
+constexpr int kSumNst = 4;                          // card ring depth
+constexpr int kSumStage = 33792;                    // Phi'^T (32768) + e^{G_C} (512), 1 KB rounded
+constexpr int kSumSA = kSumNst * kSumStage;         // bf16 X^T operand, then Z^T's at +32768
+constexpr int kSumDyn = kSumSA + 2 * 32768 + 1024;  // with alignment slack
+
+struct SummaryShared {
+  uint8_t *sm;  // kSumDyn - 1024 bytes, 1024-byte aligned
+  uint64_t *bar_full, *bar_mma;  // [kSumNst], [1]
+  uint32_t *tmem_base;
+  int *s_fail;
+  unsigned *err;
+};
+
+__device__ __forceinline__ void summary_body(const StateIn &p, const SummaryShared &sh, int chain,
+                                             int tid) {
+  const int32_t *__restrict__ cu = p.cu;
+  const int H = p.H;
+  if (cu != nullptr && p.meta->invalid) return;
+  uint8_t *sm = sh.sm;
+  const uint32_t sb = smem_u32(sm);
+  const int h = chain % H;
+  const int s = cu ? p.seq_order[chain / H] : chain / H;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int zg = warp >> 3;              // 0: X, 1: Z
+  const int quad = warp & 3;             // lane quadrant
+  const int j = quad * 32 + lane;        // tensor-memory lane / column of X or Z
+  const int half = (warp >> 2) & 1;      // which 64 key columns
+  int64_t ts, ls;
+  seq_range(cu, p.fixed_len, s, &ts, &ls);
+  const int nchunks = (int)((ls + C - 1) / C);
+  const int cbase = nchunks > 0 ? (cu ? p.off[s] : s * nchunks) : 0;
+  auto card_of = [&](int n) { return p.cards + ((size_t)(cbase + n) * H + h) * CARD_BYTES; };
+  float *res = (zg ? p.Z_out : p.X_out) + ((size_t)s * H + h) * DD * DD;
+  if (nchunks == 0) {  // X = I, Z = 0
+    for (int c = 64 * half; c < 64 * half + 64; ++c) res[(size_t)c * DD + j] = (!zg && c == j);
+    return;
+  }
+  if (warp == 0) {
+    tmem_alloc(sh.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kSumNst; ++i) mbar_init(&sh.bar_full[i], 1);
+    mbar_init(sh.bar_mma, 1);
+    fence_mbar_init();
+    *sh.s_fail = 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *sh.tmem_base;
+  auto set_col = [](int n) { return 256 * (n & 1); };
+  int loads_issued = 0, loads_done = 0;
+  uint32_t full_phase[kSumNst] = {}, mma_phase = 0u;
+  bool ok = true;
+  const bool loader = (tid == 32);
+  auto load_card = [&](int n) {
+    const int st = n % kSumNst;
+    uint8_t *dst = sm + st * kSumStage;
+    const uint8_t *src = card_of(n);
+    mbar_arrive_expect_tx(&sh.bar_full[st], 32768 + 512);
+    bulk_g2s(dst, src + CARD_PHIQ, 16384, &sh.bar_full[st]);
+    bulk_g2s(dst + 16384, src + CARD_PHIQ + 16384, 16384, &sh.bar_full[st]);
+    bulk_g2s(dst + 32768, src + CARD_D, 512, &sh.bar_full[st]);
+    // B_c^T (read by the Z group with plain loads two chunks later) into L2
+    prefetch_l2(src + CARD_BCT, 32768);
+    ++loads_issued;
+  };
+  auto wait_full = [&](int n) -> bool {
+    const int st = n % kSumNst;
+    const bool r = mbar_wait(&sh.bar_full[st], full_phase[st]);
+    full_phase[st] ^= 1u;
+    if (r) ++loads_done;
+    return r;
+  };
+  // Z group: this thread's 64 columns of B_c^T row j of chunk n (lane-interleaved in the card)
+  uint4 bcr[8];
+  auto fetch_bc = [&](int n) {
+    if (!zg || n >= nchunks) return;
+    const uint8_t *src = card_of(n) + CARD_BCT;
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8)
+      bcr[c8] = *reinterpret_cast<const uint4 *>(src + ((8 * half + c8) * 128 + j) * 16);
+  };
+  uint8_t *sa = sm + kSumSA + zg * 32768;  // this group's bf16 operand tile
+  // accumulator <- Diag(e^{G_C}) S + B_c (Z) and the bf16 operand from the 32 key columns
+  // 64 * half + 32 * qq of this thread's row, for chunk n
+  auto stage_piece = [&](int n, int qq, const float *x) {
+    const float *dv = reinterpret_cast<const float *>(sm + (n % kSumNst) * kSumStage + 32768);
+    const int q4 = 2 * half + qq;
+    float init[32];
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+      float bc[8];
+      if (zg) unpack8(bcr[qq * 4 + ch], bc);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = q4 * 32 + ch * 8 + u;
+        init[ch * 8 + u] = dv[c] * x[ch * 8 + u] + (zg ? bc[u] : 0.f);
+      }
+      *reinterpret_cast<uint4 *>(sa + sw128_chunk(j, q4 * 4 + ch, 128)) = pack8(x + ch * 8);
+    }
+    tmem_st32(tmem_addr(tb, quad * 32, set_col(n) + 128 * zg + 32 * q4), init);
+  };
+  auto issue_mma = [&](int n) {  // by thread 0
+    const uint32_t stg = sb + (n % kSumNst) * kSumStage;
+    const uint32_t id = idesc_bf16(128, 128, 0, 1);
+    for (int g = 0; g < 2; ++g)
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16(tb + set_col(n) + 128 * g, desc_kmajor(sb + kSumSA + g * 32768, 128, kk),
+                 sdesc_sw128(stg + kk * 2048, 128 * 128, 1024), id, 1u);
+    mma_commit(sh.bar_mma);
+  };
+  if (loader)
+    for (int n = 0; n < kSumNst && n < nchunks; ++n) load_card(n);
+  fetch_bc(0);
+  if (!wait_full(0)) ok = false;
+  if (ok) {
+#pragma unroll
+    for (int qq = 0; qq < 2; ++qq) {
+      float x[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) x[u] = (!zg && 64 * half + 32 * qq + u == j) ? 1.f : 0.f;
+      stage_piece(0, qq, x);
+    }
+    tmem_wait_st();
+    fence_async_smem();
+    tc_fence_before();
+  }
+  ok = named_bar_and(1, 512, ok);
+  tc_fence_after();
+  if (tid == 0 && ok) issue_mma(0);
+  fetch_bc(1);
+  for (int n = 0; n < nchunks && ok; ++n) {
+    bool good = mbar_wait(sh.bar_mma, mma_phase);
+    mma_phase ^= 1u;
+    tc_fence_after();
+    if (good && loader && n + kSumNst < nchunks) load_card(n + kSumNst);
+    const bool last = (n + 1 == nchunks);
+    if (good && !last) good = wait_full(n + 1);
+    if (good) {
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        float x[32];
+        tmem_ld32(tmem_addr(tb, quad * 32, set_col(n) + 128 * zg + 64 * half + 32 * qq), x);
+        tmem_wait_ld();
+        if (last) {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) res[(size_t)(64 * half + 32 * qq + u) * DD + j] = x[u];
+        } else {
+          stage_piece(n + 1, qq, x);
+        }
+      }
+    }
+    if (last) {
+      if (!good) ok = false;
+      break;
+    }
+    if (good) {
+      tmem_wait_st();
+      fence_async_smem();
+      tc_fence_before();
+    }
+    ok = named_bar_and(1, 512, good);
+    tc_fence_after();
+    if (!ok) break;
+    if (tid == 0) issue_mma(n + 1);
+    fetch_bc(n + 2);
+  }
+  if (!ok) {
+    if (lane == 0) atomicOr(sh.err, kErrTimeout);
+    if (loader)  // copies still in flight land (bounded) before shared memory is released
+      for (int n = loads_done; n < loads_issued; ++n) {
+        const int st = n % kSumNst;
+        if (!mbar_wait(&sh.bar_full[st], full_phase[st], 100000000ull)) break;
+        full_phase[st] ^= 1u;
+      }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, 512);
+}
+
 }  // namespace tsb
 }  // namespace kda

@@ -280,6 +280,22 @@ def test_segment_summary_vs_oracle(dtype):
     assert rel_err(np32(E), rE) <= 1e-5 and rel_err(np32(Sf), rSf) <= 1e-5
 
 
+def test_segment_summary_tensor_core_vs_oracle():
+    """The tensor-core summary pass (bf16, d = 128): one CTA walks a chain's X and Z together.
+    Ragged segments, an empty one (X = I, Z = 0 exactly) and a one-token one."""
+    lengths = [100, 0, 64, 257, 1]
+    x, cu = make_tokens(lengths, 3, 128, 128, torch.bfloat16, seed=52)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    X, Z = B.segment_summary(x["k"], x["v"], x["log_alpha"], x["beta"], cu_t)
+    assert B.kda_get_error() == B.KDA_OK
+    rX, rZ = oracle.segment_summary(np32(x["k"]), np32(x["v"]), np32(x["log_alpha"]),
+                                    np32(x["beta"]), cu)
+    check("summary_tc/X", np32(X), rX, TOL[torch.bfloat16])
+    check("summary_tc/Z", np32(Z), rZ, TOL[torch.bfloat16])
+    eye = torch.eye(128, device=DEV).expand(3, 128, 128)
+    assert torch.equal(X[1], eye) and not Z[1].any()
+
+
 def test_context_parallel_driver_one_rank():
     """cp.context_parallel_forward with the device library on a one-rank NCCL group
     equals the monolithic chunked pass from the same initial state."""
