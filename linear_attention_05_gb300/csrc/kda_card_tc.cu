@@ -180,6 +180,18 @@ static bool make_token_map(CUtensorMap *m, const void *base, int64_t T_total, in
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_rows_map_f32(CUtensorMap *m, const void *base, uint64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)DD, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)DD * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const void *la,
                            const void *beta, const int32_t *cu, int n_seq, int64_t T_total, int H,
                            unsigned flags, const ChunkWs &ws, cudaStream_t st, int part) {

@@ -1,6 +1,7 @@
 // Internal helpers shared by the libkda translation units (device side).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -195,6 +196,8 @@ cudaError_t launch_scan_combine(const float *X, const float *Z, int n_seg,
 
 // Tensor-core path (bf16, dk = dv = 128): update cards + state pass.
 bool tc_path(int dk, int dv, kda_dtype dt);
+// 2D tensor map over `rows` rows of 128 fp32 values: box 32 columns x 128 rows, 128-byte swizzle.
+bool make_rows_map_f32(CUtensorMap *m, const void *base, uint64_t rows);
 // Split prefill: sixteenths of each sequence's chunks in its leading part, or 0 when the
 // state pass would leave too few SMs idle for the trailing cards to use.
 int tc_split16(int64_t T_total, int n_seq, int H);

@@ -294,6 +294,58 @@ def test_segment_summary_tensor_core_vs_oracle():
     check("summary_tc/Z", np32(Z), rZ, TOL[torch.bfloat16])
     eye = torch.eye(128, device=DEV).expand(3, 128, 128)
     assert torch.equal(X[1], eye) and not Z[1].any()
+    # the d = 128 scan over these summaries (tensor cores, split-bf16 products)
+    S_init = inputs.state(1, 3, 128, 128, seed=53, device=DEV)[0]
+    E, Sf = B.scan_combine(X, Z, S_init)
+    rE, rSf = oracle.scan_combine(np32(X), np32(Z), np32(S_init))
+    check("summary_tc/scan_E", np32(E), rE, 1e-5)
+    check("summary_tc/scan_final", np32(Sf), rSf, 1e-5)
+
+
+def _scan_inputs(n_seg, H, seed, d=128):
+    """Contractive X (spectral norm about 0.9, as a segment's transition is) and Z, S_init of
+    unit scale."""
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    X = torch.randn((n_seg, H, d, d), generator=g, device=DEV) / (2.2 * d ** 0.5)
+    Z = torch.randn((n_seg, H, d, d), generator=g, device=DEV)
+    S = torch.randn((H, d, d), generator=g, device=DEV)
+    return X.contiguous(), Z.contiguous(), S
+
+
+@pytest.mark.parametrize("n_seg", [0, 1, 2, 3, 8, 17])
+@pytest.mark.parametrize("with_init", [False, True])
+def test_scan_combine_d128_vs_oracle(n_seg, with_init):
+    """kda_scan_combine at dk = dv = 128 (the tensor-core kernel: each fp32 operand as three
+    bf16 terms, six products per step) against the oracle's fp64 scan at the fp32 tolerance.
+    No segments, one segment (without S_init no product at all), and chains of 2 to 17 steps
+    over 3 heads."""
+    H = 3
+    X, Z, S = _scan_inputs(n_seg, H, seed=60 + n_seg)
+    S_init = S if with_init else None
+    E, Sf = B.scan_combine(X, Z, S_init)
+    assert B.kda_get_error() == B.KDA_OK
+    rE, rSf = oracle.scan_combine(np32(X), np32(Z), None if S_init is None else np32(S_init))
+    tag = f"scan_d128/n{n_seg}/{'init' if with_init else 'zero'}"
+    if n_seg:
+        check(tag + "/E", np32(E), rE, 1e-5)
+    check(tag + "/final", np32(Sf), rSf, 1e-5)
+    if not with_init and n_seg:
+        assert not E[0].any()  # E_0 = 0 exactly
+        if n_seg > 1:
+            assert torch.equal(E[1], Z[0])  # E_1 = Z_0 exactly
+
+
+def test_scan_combine_d128_one_output():
+    """Entry states only, then the final state only: each equals the call that writes both."""
+    n_seg, H = 5, 2
+    X, Z, S = _scan_inputs(n_seg, H, seed=70)
+    E, Sf = B.scan_combine(X, Z, S)
+    E2 = torch.full_like(E, float("nan"))
+    B.kda_scan_combine(X, Z, S, E2, None)
+    Sf2 = torch.full_like(Sf, float("nan"))
+    B.kda_scan_combine(X, Z, S, None, Sf2)
+    assert B.kda_get_error() == B.KDA_OK
+    assert torch.equal(E2, E) and torch.equal(Sf2, Sf)
 
 
 def test_context_parallel_driver_one_rank():
