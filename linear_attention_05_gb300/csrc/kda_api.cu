@@ -614,14 +614,15 @@ kda_status kda_trace_events(void *const *begin, void *const *end, int n) {
 kda_status kda_get_error(kda_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "stream synchronize");
-  unsigned a = 0, b = 0, c = 0, d = 0, f = 0, g = 0;
+  unsigned a = 0, b = 0, c = 0, d = 0, f = 0, g = 0, r = 0;
   if ((e = kda::chunk_take_error(&a)) != cudaSuccess) return cuda_status(e, "error word");
   if ((e = kda::decode_take_error(&b)) != cudaSuccess) return cuda_status(e, "error word");
   if ((e = kda::tc_take_error(&c)) != cudaSuccess) return cuda_status(e, "error word");
   if ((e = kda::scan_take_error(&d)) != cudaSuccess) return cuda_status(e, "error word");
   if ((e = kda::selftest_take_error(&f)) != cudaSuccess) return cuda_status(e, "error word");
   if ((e = kda::fused_take_error(&g)) != cudaSuccess) return cuda_status(e, "error word");
-  const unsigned bits = a | b | c | d | f | g;
+  if ((e = kda::bwd_take_error(&r)) != cudaSuccess) return cuda_status(e, "error word");
+  const unsigned bits = a | b | c | d | f | g | r;
   if (bits & kda::kErrTimeout) return fail(KDA_ERR_TIMEOUT, "a bounded device wait ran out");
   if (bits & kda::kErrBadSeqlens)
     return fail(KDA_ERR_INVALID_ARG, "malformed cu_seqlens / cu_segs or state_slot on device");

@@ -1,4 +1,5 @@
-// Chunked backward pass of KDA (fp32 SIMT).
+// Chunked backward pass of KDA (fp32; the batched contractions on the tensor cores at
+// fp32-level accuracy, the serial passes and element-wise work on CUDA cores).
 //
 // Gradients of L = <dO, o> + <dS_final, S_final> with respect to q, k, v,
 // log_alpha, beta, gate and the initial state. The forward is the chunked form
@@ -21,15 +22,18 @@
 //
 // Launch sequence (all on the caller's stream): chunk table; prep (forward
 // operands + K^, diag(b)K~, A); forward state pass saving S and U per chunk;
-// O = Q~ S + P U, V1 = P^T dO and R = Q~^T dO (batched GEMMs); reverse state
+// O = Q~ S + P U, V1 = P^T dO and R = Q~^T dO (batched tensor-core GEMMs); reverse state
 // pass (dS' per chunk, dU, dS_0); seven more batched 64-row GEMMs; one triangular
 // solve; the finishing kernel.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "kda_common.cuh"
+#include "tc_common.cuh"
 
 namespace kda {
+
+__device__ unsigned g_bwd_err;
 
 namespace {
 
@@ -261,7 +265,7 @@ constexpr size_t bwd_state_smem() {
 //   C = mask( sum_i alpha_i op(A_i) op(B_i) ),  C: [64, N] row-major,
 // op(A)(m, k) = a_t ? A[k * lda + m] : A[m * lda + k],
 // op(B)(k, n) = b_t ? B[n * ldb + k] : B[k * ldb + n].
-// mask 0: none; 1: keep n <= m; 2: keep n < m. 256 threads, 4 x (N/16) outputs each.
+// mask 0: none; 1: keep n <= m; 2: keep n < m.
 struct GemmTerm {
   const float *A, *B;
   size_t sA, sB;  // per-slab strides (floats)
@@ -276,141 +280,152 @@ struct GemmArgs {
   int mask;
 };
 
-constexpr int GKT = 32;  // K tile
+// On the tensor cores, at fp32-level accuracy: as
+// C^T[n][m] = sum_i alpha_i op(B_i)^T op(A_i)^T, an M = 128 (n), N = 64 (m) tcgen05 product per
+// 64-deep K tile (for N = 64 the accumulator rows 64..127 are computed from rows of the op(B)^T
+// tile that are never written, and never read back). Each fp32 operand value v enters as three bf16 terms, v0 = bf16(v),
+// v1 = bf16(v - v0), v2 = bf16(v - v0 - v1) (the differences are exact in fp32), and the six
+// products of terms a + b <= 2 are accumulated in fp32 in tensor memory (what is dropped is
+// below 2^-24 of the product). Both operands are staged as they lie in memory: op(B)^T is
+// K-major when B is stored n-major (b_t) and MN-major otherwise, op(A)^T K-major when A is
+// stored m-major (!a_t) and MN-major otherwise. The mask is applied as C is written. One CTA
+// (256 threads) per (chunk, head), three per SM; thread 0 issues the 24 MMAs of a tile, the
+// tiles of a CTA in turn.
+namespace bgt {
+constexpr int NT = 256;
+constexpr uint32_t TA = 128 * 64 * 2;  // one bf16 term of op(B)^T: 128 x 64
+constexpr uint32_t TB = 64 * 64 * 2;   // one bf16 term of op(A)^T: 64 x 64
+constexpr uint32_t SB = 3 * TA;        // the B terms after the three A terms
+constexpr uint32_t DYN = 3 * TA + 3 * TB + 1024;
+}  // namespace bgt
 
-// One K tile of op(A) (64 x 32) and op(B) (32 x N) in registers: 16-byte loads along the
-// contiguous axis of each operand (every leading dimension and tile origin is a multiple of 4).
-constexpr int GTHREADS = 128;
-constexpr int GPA = C + 4;  // sA row pitch (floats): 16-byte aligned rows
+// (a, b) -> the bf16x2 words of the pair's three terms
+__device__ __forceinline__ void split3_pair(float a, float b, uint32_t (&w)[3]) {
+  const __nv_bfloat162 t0 = __floats2bfloat162_rn(a, b);
+  const float2 f0 = __bfloat1622float2(t0);
+  const float ra = a - f0.x, rb = b - f0.y;
+  const __nv_bfloat162 t1 = __floats2bfloat162_rn(ra, rb);
+  const float2 f1 = __bfloat1622float2(t1);
+  const __nv_bfloat162 t2 = __floats2bfloat162_rn(ra - f1.x, rb - f1.y);
+  w[0] = *reinterpret_cast<const uint32_t *>(&t0);
+  w[1] = *reinterpret_cast<const uint32_t *>(&t1);
+  w[2] = *reinterpret_cast<const uint32_t *>(&t2);
+}
 
 template <int N>
-struct GemmTile {
-  static constexpr int NA = GKT * C / 4 / GTHREADS, NB = GKT * N / 4 / GTHREADS;
-  static constexpr int PB = N + 4;
-  float4 a[NA], b[NB];
-  __device__ __forceinline__ void load(const GemmTerm &t, const float *A, const float *B, int k0,
-                                       int tid) {
-#pragma unroll
-    for (int m = 0; m < NA; ++m) {
-      const int e = tid + GTHREADS * m;
-      if (t.a_t) {  // (k, 4 consecutive m)
-        const int kk = e / (C / 4), m4 = 4 * (e % (C / 4));
-        a[m] = *reinterpret_cast<const float4 *>(A + (size_t)(k0 + kk) * t.lda + m4);
-      } else {      // (m, 4 consecutive k)
-        const int mm = e / (GKT / 4), k4 = 4 * (e % (GKT / 4));
-        a[m] = *reinterpret_cast<const float4 *>(A + (size_t)mm * t.lda + k0 + k4);
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < NB; ++m) {
-      const int e = tid + GTHREADS * m;
-      if (t.b_t) {  // (n, 4 consecutive k)
-        const int n = e / (GKT / 4), k4 = 4 * (e % (GKT / 4));
-        b[m] = *reinterpret_cast<const float4 *>(B + (size_t)n * t.ldb + k0 + k4);
-      } else {      // (k, 4 consecutive n)
-        const int kk = e / (N / 4), n4 = 4 * (e % (N / 4));
-        b[m] = *reinterpret_cast<const float4 *>(B + (size_t)(k0 + kk) * t.ldb + n4);
-      }
-    }
-  }
-  // to shared memory as sA[k][m] and sB[k][n] (16-byte aligned rows), alpha folded into A
-  __device__ __forceinline__ void store(const GemmTerm &t, float *sA, float *sB, int tid) const {
-#pragma unroll
-    for (int m = 0; m < NA; ++m) {
-      const int e = tid + GTHREADS * m;
-      const float4 v = make_float4(t.alpha * a[m].x, t.alpha * a[m].y, t.alpha * a[m].z,
-                                   t.alpha * a[m].w);
-      if (t.a_t) {
-        const int kk = e / (C / 4), m4 = 4 * (e % (C / 4));
-        *reinterpret_cast<float4 *>(sA + kk * GPA + m4) = v;
-      } else {
-        const int mm = e / (GKT / 4), k4 = 4 * (e % (GKT / 4));
-        sA[(k4 + 0) * GPA + mm] = v.x; sA[(k4 + 1) * GPA + mm] = v.y;
-        sA[(k4 + 2) * GPA + mm] = v.z; sA[(k4 + 3) * GPA + mm] = v.w;
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < NB; ++m) {
-      const int e = tid + GTHREADS * m;
-      if (t.b_t) {
-        const int n = e / (GKT / 4), k4 = 4 * (e % (GKT / 4));
-        sB[(k4 + 0) * PB + n] = b[m].x; sB[(k4 + 1) * PB + n] = b[m].y;
-        sB[(k4 + 2) * PB + n] = b[m].z; sB[(k4 + 3) * PB + n] = b[m].w;
-      } else {
-        const int kk = e / (N / 4), n4 = 4 * (e % (N / 4));
-        *reinterpret_cast<float4 *>(sB + kk * PB + n4) = b[m];
-      }
-    }
-  }
-};
-
-// 128 threads; thread (ty, tx) = (tid >> 4, tid & 15) owns rows 8ty..8ty+7 and columns
-// tx * (N/16) .. + N/16 of C, read from shared memory as 16-byte vectors.
-template <int N>
-__global__ void __launch_bounds__(GTHREADS) kda_bwd_gemm(GemmArgs g, int H,
-                                                         const ChunkMeta *__restrict__ meta) {
-  constexpr int PB = N + 4, NJ = N / 16;
-  __shared__ __align__(16) float sA[GKT * GPA];
-  __shared__ __align__(16) float sB[GKT * PB];
-  const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+__global__ void __launch_bounds__(bgt::NT, 3) kda_bwd_gemm_tc(GemmArgs g, int H,
+                                                             const ChunkMeta *__restrict__ meta) {
+  using namespace tc;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_mma;
+  __shared__ uint32_t tmem_base;
+  const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (meta->invalid || ci >= meta->total_chunks) return;
+  uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sb = smem_u32(sm);
   const size_t slab = (size_t)ci * H + h;
-  const int ty = tid >> 4, tx = tid & 15;
-  float acc[8][NJ];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) acc[i][jj] = 0.f;
-  // the K tiles of all terms in order; tile i + 1 is loaded while tile i is multiplied
-  const int nt0 = g.t[0].K / GKT, ntiles = nt0 + (g.nterms > 1 ? g.t[1].K / GKT : 0);
-  auto term_of = [&](int i) -> const GemmTerm & { return i < nt0 ? g.t[0] : g.t[1]; };
-  auto k0_of = [&](int i) { return (i < nt0 ? i : i - nt0) * GKT; };
-  GemmTile<N> tile;
-  {
-    const GemmTerm &t = term_of(0);
-    tile.load(t, t.A + slab * t.sA, t.B + slab * t.sB, 0, tid);
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, 64);
+    tmem_relinquish();
   }
+  if (tid == 0) {
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tmem_base;
+  const int nt0 = g.t[0].K / 64, ntiles = nt0 + (g.nterms > 1 ? g.t[1].K / 64 : 0);
+  auto put3 = [&](uint32_t base, uint32_t term_bytes, uint32_t off, const float4 &v) {
+    uint32_t wa[3], wb[3];
+    split3_pair(v.x, v.y, wa);
+    split3_pair(v.z, v.w, wb);
+#pragma unroll
+    for (int t = 0; t < 3; ++t)
+      *reinterpret_cast<uint2 *>(sm + base + t * term_bytes + off) = make_uint2(wa[t], wb[t]);
+  };
+  bool ok = true;
   for (int i = 0; i < ntiles; ++i) {
-    __syncthreads();  // previous tile consumed
-    tile.store(term_of(i), sA, sB, tid);
+    const GemmTerm &t = i < nt0 ? g.t[0] : g.t[1];
+    const int k0 = (i < nt0 ? i : i - nt0) * 64;
+    const float *A = t.A + slab * t.sA, *B = t.B + slab * t.sB;
+    // this tile's operands into registers (16-byte loads along each operand's contiguous axis)
+    constexpr int NB = N / 16, NQ = N / 4;  // float4s of op(B)^T per thread, per row of n
+    float4 vb[NB], va[4];
+#pragma unroll
+    for (int r = 0; r < NB; ++r) {
+      const int e = tid + bgt::NT * r;
+      vb[r] = t.b_t ? *reinterpret_cast<const float4 *>(B + (size_t)(e >> 4) * t.ldb + k0 +
+                                                         4 * (e & 15))           // (n, k)
+                    : *reinterpret_cast<const float4 *>(B + (size_t)(k0 + e / NQ) * t.ldb +
+                                                         4 * (e % NQ));          // (k, n)
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int e = tid + bgt::NT * r;
+      const float4 v = t.a_t ? *reinterpret_cast<const float4 *>(
+                                   A + (size_t)(k0 + (e >> 4)) * t.lda + 4 * (e & 15))  // (k, m)
+                             : *reinterpret_cast<const float4 *>(
+                                   A + (size_t)(e >> 4) * t.lda + k0 + 4 * (e & 15));   // (m, k)
+      va[r] = make_float4(t.alpha * v.x, t.alpha * v.y, t.alpha * v.z, t.alpha * v.w);
+    }
+    // the previous tile's products are done with the shared-memory operands
+    if (i > 0 && !mbar_wait(&bar_mma, (i - 1) & 1)) ok = false;
+    tc_fence_after();
+#pragma unroll
+    for (int r = 0; r < NB; ++r) {
+      const int e = tid + bgt::NT * r;
+      put3(0, bgt::TA,
+           t.b_t ? sw128_off(e >> 4, 4 * (e & 15), 128) : sw128_off(e / NQ, 4 * (e % NQ), 64),
+           vb[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int e = tid + bgt::NT * r;
+      put3(bgt::SB, bgt::TB, sw128_off(e >> 4, 4 * (e & 15), 64), va[r]);
+    }
+    fence_async_smem();
+    tc_fence_before();
     __syncthreads();
-    if (i + 1 < ntiles) {
-      const GemmTerm &t = term_of(i + 1);
-      tile.load(t, t.A + slab * t.sA, t.B + slab * t.sB, k0_of(i + 1), tid);
-    }
-#pragma unroll 4
-    for (int kk = 0; kk < GKT; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4 *>(sA + kk * GPA + 8 * ty);
-      const float4 a1 = *reinterpret_cast<const float4 *>(sA + kk * GPA + 8 * ty + 4);
-      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      float bv[NJ];
+    tc_fence_after();
+    if (tid == 0 && ok) {
+      const uint32_t id = idesc_bf16(128, 64, t.b_t ? 0 : 1, t.a_t ? 1 : 0);
 #pragma unroll
-      for (int q = 0; q < NJ; q += 4) {
-        const float4 b4 = *reinterpret_cast<const float4 *>(sB + kk * PB + tx * NJ + q);
-        bv[q] = b4.x; bv[q + 1] = b4.y; bv[q + 2] = b4.z; bv[q + 3] = b4.w;
-      }
+      for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
+        for (int a = 0; a < 3; ++a)
 #pragma unroll
-        for (int jj = 0; jj < NJ; ++jj) acc[r][jj] = fmaf(av[r], bv[jj], acc[r][jj]);
+          for (int b = 0; a + b < 3; ++b) {
+            const uint32_t ta = sb + a * bgt::TA, tbb = sb + bgt::SB + b * bgt::TB;
+            const uint64_t ad = t.b_t ? desc_kmajor(ta, 128, kk) : desc_mnmajor(ta, 64, kk);
+            const uint64_t bd = t.a_t ? desc_mnmajor(tbb, 64, kk) : desc_kmajor(tbb, 64, kk);
+            mma_bf16(tb, ad, bd, id, (i > 0 || kk > 0 || a > 0 || b > 0) ? 1u : 0u);
+          }
+      mma_commit(&bar_mma);
     }
   }
-  float *Cm = g.Cm + slab * g.sC;
+  if (!mbar_wait(&bar_mma, (ntiles - 1) & 1)) ok = false;
+  tc_fence_after();
+  // C[m][n]: lane quadrant warp % 4 holds n = 32 (warp % 4) + lane, warp / 4 the half of m
+  if (ok && (warp & 3) * 32 < N) {
+    float v[32];
+    tmem_ld32(tmem_addr(tb, (warp & 3) * 32, 32 * (warp >> 2)), v);
+    tmem_wait_ld();
+    float *Cm = g.Cm + slab * g.sC;
+    const int n = (warp & 3) * 32 + lane;
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    const int m = 8 * ty + r;
-#pragma unroll
-    for (int q = 0; q < NJ; q += 4) {
-      const int n = tx * NJ + q;
-      float v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const bool keep = g.mask == 0 || (g.mask == 1 ? n + u <= m : n + u < m);
-        v[u] = keep ? acc[r][q + u] : 0.f;
-      }
-      *reinterpret_cast<float4 *>(Cm + (size_t)m * N + n) = make_float4(v[0], v[1], v[2], v[3]);
+    for (int j = 0; j < 32; ++j) {
+      const int m = 32 * (warp >> 2) + j;
+      const bool keep = g.mask == 0 || (g.mask == 1 ? n <= m : n < m);
+      Cm[(size_t)m * N + n] = keep ? v[j] : 0.f;
     }
+  } else if (!ok && lane == 0) {
+    atomicOr(&g_bwd_err, kErrTimeout);
   }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, 64);
 }
 
 // ---------------------------------------------------------------------------
@@ -741,7 +756,12 @@ cudaError_t gemm(const GemmTerm &t0, const GemmTerm *t1, float *Cm, int mask, in
   g.Cm = Cm;
   g.sC = sC ? sC : (size_t)C * N;
   g.mask = mask;
-  kda_bwd_gemm<N><<<dim3(mc, H), GTHREADS, 0, st>>>(g, H, meta);
+  // every contraction depth is C, dk or dv: a multiple of the 64-deep tile
+  if (t0.K % 64 != 0 || (t1 && t1->K % 64 != 0)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_gemm_tc<N>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bgt::DYN);
+  if (e != cudaSuccess) return e;
+  kda_bwd_gemm_tc<N><<<dim3(mc, H), bgt::NT, bgt::DYN, st>>>(g, H, meta);
   return cudaGetLastError();
 }
 
@@ -852,6 +872,15 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
 }
 
 }  // namespace
+
+cudaError_t bwd_take_error(unsigned *bits) {
+  unsigned v = 0, z = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_bwd_err, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbol(g_bwd_err, &z, sizeof(unsigned));
+  *bits = v;
+  return e;
+}
 
 size_t chunk_bwd_ws_bytes(int64_t T_total, int n_seq, int H, int dk, int dv) {
   return chunk_ws_bytes(T_total, n_seq, H, dk, dv) + bwd_extra_bytes(T_total, n_seq, H, dk, dv);

@@ -243,6 +243,7 @@ kda_status api_fail(kda_status st, const char *fmt, ...);
 cudaError_t chunk_take_error(unsigned *bits);
 cudaError_t decode_take_error(unsigned *bits);
 cudaError_t scan_take_error(unsigned *bits);
+cudaError_t bwd_take_error(unsigned *bits);
 cudaError_t selftest_take_error(unsigned *bits);
 
 }  // namespace kda
