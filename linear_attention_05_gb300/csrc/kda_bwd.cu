@@ -510,10 +510,56 @@ __global__ void __launch_bounds__(256) kda_bwd_solve(const float *__restrict__ A
 
 // ---------------------------------------------------------------------------
 // Finishing kernel, one block per (chunk, head): from the chunk-level cotangents
-// to the token gradients. Warp w handles token rows w, w + 8, ...; lane l the key
-// channels l + 32 i and value channels l + 32 i.
+// to the token gradients. Warp w handles token rows w, w + 8, ...; lane l the NI = dk / 32
+// consecutive key channels NI l .. NI l + NI - 1 and the NJ = dv / 32 consecutive value
+// channels NJ l .., so that every global access of a row is one 8- or 16-byte vector. The
+// per-channel rows in shared memory hold channel c at position (c % NI) 32 + c / NI: the
+// row-wise accesses (lane l, i) and the column-wise serial sums (thread = position) are then
+// both free of bank conflicts.
+template <int N>
+__device__ __forceinline__ void ldv(const float *p, float (&v)[N]) {
+  if constexpr (N == 4) {
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w;
+  } else {
+    const float2 a = *reinterpret_cast<const float2 *>(p);
+    v[0] = a.x, v[1] = a.y;
+  }
+}
+template <int N>
+__device__ __forceinline__ void ldv(const __nv_bfloat16 *p, float (&v)[N]) {
+  if constexpr (N == 4) {
+    const uint2 a = *reinterpret_cast<const uint2 *>(p);
+    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&a.x));
+    const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&a.y));
+    v[0] = x.x, v[1] = x.y, v[2] = y.x, v[3] = y.y;
+  } else {
+    const uint32_t a = *reinterpret_cast<const uint32_t *>(p);
+    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&a));
+    v[0] = x.x, v[1] = x.y;
+  }
+}
+template <int N>
+__device__ __forceinline__ void stv(float *p, const float (&v)[N]) {
+  if constexpr (N == 4)
+    *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  else
+    *reinterpret_cast<float2 *>(p) = make_float2(v[0], v[1]);
+}
+template <int N>
+__device__ __forceinline__ void stv(__nv_bfloat16 *p, const float (&v)[N]) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+  if constexpr (N == 4) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+    *reinterpret_cast<uint2 *>(p) =
+        make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+  } else {
+    *reinterpret_cast<uint32_t *>(p) = *reinterpret_cast<const uint32_t *>(&a);
+  }
+}
+
 template <int DK, int DV, typename Tio>
-__global__ void __launch_bounds__(256) kda_bwd_finish(
+__global__ void __launch_bounds__(256, 3) kda_bwd_finish(
     const Tio *__restrict__ q, const Tio *__restrict__ k, const Tio *__restrict__ v,
     const Tio *__restrict__ la, const Tio *__restrict__ beta, const Tio *__restrict__ gate,
     const Tio *__restrict__ d_out, Tio *__restrict__ dq, Tio *__restrict__ dk, Tio *__restrict__ dv, Tio *__restrict__ dla,
@@ -525,12 +571,12 @@ __global__ void __launch_bounds__(256) kda_bwd_finish(
     const float *__restrict__ Sbg, const float *__restrict__ dSbg, const float *__restrict__ Og) {
   constexpr int LK = DK + 1, NI = DK / 32, NJ = DV / 32;
   extern __shared__ float smem[];
-  float *sG = smem;             // [C][LK]  running log-decay G
-  float *sdG = sG + C * LK;     // [C][LK]  dL/dG
+  float *sG = smem;             // [C][LK]  running log-decay G (by position)
+  float *sdG = sG + C * LK;     // [C][LK]  dL/dG (by position)
   float *sB = sdG + C * LK;     // [C]      beta
-  float *sDc = sB + C;          // [DK]     e^{G_C}
-  float *sdD = sDc + DK;        // [DK]     dL/d e^{G_C} from the state hand-off
-  float *sGCp = sdD + DK;       // [8][DK]  per-warp partial dL/dG_C
+  float *sDc = sB + C;          // [DK]     e^{G_C} (by position)
+  float *sdD = sDc + DK;        // [DK]     dL/d e^{G_C} from the state hand-off (by position)
+  float *sGCp = sdD + DK;       // [8][DK]  per-warp partial dL/dG_C (by position)
   const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (meta->invalid || ci >= meta->total_chunks) return;
@@ -539,6 +585,8 @@ __global__ void __launch_bounds__(256) kda_bwd_finish(
   chunk_rows(cu, fixed_len, n_seq, off, ci, &s, &t0, &len);
   const size_t slab = (size_t)ci * H + h;
   const bool l2 = (flags & KDA_QK_L2NORM) != 0;
+  auto pos = [](int c) { return (c % NI) * 32 + c / NI; };   // channel -> position
+  auto chan = [](int p) { return NI * (p & 31) + (p >> 5); };  // position -> channel
 
   const bool logits = (flags & KDA_GATE_LOGITS) != 0;
   if (tid < C) sB[tid] = tid < len ? prep_beta(bf(beta[(size_t)(t0 + tid) * H + h]), flags) : 0.f;
@@ -561,26 +609,38 @@ __global__ void __launch_bounds__(256) kda_bwd_finish(
     for (int m = 0; m < NV; ++m) {
       const int e = 8 * (tid + 256 * m), r = e / DK, c = e % DK;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) sG[r * LK + c + u] = r < len ? prep_log_alpha(lv[m][u], flags) : 0.f;
+      for (int u = 0; u < 8; ++u)
+        sG[r * LK + pos(c + u)] = r < len ? prep_log_alpha(lv[m][u], flags) : 0.f;
+    }
+  }
+  // dL/d e^{G_C}[c] = sum_j dS'[c][j] S[c][j]: two channels per step, NJ values per lane each
+  for (int c = warp; c < DK; c += 16) {
+    float a0[NJ], b0[NJ], a1[NJ], b1[NJ];
+    ldv(dSbg + (slab * DK + c) * DV + NJ * lane, a0);
+    ldv(Sbg + (slab * DK + c) * DV + NJ * lane, b0);
+    ldv(dSbg + (slab * DK + c + 8) * DV + NJ * lane, a1);
+    ldv(Sbg + (slab * DK + c + 8) * DV + NJ * lane, b1);
+    float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < NJ; ++u) {
+      x0 = fmaf(a0[u], b0[u], x0);
+      x1 = fmaf(a1[u], b1[u], x1);
+    }
+    x0 = wsum(x0);
+    x1 = wsum(x1);
+    if (lane == 0) {
+      sdD[pos(c)] = x0;
+      sdD[pos(c + 8)] = x1;
     }
   }
   __syncthreads();
-  if (tid < DK) {
-    const int c = tid;
+  if (tid < DK) {  // position tid
     float G = 0.f;
     for (int r = 0; r < C; ++r) {
-      G += sG[r * LK + c];
-      sG[r * LK + c] = G;
+      G += sG[r * LK + tid];
+      sG[r * LK + tid] = G;
     }
-    sDc[c] = expf(G);
-  }
-  // dL/d e^{G_C}[c] = sum_j dS'[c][j] S[c][j]
-  for (int c = warp; c < DK; c += 8) {
-    const float *sb = Sbg + (slab * DK + c) * DV, *dsb = dSbg + (slab * DK + c) * DV;
-    float acc = 0.f;
-    for (int j = lane; j < DV; j += 32) acc = fmaf(dsb[j], sb[j], acc);
-    acc = wsum(acc);
-    if (lane == 0) sdD[c] = acc;
+    sDc[tid] = expf(G);
   }
   __syncthreads();
 
@@ -590,16 +650,23 @@ __global__ void __launch_bounds__(256) kda_bwd_finish(
   for (int r = warp; r < C; r += 8) {
     if (r >= len) {
 #pragma unroll
-      for (int i = 0; i < NI; ++i) sdG[r * LK + lane + 32 * i] = 0.f;
+      for (int i = 0; i < NI; ++i) sdG[r * LK + 32 * i + lane] = 0.f;
       continue;
     }
     const size_t tok = (size_t)(t0 + r) * H + h;
     const float b = sB[r];
-    float kn[NI], qn[NI], sk = 0.f, sq = 0.f;
+    const size_t rowk = (slab * C + r) * DK + NI * lane;
+    float kn[NI], qn[NI], y[NI], y2[NI], dKh[NI], dQt[NI], dKd[NI];
+    ldv(k + tok * DK + NI * lane, kn);
+    ldv(q + tok * DK + NI * lane, qn);
+    ldv(Yg + rowk, y);
+    ldv(dBkg + rowk, y2);
+    ldv(dKhg + rowk, dKh);
+    ldv(dQtg + rowk, dQt);
+    ldv(dKdg + rowk, dKd);
+    float sk = 0.f, sq = 0.f;
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-      kn[i] = bf(k[tok * DK + lane + 32 * i]);
-      qn[i] = bf(q[tok * DK + lane + 32 * i]);
       sk = fmaf(kn[i], kn[i], sk);
       sq = fmaf(qn[i], qn[i], sq);
     }
@@ -613,20 +680,19 @@ __global__ void __launch_bounds__(256) kda_bwd_finish(
         qn[i] *= rq;
       }
     }
-    const size_t rowk = (slab * C + r) * DK;
     float dkn[NI], dqn[NI], dbk = 0.f;
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-      const int c = lane + 32 * i;
-      const float G = sG[r * LK + c], eP = expf(G), eN = expf(-G), Dc = sDc[c];
+      const int p = 32 * i + lane;
+      const float G = sG[r * LK + p], eP = expf(G), eN = expf(-G), Dc = sDc[p];
       const float Kt = kn[i] * eP, Kh = kn[i] * eN, Qt = qn[i] * eP, Kd = Kh * Dc;
-      const float y = Yg[rowk + c] + dBkg[rowk + c];
-      const float dKt = b * y, dKh = dKhg[rowk + c], dQt = dQtg[rowk + c], dKd = dKdg[rowk + c];
-      dkn[i] = dKt * eP + dKh * eN + dKd * eN * Dc;
-      dqn[i] = dQt * eP;
-      sdG[r * LK + c] = dKt * Kt - dKh * Kh + dQt * Qt - dKd * Kd;
-      gcp[i] = fmaf(dKd, Kd, gcp[i]);
-      dbk = fmaf(Kt, y, dbk);
+      const float yy = y[i] + y2[i];
+      const float dKt = b * yy;
+      dkn[i] = dKt * eP + dKh[i] * eN + dKd[i] * eN * Dc;
+      dqn[i] = dQt[i] * eP;
+      sdG[r * LK + p] = dKt * Kt - dKh[i] * Kh + dQt[i] * Qt - dKd[i] * Kd;
+      gcp[i] = fmaf(dKd[i], Kd, gcp[i]);
+      dbk = fmaf(Kt, yy, dbk);
     }
     if (l2) {  // d(x / |x|) : dx = r (dn - n (n . dn))
       float pk = 0.f, pq = 0.f;
@@ -643,44 +709,52 @@ __global__ void __launch_bounds__(256) kda_bwd_finish(
         dqn[i] = rq * (dqn[i] - qn[i] * pq);
       }
     }
-#pragma unroll
-    for (int i = 0; i < NI; ++i) {
-      dk[tok * DK + lane + 32 * i] = to_out<Tio>(dkn[i]);
-      dq[tok * DK + lane + 32 * i] = to_out<Tio>(dqn[i]);
-    }
-    const size_t rowv = (slab * C + r) * DV;
+    stv(dk + tok * DK + NI * lane, dkn);
+    stv(dq + tok * DK + NI * lane, dqn);
+    const size_t rowv = (slab * C + r) * DV + NJ * lane;
+    float vv[NJ], g[NJ], dvv[NJ];
+    ldv(v + tok * DV + NJ * lane, vv);
+    ldv(dBvg + rowv, g);
     float dbv = 0.f;
 #pragma unroll
-    for (int i = 0; i < NJ; ++i) {
-      const int j = lane + 32 * i;
-      const float g = dBvg[rowv + j];
-      dbv = fmaf(bf(v[tok * DV + j]), g, dbv);
-      dv[tok * DV + j] = to_out<Tio>(b * g);
-      if (dgate) {
-        float dg = scale * bf(d_out[tok * DV + j]) * Og[rowv + j];
-        if (logits) {  // d sigmoid(x) / dx = s (1 - s)
-          const float gs = sigmoid_f(bf(gate[tok * DV + j]));
-          dg *= gs * (1.f - gs);
+    for (int j = 0; j < NJ; ++j) {
+      dbv = fmaf(vv[j], g[j], dbv);
+      dvv[j] = b * g[j];
+    }
+    stv(dv + tok * DV + NJ * lane, dvv);
+    if (dgate) {
+      float dov[NJ], ov[NJ], dg[NJ];
+      ldv(d_out + tok * DV + NJ * lane, dov);
+      ldv(Og + rowv, ov);
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) dg[j] = scale * dov[j] * ov[j];
+      if (logits) {  // d sigmoid(x) / dx = s (1 - s)
+        float gv[NJ];
+        ldv(gate + tok * DV + NJ * lane, gv);
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          const float gs = sigmoid_f(gv[j]);
+          dg[j] *= gs * (1.f - gs);
         }
-        dgate[tok * DV + j] = to_out<Tio>(dg);
       }
+      stv(dgate + tok * DV + NJ * lane, dg);
     }
     float db = wsum(dbk) + wsum(dbv);
     if (logits) db *= b * (1.f - b);
     if (lane == 0) dbeta[tok] = to_out<Tio>(db);
   }
 #pragma unroll
-  for (int i = 0; i < NI; ++i) sGCp[warp * DK + lane + 32 * i] = gcp[i];
+  for (int i = 0; i < NI; ++i) sGCp[warp * DK + 32 * i + lane] = gcp[i];
   __syncthreads();
-  if (tid < DK) {
-    const int c = tid;
-    float dGC = sdD[c] * sDc[c];
+  if (tid < DK) {  // position tid, channel chan(tid)
+    const int c = chan(tid);
+    float dGC = sdD[tid] * sDc[tid];
 #pragma unroll
-    for (int w = 0; w < 8; ++w) dGC += sGCp[w * DK + c];
+    for (int w = 0; w < 8; ++w) dGC += sGCp[w * DK + tid];
     // G_r = sum_{s <= r} log_alpha_s and G_C = G_63: reverse cumulative sum
     float acc = 0.f;
     for (int r = C - 1; r >= 0; --r) {
-      acc += sdG[r * LK + c];
+      acc += sdG[r * LK + tid];
       if (r < len) {
         const size_t gi = ((size_t)(t0 + r) * H + h) * DK + c;
         float d = acc + dGC;
