@@ -1,5 +1,6 @@
-// Chunked backward pass of KDA (fp32; the batched contractions on the tensor cores at
-// fp32-level accuracy, the serial passes and element-wise work on CUDA cores).
+// Chunked backward pass of KDA (fp32; the batched contractions and, at dk = dv = 128, the
+// reverse state pass on the tensor cores at fp32-level accuracy; the forward replay, the
+// substitutions and the element-wise work on CUDA cores).
 //
 // Gradients of L = <dO, o> + <dS_final, S_final> with respect to q, k, v,
 // log_alpha, beta, gate and the initial state. The forward is the chunked form
@@ -259,6 +260,257 @@ template <int DK>
 constexpr size_t bwd_state_smem() {
   return sizeof(float) * (DK * (RBV + 4) + C * (RBV + 4) + C * (DK + 4) + DK * (C + 4) + DK);
 }
+
+// The reverse state pass on the tensor cores (dk = dv = 128), one CTA (256 threads) per
+// (sequence, head). The state is kept transposed in tensor memory, dS^T[j][c] (lane = value
+// column j, column = key c), and each chunk, last to first, runs
+//   dU^T  = dS'^T K_d^T + V1^T                    (M = 128 j, N = 64 tokens, K = 128 c)
+//   dS^T  = Diag(e^{G_C}) dS'^T + R^T - dU^T W     (M = 128 j, N = 128 c,     K = 64 tokens)
+// with the accumulator of the second product pre-loaded with the first two terms. Every fp32
+// operand enters as three bf16 terms (v0 = bf16(v), v1 = bf16(v - v0), v2 = bf16(v - v0 - v1))
+// and the six products of terms a + b <= 2 are accumulated in fp32, so the pass keeps fp32-level
+// accuracy. Shared memory: the A operand (the terms of dS'^T, then of dU^T, K-major) and the B
+// operands (the terms of K_d, K-major, and of W, MN-major: both are [token][c] in memory).
+namespace bst {
+constexpr int NT = 256;
+constexpr uint32_t SA = 0;            // 3 x 32 KB: dS'^T terms (128 x 128), later dU^T (128 x 64)
+constexpr uint32_t SB1 = 3 * 32768;   // 3 x 16 KB: K_d terms, 64 token rows x 128 c
+constexpr uint32_t SB2 = SB1 + 3 * 16384;  // 3 x 16 KB: W terms, 64 token rows x 128 c
+constexpr uint32_t DYN = SB2 + 3 * 16384 + 1024;
+constexpr int TS = 0;                 // tensor memory: the state dS^T in columns [0, 128)
+constexpr int TU = 128;               //   dU^T in columns [128, 192)
+}  // namespace bst
+
+// (a, b) -> the bf16x2 words of the pair's three terms
+__device__ __forceinline__ void bst_split(float a, float b, uint32_t (&w)[3]) {
+  const __nv_bfloat162 t0 = __floats2bfloat162_rn(a, b);
+  const float2 f0 = __bfloat1622float2(t0);
+  const float ra = a - f0.x, rb = b - f0.y;
+  const __nv_bfloat162 t1 = __floats2bfloat162_rn(ra, rb);
+  const float2 f1 = __bfloat1622float2(t1);
+  const __nv_bfloat162 t2 = __floats2bfloat162_rn(ra - f1.x, rb - f1.y);
+  w[0] = *reinterpret_cast<const uint32_t *>(&t0);
+  w[1] = *reinterpret_cast<const uint32_t *>(&t1);
+  w[2] = *reinterpret_cast<const uint32_t *>(&t2);
+}
+
+__global__ void __launch_bounds__(bst::NT, 1) kda_bwd_state_tc(
+    const float *__restrict__ dS_final, float *__restrict__ dS_init,
+    const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len, int H,
+    const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
+    const float *__restrict__ Wg, const float *__restrict__ Kdg, const float *__restrict__ Dg,
+    const float *__restrict__ V1g, const float *__restrict__ Rg, float *__restrict__ dSb,
+    float *__restrict__ dUg) {
+  using namespace tc;
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_mma;
+  __shared__ uint32_t tmem_base;
+  if (meta->invalid) return;
+  uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sb = smem_u32(sm);
+  const int chain = blockIdx.x, s = chain / H, h = chain % H, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31, quad = warp & 3, hh = warp >> 2;
+  // this thread: value column j (tensor-memory lane), key columns 64 hh .. + 64 of the state,
+  // tokens 32 hh .. + 32 of dU
+  const int j = quad * 32 + lane;
+  int64_t ls;
+  if (cu) ls = (int64_t)cu[s + 1] - cu[s];
+  else ls = fixed_len;
+  const int nchunks = (int)((ls + C - 1) / C);
+  const size_t st0 = ((size_t)s * H + h) * D * D;  // this chain's [dk][dv] state slab
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, 256);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = tmem_base;
+  const uint32_t trow = tmem_addr(tb, quad * 32, 0);
+  {  // the state entering the last chunk: dS_final (or 0)
+    float v[32];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        const int c = 64 * hh + 32 * half + u;
+        v[u] = dS_final ? dS_final[st0 + (size_t)c * D + j] : 0.f;
+      }
+      tmem_st32(trow + bst::TS + 64 * hh + 32 * half, v);
+    }
+    tmem_wait_st();
+  }
+  uint32_t phase = 0;
+  bool ok = true;
+  for (int jc = nchunks - 1; jc >= 0; --jc) {
+    const size_t slab = (size_t)(off[s] + jc) * H + h;
+    if (tid == 0 && jc > 0) {  // the next chunk's operands into L2
+      const size_t sp = slab - H;
+      prefetch_l2(Wg + sp * C * D, C * D * 4);
+      prefetch_l2(Kdg + sp * C * D, C * D * 4);
+      prefetch_l2(V1g + sp * C * D, C * D * 4);
+      prefetch_l2(Rg + sp * D * D, D * D * 4);
+    }
+    // R^T and V1^T of this thread's row (read in steps 2 and 4), issued first
+    float rr[64], v1[32];
+#pragma unroll
+    for (int u = 0; u < 64; ++u) rr[u] = Rg[(slab * D + 64 * hh + u) * D + j];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) v1[u] = V1g[(slab * C + 32 * hh + u) * D + j];
+    // (1) the terms of K_d and W ([token][c], 16-byte loads) into their B tiles
+    {
+      const float *Kd = Kdg + slab * C * D, *W = Wg + slab * C * D;
+      float4 xk[8], xw[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        xk[m] = *reinterpret_cast<const float4 *>(Kd + 4 * (tid + bst::NT * m));
+        xw[m] = *reinterpret_cast<const float4 *>(W + 4 * (tid + bst::NT * m));
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int e = tid + bst::NT * m;
+        const uint32_t o = sw128_off(e >> 5, 4 * (e & 31), 64);
+        uint32_t wa[3], wb[3];
+        bst_split(xk[m].x, xk[m].y, wa);
+        bst_split(xk[m].z, xk[m].w, wb);
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+          *reinterpret_cast<uint2 *>(sm + bst::SB1 + t * 16384 + o) = make_uint2(wa[t], wb[t]);
+        bst_split(xw[m].x, xw[m].y, wa);
+        bst_split(xw[m].z, xw[m].w, wb);
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+          *reinterpret_cast<uint2 *>(sm + bst::SB2 + t * 16384 + o) = make_uint2(wa[t], wb[t]);
+      }
+    }
+    // (2) dS' (the state leaving chunk jc) out; its terms into the A tile; the accumulator
+    //     pre-loaded with e^{G_C} dS' + R
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int cb = 64 * hh + 32 * half;  // first key column of this half
+      float v[32], dd[32];
+      tmem_ld32(trow + bst::TS + cb, v);
+#pragma unroll
+      for (int u = 0; u < 32; u += 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(Dg + slab * D + cb + u);
+        dd[u] = x.x, dd[u + 1] = x.y, dd[u + 2] = x.z, dd[u + 3] = x.w;
+      }
+      tmem_wait_ld();
+#pragma unroll
+      for (int u = 0; u < 32; ++u) dSb[(slab * D + cb + u) * D + j] = v[u];
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        uint32_t w[3][4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          uint32_t t3[3];
+          bst_split(v[8 * q8 + 2 * p], v[8 * q8 + 2 * p + 1], t3);
+          w[0][p] = t3[0], w[1][p] = t3[1], w[2][p] = t3[2];
+        }
+        const uint32_t o = sw128_chunk(j, (cb >> 3) + q8, 128);
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+          *reinterpret_cast<uint4 *>(sm + bst::SA + t * 32768 + o) =
+              make_uint4(w[t][0], w[t][1], w[t][2], w[t][3]);
+      }
+#pragma unroll
+      for (int u = 0; u < 32; ++u) v[u] = fmaf(dd[u], v[u], rr[32 * half + u]);
+      tmem_st32(trow + bst::TS + cb, v);
+    }
+    tmem_wait_st();
+    fence_async_smem();
+    tc_fence_before();
+    ok = named_bar_and(1, bst::NT, ok);
+    tc_fence_after();
+    if (!ok) break;
+    // (3) dU^T = dS'^T K_d^T (six products of terms per K step)
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+        for (int a = 0; a < 3; ++a)
+#pragma unroll
+          for (int b = 0; a + b < 3; ++b)
+            mma_bf16(tb + bst::TU, desc_kmajor(sb + bst::SA + a * 32768, 128, kk),
+                     desc_kmajor(sb + bst::SB1 + b * 16384, 64, kk), id,
+                     (kk > 0 || a > 0 || b > 0) ? 1u : 0u);
+      mma_commit(&bar_mma);
+    }
+    ok = mbar_wait(&bar_mma, phase) && ok;
+    phase ^= 1u;
+    tc_fence_after();
+    // (4) dU = dU^T + V1^T out; its terms into the A tile (K = the chunk's 64 tokens)
+    if (ok) {
+      float u32[32];
+      tmem_ld32(trow + bst::TU + 32 * hh, u32);
+      tmem_wait_ld();
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        u32[u] += v1[u];
+        dUg[(slab * C + 32 * hh + u) * D + j] = u32[u];
+      }
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        uint32_t w[3][4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          uint32_t t3[3];
+          bst_split(u32[8 * q8 + 2 * p], u32[8 * q8 + 2 * p + 1], t3);
+          w[0][p] = t3[0], w[1][p] = t3[1], w[2][p] = t3[2];
+        }
+        const uint32_t o = sw128_chunk(j, 4 * hh + q8, 128);
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+          *reinterpret_cast<uint4 *>(sm + bst::SA + t * 16384 + o) =
+              make_uint4(w[t][0], w[t][1], w[t][2], w[t][3]);
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    ok = named_bar_and(1, bst::NT, ok);
+    tc_fence_after();
+    if (!ok) break;
+    // (5) dS^T = (e^{G_C} dS'^T + R^T) - dU^T W
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(128, 128, 0, 1) | kNegateA;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int a = 0; a < 3; ++a)
+#pragma unroll
+          for (int b = 0; a + b < 3; ++b)
+            mma_bf16(tb + bst::TS, desc_kmajor(sb + bst::SA + a * 16384, 128, kk),
+                     desc_mnmajor(sb + bst::SB2 + b * 16384, 64, kk), id, 1u);
+      mma_commit(&bar_mma);
+    }
+    ok = mbar_wait(&bar_mma, phase) && ok;
+    phase ^= 1u;
+    tc_fence_after();
+    ok = named_bar_and(1, bst::NT, ok);
+    if (!ok) break;
+  }
+  if (ok && dS_init) {  // the state entering the first chunk
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float v[32];
+      tmem_ld32(trow + bst::TS + 64 * hh + 32 * half, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int u = 0; u < 32; ++u) dS_init[st0 + (size_t)(64 * hh + 32 * half + u) * D + j] = v[u];
+    }
+  }
+  if (!ok && lane == 0) atomicOr(&g_bwd_err, kErrTimeout);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, 256);
+}
+
 
 // ---------------------------------------------------------------------------
 // Batched 64-row GEMM over (chunk, head) slabs:
@@ -883,7 +1135,14 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
   for (int r0 = 0; r0 < DK; r0 += C)
     KDA_TRY(gemm<DV>(term(fw.Q + r0, sk, DK, 1, w.dO, sv, DV, 0, C, 1.f), nullptr,
                      w.R + (size_t)r0 * DV, 0, mc, H, fw.meta, st, ss2));
-  {
+  if (DK == 128 && DV == 128) {  // on the tensor cores
+    KDA_TRY(cudaFuncSetAttribute(kda_bwd_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bst::DYN));
+    kda_bwd_state_tc<<<n_seq * H, bst::NT, bst::DYN, st>>>(
+        dSf, dS0, cu, n_seq, fixed_len, H, fw.meta, fw.seq_chunk_off, fw.W, fw.Kd, fw.D, w.V1,
+        w.R, w.dSb, w.dU);
+    KDA_TRY(cudaGetLastError());
+  } else {
     auto kern = kda_bwd_state<DK, DV>;
     constexpr size_t sm = bwd_state_smem<DK>();
     KDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));

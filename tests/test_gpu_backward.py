@@ -74,10 +74,11 @@ def test_backward_ragged_vs_autograd(dk, dv, dtype):
     _check(got, ref, TOL[dtype])
 
 
-def test_backward_without_gate_norm_or_states():
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_without_gate_norm_or_states(d):
     """No gate (no dgate), no L2 norm, zero initial state, no final-state cotangent,
-    fixed-length sequences (cu_seqlens NULL)."""
-    H, dk, dv, n_seq, L = 3, 64, 64, 2, 160
+    fixed-length sequences (cu_seqlens NULL); d = 128 takes the tensor-core reverse pass."""
+    H, dk, dv, n_seq, L = 3, d, d, 2, 160
     x = inputs.tokens(n_seq * L, H, dk, dv, torch.float32, seed=44, device=DEV, with_gate=False)
     d_out, _ = _cotangents(n_seq * L, n_seq, H, dk, dv, torch.float32, 45, final=False)
     got = B.chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], None, None, d_out,
