@@ -746,8 +746,7 @@ def bench_backward(dev, pk, stream, reps=5):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
     return {"workload": "backward of prefill B=4 T=4096 H=16 dk=dv=128, bf16 in/out, fp32 "
-                        "arithmetic (batched contractions and the reverse state pass on the tensor cores, forward "
-                        "replay on CUDA cores)",
+                        "arithmetic (batched contractions and both state passes on the tensor cores)",
             "value": round(T / (ms * 1e-3) / 1e6, 3), "unit": "Mtok/s", "ms": round(ms, 3),
             "workspace_bytes": ws.numel(), "gpu_launches": 18 * reps}
 

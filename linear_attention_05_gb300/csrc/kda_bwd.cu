@@ -1,6 +1,6 @@
 // Chunked backward pass of KDA (fp32; the batched contractions and, at dk = dv = 128, the
-// reverse state pass on the tensor cores at fp32-level accuracy; the forward replay, the
-// substitutions and the element-wise work on CUDA cores).
+// forward replay's and the reverse state pass on the tensor cores at fp32-level accuracy; the
+// preparation, the substitutions and the element-wise work on CUDA cores).
 //
 // Gradients of L = <dO, o> + <dS_final, S_final> with respect to q, k, v,
 // log_alpha, beta, gate and the initial state. The forward is the chunked form
@@ -261,12 +261,16 @@ constexpr size_t bwd_state_smem() {
   return sizeof(float) * (DK * (RBV + 4) + C * (RBV + 4) + C * (DK + 4) + DK * (C + 4) + DK);
 }
 
-// The reverse state pass on the tensor cores (dk = dv = 128), one CTA (256 threads) per
-// (sequence, head). The state is kept transposed in tensor memory, dS^T[j][c] (lane = value
-// column j, column = key c), and each chunk, last to first, runs
+// The state passes of the backward on the tensor cores (dk = dv = 128), one CTA (256 threads)
+// per (sequence, head), the state kept transposed in tensor memory (lane = value column j,
+// column = key c). Reverse (FWD = false), each chunk last to first:
 //   dU^T  = dS'^T K_d^T + V1^T                    (M = 128 j, N = 64 tokens, K = 128 c)
 //   dS^T  = Diag(e^{G_C}) dS'^T + R^T - dU^T W     (M = 128 j, N = 128 c,     K = 64 tokens)
-// with the accumulator of the second product pre-loaded with the first two terms. Every fp32
+// writing dS' and dU per chunk. The forward replay (FWD = true), first to last, is the same
+// pair of products with the roles of W and K_d swapped:
+//   U^T   = U~^T - S^T W^T,      S'^T = Diag(e^{G_C}) S^T + U^T K_d
+// writing S and U per chunk. The accumulator of the second product is pre-loaded with its
+// first terms. Every fp32
 // operand enters as three bf16 terms (v0 = bf16(v), v1 = bf16(v - v0), v2 = bf16(v - v0 - v1))
 // and the six products of terms a + b <= 2 are accumulated in fp32, so the pass keeps fp32-level
 // accuracy. Shared memory: the A operand (the terms of dS'^T, then of dU^T, K-major) and the B
@@ -294,13 +298,18 @@ __device__ __forceinline__ void bst_split(float a, float b, uint32_t (&w)[3]) {
   w[2] = *reinterpret_cast<const uint32_t *>(&t2);
 }
 
+// S_first: the state entering the first step (dS_final, or S_0), or null for 0; S_last: where
+// the state after the last step goes (dS_0), or null. B1g, B2g: the [token][c] operands of the
+// first and second product (K_d and W reversed, W and K_d forward); Xg: V1 or U~ ([token][j]);
+// Rg: R ([c][j], reverse only); Sb, Ub: the per-chunk state and dU or U.
+template <bool FWD>
 __global__ void __launch_bounds__(bst::NT, 1) kda_bwd_state_tc(
-    const float *__restrict__ dS_final, float *__restrict__ dS_init,
+    const float *__restrict__ S_first, float *__restrict__ S_last,
     const int32_t *__restrict__ cu, int n_seq, int64_t fixed_len, int H,
     const ChunkMeta *__restrict__ meta, const int *__restrict__ off,
-    const float *__restrict__ Wg, const float *__restrict__ Kdg, const float *__restrict__ Dg,
-    const float *__restrict__ V1g, const float *__restrict__ Rg, float *__restrict__ dSb,
-    float *__restrict__ dUg) {
+    const float *__restrict__ B1g, const float *__restrict__ B2g, const float *__restrict__ Dg,
+    const float *__restrict__ Xg, const float *__restrict__ Rg, float *__restrict__ Sb,
+    float *__restrict__ Ub) {
   using namespace tc;
   constexpr int D = 128;
   extern __shared__ uint8_t smem_raw[];
@@ -332,14 +341,14 @@ __global__ void __launch_bounds__(bst::NT, 1) kda_bwd_state_tc(
   tc_fence_after();
   const uint32_t tb = tmem_base;
   const uint32_t trow = tmem_addr(tb, quad * 32, 0);
-  {  // the state entering the last chunk: dS_final (or 0)
+  {  // the state entering the first step
     float v[32];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
         const int c = 64 * hh + 32 * half + u;
-        v[u] = dS_final ? dS_final[st0 + (size_t)c * D + j] : 0.f;
+        v[u] = S_first ? S_first[st0 + (size_t)c * D + j] : 0.f;
       }
       tmem_st32(trow + bst::TS + 64 * hh + 32 * half, v);
     }
@@ -347,24 +356,25 @@ __global__ void __launch_bounds__(bst::NT, 1) kda_bwd_state_tc(
   }
   uint32_t phase = 0;
   bool ok = true;
-  for (int jc = nchunks - 1; jc >= 0; --jc) {
+  for (int step = 0; step < nchunks; ++step) {
+    const int jc = FWD ? step : nchunks - 1 - step;
     const size_t slab = (size_t)(off[s] + jc) * H + h;
-    if (tid == 0 && jc > 0) {  // the next chunk's operands into L2
-      const size_t sp = slab - H;
-      prefetch_l2(Wg + sp * C * D, C * D * 4);
-      prefetch_l2(Kdg + sp * C * D, C * D * 4);
-      prefetch_l2(V1g + sp * C * D, C * D * 4);
-      prefetch_l2(Rg + sp * D * D, D * D * 4);
+    if (tid == 0 && step + 1 < nchunks) {  // the next chunk's operands into L2
+      const size_t sp = FWD ? slab + H : slab - H;
+      prefetch_l2(B1g + sp * C * D, C * D * 4);
+      prefetch_l2(B2g + sp * C * D, C * D * 4);
+      prefetch_l2(Xg + sp * C * D, C * D * 4);
+      if (!FWD) prefetch_l2(Rg + sp * D * D, D * D * 4);
     }
-    // R^T and V1^T of this thread's row (read in steps 2 and 4), issued first
+    // R^T and V1^T (or U~^T) of this thread's row (read in steps 2 and 4), issued first
     float rr[64], v1[32];
 #pragma unroll
-    for (int u = 0; u < 64; ++u) rr[u] = Rg[(slab * D + 64 * hh + u) * D + j];
+    for (int u = 0; u < 64; ++u) rr[u] = FWD ? 0.f : Rg[(slab * D + 64 * hh + u) * D + j];
 #pragma unroll
-    for (int u = 0; u < 32; ++u) v1[u] = V1g[(slab * C + 32 * hh + u) * D + j];
-    // (1) the terms of K_d and W ([token][c], 16-byte loads) into their B tiles
+    for (int u = 0; u < 32; ++u) v1[u] = Xg[(slab * C + 32 * hh + u) * D + j];
+    // (1) the terms of the two [token][c] operands (16-byte loads) into their B tiles
     {
-      const float *Kd = Kdg + slab * C * D, *W = Wg + slab * C * D;
+      const float *Kd = B1g + slab * C * D, *W = B2g + slab * C * D;
       float4 xk[8], xw[8];
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
@@ -402,7 +412,7 @@ __global__ void __launch_bounds__(bst::NT, 1) kda_bwd_state_tc(
       }
       tmem_wait_ld();
 #pragma unroll
-      for (int u = 0; u < 32; ++u) dSb[(slab * D + cb + u) * D + j] = v[u];
+      for (int u = 0; u < 32; ++u) Sb[(slab * D + cb + u) * D + j] = v[u];
 #pragma unroll
       for (int q8 = 0; q8 < 4; ++q8) {
         uint32_t w[3][4];
@@ -419,7 +429,7 @@ __global__ void __launch_bounds__(bst::NT, 1) kda_bwd_state_tc(
               make_uint4(w[t][0], w[t][1], w[t][2], w[t][3]);
       }
 #pragma unroll
-      for (int u = 0; u < 32; ++u) v[u] = fmaf(dd[u], v[u], rr[32 * half + u]);
+      for (int u = 0; u < 32; ++u) v[u] = FWD ? dd[u] * v[u] : fmaf(dd[u], v[u], rr[32 * half + u]);
       tmem_st32(trow + bst::TS + cb, v);
     }
     tmem_wait_st();
@@ -452,8 +462,8 @@ __global__ void __launch_bounds__(bst::NT, 1) kda_bwd_state_tc(
       tmem_wait_ld();
 #pragma unroll
       for (int u = 0; u < 32; ++u) {
-        u32[u] += v1[u];
-        dUg[(slab * C + 32 * hh + u) * D + j] = u32[u];
+        u32[u] = FWD ? v1[u] - u32[u] : u32[u] + v1[u];
+        Ub[(slab * C + 32 * hh + u) * D + j] = u32[u];
       }
 #pragma unroll
       for (int q8 = 0; q8 < 4; ++q8) {
@@ -478,7 +488,7 @@ __global__ void __launch_bounds__(bst::NT, 1) kda_bwd_state_tc(
     if (!ok) break;
     // (5) dS^T = (e^{G_C} dS'^T + R^T) - dU^T W
     if (tid == 0) {
-      const uint32_t id = idesc_bf16(128, 128, 0, 1) | kNegateA;
+      const uint32_t id = idesc_bf16(128, 128, 0, 1) | (FWD ? 0u : kNegateA);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
@@ -495,14 +505,14 @@ __global__ void __launch_bounds__(bst::NT, 1) kda_bwd_state_tc(
     ok = named_bar_and(1, bst::NT, ok);
     if (!ok) break;
   }
-  if (ok && dS_init) {  // the state entering the first chunk
+  if (ok && S_last) {  // the state after the last step
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       float v[32];
       tmem_ld32(trow + bst::TS + 64 * hh + 32 * half, v);
       tmem_wait_ld();
 #pragma unroll
-      for (int u = 0; u < 32; ++u) dS_init[st0 + (size_t)(64 * hh + 32 * half + u) * D + j] = v[u];
+      for (int u = 0; u < 32; ++u) S_last[st0 + (size_t)(64 * hh + 32 * half + u) * D + j] = v[u];
     }
   }
   if (!ok && lane == 0) atomicOr(&g_bwd_err, kErrTimeout);
@@ -1112,10 +1122,20 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
   ps.Kh = w.Kh; ps.Bk = w.Bk; ps.A = w.A;
   KDA_TRY(launch_prep(q, k, v, la, beta, cu, n_seq, T_total, H, DK, DV, flags, dt, fw, true, st,
                       ps));
-  StateSave ss;  // the replay saves S and U only; O comes from a batched GEMM below
-  ss.Sb = w.Sb; ss.Ub = w.Ub;
-  KDA_TRY(launch_state_pass(0, flags, nullptr, nullptr, S0, nullptr, nullptr, nullptr, cu, n_seq,
-                            T_total, H, DK, DV, scale, dt, fw, st, CkptOut(), ss));
+  // the forward replay saves S and U per chunk only; O comes from a batched GEMM below
+  if (DK == 128 && DV == 128) {  // on the tensor cores
+    KDA_TRY(cudaFuncSetAttribute(kda_bwd_state_tc<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bst::DYN));
+    kda_bwd_state_tc<true><<<n_seq * H, bst::NT, bst::DYN, st>>>(
+        S0, nullptr, cu, n_seq, fixed_len, H, fw.meta, fw.seq_chunk_off, fw.W, fw.Kd, fw.D, fw.U,
+        nullptr, w.Sb, w.Ub);
+    KDA_TRY(cudaGetLastError());
+  } else {
+    StateSave ss;
+    ss.Sb = w.Sb; ss.Ub = w.Ub;
+    KDA_TRY(launch_state_pass(0, flags, nullptr, nullptr, S0, nullptr, nullptr, nullptr, cu,
+                              n_seq, T_total, H, DK, DV, scale, dt, fw, st, CkptOut(), ss));
+  }
   kda_bwd_dO<DV, Tio><<<dim3(mc, H), 256, 0, st>>>((const Tio *)d_out, (const Tio *)gate, cu,
                                                    n_seq, fixed_len, H, scale, flags, fw.meta,
                                                    fw.seq_chunk_off, w.dO);
@@ -1136,10 +1156,10 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
     KDA_TRY(gemm<DV>(term(fw.Q + r0, sk, DK, 1, w.dO, sv, DV, 0, C, 1.f), nullptr,
                      w.R + (size_t)r0 * DV, 0, mc, H, fw.meta, st, ss2));
   if (DK == 128 && DV == 128) {  // on the tensor cores
-    KDA_TRY(cudaFuncSetAttribute(kda_bwd_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)bst::DYN));
-    kda_bwd_state_tc<<<n_seq * H, bst::NT, bst::DYN, st>>>(
-        dSf, dS0, cu, n_seq, fixed_len, H, fw.meta, fw.seq_chunk_off, fw.W, fw.Kd, fw.D, w.V1,
+    KDA_TRY(cudaFuncSetAttribute(kda_bwd_state_tc<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bst::DYN));
+    kda_bwd_state_tc<false><<<n_seq * H, bst::NT, bst::DYN, st>>>(
+        dSf, dS0, cu, n_seq, fixed_len, H, fw.meta, fw.seq_chunk_off, fw.Kd, fw.W, fw.D, w.V1,
         w.R, w.dSb, w.dU);
     KDA_TRY(cudaGetLastError());
   } else {
