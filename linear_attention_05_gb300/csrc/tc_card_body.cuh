@@ -171,12 +171,19 @@ __device__ __forceinline__ bool card_body(const CardIn &in, const CardGroup &G, 
       for (int u = 0; u < 8; ++u) {
         ssk[i] = fmaf(kk[u], kk[u], ssk[i]);
         ssq[i] = fmaf(qq[u], qq[u], ssq[i]);
-        // with gate logits: log(alpha) = max(-e^a, log 1/2)
-        la8[i][u] = r >= len ? 0.f
-                    : (flags & KDA_GATE_LOGITS) ? fmaxf(-__expf(la8[i][u]), kLogHalf)
-                                                : la8[i][u];
-        if (dbg && r < len && !(la8[i][u] >= kLogAlphaMin && la8[i][u] <= 0.f))
-          atomicOr(G.err, kErrPrecondition);
+      }
+      // with gate logits: log(alpha) = max(-e^a, log 1/2) (uniform branches: the exponentials
+      // and the checks are not evaluated when their flag is off)
+      if (flags & KDA_GATE_LOGITS)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) la8[i][u] = fmaxf(-__expf(la8[i][u]), kLogHalf);
+      if (dbg && r < len)
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (!(la8[i][u] >= kLogAlphaMin && la8[i][u] <= 0.f)) atomicOr(G.err, kErrPrecondition);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (r >= len) la8[i][u] = 0.f;
         tot[u] += la8[i][u];
       }
     }
