@@ -39,17 +39,17 @@ using namespace tcl;
 constexpr int A_X1 = 0;          // 32768: [k|Kt ; q|Qt] 128-row tile; later P (64-row) at 0
 constexpr int A_LA = 32768;      // 16384: log_alpha -> Kh -> Kd (64-row tile)
 constexpr int A_V = 49152;       // 16384: V (64-row tile)
-constexpr int A_M = 65536;       // 16640: M (fp32, 64 x 65 padded); later W^T (128-row x 64)
-constexpr int A_T = 82176;       // 16640: T (fp32, 64 x 65 padded)
-constexpr int A_TB = 99328;      // 8192:  T' = T diag(b) (bf16 64-row tile); later identity
-constexpr int A_XT = 107520;     // 3072:  block temporaries of the solve
+constexpr int A_M = 65536;       // 17408: M (fp32, 64 x 68 padded); later W^T (128-row x 64)
+constexpr int A_T = 82944;       // 17408: T (fp32, 64 x 68 padded)
+constexpr int A_TB = 100352;     // 8192:  T' = T diag(b) (bf16 64-row tile); later identity
+constexpr int A_XT = 108544;     // 3072:  block temporaries of the solve
 constexpr int A_UL = 82944;      // 16384: after GEMM 2, the low bf16 part of Ut^T (128-row
-                                 // K-major tile) in the dead T (and the gap after it)
-constexpr int A_BODY = 110592;        // bytes of one group region
+                                 // K-major tile) in the dead T
+constexpr int A_BODY = 111616;        // bytes of one group region
 constexpr int A_DYN = A_BODY + 1024;  // one group, with alignment slack
 constexpr uint32_t A_TMA_BYTES = 8 * 8192;
 
-__device__ __forceinline__ int mix(int r, int c) { return r * 65 + c; }
+__device__ __forceinline__ int mix(int r, int c) { return r * 68 + c; }
 
 // The inputs of the cards.
 struct CardIn {
@@ -284,9 +284,11 @@ __device__ __forceinline__ bool card_body(const CardIn &in, const CardGroup &G, 
       float *Ms = reinterpret_cast<float *>(sm + A_M);
       const float b = s_b[r];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 32; i += 4) {  // 16-byte stores (68-float rows)
         const int col = 32 * grp + i;
-        Ms[mix(r, col)] = col < r ? b * a[i] : 0.f;
+        *reinterpret_cast<float4 *>(Ms + mix(r, col)) =
+            make_float4(col < r ? b * a[i] : 0.f, col + 1 < r ? b * a[i + 1] : 0.f,
+                        col + 2 < r ? b * a[i + 2] : 0.f, col + 3 < r ? b * a[i + 3] : 0.f);
       }
     }
     // Kh is no longer read by the tensor cores: Kd = Kh * e^{G_C} in place
@@ -335,20 +337,34 @@ __device__ __forceinline__ bool card_body(const CardIn &in, const CardGroup &G, 
       const int ro = 16 * (a + 1), co = 16 * a;
       float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {  // X = M_{a+1,a} T_aa; T_aa[k][j] = 0 for k < j
-        const float t = k >= j ? Ts[mix(co + k, co + j)] : 0.f;
-        x0 = fmaf(Ms[mix(ro + i0, co + k)], t, x0);
-        x1 = fmaf(Ms[mix(ro + i0 + 1, co + k)], t, x1);
+      for (int k4 = 0; k4 < 16; k4 += 4) {  // X = M_{a+1,a} T_aa; T_aa[k][j] = 0 for k < j
+        const float4 m0 = *reinterpret_cast<const float4 *>(Ms + mix(ro + i0, co + k4));
+        const float4 m1 = *reinterpret_cast<const float4 *>(Ms + mix(ro + i0 + 1, co + k4));
+        const float a0[4] = {m0.x, m0.y, m0.z, m0.w}, a1[4] = {m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int k = k4 + u;
+          const float t = k >= j ? Ts[mix(co + k, co + j)] : 0.f;
+          x0 = fmaf(a0[u], t, x0);
+          x1 = fmaf(a1[u], t, x1);
+        }
       }
       Xt[(tid >> 7) * 256 + i0 * 16 + j] = x0;
       Xt[(tid >> 7) * 256 + (i0 + 1) * 16 + j] = x1;
       named_bar(G.bar_main, 256);
       float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {  // T_{a+1,a} = -T_{a+1,a+1} X; T_bb[i][k] = 0 for k > i
-        const float xk = Xt[(tid >> 7) * 256 + k * 16 + j];
-        if (k <= i0) y0 = fmaf(Ts[mix(ro + i0, ro + k)], xk, y0);
-        if (k <= i0 + 1) y1 = fmaf(Ts[mix(ro + i0 + 1, ro + k)], xk, y1);
+      for (int k4 = 0; k4 < 16; k4 += 4) {  // T_{a+1,a} = -T_{a+1,a+1} X; T_bb[i][k] = 0, k > i
+        const float4 t0 = *reinterpret_cast<const float4 *>(Ts + mix(ro + i0, ro + k4));
+        const float4 t1 = *reinterpret_cast<const float4 *>(Ts + mix(ro + i0 + 1, ro + k4));
+        const float b0[4] = {t0.x, t0.y, t0.z, t0.w}, b1[4] = {t1.x, t1.y, t1.z, t1.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int k = k4 + u;
+          const float xk = Xt[(tid >> 7) * 256 + k * 16 + j];
+          if (k <= i0) y0 = fmaf(b0[u], xk, y0);
+          if (k <= i0 + 1) y1 = fmaf(b1[u], xk, y1);
+        }
       }
       Ts[mix(ro + i0, co + j)] = -y0;
       Ts[mix(ro + i0 + 1, co + j)] = -y1;
@@ -360,10 +376,20 @@ __device__ __forceinline__ bool card_body(const CardIn &in, const CardGroup &G, 
       // Y = M_21 T_11, T_11[k][j] = 0 for k < j (not stored there: masked). The loop runs
       // over all k in every lane: a lane-dependent start made the warps diverge.
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float t = k >= j ? Ts[mix(k, j)] : 0.f;
+      for (int k4 = 0; k4 < 32; k4 += 4) {
+        float mr[4][4];  // rows 32 + i0 + u, columns k4 .. k4 + 3 (warp-uniform 16-byte loads)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) y[u] = fmaf(Ms[mix(32 + i0 + u, k)], t, y[u]);
+        for (int u = 0; u < 4; ++u) {
+          const float4 m = *reinterpret_cast<const float4 *>(Ms + mix(32 + i0 + u, k4));
+          mr[u][0] = m.x, mr[u][1] = m.y, mr[u][2] = m.z, mr[u][3] = m.w;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int k = k4 + kk;
+          const float t = k >= j ? Ts[mix(k, j)] : 0.f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) y[u] = fmaf(mr[u][kk], t, y[u]);
+        }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) Ts[mix(i0 + u, 32 + j)] = y[u];
@@ -372,12 +398,22 @@ __device__ __forceinline__ bool card_body(const CardIn &in, const CardGroup &G, 
       // T_21 = -T_22 Y, T_22[i][k] = 0 for k > i (masked): every warp runs all 32 steps, so
       // the warps with the lower rows no longer hold the barrier for those with the higher
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float yk = Ts[mix(k, 32 + j)];
+      for (int k4 = 0; k4 < 32; k4 += 4) {
+        float tr[4][4];  // rows 32 + i0 + u, columns 32 + k4 .. + 3 (masked below)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float t = k <= i0 + u ? Ts[mix(32 + i0 + u, 32 + k)] : 0.f;
-          z[u] = fmaf(t, yk, z[u]);
+          const float4 v = *reinterpret_cast<const float4 *>(Ts + mix(32 + i0 + u, 32 + k4));
+          tr[u][0] = v.x, tr[u][1] = v.y, tr[u][2] = v.z, tr[u][3] = v.w;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int k = k4 + kk;
+          const float yk = Ts[mix(k, 32 + j)];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float t = k <= i0 + u ? tr[u][kk] : 0.f;
+            z[u] = fmaf(t, yk, z[u]);
+          }
         }
       }
 #pragma unroll
@@ -389,11 +425,15 @@ __device__ __forceinline__ bool card_body(const CardIn &in, const CardGroup &G, 
       const int r = tid >> 2, qc = tid & 3;
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
-        float e[8];
+        float e[8], tv[8];
+        const float4 v0 = *reinterpret_cast<const float4 *>(Ts + mix(r, qc * 16 + ch * 8));
+        const float4 v1 = *reinterpret_cast<const float4 *>(Ts + mix(r, qc * 16 + ch * 8 + 4));
+        tv[0] = v0.x, tv[1] = v0.y, tv[2] = v0.z, tv[3] = v0.w;
+        tv[4] = v1.x, tv[5] = v1.y, tv[6] = v1.z, tv[7] = v1.w;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const int j = qc * 16 + ch * 8 + u;
-          e[u] = (j <= r) ? Ts[mix(r, j)] * s_b[j] : 0.f;
+          e[u] = (j <= r) ? tv[u] * s_b[j] : 0.f;
         }
         *reinterpret_cast<uint4 *>(sm + A_TB + sw128_chunk(r, qc * 2 + ch, 64)) = pack8(e);
       }
