@@ -540,10 +540,12 @@ __device__ __forceinline__ bool card_body(const CardIn &in, const CardGroup &G, 
             pack8(t32 + ch * 8);
     };
     // twelve 4 KB staging blocks in regions dead by now: the Qt rows and Kt's second atom
-    // column [8192, 32768), W^T [65536, 81920) and the identity [99328, 107520); P, Kd and
-    // both Ut^T tiles stay intact for GEMMs 3b/4b
+    // column [A_X1 + 8192, A_LA), W^T [A_M, A_M + 16384) and the identity [A_TB, A_TB + 8192);
+    // P, Kd and both Ut^T tiles stay intact for GEMMs 3b/4b
+    static_assert(A_X1 + 8192 + 6 * 4096 == A_LA && A_TB + 8192 <= A_XT, "staging blocks");
     auto stage_block = [&](int i) -> uint8_t * {
-      return sm + (i < 6 ? 8192 + i * 4096 : (i < 10 ? 65536 + (i - 6) * 4096 : 99328 + (i - 10) * 4096));
+      return sm + (i < 6 ? A_X1 + 8192 + i * 4096
+                         : (i < 10 ? A_M + (i - 6) * 4096 : A_TB + (i - 10) * 4096));
     };
     uint8_t *blk = stage_block(grp * 4 + quad);  // (quadrant, atom grp)
     uint8_t *blk2 = stage_block(8 + quad);       // (quadrant, atom 2), shared by grp 0/1
