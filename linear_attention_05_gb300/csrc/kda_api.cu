@@ -40,26 +40,6 @@ struct Tracer {
   }
 };
 
-// Library-owned stream (one per device) that carries the trailing cards of a split prefill.
-cudaError_t split_card_stream(cudaStream_t *out) {
-  constexpr int kMaxDev = 64;
-  static std::mutex mu;
-  static cudaStream_t streams[kMaxDev] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (streams[dev] == nullptr) {
-    cudaStream_t s = nullptr;
-    e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
-    if (e != cudaSuccess) return e;
-    streams[dev] = s;
-  }
-  *out = streams[dev];
-  return cudaSuccess;
-}
-
 kda_status fail(kda_status st, const char *fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -119,6 +99,27 @@ kda_status common_checks(int64_t T_total, int n_seq, int H, int dk, int dv, int 
 }  // namespace
 
 namespace kda {
+// Library-owned stream (one per device): the trailing cards of a split prefill, and the
+// backward's work beside its forward replay.
+cudaError_t side_stream(cudaStream_t *out) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static cudaStream_t streams[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (streams[dev] == nullptr) {
+    cudaStream_t s = nullptr;
+    e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return e;
+    streams[dev] = s;
+  }
+  *out = streams[dev];
+  return cudaSuccess;
+}
+
 // Sets this thread's kda_last_error_string() message and returns `st`.
 kda_status api_fail(kda_status st, const char *fmt, ...) {
   va_list ap;
@@ -178,7 +179,7 @@ static kda_status split_prefill(const void *q, const void *k, const void *v,
                                 int64_t T_total, int H, float scale, unsigned flags,
                                 const kda::ChunkWs &ws, cudaStream_t s, Tracer &tr) {
   cudaStream_t side = nullptr;
-  kda_status st = cuda_status(split_card_stream(&side), "card stream");
+  kda_status st = cuda_status(kda::side_stream(&side), "card stream");
   if (st != KDA_OK) return st;
   cudaEvent_t ev[2] = {nullptr, nullptr};
   for (cudaEvent_t &e : ev) {

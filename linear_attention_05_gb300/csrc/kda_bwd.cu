@@ -1101,28 +1101,38 @@ cudaError_t gemm(const GemmTerm &t0, const GemmTerm *t1, float *Cm, int mask, in
   return cudaGetLastError();
 }
 
-template <int DK, int DV, typename Tio>
-cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, const void *beta,
-                  const void *gate, const float *S0, const void *d_out, const float *dSf,
-                  void *dq, void *dk, void *dv, void *dla, void *dbeta, void *dgate, float *dS0,
-                  const int32_t *cu, int n_seq, int64_t T_total, int H, float scale,
-                  unsigned flags, kda_dtype dt, void *ws_raw, cudaStream_t st) {
-  BwdWs w = bwd_ws_carve(ws_raw, T_total, n_seq, H, DK, DV);
-  const ChunkWs &fw = w.fw;
-  const int mc = fw.max_chunks;
-  const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
-  cudaError_t e;
 #define KDA_TRY(x)              \
   do {                          \
     e = (x);                    \
     if (e != cudaSuccess) return e; \
   } while (0)
-  KDA_TRY(launch_chunk_table(cu, n_seq, T_total, fw, st));
+
+// The prep, both state passes and the products between them, on two streams (the schedule is
+// drawn in bwd_t). `forked` is set once the side stream depends on st; the caller joins it back.
+template <int DK, int DV, typename Tio>
+cudaError_t mid_passes(const void *q, const void *k, const void *v, const void *la,
+                       const void *beta, const void *gate, const float *S0, const void *d_out,
+                       const float *dSf, float *dS0, const int32_t *cu, int n_seq, int64_t T_total,
+                       int H, float scale, unsigned flags, kda_dtype dt, const BwdWs &w,
+                       cudaStream_t st, cudaStream_t side, cudaEvent_t (&ev)[4], bool &forked) {
+  const ChunkWs &fw = w.fw;
+  const int mc = fw.max_chunks;
+  const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
+  cudaError_t e;
+  KDA_TRY(cudaEventRecord(ev[0], st));  // the chunk table is in place
+  KDA_TRY(cudaStreamWaitEvent(side, ev[0], 0));
+  forked = true;
+  // side: the gated output gradient (needs only the chunk table)
+  kda_bwd_dO<DV, Tio><<<dim3(mc, H), 256, 0, side>>>((const Tio *)d_out, (const Tio *)gate, cu,
+                                                     n_seq, fixed_len, H, scale, flags, fw.meta,
+                                                     fw.seq_chunk_off, w.dO);
+  KDA_TRY(cudaGetLastError());
   PrepSave ps;
   ps.Kh = w.Kh; ps.Bk = w.Bk; ps.A = w.A;
   KDA_TRY(launch_prep(q, k, v, la, beta, cu, n_seq, T_total, H, DK, DV, flags, dt, fw, true, st,
                       ps));
-  // the forward replay saves S and U per chunk only; O comes from a batched GEMM below
+  KDA_TRY(cudaEventRecord(ev[1], st));  // the prep's outputs are in place
+  // st: the forward replay saves S and U per chunk only; O comes from a batched GEMM below
   if (DK == 128 && DV == 128) {  // on the tensor cores
     KDA_TRY(cudaFuncSetAttribute(kda_bwd_state_tc<true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bst::DYN));
@@ -1136,29 +1146,22 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
     KDA_TRY(launch_state_pass(0, flags, nullptr, nullptr, S0, nullptr, nullptr, nullptr, cu,
                               n_seq, T_total, H, DK, DV, scale, dt, fw, st, CkptOut(), ss));
   }
-  kda_bwd_dO<DV, Tio><<<dim3(mc, H), 256, 0, st>>>((const Tio *)d_out, (const Tio *)gate, cu,
-                                                   n_seq, fixed_len, H, scale, flags, fw.meta,
-                                                   fw.seq_chunk_off, w.dO);
-  KDA_TRY(cudaGetLastError());
   const size_t sk = (size_t)C * DK, sv = (size_t)C * DV, scc = (size_t)C * C,
                ss2 = (size_t)DK * DV;
-  // O = Q~ S + P U (pre-gate chunk output, for dg)
-  {
-    GemmTerm t2 = term(fw.P, scc, C, 0, w.Ub, sv, DV, 0, C, 1.f);
-    KDA_TRY(gemm<DV>(term(fw.Q, sk, DK, 0, w.Sb, ss2, DV, 0, DK, 1.f), &t2, w.O, 0, mc, H,
-                     fw.meta, st));
-  }
-  // the state-independent parts of the reverse step: V1 = P^T dO, R = Q~^T dO (dk rows,
+  // side: the state-independent parts of the reverse step: V1 = P^T dO, R = Q~^T dO (dk rows,
   // computed in 64-row halves)
+  KDA_TRY(cudaStreamWaitEvent(side, ev[1], 0));
   KDA_TRY(gemm<DV>(term(fw.P, scc, C, 1, w.dO, sv, DV, 0, C, 1.f), nullptr, w.V1, 0, mc, H,
-                   fw.meta, st));
+                   fw.meta, side));
   for (int r0 = 0; r0 < DK; r0 += C)
     KDA_TRY(gemm<DV>(term(fw.Q + r0, sk, DK, 1, w.dO, sv, DV, 0, C, 1.f), nullptr,
-                     w.R + (size_t)r0 * DV, 0, mc, H, fw.meta, st, ss2));
+                     w.R + (size_t)r0 * DV, 0, mc, H, fw.meta, side, ss2));
+  KDA_TRY(cudaEventRecord(ev[2], side));  // dO, V1 and R are in place
+  // side: the reverse state pass
   if (DK == 128 && DV == 128) {  // on the tensor cores
     KDA_TRY(cudaFuncSetAttribute(kda_bwd_state_tc<false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bst::DYN));
-    kda_bwd_state_tc<false><<<n_seq * H, bst::NT, bst::DYN, st>>>(
+    kda_bwd_state_tc<false><<<n_seq * H, bst::NT, bst::DYN, side>>>(
         dSf, dS0, cu, n_seq, fixed_len, H, fw.meta, fw.seq_chunk_off, fw.Kd, fw.W, fw.D, w.V1,
         w.R, w.dSb, w.dU);
     KDA_TRY(cudaGetLastError());
@@ -1166,10 +1169,17 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
     auto kern = kda_bwd_state<DK, DV>;
     constexpr size_t sm = bwd_state_smem<DK>();
     KDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-    kern<<<dim3(n_seq * H, DV / RBV), 256, sm, st>>>(dSf, dS0, cu, n_seq, fixed_len, H, fw.meta,
-                                                     fw.seq_chunk_off, fw.W, fw.Kd, fw.D, w.V1,
-                                                     w.R, w.dSb, w.dU);
+    kern<<<dim3(n_seq * H, DV / RBV), 256, sm, side>>>(dSf, dS0, cu, n_seq, fixed_len, H,
+                                                       fw.meta, fw.seq_chunk_off, fw.W, fw.Kd,
+                                                       fw.D, w.V1, w.R, w.dSb, w.dU);
     KDA_TRY(cudaGetLastError());
+  }
+  // st, after the replay and R: O = Q~ S + P U (pre-gate chunk output, for dg)
+  KDA_TRY(cudaStreamWaitEvent(st, ev[2], 0));
+  {
+    GemmTerm t2 = term(fw.P, scc, C, 0, w.Ub, sv, DV, 0, C, 1.f);
+    KDA_TRY(gemm<DV>(term(fw.Q, sk, DK, 0, w.Sb, ss2, DV, 0, DK, 1.f), &t2, w.O, 0, mc, H,
+                     fw.meta, st));
   }
   // dP = lower(dO U^T)
   KDA_TRY(gemm<C>(term(w.dO, sv, DV, 0, w.Ub, sv, DV, 1, DV, 1.f), nullptr, w.dP, 1, mc, H,
@@ -1180,6 +1190,50 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
     KDA_TRY(gemm<DK>(term(w.dO, sv, DV, 0, w.Sb, ss2, DV, 1, DV, 1.f), &t2, w.dQt, 0, mc, H,
                      fw.meta, st));
   }
+  return cudaSuccess;
+}
+
+template <int DK, int DV, typename Tio>
+cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, const void *beta,
+                  const void *gate, const float *S0, const void *d_out, const float *dSf,
+                  void *dq, void *dk, void *dv, void *dla, void *dbeta, void *dgate, float *dS0,
+                  const int32_t *cu, int n_seq, int64_t T_total, int H, float scale,
+                  unsigned flags, kda_dtype dt, void *ws_raw, cudaStream_t st) {
+  BwdWs w = bwd_ws_carve(ws_raw, T_total, n_seq, H, DK, DV);
+  const ChunkWs &fw = w.fw;
+  const int mc = fw.max_chunks;
+  const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
+  cudaError_t e;
+  KDA_TRY(launch_chunk_table(cu, n_seq, T_total, fw, st));
+  // The two state passes each run one CTA per (sequence, head) and do not depend on each other,
+  // so they run side by side, together with the batched products around them:
+  //   stream st:    prep -> forward replay ---------------------> O -> dP -> dQ~ -> (join) ...
+  //   side stream:  dO ---------> V1, R (after the prep) -> reverse pass ------------^
+  // The replay directly follows the prep in st, so its CTAs reach the SMs before those of the
+  // products on the side stream; O waits for R, so the reverse pass (next in the side stream)
+  // is placed before O's CTAs fill the GPU. Events fork the side stream off st and join it
+  // back, also after a failed launch, so the call stays ordered on st (and can be captured).
+  cudaStream_t side = nullptr;
+  KDA_TRY(side_stream(&side));
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  for (cudaEvent_t &x : ev) {
+    e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
+    if (e != cudaSuccess) break;
+  }
+  bool forked = false;
+  if (e == cudaSuccess) e = mid_passes<DK, DV, Tio>(q, k, v, la, beta, gate, S0, d_out, dSf, dS0,
+                                                    cu, n_seq, T_total, H, scale, flags, dt, w,
+                                                    st, side, ev, forked);
+  if (forked) {  // join the side stream back into st
+    cudaError_t j = cudaEventRecord(ev[3], side);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(st, ev[3], 0);
+    if (e == cudaSuccess) e = j;
+  }
+  for (cudaEvent_t x : ev)
+    if (x) cudaEventDestroy(x);
+  if (e != cudaSuccess) return e;
+  const size_t sk = (size_t)C * DK, sv = (size_t)C * DV, scc = (size_t)C * C,
+               ss2 = (size_t)DK * DV;
   // dK_d = U dS'^T
   KDA_TRY(gemm<DK>(term(w.Ub, sv, DV, 0, w.dSb, ss2, DV, 1, DV, 1.f), nullptr, w.dKd, 0, mc, H,
                    fw.meta, st));

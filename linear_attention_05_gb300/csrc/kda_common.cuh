@@ -236,6 +236,9 @@ cudaError_t launch_chunk_bwd(const void *q, const void *k, const void *v, const 
                              int n_seq, int64_t T_total, int H, int dk_, int dv_, float scale,
                              unsigned flags, kda_dtype dt, void *ws, cudaStream_t st);
 
+// The library's second stream on the current device (created once, non-blocking).
+cudaError_t side_stream(cudaStream_t *out);
+
 // Sets the calling thread's kda_last_error_string() message; returns `st`.
 kda_status api_fail(kda_status st, const char *fmt, ...);
 
