@@ -146,24 +146,50 @@ __global__ void __launch_bounds__(1024) kda_chunk_table(const int32_t *cu, int n
 }
 
 // ---------------------------------------------------------------------------
-// Stage A: per (chunk, head) preparation. 256 threads.
+// Stage A: per (chunk, head) preparation. 256 threads, one CTA per (chunk, head), two CTAs per
+// SM (115,456 bytes of shared memory at dk = dv = 128), so that one CTA's global loads and
+// stores overlap the other's arithmetic.
+// The [64][d] fp32 tiles are stored without padding, the 16-byte chunk x of row r at x ^ (r & 7):
+// a warp reading four channels of eight different rows, or one channel of a row per lane, hits
+// every bank once. The products read their operands as 16-byte vectors (one shared-memory
+// instruction per four FMAs of a thread). V takes the tile of Qt once the Gram products have
+// read it; the log-alpha partial sums of the decay take the Gram tile before it is written.
+template <int DK, int DV>
+struct PrepLayout {
+  static constexpr int DQV = DK > DV ? DK : DV;
+  static constexpr int KT = 0, KH = KT + C * DK, QV = KH + C * DK, A = QV + C * DQV,
+                       B = A + C * C, GC = B + C;
+  static constexpr int FLOATS = GC + DK;
+  static_assert(256 <= C * C, "the decay's partial sums fit in the Gram tile");
+};
+
+// element (r, c) of a swizzled tile with D floats per row; v4: the 16-byte chunk holding c
+template <int D>
+__device__ __forceinline__ int swz(int r, int c) {
+  return r * D + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3));
+}
+__device__ __forceinline__ float4 lds4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void sts4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ float4 mul4(float4 x, float b) {
+  return make_float4(x.x * b, x.y * b, x.z * b, x.w * b);
+}
+
 template <int DK, int DV, typename Tin>
-__global__ void __launch_bounds__(256) kda_prep_simt(
+__global__ void __launch_bounds__(256, 2) kda_prep_simt(
     const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
     const Tin *__restrict__ la, const Tin *__restrict__ beta, const int32_t *__restrict__ cu,
     int n_seq, int64_t fixed_len, int H, unsigned flags, const ChunkMeta *__restrict__ meta,
     const int *__restrict__ off, float *__restrict__ Wg, float *__restrict__ Ug,
     float *__restrict__ Qg, float *__restrict__ Kdg, float *__restrict__ Pg,
     float *__restrict__ Dg, int need_q, PrepSave save) {
-  constexpr int LK = DK + 1, LV = DV + 1, LA = C + 1;
-  extern __shared__ float smem[];
-  float *sKt = smem;             // [C][LK]  k*e^{G}, then b*Kt, then W
-  float *sKh = sKt + C * LK;     // [C][LK]  k*e^{-G}
-  float *sQt = sKh + C * LK;     // [C][LK]  q*e^{G}
-  float *sV = sQt + C * LK;      // [C][LV]  v, then b*v, then Ut
-  float *sA = sV + C * LV;       // [C][LA]  strict-lower diag(b) Kt Kh^T
-  float *sB = sA + C * LA;       // [C]      beta
-  float *sGC = sB + C;           // [DK]     e^{G_C}
+  using Ly = PrepLayout<DK, DV>;
+  extern __shared__ __align__(16) float smem[];
+  float *sKt = smem + Ly::KT;  // [C][DK]  log alpha, then k*e^{G}, then b*Kt, then W
+  float *sKh = smem + Ly::KH;  // [C][DK]  k, then k*e^{-G}
+  float *sQV = smem + Ly::QV;  // [C][DK]  q, then q*e^{G}; then [C][DV] b*v, then Ut
+  float *sA = smem + Ly::A;    // [C][C]   strict-lower diag(b) Kt Kh^T (first: partial sums)
+  float *sB = smem + Ly::B;    // [C]      beta
+  float *sGC = smem + Ly::GC;  // [DK]     e^{G_C}
 
   const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   if (meta->invalid || ci >= meta->total_chunks) return;
@@ -173,12 +199,16 @@ __global__ void __launch_bounds__(256) kda_prep_simt(
   const int j = ci - off[s];
   const int64_t t0 = ts + (int64_t)j * C;
   const int len = (int)min((int64_t)C, ls - (int64_t)j * C);
+  const size_t slab = (size_t)ci * H + h;
 
-  // load (rows >= len are zero: no write, no read-out, no decay). 8-element vectors, all of a
-  // tensor's loads issued before its shared-memory stores.
+  // load q, k, log alpha and beta (rows >= len are zero: no write, no read-out, no decay),
+  // every load issued before any use. Each row of q and k is held by DK / 8 consecutive lanes,
+  // so the L2 norms are reduced in registers.
   {
-    constexpr int NVK = C * DK / 8 / 256, NVV = C * DV / 8 / 256;
+    constexpr int NVK = C * DK / 8 / 256, LPR = DK / 8;
     float kv[NVK][8], qv[NVK][8], lv[NVK][8];
+    float b = 0.f;
+    if (tid < len) b = to_f32(beta[(size_t)(t0 + tid) * H + h]);
 #pragma unroll
     for (int m = 0; m < NVK; ++m) {
       const int e = 8 * (tid + 256 * m), r = e / DK, c = e % DK;
@@ -192,21 +222,127 @@ __global__ void __launch_bounds__(256) kda_prep_simt(
         for (int u = 0; u < 8; ++u) kv[m][u] = qv[m][u] = lv[m][u] = 0.f;
       }
     }
+    if (tid < C) {
+      b = tid < len ? prep_beta(b, flags) : 0.f;
+      if ((flags & KDA_DEBUG_CHECK) && tid < len && !(b >= 0.f && b <= 1.f)) set_err(kErrPrecondition);
+      sB[tid] = b;
+    }
+    if (flags & KDA_QK_L2NORM) {  // rows >= len are zero and stay zero
+#pragma unroll
+      for (int m = 0; m < NVK; ++m) {
+        float sk = 0.f, sq = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          sk = fmaf(kv[m][u], kv[m][u], sk);
+          sq = fmaf(qv[m][u], qv[m][u], sq);
+        }
+#pragma unroll
+        for (int o = 1; o < LPR; o <<= 1) {
+          sk += __shfl_xor_sync(0xffffffffu, sk, o);
+          sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        }
+        const float rk = rsqrtf(sk + kL2Eps), rq = rsqrtf(sq + kL2Eps);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          kv[m][u] *= rk;
+          qv[m][u] *= rq;
+        }
+      }
+    }
 #pragma unroll
     for (int m = 0; m < NVK; ++m) {
       const int e = 8 * (tid + 256 * m), r = e / DK, c = e % DK;
+      float l[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        float l = 0.f;
+        l[u] = 0.f;
         if (r < len) {
-          l = prep_log_alpha(lv[m][u], flags);
-          if ((flags & KDA_DEBUG_CHECK) && !(l >= kLogAlphaMin && l <= 0.f)) set_err(kErrPrecondition);
+          l[u] = prep_log_alpha(lv[m][u], flags);
+          if ((flags & KDA_DEBUG_CHECK) && !(l[u] >= kLogAlphaMin && l[u] <= 0.f)) set_err(kErrPrecondition);
         }
-        sKh[r * LK + c + u] = kv[m][u];
-        sQt[r * LK + c + u] = qv[m][u];
-        sKt[r * LK + c + u] = l;
+      }
+#pragma unroll
+      for (int h4 = 0; h4 < 8; h4 += 4) {
+        const int o = swz<DK>(r, c + h4);
+        sts4(sKh + o, make_float4(kv[m][h4], kv[m][h4 + 1], kv[m][h4 + 2], kv[m][h4 + 3]));
+        sts4(sQV + o, make_float4(qv[m][h4], qv[m][h4 + 1], qv[m][h4 + 2], qv[m][h4 + 3]));
+        sts4(sKt + o, make_float4(l[h4], l[h4 + 1], l[h4 + 2], l[h4 + 3]));
       }
     }
+  }
+  __syncthreads();
+
+  // running log-decay G per key channel and the decayed operands: TPC threads per channel,
+  // each over RPT consecutive rows, offset by the sums of the rows before them
+  {
+    constexpr int TPC = 256 / DK, RPT = C / TPC;
+    const int c = tid % DK, part = tid / DK, rb = part * RPT;
+    float *sPart = sA;
+    float sum = 0.f;
+#pragma unroll 8
+    for (int r = rb; r < rb + RPT; ++r) sum += sKt[swz<DK>(r, c)];
+    sPart[part * DK + c] = sum;
+    __syncthreads();
+    float G = 0.f;
+    for (int p = 0; p < part; ++p) G += sPart[p * DK + c];
+#pragma unroll 4
+    for (int r = rb; r < rb + RPT; ++r) {
+      const int o = swz<DK>(r, c);
+      G += sKt[o];  // log_alpha (0 on padded rows)
+      const float ep = expf(G), en = expf(-G);
+      const float kn = sKh[o];
+      sKt[o] = kn * ep;
+      sKh[o] = kn * en;
+      sQV[o] *= ep;
+    }
+    if (part == TPC - 1) sGC[c] = expf(G);
+  }
+  __syncthreads();
+
+  // Gram blocks: A = strict_lower(diag(b) Kt Kh^T), P = lower(Qt Kh^T). Thread (rg, cg) owns
+  // rows rg + 16 i and columns cg + 16 j (i, j < 4); a step reads four channels of each row.
+  {
+    const int rg = tid >> 4, cg = tid & 15;
+    float a[4][4] = {}, p[4][4] = {};
+#pragma unroll 2
+    for (int c = 0; c < DK; c += 4) {
+      float4 kt[4], qt[4], kh[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        kt[i] = lds4(sKt + swz<DK>(rg + 16 * i, c));
+        qt[i] = lds4(sQV + swz<DK>(rg + 16 * i, c));
+        kh[i] = lds4(sKh + swz<DK>(cg + 16 * i, c));
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          a[i][jj] = fmaf(kt[i].x, kh[jj].x, a[i][jj]);
+          a[i][jj] = fmaf(kt[i].y, kh[jj].y, a[i][jj]);
+          a[i][jj] = fmaf(kt[i].z, kh[jj].z, a[i][jj]);
+          a[i][jj] = fmaf(kt[i].w, kh[jj].w, a[i][jj]);
+          p[i][jj] = fmaf(qt[i].x, kh[jj].x, p[i][jj]);
+          p[i][jj] = fmaf(qt[i].y, kh[jj].y, p[i][jj]);
+          p[i][jj] = fmaf(qt[i].z, kh[jj].z, p[i][jj]);
+          p[i][jj] = fmaf(qt[i].w, kh[jj].w, p[i][jj]);
+        }
+    }
+    float *Pout = Pg + slab * C * C;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int r = rg + 16 * i, c2 = cg + 16 * jj;
+        sA[r * C + c2] = c2 < r ? sB[r] * a[i][jj] : 0.f;
+        Pout[r * C + c2] = c2 <= r ? p[i][jj] : 0.f;
+      }
+  }
+  __syncthreads();
+
+  // v is loaded while Qt, Kd = Kh * e^{G_C}, e^{G_C} and the save of Kh are written and the
+  // right-hand side Kt is scaled by beta; once every read of Qt is done, b*v takes its tile
+  {
+    constexpr int NVV = C * DV / 8 / 256, NK4 = C * DK / 4 / 256;
     float vv[NVV][8];
 #pragma unroll
     for (int m = 0; m < NVV; ++m) {
@@ -218,134 +354,89 @@ __global__ void __launch_bounds__(256) kda_prep_simt(
         for (int u = 0; u < 8; ++u) vv[m][u] = 0.f;
       }
     }
+    float *Qout = Qg + slab * C * DK, *Kdout = Kdg + slab * C * DK;
+#pragma unroll
+    for (int m = 0; m < NK4; ++m) {
+      const int e = 4 * (tid + 256 * m), r = e / DK, c = e % DK, o = swz<DK>(r, c);
+      const float4 kh = lds4(sKh + o), g = lds4(sGC + c);
+      sts4(Kdout + e, make_float4(kh.x * g.x, kh.y * g.y, kh.z * g.z, kh.w * g.w));
+      if (save.Kh) sts4(save.Kh + slab * C * DK + e, kh);
+      if (need_q) sts4(Qout + e, lds4(sQV + o));
+      sts4(sKt + o, mul4(lds4(sKt + o), sB[r]));
+    }
+    if (tid < DK) Dg[slab * DK + tid] = sGC[tid];
+    __syncthreads();  // Qt is read
 #pragma unroll
     for (int m = 0; m < NVV; ++m) {
       const int e = 8 * (tid + 256 * m), r = e / DV, c = e % DV;
+      const float b = sB[r];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) sV[r * LV + c + u] = vv[m][u];
+      for (int h4 = 0; h4 < 8; h4 += 4)
+        sts4(sQV + swz<DV>(r, c + h4),
+             make_float4(vv[m][h4] * b, vv[m][h4 + 1] * b, vv[m][h4 + 2] * b, vv[m][h4 + 3] * b));
     }
-  }
-  if (tid < C) {
-    float b = tid < len ? prep_beta(to_f32(beta[(size_t)(t0 + tid) * H + h]), flags) : 0.f;
-    if ((flags & KDA_DEBUG_CHECK) && tid < len && !(b >= 0.f && b <= 1.f)) set_err(kErrPrecondition);
-    sB[tid] = b;
-  }
-  __syncthreads();
-
-  // L2 normalisation of q and k rows: one warp per row
-  if (flags & KDA_QK_L2NORM) {
-    const int lane = tid & 31, w = tid >> 5;
-    for (int r = w; r < C; r += 8) {
-      float sk = 0.f, sq = 0.f;
-      for (int c = lane; c < DK; c += 32) {
-        float a = sKh[r * LK + c], b = sQt[r * LK + c];
-        sk += a * a;
-        sq += b * b;
-      }
-      sk = warp_sum(sk);
-      sq = warp_sum(sq);
-      float rk = rsqrtf(sk + kL2Eps), rq = rsqrtf(sq + kL2Eps);
-      for (int c = lane; c < DK; c += 32) {
-        sKh[r * LK + c] *= rk;
-        sQt[r * LK + c] *= rq;
-      }
-    }
-    __syncthreads();
-  }
-
-  // running log-decay G per key channel and the decayed operands
-  if (tid < DK) {
-    const int c = tid;
-    float G = 0.f;
-    for (int r = 0; r < C; ++r) {
-      G += sKt[r * LK + c];  // log_alpha (0 on padded rows)
-      float ep = expf(G), en = expf(-G);
-      float kn = sKh[r * LK + c];
-      sKt[r * LK + c] = kn * ep;
-      sKh[r * LK + c] = kn * en;
-      sQt[r * LK + c] *= ep;
-    }
-    sGC[c] = expf(G);
-  }
-  __syncthreads();
-
-  const size_t slab = (size_t)ci * H + h;
-  // Gram blocks: A = strict_lower(diag(b) Kt Kh^T), P = lower(Qt Kh^T); 4x4 per thread
-  {
-    const int rb = (tid >> 4) * 4, cb = (tid & 15) * 4;
-    float a[4][4] = {}, p[4][4] = {};
-    for (int c = 0; c < DK; ++c) {
-      float kt[4], qt[4], kh[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        kt[i] = sKt[(rb + i) * LK + c];
-        qt[i] = sQt[(rb + i) * LK + c];
-        kh[i] = sKh[(cb + i) * LK + c];
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          a[i][jj] = fmaf(kt[i], kh[jj], a[i][jj]);
-          p[i][jj] = fmaf(qt[i], kh[jj], p[i][jj]);
-        }
-    }
-    float *Pout = Pg + slab * C * C;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        int r = rb + i, c2 = cb + jj;
-        sA[r * LA + c2] = c2 < r ? sB[r] * a[i][jj] : 0.f;
-        Pout[r * C + c2] = c2 <= r ? p[i][jj] : 0.f;
-        if (save.A) save.A[slab * C * C + r * C + c2] = sA[r * LA + c2];
-      }
-  }
-  __syncthreads();
-
-  // write Qt, Kd = Kh * e^{G_C}, e^{G_C}; scale the right-hand sides by beta
-  float *Qout = Qg + slab * C * DK, *Kdout = Kdg + slab * C * DK;
-  for (int e = tid; e < C * DK; e += 256) {
-    int r = e / DK, c = e % DK;
-    if (need_q) Qout[e] = sQt[r * LK + c];
-    Kdout[e] = sKh[r * LK + c] * sGC[c];
-    if (save.Kh) save.Kh[slab * C * DK + e] = sKh[r * LK + c];
-  }
-  if (tid < DK) Dg[slab * DK + tid] = sGC[tid];
-  for (int e = tid; e < C * DK; e += 256) {
-    int r = e / DK, c = e % DK;
-    sKt[r * LK + c] *= sB[r];
-    if (save.Bk) save.Bk[slab * C * DK + e] = sKt[r * LK + c];
-  }
-  for (int e = tid; e < C * DV; e += 256) {
-    int r = e / DV, c = e % DV;
-    sV[r * LV + c] *= sB[r];
   }
   __syncthreads();
 
   // (I + A) X = [b Kt | b V], forward substitution: one thread per column, the column in
   // registers (indices fixed at compile time), each row's dot product in four partial sums
+  // (column i into sum i mod 4), the row of A read as 16-byte vectors. The saved b*Kt column
+  // is written from the registers it is solved in.
   if (tid < DK + DV) {
-    float *col = tid < DK ? sKt + tid : sV + (tid - DK);
-    const int ld = tid < DK ? LK : LV;
+    const bool kcol = tid < DK;
+    const int c = kcol ? tid : tid - DK, D = kcol ? DK : DV;
+    float *base = kcol ? sKt : sQV;
+    int coff[8];  // swizzled offset of column c in a row r with r & 7 = i
+#pragma unroll
+    for (int i = 0; i < 8; ++i) coff[i] = (((c >> 2) ^ i) << 2) | (c & 3);
     float x[C];
 #pragma unroll
-    for (int r = 0; r < C; ++r) x[r] = col[r * ld];
+    for (int r = 0; r < C; ++r) x[r] = base[r * D + coff[r & 7]];
+    if (save.Bk && kcol) {
+      float *bk = save.Bk + slab * C * DK + c;
+#pragma unroll
+      for (int r = 0; r < C; ++r) bk[r * DK] = x[r];
+    }
 #pragma unroll
     for (int r = 1; r < C; ++r) {
-      const float *Ar = sA + r * LA;
+      const float *Ar = sA + r * C;
       float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < r; ++i) p[i & 3] = fmaf(Ar[i], x[i], p[i & 3]);
+      for (int i = 0; i < r; i += 4) {
+        const float4 a4 = lds4(Ar + i);
+        p[0] = fmaf(a4.x, x[i], p[0]);
+        if (i + 1 < r) p[1] = fmaf(a4.y, x[i + 1], p[1]);
+        if (i + 2 < r) p[2] = fmaf(a4.z, x[i + 2], p[2]);
+        if (i + 3 < r) p[3] = fmaf(a4.w, x[i + 3], p[3]);
+      }
       x[r] -= (p[0] + p[1]) + (p[2] + p[3]);
     }
 #pragma unroll
-    for (int r = 1; r < C; ++r) col[r * ld] = x[r];
+    for (int r = 1; r < C; ++r) base[r * D + coff[r & 7]] = x[r];
   }
   __syncthreads();
-  float *Wout = Wg + slab * C * DK, *Uout = Ug + slab * C * DV;
-  for (int e = tid; e < C * DK; e += 256) Wout[e] = sKt[(e / DK) * LK + e % DK];
-  for (int e = tid; e < C * DV; e += 256) Uout[e] = sV[(e / DV) * LV + e % DV];
+
+  // write W, Ut and the save of A
+  {
+    float *Wout = Wg + slab * C * DK, *Uout = Ug + slab * C * DV;
+    constexpr int NK4 = C * DK / 4 / 256, NV4 = C * DV / 4 / 256, NA4 = C * C / 4 / 256;
+#pragma unroll
+    for (int m = 0; m < NK4; ++m) {
+      const int e = 4 * (tid + 256 * m);
+      sts4(Wout + e, lds4(sKt + swz<DK>(e / DK, e % DK)));
+    }
+#pragma unroll
+    for (int m = 0; m < NV4; ++m) {
+      const int e = 4 * (tid + 256 * m);
+      sts4(Uout + e, lds4(sQV + swz<DV>(e / DV, e % DV)));
+    }
+    if (save.A)
+#pragma unroll
+      for (int m = 0; m < NA4; ++m) {
+        const int e = 4 * (tid + 256 * m);
+        sts4(save.A + slab * C * C + e, lds4(sA + e));
+      }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -596,7 +687,7 @@ __global__ void __launch_bounds__(256) kda_state_simt(
 
 template <int DK, int DV>
 constexpr size_t prep_smem() {
-  return sizeof(float) * (3 * C * (DK + 1) + C * (DV + 1) + C * (C + 1) + C + DK);
+  return sizeof(float) * PrepLayout<DK, DV>::FLOATS;
 }
 // shared memory of the state pass: without an output (segment summaries, the backward's
 // forward replay) the Q~^T and P^T buffers are left out
@@ -614,6 +705,10 @@ cudaError_t launch_prep_t(const void *q, const void *k, const void *v, const voi
   auto kern = kda_prep_simt<DK, DV, Tin>;
   constexpr size_t sm = prep_smem<DK, DV>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  // two CTAs per SM need the largest shared-memory carveout
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
   dim3 grid(ws.max_chunks, H);
