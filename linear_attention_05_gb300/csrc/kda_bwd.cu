@@ -699,74 +699,81 @@ __global__ void __launch_bounds__(256) kda_bwd_solve(const float *__restrict__ A
                                                      float *__restrict__ Y1,
                                                      float *__restrict__ Y2, int H,
                                                      const ChunkMeta *__restrict__ meta) {
-  constexpr int NC = N1 + N2, LA = C + 1, LY = NC + 1;
-  extern __shared__ float smem[];
-  float *sA = smem;          // [C][LA]
-  float *sY = sA + C * LA;   // [C][LY]
+  // A is held transposed (row r of sAt = column r of A, padded to 68 floats so every row starts
+  // on a 16-byte boundary): row r's dot product reads 16-byte vectors. Y is held unpadded.
+  constexpr int NC = N1 + N2, LA = C + 4;
+  extern __shared__ __align__(16) float smem[];
+  float *sAt = smem;         // [C][LA]  sAt[c][r] = A[r][c]
+  float *sY = sAt + C * LA;  // [C][NC]
   const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   if (meta->invalid || ci >= meta->total_chunks) return;
   const size_t slab = (size_t)ci * H + h;
   float *y1 = Y1 + slab * C * N1, *y2 = Y2 + slab * C * N2;
-  {  // 16-byte loads, all issued before their stores
+  {  // 16-byte loads, all issued before their stores. A: lane = row, so that the transposed
+     // stores of a warp fall in different banks
     constexpr int NA = C * C / 4 / 256, NY1 = C * N1 / 4 / 256, NY2 = C * N2 / 4 / 256;
     float4 ra[NA], r1[NY1], r2[NY2];
+    const int ar = tid % C, ac = 4 * (tid / C);  // row and first column of this thread's A loads
 #pragma unroll
     for (int m = 0; m < NA; ++m)
-      ra[m] = *reinterpret_cast<const float4 *>(Ag + slab * C * C + 4 * (tid + 256 * m));
+      ra[m] = *reinterpret_cast<const float4 *>(Ag + slab * C * C + ar * C + ac + 16 * m);
 #pragma unroll
     for (int m = 0; m < NY1; ++m) r1[m] = *reinterpret_cast<const float4 *>(y1 + 4 * (tid + 256 * m));
 #pragma unroll
     for (int m = 0; m < NY2; ++m) r2[m] = *reinterpret_cast<const float4 *>(y2 + 4 * (tid + 256 * m));
 #pragma unroll
     for (int m = 0; m < NA; ++m) {
-      const int e = 4 * (tid + 256 * m), r = e / C, c = e % C;
-      sA[r * LA + c] = ra[m].x; sA[r * LA + c + 1] = ra[m].y;
-      sA[r * LA + c + 2] = ra[m].z; sA[r * LA + c + 3] = ra[m].w;
+      const int c = ac + 16 * m;
+      sAt[(c + 0) * LA + ar] = ra[m].x; sAt[(c + 1) * LA + ar] = ra[m].y;
+      sAt[(c + 2) * LA + ar] = ra[m].z; sAt[(c + 3) * LA + ar] = ra[m].w;
     }
 #pragma unroll
     for (int m = 0; m < NY1; ++m) {
       const int e = 4 * (tid + 256 * m), r = e / N1, c = e % N1;
-      sY[r * LY + c] = r1[m].x; sY[r * LY + c + 1] = r1[m].y;
-      sY[r * LY + c + 2] = r1[m].z; sY[r * LY + c + 3] = r1[m].w;
+      *reinterpret_cast<float4 *>(sY + r * NC + c) = r1[m];
     }
 #pragma unroll
     for (int m = 0; m < NY2; ++m) {
       const int e = 4 * (tid + 256 * m), r = e / N2, c = e % N2;
-      sY[r * LY + N1 + c] = r2[m].x; sY[r * LY + N1 + c + 1] = r2[m].y;
-      sY[r * LY + N1 + c + 2] = r2[m].z; sY[r * LY + N1 + c + 3] = r2[m].w;
+      *reinterpret_cast<float4 *>(sY + r * NC + N1 + c) = r2[m];
     }
   }
   __syncthreads();
   // (I + A)^T X = Y, back substitution: one thread per column, the column in registers
-  // (indices fixed at compile time), each row's dot product in four partial sums
+  // (indices fixed at compile time), each row's dot product in four partial sums (row s into
+  // sum s mod 4), column r of A read as 16-byte vectors of sAt's row r
   if (tid < NC) {
     float *col = sY + tid;
     float x[C];
 #pragma unroll
-    for (int r = 0; r < C; ++r) x[r] = col[r * LY];
+    for (int r = 0; r < C; ++r) x[r] = col[r * NC];
 #pragma unroll
     for (int r = C - 2; r >= 0; --r) {
+      const float *At = sAt + r * LA;
       float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int s = r + 1; s < C; ++s) p[s & 3] = fmaf(sA[s * LA + r], x[s], p[s & 3]);
+      for (int s4 = (r + 1) & ~3; s4 < C; s4 += 4) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(At + s4);
+        if (s4 + 0 > r) p[0] = fmaf(a4.x, x[s4 + 0], p[0]);
+        if (s4 + 1 > r) p[1] = fmaf(a4.y, x[s4 + 1], p[1]);
+        if (s4 + 2 > r) p[2] = fmaf(a4.z, x[s4 + 2], p[2]);
+        if (s4 + 3 > r) p[3] = fmaf(a4.w, x[s4 + 3], p[3]);
+      }
       x[r] -= (p[0] + p[1]) + (p[2] + p[3]);
     }
 #pragma unroll
-    for (int r = 0; r < C - 1; ++r) col[r * LY] = x[r];
+    for (int r = 0; r < C - 1; ++r) col[r * NC] = x[r];
   }
   __syncthreads();
 #pragma unroll 4
   for (int e = 4 * tid; e < C * N1; e += 1024) {
     const int r = e / N1, c = e % N1;
-    *reinterpret_cast<float4 *>(y1 + e) = make_float4(sY[r * LY + c], sY[r * LY + c + 1],
-                                                     sY[r * LY + c + 2], sY[r * LY + c + 3]);
+    *reinterpret_cast<float4 *>(y1 + e) = *reinterpret_cast<const float4 *>(sY + r * NC + c);
   }
 #pragma unroll 4
   for (int e = 4 * tid; e < C * N2; e += 1024) {
     const int r = e / N2, c = e % N2;
-    *reinterpret_cast<float4 *>(y2 + e) =
-        make_float4(sY[r * LY + N1 + c], sY[r * LY + N1 + c + 1], sY[r * LY + N1 + c + 2],
-                    sY[r * LY + N1 + c + 3]);
+    *reinterpret_cast<float4 *>(y2 + e) = *reinterpret_cast<const float4 *>(sY + r * NC + N1 + c);
   }
 }
 
@@ -1243,7 +1250,7 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
   // [dB_k | dB_v] = T^T [dW | dU]   (in place)
   {
     auto kern = kda_bwd_solve<DK, DV>;
-    constexpr size_t sm = sizeof(float) * (C * (C + 1) + C * (DK + DV + 1));
+    constexpr size_t sm = sizeof(float) * (C * (C + 4) + C * (DK + DV));
     KDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
     kern<<<dim3(mc, H), 256, sm, st>>>(w.A, w.dW, w.dU, H, fw.meta);
     KDA_TRY(cudaGetLastError());
