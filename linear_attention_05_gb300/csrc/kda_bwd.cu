@@ -1049,34 +1049,48 @@ struct BwdWs {
   float *Kh, *Bk, *A, *Sb, *dSb, *R, *Ub, *O, *dO, *dU, *V1, *dP, *dQt, *dKd, *dW, *dM, *Y, *dKh;
 };
 
+// Per-slab buffer sizes of the backward's workspace (after the forward prep's part).
+struct BwdSizes {
+  size_t mk, mv, mc, ms;
+  BwdSizes(int64_t T_total, int n_seq, int H, int dk, int dv) {
+    const size_t per = ((size_t)(T_total / C) + (size_t)n_seq + 1) * H;
+    mk = align_up(sizeof(float) * per * C * dk, 256);
+    mv = align_up(sizeof(float) * per * C * dv, 256);
+    mc = align_up(sizeof(float) * per * C * C, 256);
+    ms = align_up(sizeof(float) * per * dk * dv, 256);
+  }
+  // R, V1 and dO are last read before the side stream joins back; dK_d, dW, Y, dK^ and dA are
+  // first written after it, so the two sets share one region
+  size_t early() const { return ms + 2 * mv; }
+  size_t late() const { return 4 * mk + mc; }
+  size_t shared() const { return early() > late() ? early() : late(); }
+  size_t bytes() const { return 3 * mk + 3 * mv + 2 * mc + 2 * ms + shared(); }
+};
+
 size_t bwd_extra_bytes(int64_t T_total, int n_seq, int H, int dk, int dv) {
-  const size_t per = ((size_t)(T_total / C) + (size_t)n_seq + 1) * H;
-  const size_t mk = align_up(sizeof(float) * per * C * dk, 256);
-  const size_t mv = align_up(sizeof(float) * per * C * dv, 256);
-  const size_t mc = align_up(sizeof(float) * per * C * C, 256);
-  const size_t ms = align_up(sizeof(float) * per * dk * dv, 256);
-  return 7 * mk + 5 * mv + 3 * mc + 3 * ms;
+  return BwdSizes(T_total, n_seq, H, dk, dv).bytes();
 }
 
 BwdWs bwd_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int dv) {
   BwdWs w;
   w.fw = chunk_ws_carve(ws, T_total, n_seq, H, dk, dv);
   char *p = (char *)ws + chunk_ws_bytes(T_total, n_seq, H, dk, dv);
-  const size_t per = ((size_t)(T_total / C) + (size_t)n_seq + 1) * H;
-  const size_t mk = align_up(sizeof(float) * per * C * dk, 256);
-  const size_t mv = align_up(sizeof(float) * per * C * dv, 256);
-  const size_t mc = align_up(sizeof(float) * per * C * C, 256);
-  const size_t ms = align_up(sizeof(float) * per * dk * dv, 256);
+  const BwdSizes z(T_total, n_seq, H, dk, dv);
   auto take = [&](size_t n) {
     float *r = (float *)p;
     p += n;
     return r;
   };
-  w.Kh = take(mk); w.Bk = take(mk); w.dQt = take(mk); w.dKd = take(mk); w.dW = take(mk);
-  w.Y = take(mk); w.dKh = take(mk);
-  w.Ub = take(mv); w.O = take(mv); w.dO = take(mv); w.dU = take(mv); w.V1 = take(mv);
-  w.A = take(mc); w.dP = take(mc); w.dM = take(mc);
-  w.Sb = take(ms); w.dSb = take(ms); w.R = take(ms);
+  // live from their first write to the finishing kernel
+  w.Kh = take(z.mk); w.Bk = take(z.mk); w.dQt = take(z.mk);
+  w.Ub = take(z.mv); w.O = take(z.mv); w.dU = take(z.mv);
+  w.A = take(z.mc); w.dP = take(z.mc);
+  w.Sb = take(z.ms); w.dSb = take(z.ms);
+  // the shared region: first R, V1, dO, then dK_d, dW, Y, dK^, dA
+  char *const sh = p;
+  w.R = take(z.ms); w.V1 = take(z.mv); w.dO = take(z.mv);
+  p = sh;
+  w.dKd = take(z.mk); w.dW = take(z.mk); w.Y = take(z.mk); w.dKh = take(z.mk); w.dM = take(z.mc);
   return w;
 }
 
