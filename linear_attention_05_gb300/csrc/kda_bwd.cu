@@ -540,6 +540,9 @@ struct GemmArgs {
   float *Cm;
   size_t sC;
   int mask;
+  // paired kernel: t[0] -> Cm and t[1] -> Cm2 (no mask), their K tiles in turn; with dot, also
+  // dot[n] = sum_k op(B_0)[k][n] op(B_1)[k][n] per slab (both B stored n-major)
+  float *Cm2, *dot;
 };
 
 // On the tensor cores, at fp32-level accuracy: as
@@ -574,20 +577,22 @@ __device__ __forceinline__ void split3_pair(float a, float b, uint32_t (&w)[3]) 
   w[2] = *reinterpret_cast<const uint32_t *>(&t2);
 }
 
-template <int N>
-__global__ void __launch_bounds__(bgt::NT, 3) kda_bwd_gemm_tc(GemmArgs g, int H,
-                                                             const ChunkMeta *__restrict__ meta) {
+template <int N, bool PAIRED = false>
+__global__ void __launch_bounds__(bgt::NT, PAIRED ? 2 : 3)
+    kda_bwd_gemm_tc(GemmArgs g, int H, const ChunkMeta *__restrict__ meta) {
   using namespace tc;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_mma;
   __shared__ uint32_t tmem_base;
+  __shared__ float s_dot[N];  // paired mode with dot: the row sums, tile by tile
   const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (meta->invalid || ci >= meta->total_chunks) return;
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(sm);
   const size_t slab = (size_t)ci * H + h;
+  const uint32_t ncols = PAIRED ? 128 : 64;  // one or two 64-column accumulators
   if (warp == 0) {
-    tmem_alloc(&tmem_base, 64);
+    tmem_alloc(&tmem_base, ncols);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -609,8 +614,11 @@ __global__ void __launch_bounds__(bgt::NT, 3) kda_bwd_gemm_tc(GemmArgs g, int H,
   };
   bool ok = true;
   for (int i = 0; i < ntiles; ++i) {
-    const GemmTerm &t = i < nt0 ? g.t[0] : g.t[1];
-    const int k0 = (i < nt0 ? i : i - nt0) * 64;
+    // paired: the two terms' tiles in turn (equal depths); else the first term's, then the second's
+    const int term = PAIRED ? (i & 1) : (i < nt0 ? 0 : 1);
+    const int kt = PAIRED ? (i >> 1) : (i < nt0 ? i : i - nt0);
+    const GemmTerm &t = g.t[term];
+    const int k0 = kt * 64;
     const float *A = t.A + slab * t.sA, *B = t.B + slab * t.sB;
     // this tile's operands into registers (16-byte loads along each operand's contiguous axis)
     constexpr int NB = N / 16, NQ = N / 4;  // float4s of op(B)^T per thread, per row of n
@@ -635,12 +643,33 @@ __global__ void __launch_bounds__(bgt::NT, 3) kda_bwd_gemm_tc(GemmArgs g, int H,
     // the previous tile's products are done with the shared-memory operands
     if (i > 0 && !mbar_wait(&bar_mma, (i - 1) & 1)) ok = false;
     tc_fence_after();
+    const bool dot = PAIRED && g.dot && term == 1;
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       const int e = tid + bgt::NT * r;
-      put3(0, bgt::TA,
-           t.b_t ? sw128_off(e >> 4, 4 * (e & 15), 128) : sw128_off(e / NQ, 4 * (e % NQ), 64),
-           vb[r]);
+      const uint32_t o =
+          t.b_t ? sw128_off(e >> 4, 4 * (e & 15), 128) : sw128_off(e / NQ, 4 * (e % NQ), 64);
+      if (dot) {
+        // the first term's B values at these positions, as their three terms still in shared
+        // memory (written by this thread; their sum is the fp32 value to within 2^-27 of it)
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int tt = 0; tt < 3; ++tt) {
+          const uint2 w = *reinterpret_cast<const uint2 *>(sm + tt * bgt::TA + o);
+          const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.x));
+          const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.y));
+          x[0] += lo.x, x[1] += lo.y, x[2] += hi.x, x[3] += hi.y;
+        }
+        float d = x[0] * vb[r].x;
+        d = fmaf(x[1], vb[r].y, d);
+        d = fmaf(x[2], vb[r].z, d);
+        d = fmaf(x[3], vb[r].w, d);
+#pragma unroll
+        for (int sh = 1; sh < 16; sh <<= 1) d += __shfl_xor_sync(0xffffffffu, d, sh);
+        // row e >> 4 is held by 16 consecutive lanes; the first of them adds the row's sum
+        if ((tid & 15) == 0) s_dot[e >> 4] = (kt == 0 ? 0.f : s_dot[e >> 4]) + d;
+      }
+      put3(0, bgt::TA, o, vb[r]);
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -662,7 +691,9 @@ __global__ void __launch_bounds__(bgt::NT, 3) kda_bwd_gemm_tc(GemmArgs g, int H,
             const uint32_t ta = sb + a * bgt::TA, tbb = sb + bgt::SB + b * bgt::TB;
             const uint64_t ad = t.b_t ? desc_kmajor(ta, 128, kk) : desc_mnmajor(ta, 64, kk);
             const uint64_t bd = t.a_t ? desc_mnmajor(tbb, 64, kk) : desc_kmajor(tbb, 64, kk);
-            mma_bf16(tb, ad, bd, id, (i > 0 || kk > 0 || a > 0 || b > 0) ? 1u : 0u);
+            const bool first = PAIRED ? kt == 0 : i == 0;
+            mma_bf16(tb + (PAIRED ? 64u * term : 0u), ad, bd, id,
+                     (!first || kk > 0 || a > 0 || b > 0) ? 1u : 0u);
           }
       mma_commit(&bar_mma);
     }
@@ -671,23 +702,27 @@ __global__ void __launch_bounds__(bgt::NT, 3) kda_bwd_gemm_tc(GemmArgs g, int H,
   tc_fence_after();
   // C[m][n]: lane quadrant warp % 4 holds n = 32 (warp % 4) + lane, warp / 4 the half of m
   if (ok && (warp & 3) * 32 < N) {
-    float v[32];
-    tmem_ld32(tmem_addr(tb, (warp & 3) * 32, 32 * (warp >> 2)), v);
-    tmem_wait_ld();
-    float *Cm = g.Cm + slab * g.sC;
-    const int n = (warp & 3) * 32 + lane;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int m = 32 * (warp >> 2) + j;
-      const bool keep = g.mask == 0 || (g.mask == 1 ? n <= m : n < m);
-      Cm[(size_t)m * N + n] = keep ? v[j] : 0.f;
+    for (int acc = 0; acc < (PAIRED ? 2 : 1); ++acc) {
+      float v[32];
+      tmem_ld32(tmem_addr(tb, (warp & 3) * 32, 64 * acc + 32 * (warp >> 2)), v);
+      tmem_wait_ld();
+      float *Cm = (acc ? g.Cm2 : g.Cm) + slab * g.sC;
+      const int n = (warp & 3) * 32 + lane;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int m = 32 * (warp >> 2) + j;
+        const bool keep = g.mask == 0 || (g.mask == 1 ? n <= m : n < m);
+        Cm[(size_t)m * N + n] = keep ? v[j] : 0.f;
+      }
     }
   } else if (!ok && lane == 0) {
     atomicOr(&g_bwd_err, kErrTimeout);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tb, 64);
+  if (PAIRED && g.dot && tid < N) g.dot[slab * N + tid] = s_dot[tid];
+  if (warp == 0) tmem_dealloc(tb, ncols);
 }
 
 // ---------------------------------------------------------------------------
@@ -837,7 +872,7 @@ __global__ void __launch_bounds__(256, 3) kda_bwd_finish(
     const int *__restrict__ off, const float *__restrict__ Yg, const float *__restrict__ dBkg,
     const float *__restrict__ dBvg, const float *__restrict__ dKhg,
     const float *__restrict__ dQtg, const float *__restrict__ dKdg,
-    const float *__restrict__ Sbg, const float *__restrict__ dSbg, const float *__restrict__ Og) {
+    const float *__restrict__ dDg, const float *__restrict__ Og) {
   constexpr int LK = DK + 1, NI = DK / 32, NJ = DV / 32;
   extern __shared__ float smem[];
   float *sG = smem;             // [C][LK]  running log-decay G (by position)
@@ -882,26 +917,8 @@ __global__ void __launch_bounds__(256, 3) kda_bwd_finish(
         sG[r * LK + pos(c + u)] = r < len ? prep_log_alpha(lv[m][u], flags) : 0.f;
     }
   }
-  // dL/d e^{G_C}[c] = sum_j dS'[c][j] S[c][j]: two channels per step, NJ values per lane each
-  for (int c = warp; c < DK; c += 16) {
-    float a0[NJ], b0[NJ], a1[NJ], b1[NJ];
-    ldv(dSbg + (slab * DK + c) * DV + NJ * lane, a0);
-    ldv(Sbg + (slab * DK + c) * DV + NJ * lane, b0);
-    ldv(dSbg + (slab * DK + c + 8) * DV + NJ * lane, a1);
-    ldv(Sbg + (slab * DK + c + 8) * DV + NJ * lane, b1);
-    float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-    for (int u = 0; u < NJ; ++u) {
-      x0 = fmaf(a0[u], b0[u], x0);
-      x1 = fmaf(a1[u], b1[u], x1);
-    }
-    x0 = wsum(x0);
-    x1 = wsum(x1);
-    if (lane == 0) {
-      sdD[pos(c)] = x0;
-      sdD[pos(c + 8)] = x1;
-    }
-  }
+  // dL/d e^{G_C}[c] = sum_j dS'[c][j] S[c][j], from the paired dK_d / dW products
+  if (tid < DK) sdD[pos(tid)] = dDg[slab * DK + tid];
   __syncthreads();
   if (tid < DK) {  // position tid
     float G = 0.f;
@@ -1047,22 +1064,24 @@ constexpr size_t bwd_finish_smem() {
 struct BwdWs {
   ChunkWs fw;
   float *Kh, *Bk, *A, *Sb, *dSb, *R, *Ub, *O, *dO, *dU, *V1, *dP, *dQt, *dKd, *dW, *dM, *Y, *dKh;
+  float *dD;  // [slab][dk] sum_j dS'[c][j] S[c][j]
 };
 
 // Per-slab buffer sizes of the backward's workspace (after the forward prep's part).
 struct BwdSizes {
-  size_t mk, mv, mc, ms;
+  size_t mk, mv, mc, ms, md;
   BwdSizes(int64_t T_total, int n_seq, int H, int dk, int dv) {
     const size_t per = ((size_t)(T_total / C) + (size_t)n_seq + 1) * H;
     mk = align_up(sizeof(float) * per * C * dk, 256);
     mv = align_up(sizeof(float) * per * C * dv, 256);
     mc = align_up(sizeof(float) * per * C * C, 256);
     ms = align_up(sizeof(float) * per * dk * dv, 256);
+    md = align_up(sizeof(float) * per * dk, 256);
   }
-  // R, V1 and dO are last read before the side stream joins back; dK_d, dW, Y, dK^ and dA are
-  // first written after it, so the two sets share one region
+  // R, V1 and dO are last read before the side stream joins back; dK_d, dW, dD, Y, dK^ and dA
+  // are first written after it, so the two sets share one region
   size_t early() const { return ms + 2 * mv; }
-  size_t late() const { return 4 * mk + mc; }
+  size_t late() const { return 4 * mk + mc + md; }
   size_t shared() const { return early() > late() ? early() : late(); }
   size_t bytes() const { return 3 * mk + 3 * mv + 2 * mc + 2 * ms + shared(); }
 };
@@ -1086,11 +1105,12 @@ BwdWs bwd_ws_carve(void *ws, int64_t T_total, int n_seq, int H, int dk, int dv) 
   w.Ub = take(z.mv); w.O = take(z.mv); w.dU = take(z.mv);
   w.A = take(z.mc); w.dP = take(z.mc);
   w.Sb = take(z.ms); w.dSb = take(z.ms);
-  // the shared region: first R, V1, dO, then dK_d, dW, Y, dK^, dA
+  // the shared region: first R, V1, dO, then dK_d, dW, Y, dK^, dA, dD
   char *const sh = p;
   w.R = take(z.ms); w.V1 = take(z.mv); w.dO = take(z.mv);
   p = sh;
   w.dKd = take(z.mk); w.dW = take(z.mk); w.Y = take(z.mk); w.dKh = take(z.mk); w.dM = take(z.mc);
+  w.dD = take(z.md);
   return w;
 }
 
@@ -1113,6 +1133,8 @@ cudaError_t gemm(const GemmTerm &t0, const GemmTerm *t1, float *Cm, int mask, in
   g.Cm = Cm;
   g.sC = sC ? sC : (size_t)C * N;
   g.mask = mask;
+  g.Cm2 = nullptr;
+  g.dot = nullptr;
   // every contraction depth is C, dk or dv: a multiple of the 64-deep tile
   if (t0.K % 64 != 0 || (t1 && t1->K % 64 != 0)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(kda_bwd_gemm_tc<N>,
@@ -1214,6 +1236,29 @@ cudaError_t mid_passes(const void *q, const void *k, const void *v, const void *
   return cudaSuccess;
 }
 
+// Two products of one launch, C0 = op(A_0) op(B_0) and C1 = op(A_1) op(B_1) (equal depths, no
+// mask), and with dot: dot[n] = sum_k op(B_0)[k][n] op(B_1)[k][n] (both B stored n-major).
+template <int N>
+cudaError_t gemm_paired(const GemmTerm &t0, float *C0, const GemmTerm &t1, float *C1, float *dot,
+                        int mc, int H, const ChunkMeta *meta, cudaStream_t st) {
+  GemmArgs g;
+  g.t[0] = t0;
+  g.t[1] = t1;
+  g.nterms = 2;
+  g.Cm = C0;
+  g.sC = (size_t)C * N;
+  g.mask = 0;
+  g.Cm2 = C1;
+  g.dot = dot;
+  if (t0.K % 64 != 0 || t1.K != t0.K) return cudaErrorInvalidValue;
+  if (dot && !(t0.b_t && t1.b_t && t0.ldb == t1.ldb)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_gemm_tc<N, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bgt::DYN);
+  if (e != cudaSuccess) return e;
+  kda_bwd_gemm_tc<N, true><<<dim3(mc, H), bgt::NT, bgt::DYN, st>>>(g, H, meta);
+  return cudaGetLastError();
+}
+
 template <int DK, int DV, typename Tio>
 cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, const void *beta,
                   const void *gate, const float *S0, const void *d_out, const float *dSf,
@@ -1255,12 +1300,11 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
   if (e != cudaSuccess) return e;
   const size_t sk = (size_t)C * DK, sv = (size_t)C * DV, scc = (size_t)C * C,
                ss2 = (size_t)DK * DV;
-  // dK_d = U dS'^T
-  KDA_TRY(gemm<DK>(term(w.Ub, sv, DV, 0, w.dSb, ss2, DV, 1, DV, 1.f), nullptr, w.dKd, 0, mc, H,
-                   fw.meta, st));
-  // dW = -dU S^T
-  KDA_TRY(gemm<DK>(term(w.dU, sv, DV, 0, w.Sb, ss2, DV, 1, DV, -1.f), nullptr, w.dW, 0, mc, H,
-                   fw.meta, st));
+  // dK_d = U dS'^T and dW = -dU S^T in one launch, with dD[c] = sum_j dS'[c][j] S[c][j] (the
+  // gradient reaching e^{G_C} through the state hand-off)
+  KDA_TRY(gemm_paired<DK>(term(w.Ub, sv, DV, 0, w.dSb, ss2, DV, 1, DV, 1.f), w.dKd,
+                          term(w.dU, sv, DV, 0, w.Sb, ss2, DV, 1, DV, -1.f), w.dW, w.dD, mc, H,
+                          fw.meta, st));
   // [dB_k | dB_v] = T^T [dW | dU]   (in place)
   {
     auto kern = kda_bwd_solve<DK, DV>;
@@ -1292,7 +1336,7 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
         (const Tio *)q, (const Tio *)k, (const Tio *)v, (const Tio *)la, (const Tio *)beta,
         (const Tio *)gate, (const Tio *)d_out, (Tio *)dq, (Tio *)dk, (Tio *)dv, (Tio *)dla, (Tio *)dbeta,
         gate ? (Tio *)dgate : nullptr, cu, n_seq, fixed_len, H, scale, flags, fw.meta,
-        fw.seq_chunk_off, w.Y, w.dW, w.dU, w.dKh, w.dQt, w.dKd, w.Sb, w.dSb, w.O);
+        fw.seq_chunk_off, w.Y, w.dW, w.dU, w.dKh, w.dQt, w.dKd, w.dD, w.O);
     KDA_TRY(cudaGetLastError());
   }
 #undef KDA_TRY
