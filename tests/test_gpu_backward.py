@@ -129,3 +129,26 @@ def test_backward_repeatable_bitwise():
                     d_fin, cu_t)
     for n in GRADS:
         assert torch.equal(a[n], b[n]), n
+
+
+@pytest.mark.parametrize("d,varlen", [(128, True), (128, False), (64, True)])
+def test_backward_all_sequences_empty(d, varlen):
+    """T_total = 0 with three sequences: every chain is empty, so the cotangent of the initial
+    state is that of the final state, unchanged (a product over zero transitions), and no
+    kernel touches a token row (the token tensors have none)."""
+    n_seq, H = 3, 2
+    dt = torch.bfloat16 if d == 128 else torch.float32
+    tok = lambda w: torch.empty((0, H, w), dtype=dt, device=DEV)
+    x = {"q": tok(d), "k": tok(d), "v": tok(d), "log_alpha": tok(d), "gate": tok(d),
+         "beta": torch.empty((0, H), dtype=dt, device=DEV)}
+    S0 = inputs.state(n_seq, H, d, d, seed=71, device=DEV)
+    g = torch.Generator(device="cpu").manual_seed(72)
+    d_fin = torch.randn((n_seq, H, d, d), generator=g).to(DEV)
+    cu = torch.zeros(n_seq + 1, dtype=torch.int32, device=DEV) if varlen else None
+    r = B.chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], S0, tok(d),
+                    d_fin, cu, n_seq=n_seq)
+    torch.cuda.synchronize()
+    assert B.kda_get_error() == B.KDA_OK
+    assert torch.equal(r["dS0"], d_fin)
+    for n in ("dq", "dk", "dv", "dlog_alpha", "dbeta", "dgate"):
+        assert r[n].numel() == 0, n
