@@ -75,3 +75,64 @@ def test_split_prefill_graph_replay_is_bitwise_eager(varlen):
     assert torch.equal(out_g, out)
     assert torch.equal(fs_g, fs)
     assert not torch.equal(out_g, out_e)
+
+
+def test_backward_graph_replay_is_bitwise_eager():
+    """kda_chunk_bwd forks the library's second stream off the caller's and joins it back (the
+    two state passes run side by side); captured in a CUDA graph, the call replays bit for bit
+    like the eager call and follows new inputs written in place."""
+    lengths = [300, 129]
+    T, n, Hb, d = sum(lengths), len(lengths), 2, 128
+    x = inputs.tokens(T, Hb, d, d, torch.bfloat16, seed=85, device=DEV)
+    s0 = inputs.state(n, Hb, d, d, seed=86, device=DEV)
+    g = torch.Generator(device="cpu").manual_seed(87)
+    d_out = torch.randn((T, Hb, d), generator=g).to(torch.bfloat16).to(DEV)
+    d_fin = torch.randn((n, Hb, d, d), generator=g).to(DEV)
+    cu = torch.tensor([0, lengths[0], T], dtype=torch.int32, device=DEV)
+    ws = torch.empty(B.kda_chunk_bwd_workspace_size(T, n, Hb, d, d), dtype=torch.uint8,
+                     device=DEV)
+    grads = {nm: torch.empty_like(x[src]) for nm, src in (
+        ("dq", "q"), ("dk", "k"), ("dv", "v"), ("dlog_alpha", "log_alpha"), ("dbeta", "beta"),
+        ("dgate", "gate"))}
+    grads["dS0"] = torch.empty((n, Hb, d, d), dtype=torch.float32, device=DEV)
+
+    def call():
+        B.kda_chunk_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], s0, d_out,
+                        d_fin, grads["dq"], grads["dk"], grads["dv"], grads["dlog_alpha"],
+                        grads["dbeta"], grads["dgate"], grads["dS0"], cu, n, workspace=ws)
+
+    call()
+    torch.cuda.synchronize()
+    assert B.kda_get_error() == B.KDA_OK
+    eager = {nm: t.clone() for nm, t in grads.items()}
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up on the capture stream
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    for t in grads.values():
+        t.zero_()
+    with torch.cuda.graph(graph):
+        call()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert B.kda_get_error() == B.KDA_OK
+    for nm, t in grads.items():
+        assert torch.equal(t, eager[nm]), nm
+
+    # new inputs and cotangents written in place: the replay follows them
+    x2 = inputs.tokens(T, Hb, d, d, torch.bfloat16, seed=89, device=DEV)
+    for nm in ("q", "k", "v", "log_alpha", "beta", "gate"):
+        x[nm].copy_(x2[nm])
+    d_out.copy_(torch.randn((T, Hb, d), generator=g).to(torch.bfloat16).to(DEV))
+    graph.replay()
+    torch.cuda.synchronize()
+    replayed = {nm: t.clone() for nm, t in grads.items()}
+    call()
+    torch.cuda.synchronize()
+    assert B.kda_get_error() == B.KDA_OK
+    for nm, t in grads.items():
+        assert torch.equal(replayed[nm], t), nm
+    assert not torch.equal(replayed["dq"], eager["dq"])
