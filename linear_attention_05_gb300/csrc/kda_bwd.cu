@@ -548,14 +548,16 @@ struct GemmArgs {
 // On the tensor cores, at fp32-level accuracy: as
 // C^T[n][m] = sum_i alpha_i op(B_i)^T op(A_i)^T, an M = 128 (n), N = 64 (m) tcgen05 product per
 // 64-deep K tile (for N = 64 the accumulator rows 64..127 are computed from rows of the op(B)^T
-// tile that are never written, and never read back). Each fp32 operand value v enters as three bf16 terms, v0 = bf16(v),
-// v1 = bf16(v - v0), v2 = bf16(v - v0 - v1) (the differences are exact in fp32), and the six
-// products of terms a + b <= 2 are accumulated in fp32 in tensor memory (what is dropped is
-// below 2^-24 of the product). Both operands are staged as they lie in memory: op(B)^T is
+// tile that are never written, and never read back). Each fp32 operand value v enters as three
+// bf16 terms, v0 = bf16(v), v1 = bf16(v - v0), v2 = bf16(v - v0 - v1) (the differences are
+// exact in fp32), and the six products of terms a + b <= 2 are accumulated in fp32 in tensor
+// memory (what is dropped is below 2^-24 of the product). Both operands are staged as they lie in memory: op(B)^T is
 // K-major when B is stored n-major (b_t) and MN-major otherwise, op(A)^T K-major when A is
 // stored m-major (!a_t) and MN-major otherwise. The mask is applied as C is written. One CTA
 // (256 threads) per (chunk, head), three per SM; thread 0 issues the 24 MMAs of a tile, the
-// tiles of a CTA in turn.
+// tiles of a CTA in turn. The paired instantiation (PAIRED) computes two products of equal
+// depth into two accumulators, their K tiles alternating, at two CTAs per SM: with the per-row
+// sums of GemmArgs::dot it needs more than the 80 registers a thread of three CTAs per SM.
 namespace bgt {
 constexpr int NT = 256;
 constexpr uint32_t TA = 128 * 64 * 2;  // one bf16 term of op(B)^T: 128 x 64
