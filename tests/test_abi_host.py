@@ -236,3 +236,24 @@ def test_selftest_wait_timeout_rejects_bad_limit(lib):
     # checked before any launch: no GPU needed
     assert lib.kda_selftest_wait_timeout(0, None) == B.KDA_ERR_INVALID_ARG
     assert lib.kda_selftest_wait_timeout(2_000_000, None) == B.KDA_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No fallback: with libkda.so absent, loading raises (in a fresh process, so that this
+    session's loaded handle is not reused)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import sys\n"
+            "from linear_attention_05_gb300 import binding as B\n"
+            "try:\n"
+            f"    B.load({str(tmp_path / 'libkda.so')!r})\n"
+            "except RuntimeError as e:\n"
+            "    print('raised:', e)\n"
+            "    sys.exit(0)\n"
+            "sys.exit(1)\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "not found" in r.stdout
