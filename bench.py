@@ -748,7 +748,7 @@ def bench_backward(dev, pk, stream, reps=5):
     return {"workload": "backward of prefill B=4 T=4096 H=16 dk=dv=128, bf16 in/out, fp32 "
                         "arithmetic (batched contractions and both state passes on the tensor cores)",
             "value": round(T / (ms * 1e-3) / 1e6, 3), "unit": "Mtok/s", "ms": round(ms, 3),
-            "workspace_bytes": ws.numel(), "gpu_launches": 17 * reps}
+            "workspace_bytes": ws.numel(), "gpu_launches": 15 * reps}
 
 
 def bench_gates(dev, pk, stream, reps=20):

@@ -535,14 +535,16 @@ struct GemmTerm {
   float alpha;
 };
 struct GemmArgs {
-  GemmTerm t[2];
+  GemmTerm t[3];
   int nterms;
   float *Cm;
   size_t sC;
   int mask;
-  // paired kernel: t[0] -> Cm and t[1] -> Cm2 (no mask), their K tiles in turn; with dot, also
+  // multi-product kernel (NPROD = 2 or 3): t[p] -> Cm / Cm2 / Cm3 with strides sC / sC2 / sC3
+  // (no mask), their K tiles in turn; with two products and dot, also
   // dot[n] = sum_k op(B_0)[k][n] op(B_1)[k][n] per slab (both B stored n-major)
-  float *Cm2, *dot;
+  float *Cm2, *Cm3, *dot;
+  size_t sC2, sC3;
 };
 
 // On the tensor cores, at fp32-level accuracy: as
@@ -555,9 +557,10 @@ struct GemmArgs {
 // K-major when B is stored n-major (b_t) and MN-major otherwise, op(A)^T K-major when A is
 // stored m-major (!a_t) and MN-major otherwise. The mask is applied as C is written. One CTA
 // (256 threads) per (chunk, head), three per SM; thread 0 issues the 24 MMAs of a tile, the
-// tiles of a CTA in turn. The paired instantiation (PAIRED) computes two products of equal
-// depth into two accumulators, their K tiles alternating, at two CTAs per SM: with the per-row
-// sums of GemmArgs::dot it needs more than the 80 registers a thread of three CTAs per SM.
+// tiles of a CTA in turn. The multi-product instantiations (NPROD = 2, 3) compute two or three
+// products of equal depth into their own accumulators, their K tiles in turn, at two CTAs per
+// SM: with the per-row sums of GemmArgs::dot they need more than the 80 registers a thread of
+// three CTAs per SM.
 namespace bgt {
 constexpr int NT = 256;
 constexpr uint32_t TA = 128 * 64 * 2;  // one bf16 term of op(B)^T: 128 x 64
@@ -579,20 +582,21 @@ __device__ __forceinline__ void split3_pair(float a, float b, uint32_t (&w)[3]) 
   w[2] = *reinterpret_cast<const uint32_t *>(&t2);
 }
 
-template <int N, bool PAIRED = false>
-__global__ void __launch_bounds__(bgt::NT, PAIRED ? 2 : 3)
+template <int N, int NPROD = 1>
+__global__ void __launch_bounds__(bgt::NT, NPROD > 1 ? 2 : 3)
     kda_bwd_gemm_tc(GemmArgs g, int H, const ChunkMeta *__restrict__ meta) {
   using namespace tc;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_mma;
   __shared__ uint32_t tmem_base;
-  __shared__ float s_dot[N];  // paired mode with dot: the row sums, tile by tile
+  __shared__ float s_dot[N];  // two products with dot: the row sums, tile by tile
   const int ci = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (meta->invalid || ci >= meta->total_chunks) return;
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(sm);
   const size_t slab = (size_t)ci * H + h;
-  const uint32_t ncols = PAIRED ? 128 : 64;  // one or two 64-column accumulators
+  // one 64-column accumulator per product (an allocation is a power of two)
+  const uint32_t ncols = NPROD == 1 ? 64 : (NPROD == 2 ? 128 : 256);
   if (warp == 0) {
     tmem_alloc(&tmem_base, ncols);
     tmem_relinquish();
@@ -605,7 +609,9 @@ __global__ void __launch_bounds__(bgt::NT, PAIRED ? 2 : 3)
   __syncthreads();
   tc_fence_after();
   const uint32_t tb = tmem_base;
-  const int nt0 = g.t[0].K / 64, ntiles = nt0 + (g.nterms > 1 ? g.t[1].K / 64 : 0);
+  const int nt0 = g.t[0].K / 64;
+  int ntiles = 0;
+  for (int q = 0; q < g.nterms; ++q) ntiles += g.t[q].K / 64;
   // A CTA holds one K tile of operands in flight (registers, then shared memory), so with more
   // than one tile the operand slabs of every term are prefetched into L2 at the start: later
   // tiles then load from L2 (2.81 -> 2.72 ms for the backward call). Each range lies within
@@ -627,9 +633,10 @@ __global__ void __launch_bounds__(bgt::NT, PAIRED ? 2 : 3)
   };
   bool ok = true;
   for (int i = 0; i < ntiles; ++i) {
-    // paired: the two terms' tiles in turn (equal depths); else the first term's, then the second's
-    const int term = PAIRED ? (i & 1) : (i < nt0 ? 0 : 1);
-    const int kt = PAIRED ? (i >> 1) : (i < nt0 ? i : i - nt0);
+    // several products: their tiles in turn (equal depths); else the first term's, then the
+    // second's
+    const int term = NPROD > 1 ? i % NPROD : (i < nt0 ? 0 : 1);
+    const int kt = NPROD > 1 ? i / NPROD : (i < nt0 ? i : i - nt0);
     const GemmTerm &t = g.t[term];
     const int k0 = kt * 64;
     const float *A = t.A + slab * t.sA, *B = t.B + slab * t.sB;
@@ -656,7 +663,7 @@ __global__ void __launch_bounds__(bgt::NT, PAIRED ? 2 : 3)
     // the previous tile's products are done with the shared-memory operands
     if (i > 0 && !mbar_wait(&bar_mma, (i - 1) & 1)) ok = false;
     tc_fence_after();
-    const bool dot = PAIRED && g.dot && term == 1;
+    const bool dot = NPROD == 2 && g.dot && term == 1;
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       const int e = tid + bgt::NT * r;
@@ -704,8 +711,8 @@ __global__ void __launch_bounds__(bgt::NT, PAIRED ? 2 : 3)
             const uint32_t ta = sb + a * bgt::TA, tbb = sb + bgt::SB + b * bgt::TB;
             const uint64_t ad = t.b_t ? desc_kmajor(ta, 128, kk) : desc_mnmajor(ta, 64, kk);
             const uint64_t bd = t.a_t ? desc_mnmajor(tbb, 64, kk) : desc_kmajor(tbb, 64, kk);
-            const bool first = PAIRED ? kt == 0 : i == 0;
-            mma_bf16(tb + (PAIRED ? 64u * term : 0u), ad, bd, id,
+            const bool first = NPROD > 1 ? kt == 0 : i == 0;
+            mma_bf16(tb + (NPROD > 1 ? 64u * term : 0u), ad, bd, id,
                      (!first || kk > 0 || a > 0 || b > 0) ? 1u : 0u);
           }
       mma_commit(&bar_mma);
@@ -716,11 +723,12 @@ __global__ void __launch_bounds__(bgt::NT, PAIRED ? 2 : 3)
   // C[m][n]: lane quadrant warp % 4 holds n = 32 (warp % 4) + lane, warp / 4 the half of m
   if (ok && (warp & 3) * 32 < N) {
 #pragma unroll
-    for (int acc = 0; acc < (PAIRED ? 2 : 1); ++acc) {
+    for (int acc = 0; acc < NPROD; ++acc) {
       float v[32];
       tmem_ld32(tmem_addr(tb, (warp & 3) * 32, 64 * acc + 32 * (warp >> 2)), v);
       tmem_wait_ld();
-      float *Cm = (acc ? g.Cm2 : g.Cm) + slab * g.sC;
+      float *Cm = acc == 0 ? g.Cm + slab * g.sC
+                           : (acc == 1 ? g.Cm2 + slab * g.sC2 : g.Cm3 + slab * g.sC3);
       const int n = (warp & 3) * 32 + lane;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -734,7 +742,7 @@ __global__ void __launch_bounds__(bgt::NT, PAIRED ? 2 : 3)
   }
   tc_fence_before();
   __syncthreads();
-  if (PAIRED && g.dot && tid < N) g.dot[slab * N + tid] = s_dot[tid];
+  if (NPROD == 2 && g.dot && tid < N) g.dot[slab * N + tid] = s_dot[tid];
   if (warp == 0) tmem_dealloc(tb, ncols);
 }
 
@@ -1145,11 +1153,13 @@ cudaError_t gemm(const GemmTerm &t0, const GemmTerm *t1, float *Cm, int mask, in
   GemmArgs g;
   g.t[0] = t0;
   g.t[1] = t1 ? *t1 : t0;
+  g.t[2] = t0;
   g.nterms = t1 ? 2 : 1;
   g.Cm = Cm;
   g.sC = sC ? sC : (size_t)C * N;
   g.mask = mask;
-  g.Cm2 = nullptr;
+  g.Cm2 = g.Cm3 = nullptr;
+  g.sC2 = g.sC3 = 0;
   g.dot = nullptr;
   // every contraction depth is C, dk or dv: a multiple of the 64-deep tile
   if (t0.K % 64 != 0 || (t1 && t1->K % 64 != 0)) return cudaErrorInvalidValue;
@@ -1157,6 +1167,37 @@ cudaError_t gemm(const GemmTerm &t0, const GemmTerm *t1, float *Cm, int mask, in
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, bgt::DYN);
   if (e != cudaSuccess) return e;
   kda_bwd_gemm_tc<N><<<dim3(mc, H), bgt::NT, bgt::DYN, st>>>(g, H, meta);
+  return cudaGetLastError();
+}
+
+// NP (2 or 3) products of one launch, C_p = op(A_p) op(B_p) with per-slab stride sC_p (equal
+// depths, no mask); with two products and dot, also dot[n] = sum_k op(B_0)[k][n] op(B_1)[k][n]
+// (both B stored n-major).
+template <int N, int NP>
+cudaError_t gemm_products(const GemmTerm (&t)[NP], float *const (&Cs)[NP],
+                          const size_t (&sCs)[NP], float *dot, int mc, int H,
+                          const ChunkMeta *meta, cudaStream_t st) {
+  static_assert(NP == 2 || NP == 3, "two or three products");
+  GemmArgs g;
+  for (int p = 0; p < 3; ++p) g.t[p] = t[p < NP ? p : 0];
+  g.nterms = NP;
+  g.Cm = Cs[0];
+  g.sC = sCs[0];
+  g.Cm2 = Cs[1];
+  g.sC2 = sCs[1];
+  g.Cm3 = NP == 3 ? Cs[NP - 1] : nullptr;
+  g.sC3 = NP == 3 ? sCs[NP - 1] : 0;
+  g.mask = 0;
+  g.dot = dot;
+  if (t[0].K % 64 != 0) return cudaErrorInvalidValue;
+  for (int p = 1; p < NP; ++p)
+    if (t[p].K != t[0].K) return cudaErrorInvalidValue;
+  if (dot && !(NP == 2 && t[0].b_t && t[1].b_t && t[0].ldb == t[1].ldb))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(kda_bwd_gemm_tc<N, NP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bgt::DYN);
+  if (e != cudaSuccess) return e;
+  kda_bwd_gemm_tc<N, NP><<<dim3(mc, H), bgt::NT, bgt::DYN, st>>>(g, H, meta);
   return cudaGetLastError();
 }
 
@@ -1208,13 +1249,23 @@ cudaError_t mid_passes(const void *q, const void *k, const void *v, const void *
   const size_t sk = (size_t)C * DK, sv = (size_t)C * DV, scc = (size_t)C * C,
                ss2 = (size_t)DK * DV;
   // side: the state-independent parts of the reverse step: V1 = P^T dO, R = Q~^T dO (dk rows,
-  // computed in 64-row halves)
+  // computed in 64-row halves), as the products of one launch that share dO
   KDA_TRY(cudaStreamWaitEvent(side, ev[1], 0));
-  KDA_TRY(gemm<DV>(term(fw.P, scc, C, 1, w.dO, sv, DV, 0, C, 1.f), nullptr, w.V1, 0, mc, H,
-                   fw.meta, side));
-  for (int r0 = 0; r0 < DK; r0 += C)
-    KDA_TRY(gemm<DV>(term(fw.Q + r0, sk, DK, 1, w.dO, sv, DV, 0, C, 1.f), nullptr,
-                     w.R + (size_t)r0 * DV, 0, mc, H, fw.meta, side, ss2));
+  {
+    const GemmTerm tv = term(fw.P, scc, C, 1, w.dO, sv, DV, 0, C, 1.f);
+    const GemmTerm tr0 = term(fw.Q, sk, DK, 1, w.dO, sv, DV, 0, C, 1.f);
+    if (DK == 2 * C) {
+      const GemmTerm tp[3] = {tv, tr0, term(fw.Q + C, sk, DK, 1, w.dO, sv, DV, 0, C, 1.f)};
+      float *const cp[3] = {w.V1, w.R, w.R + (size_t)C * DV};
+      const size_t sp[3] = {sv, ss2, ss2};
+      KDA_TRY((gemm_products<DV, 3>(tp, cp, sp, nullptr, mc, H, fw.meta, side)));
+    } else {
+      const GemmTerm tp[2] = {tv, tr0};
+      float *const cp[2] = {w.V1, w.R};
+      const size_t sp[2] = {sv, ss2};
+      KDA_TRY((gemm_products<DV, 2>(tp, cp, sp, nullptr, mc, H, fw.meta, side)));
+    }
+  }
   KDA_TRY(cudaEventRecord(ev[2], side));  // dO, V1 and R are in place
   // side: the reverse state pass
   if (DK == 128 && DV == 128) {  // on the tensor cores
@@ -1250,29 +1301,6 @@ cudaError_t mid_passes(const void *q, const void *k, const void *v, const void *
                      fw.meta, st));
   }
   return cudaSuccess;
-}
-
-// Two products of one launch, C0 = op(A_0) op(B_0) and C1 = op(A_1) op(B_1) (equal depths, no
-// mask), and with dot: dot[n] = sum_k op(B_0)[k][n] op(B_1)[k][n] (both B stored n-major).
-template <int N>
-cudaError_t gemm_paired(const GemmTerm &t0, float *C0, const GemmTerm &t1, float *C1, float *dot,
-                        int mc, int H, const ChunkMeta *meta, cudaStream_t st) {
-  GemmArgs g;
-  g.t[0] = t0;
-  g.t[1] = t1;
-  g.nterms = 2;
-  g.Cm = C0;
-  g.sC = (size_t)C * N;
-  g.mask = 0;
-  g.Cm2 = C1;
-  g.dot = dot;
-  if (t0.K % 64 != 0 || t1.K != t0.K) return cudaErrorInvalidValue;
-  if (dot && !(t0.b_t && t1.b_t && t0.ldb == t1.ldb)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(kda_bwd_gemm_tc<N, true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bgt::DYN);
-  if (e != cudaSuccess) return e;
-  kda_bwd_gemm_tc<N, true><<<dim3(mc, H), bgt::NT, bgt::DYN, st>>>(g, H, meta);
-  return cudaGetLastError();
 }
 
 template <int DK, int DV, typename Tio>
@@ -1318,9 +1346,13 @@ cudaError_t bwd_t(const void *q, const void *k, const void *v, const void *la, c
                ss2 = (size_t)DK * DV;
   // dK_d = U dS'^T and dW = -dU S^T in one launch, with dD[c] = sum_j dS'[c][j] S[c][j] (the
   // gradient reaching e^{G_C} through the state hand-off)
-  KDA_TRY(gemm_paired<DK>(term(w.Ub, sv, DV, 0, w.dSb, ss2, DV, 1, DV, 1.f), w.dKd,
-                          term(w.dU, sv, DV, 0, w.Sb, ss2, DV, 1, DV, -1.f), w.dW, w.dD, mc, H,
-                          fw.meta, st));
+  {
+    const GemmTerm tp[2] = {term(w.Ub, sv, DV, 0, w.dSb, ss2, DV, 1, DV, 1.f),
+                            term(w.dU, sv, DV, 0, w.Sb, ss2, DV, 1, DV, -1.f)};
+    float *const cp[2] = {w.dKd, w.dW};
+    const size_t sp[2] = {sk, sk};
+    KDA_TRY((gemm_products<DK, 2>(tp, cp, sp, w.dD, mc, H, fw.meta, st)));
+  }
   // [dB_k | dB_v] = T^T [dW | dU]   (in place)
   {
     auto kern = kda_bwd_solve<DK, DV>;
