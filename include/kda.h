@@ -104,7 +104,7 @@ const char *kda_version(void);
  *
  * Scheduling (bf16, dk = dv = 128, at most 112 (sequence, head) pairs and
  * >= 16 chunks per sequence on average): the call splits every sequence after
- * floor(n_chunks * 12 / 16) chunks. The state pass of the
+ * floor(n_chunks * 47 / 64) chunks. The state pass of the
  * leading parts then runs on `stream` beside the card launch of the trailing
  * parts on a library-owned stream; events fork that stream off `stream` and
  * join it back before the call returns, so all work stays ordered on

@@ -155,7 +155,8 @@ int kda_chunk_fwd_launches(int64_t T_total, int n_seq, int H, int dk, int dv, in
   if (tc && !varlen && kda::fused_shape(T_total, n_seq, H) && kda::fused_ctas(n_seq, H) > 0)
     return 1;  // the persistent prefill
   const int table = (!tc || varlen) ? 1 : 0;
-  return table + ((tc && kda::tc_split16(T_total, n_seq, H) > 0) ? 4 : 2);
+  const int parts = tc ? kda::tc_split_parts(T_total, n_seq, H) : 0;
+  return table + (parts > 1 ? 2 * parts : 2);
 }
 
 size_t kda_segment_summary_workspace_size(int64_t T_total, int n_seg, int H, int dk, int dv,
@@ -165,13 +166,14 @@ size_t kda_segment_summary_workspace_size(int64_t T_total, int n_seg, int H, int
 
 }  // extern "C"
 
-// Tensor-core prefill split in two parts per sequence (ws.split16 > 0), after the chunk table:
-//   stream s:     leading cards -> state pass over the leading parts -> state pass, trailing
-//   card stream:                   trailing cards (beside the first state pass)
-// The first state pass follows the leading cards in s, so its CTAs are placed on the idle GPU
-// before those of the trailing cards (which reach the GPU through an event); the trailing
-// cards then take the SMs it leaves free. Events fork the card stream off s and join it back,
-// so the call stays ordered on s (and can be captured).
+// Tensor-core prefill split into ws.nparts parts per sequence, after the chunk table. For three:
+//   stream s:     cards 0 -> state pass 0 -> state pass 1 -> state pass 2
+//   card stream:              cards 1        cards 2
+// Part p's cards run beside the state pass over part p - 1. They wait for the state pass over
+// part p - 2, so that they become ready together with the pass over part p - 1, which is
+// enqueued first: the pass's CTAs are placed on the SMs the earlier pass leaves before the
+// cards take the rest. Events fork the card stream off s and join it back, so the call stays
+// ordered on s (and can be captured).
 static kda_status split_prefill(const void *q, const void *k, const void *v,
                                 const void *log_alpha, const void *beta, const void *gate,
                                 void *out, const float *initial_state, float *final_state,
@@ -181,11 +183,17 @@ static kda_status split_prefill(const void *q, const void *k, const void *v,
   cudaStream_t side = nullptr;
   kda_status st = cuda_status(kda::side_stream(&side), "card stream");
   if (st != KDA_OK) return st;
-  cudaEvent_t ev[2] = {nullptr, nullptr};
-  for (cudaEvent_t &e : ev) {
-    st = cuda_status(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "event");
-    if (st != KDA_OK) break;
+  const int K = ws.nparts;
+  // per part: its cards are built (card_ev) and its state pass is done (pass_ev); the join
+  cudaEvent_t card_ev[kda::kMaxParts] = {}, pass_ev[kda::kMaxParts] = {}, join_ev = nullptr;
+  auto make = [&](cudaEvent_t *e) {
+    return cuda_status(cudaEventCreateWithFlags(e, cudaEventDisableTiming), "event");
+  };
+  for (int p = 0; p < K && st == KDA_OK; ++p) {
+    st = make(&card_ev[p]);
+    if (st == KDA_OK && p + 2 < K) st = make(&pass_ev[p]);
   }
+  if (st == KDA_OK) st = make(&join_ev);
   auto cards = [&](int part, cudaStream_t on) {
     return cuda_status(tr.at(on, [&] {
                          return kda::launch_card_tc(q, k, v, log_alpha, beta, cu_seqlens, n_seq,
@@ -201,23 +209,37 @@ static kda_status split_prefill(const void *q, const void *k, const void *v,
                        }),
                        "state pass");
   };
+  auto record = [&](cudaEvent_t e, cudaStream_t on) {
+    return cuda_status(cudaEventRecord(e, on), "event record");
+  };
+  auto wait = [&](cudaStream_t on, cudaEvent_t e) {
+    return cuda_status(cudaStreamWaitEvent(on, e, 0), "stream wait");
+  };
   bool forked = false;
   if (st == KDA_OK) st = cards(0, s);
-  if (st == KDA_OK) st = cuda_status(cudaEventRecord(ev[0], s), "event record");
+  if (st == KDA_OK) st = record(card_ev[0], s);
   if (st == KDA_OK) st = state(0);
-  if (st == KDA_OK) st = cuda_status(cudaStreamWaitEvent(side, ev[0], 0), "stream wait");
   if (st == KDA_OK) {
-    forked = true;
-    st = cards(1, side);
+    st = wait(side, card_ev[0]);
+    forked = st == KDA_OK;
   }
-  if (forked) {  // join the card stream back into s, also after a failed launch
-    kda_status j = cuda_status(cudaEventRecord(ev[1], side), "event record");
-    if (j == KDA_OK) j = cuda_status(cudaStreamWaitEvent(s, ev[1], 0), "stream wait");
-    if (st == KDA_OK) st = j;
+  for (int p = 1; p < K && st == KDA_OK; ++p) {
+    if (p >= 2) st = wait(side, pass_ev[p - 2]);
+    if (st == KDA_OK) st = cards(p, side);
+    if (st == KDA_OK) st = record(card_ev[p], side);
+    if (st == KDA_OK && p + 1 < K) st = record(pass_ev[p - 1], s);
+    if (st == KDA_OK) st = wait(s, card_ev[p]);
+    if (st == KDA_OK) st = state(p);
   }
-  if (st == KDA_OK) st = state(1);
-  for (cudaEvent_t e : ev)
+  if (forked && st != KDA_OK) {  // join the card stream back into s after a failed step
+    kda_status j = record(join_ev, side);
+    if (j == KDA_OK) wait(s, join_ev);
+  }
+  for (cudaEvent_t e : card_ev)
     if (e) cudaEventDestroy(e);
+  for (cudaEvent_t e : pass_ev)
+    if (e) cudaEventDestroy(e);
+  if (join_ev) cudaEventDestroy(join_ev);
   return st;
 }
 
@@ -281,7 +303,7 @@ static kda_status chunk_fwd_impl(const void *q, const void *k, const void *v,
         "chunk table");
     if (st != KDA_OK) return st;
   }
-  if (tc && ws.split16 > 0)
+  if (tc && ws.nparts > 1)
     return split_prefill(q, k, v, log_alpha, beta, gate, out, initial_state, final_state, ck,
                          cu_seqlens, n_seq, T_total, H, scale, flags, ws, s, tr);
   st = cuda_status(tr([&] {

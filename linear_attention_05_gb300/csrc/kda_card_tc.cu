@@ -32,8 +32,8 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
     const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_v,
     const __nv_bfloat16 *__restrict__ beta, const int32_t *__restrict__ cu, int n_seq,
     int64_t fixed_len, int H, unsigned flags, const ChunkMeta *__restrict__ meta,
-    const int *__restrict__ off, const int *__restrict__ off_lo, int chunk_part, int split16,
-    uint8_t *__restrict__ cards) {
+    const int *__restrict__ off, int chunk_part, int b_lo, int b_hi,
+    const int *__restrict__ off_blo, const int *__restrict__ off_bhi, uint8_t *__restrict__ cards) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_base;
@@ -41,36 +41,39 @@ __global__ void __launch_bounds__(256, 2) kda_card_tc(
 
   const int h = blockIdx.y, tid = threadIdx.x;
   // global chunk ci of this CTA, its sequence s and its chunk jc within s: all chunks
-  // (chunk_part < 0), or the x-th chunk of the leading (chunk_part 0) or trailing (chunk_part 1)
-  // parts of the sequences, in sequence order. Without cu_seqlens every sequence has n chunks
-  // and the chunk table is not used.
+  // (chunk_part < 0), or the x-th chunk of part chunk_part of the sequences, in sequence order.
+  // A part of a sequence with n chunks holds its chunks [n * b_lo / 64, n * b_hi / 64). Without
+  // cu_seqlens every sequence has n chunks and the chunk table is not used; with them, off_blo
+  // and off_bhi hold the running sums over the sequences of the part's first and end chunk
+  // (off_blo == nullptr: the first part, which starts at 0; off_bhi == off: the last part).
   int ci = blockIdx.x, s, jc;
   if (cu == nullptr) {
-    const int n = (int)((fixed_len + C - 1) / C), m = n * split16 / 16;
-    const int per = chunk_part == 0 ? m : (chunk_part == 1 ? n - m : n);
+    const int n = (int)((fixed_len + C - 1) / C);
+    const int lo = chunk_part < 0 ? 0 : (int)((int64_t)n * b_lo / 64);
+    const int per = (chunk_part < 0 ? n : (int)((int64_t)n * b_hi / 64)) - lo;
     if (per == 0 || ci >= n_seq * per) return;
     s = ci / per;
-    jc = ci - s * per + (chunk_part == 1 ? m : 0);
+    jc = ci - s * per + lo;
     ci = s * n + jc;
   } else {
     if (meta->invalid) return;
-    if (chunk_part == 0) {
-      if (ci >= meta->lo_chunks) return;
-      const int s0 = find_seq(off_lo, n_seq, ci);
-      ci = off[s0] + (ci - off_lo[s0]);
-    } else if (chunk_part == 1) {
-      if (ci >= meta->total_chunks - meta->lo_chunks) return;
-      int lo = 0, hi = n_seq - 1;  // largest s whose trailing part starts at or before ci
+    if (chunk_part >= 0) {
+      // part-local offset of sequence t: its part's chunks in all earlier sequences
+      auto pre = [&](int t) { return off_bhi[t] - (off_blo ? off_blo[t] : 0); };
+      if (ci >= pre(n_seq)) return;
+      int lo = 0, hi = n_seq - 1;  // largest s whose part starts at or before ci
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (off[mid] - off_lo[mid] <= ci) lo = mid; else hi = mid - 1;
+        if (pre(mid) <= ci) lo = mid; else hi = mid - 1;
       }
-      ci = off[lo] + (off_lo[lo + 1] - off_lo[lo]) + (ci - (off[lo] - off_lo[lo]));
-    } else if (ci >= meta->total_chunks) {
-      return;
+      s = lo;
+      jc = (off_blo ? off_blo[s + 1] - off_blo[s] : 0) + (ci - pre(s));
+      ci = off[s] + jc;
+    } else {
+      if (ci >= meta->total_chunks) return;
+      s = find_seq(off, n_seq, ci);
+      jc = ci - off[s];
     }
-    s = find_seq(off, n_seq, ci);
-    jc = ci - off[s];
   }
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   int64_t ts, ls;
@@ -102,21 +105,30 @@ bool tc_path(int dk, int dv, kda_dtype dt) {
 }
 
 // The state pass runs one CTA per (sequence, head). With at most 112 of them (three
-// quarters of a 152-SM GPU's SMs) and at least 16 chunks per sequence on average, the cards
-// of each sequence's last 4/16 are built on the idle SMs while the state pass walks the first
-// 12/16 (the fraction measured best on the prefill workload).
-int tc_split16(int64_t T_total, int n_seq, int H) {
-  constexpr int kLeadingSixteenths = 12;
+// quarters of a 152-SM GPU's SMs) and at least 16 chunks per sequence on average, the cards of
+// each sequence's later part are built on the idle SMs while the state pass walks the earlier
+// one. Measured on the prefill workload (4 x 4096 tokens, 16 heads), in 64ths of each
+// sequence's chunks: a boundary at 47 took 0.3600 ms, at 45/46/48/49/50 0.3618/0.3610/0.3623/
+// 0.3655/0.3682 ms; three parts (boundaries 41-45 and 56-59) 0.371-0.385 ms, their short state
+// passes paying the pass's start-up (about 9 us) once more.
+int tc_split_parts(int64_t T_total, int n_seq, int H, int *bound64) {
+  constexpr int kParts = 2;
+  constexpr int kBound[kParts + 1] = {0, 47, 64};
   if (n_seq <= 0 || (int64_t)n_seq * H > 112 || T_total < (int64_t)16 * C * n_seq) return 0;
-  return kLeadingSixteenths;
+  if (bound64)
+    for (int i = 0; i <= kParts; ++i) bound64[i] = kBound[i];
+  return kParts;
 }
 
 size_t tc_ws_bytes(int64_t T_total, int n_seq, int H) {
   const size_t mc = (size_t)(T_total / C) + (size_t)n_seq + 1;
   size_t b = align_up(sizeof(ChunkMeta), 256);
-  b += 3 * align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
-  if (tc_split16(T_total, n_seq, H) > 0)
-    b += align_up(sizeof(float) * (size_t)n_seq * H * DD * DD, 256);
+  b += 2 * align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
+  const int parts = tc_split_parts(T_total, n_seq, H);
+  if (parts > 1) {
+    b += align_up(sizeof(int) * (size_t)(parts - 1) * (n_seq + 1), 256);
+    b += (parts > 2 ? 2 : 1) * align_up(sizeof(float) * (size_t)n_seq * H * DD * DD, 256);
+  }
   if (fused_shape(T_total, n_seq, H)) b += fused_flag_bytes(T_total, n_seq, H);
   b += (size_t)mc * H * CARD_BYTES;
   return b;
@@ -131,14 +143,17 @@ ChunkWs tc_ws_carve(void *ws, int64_t T_total, int n_seq, int H) {
   p += align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
   w.seq_order = (int *)p;
   p += align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
-  w.split16 = tc_split16(T_total, n_seq, H);
-  if (w.split16 > 0) {
-    w.seq_chunk_lo = (int *)p;
-    p += align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
-    w.mid = (float *)p;
-    p += align_up(sizeof(float) * (size_t)n_seq * H * DD * DD, 256);
-  } else {
-    p += align_up(sizeof(int) * (size_t)(n_seq + 1), 256);
+  w.nparts = tc_split_parts(T_total, n_seq, H, w.bound64);
+  if (w.nparts > 1) {
+    w.seq_chunk_b = (int *)p;
+    p += align_up(sizeof(int) * (size_t)(w.nparts - 1) * (n_seq + 1), 256);
+    const size_t mb = align_up(sizeof(float) * (size_t)n_seq * H * DD * DD, 256);
+    w.mid[0] = (float *)p;
+    p += mb;
+    if (w.nparts > 2) {
+      w.mid[1] = (float *)p;
+      p += mb;
+    }
   }
   if (fused_shape(T_total, n_seq, H)) {
     const size_t fb = fused_flag_bytes(T_total, n_seq, H);
@@ -204,16 +219,21 @@ cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const vo
       cudaFuncSetAttribute(kda_card_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, A_DYN);
   if (e != cudaSuccess) return e;
   const int64_t fixed_len = (cu == nullptr && n_seq > 0) ? T_total / n_seq : 0;
-  // CTAs beyond a part's chunk count (known on the device only) return at once. Leading parts
-  // hold at most split16/16 of all chunks; trailing parts at most the rest plus one per sequence.
-  int grid = ws.max_chunks;
-  if (part == 0) grid = (int)((int64_t)ws.max_chunks * ws.split16 / 16) + 1;
-  if (part == 1)
+  // CTAs beyond a part's chunk count (known on the device only) return at once. A part spanning
+  // the 64ths [b_lo, b_hi) holds at most that fraction of all chunks plus one per sequence.
+  int grid = ws.max_chunks, b_lo = 0, b_hi = 64;
+  const int *off_blo = nullptr, *off_bhi = ws.seq_chunk_off;
+  if (part >= 0) {
+    b_lo = ws.bound64[part];
+    b_hi = ws.bound64[part + 1];
+    if (part > 0) off_blo = ws.seq_chunk_b + (size_t)(part - 1) * (n_seq + 1);
+    if (part + 1 < ws.nparts) off_bhi = ws.seq_chunk_b + (size_t)part * (n_seq + 1);
     grid = (int)std::min<int64_t>(ws.max_chunks,
-                                  (int64_t)ws.max_chunks * (16 - ws.split16) / 16 + n_seq + 1);
+                                  (int64_t)ws.max_chunks * (b_hi - b_lo) / 64 + n_seq + 1);
+  }
   kda_card_tc<<<dim3(grid, H), 256, A_DYN, st>>>(
       mk, mq, mla, mv, (const __nv_bfloat16 *)beta, cu, n_seq, fixed_len, H, flags, ws.meta,
-      ws.seq_chunk_off, ws.seq_chunk_lo, part, ws.split16, ws.cards);
+      ws.seq_chunk_off, part, b_lo, b_hi, off_blo, off_bhi, ws.cards);
   return cudaGetLastError();
 }
 

@@ -77,13 +77,14 @@ __device__ int block_exclusive_scan(int local, int *warp_tot) {
   return warp_tot[w] + incl - local;
 }
 
-// One block: validate cu_seqlens and build per-sequence chunk offsets. With off_lo given,
-// also the offsets of the leading parts (floor(n_s * split16 / 16) chunks of sequence s)
-// that a split prefill processes first.
+// One block: validate cu_seqlens and build per-sequence chunk offsets. For a split prefill
+// with nb inner part boundaries (bound64[0 .. nb), in 64ths of each sequence's chunks), also
+// the running sums over the sequences of floor(n_s * bound64[i] / 64), one [n_seq + 1] array
+// per boundary in off_b.
 __global__ void __launch_bounds__(1024) kda_chunk_table(const int32_t *cu, int n_seq,
                                                         int64_t T_total, ChunkMeta *meta,
-                                                        int *off, int split16, int *off_lo,
-                                                        int *order) {
+                                                        int *off, int nb, int4 bound64,
+                                                        int *off_b, int *order) {
   __shared__ int warp_tot[32];
   __shared__ int bad;
   __shared__ int s_chunks[kOrderMax];
@@ -98,11 +99,10 @@ __global__ void __launch_bounds__(1024) kda_chunk_table(const int32_t *cu, int n
     const int64_t len = cu ? (int64_t)cu[s + 1] - cu[s] : fixed_len;
     return len < 0 ? 0 : (int)((len + C - 1) / C);
   };
-  int local = 0, local_lo = 0;
+  int local = 0;
   for (int s = s_lo; s < s_hi; ++s) {
     if (cu && (int64_t)cu[s + 1] - cu[s] < 0) bad = 1;
     local += chunks_of(s);
-    local_lo += chunks_of(s) * split16 / 16;
   }
   if (cu && tid == 0 && (cu[0] != 0 || (int64_t)cu[n_seq] != T_total)) bad = 1;
   int run = block_exclusive_scan(local, warp_tot);
@@ -111,14 +111,19 @@ __global__ void __launch_bounds__(1024) kda_chunk_table(const int32_t *cu, int n
     run += chunks_of(s);
   }
   if (s_hi == n_seq && s_lo < s_hi) off[n_seq] = run;
-  if (off_lo) {
-    int run_lo = block_exclusive_scan(local_lo, warp_tot);
+  for (int i = 0; i < nb; ++i) {  // nb is uniform: every thread takes part in each scan
+    const int b = i == 0 ? bound64.x : bound64.y;
+    auto lead = [&](int s) { return (int)((int64_t)chunks_of(s) * b / 64); };
+    int local_b = 0;
+    for (int s = s_lo; s < s_hi; ++s) local_b += lead(s);
+    int *ob = off_b + (size_t)i * (n_seq + 1);
+    int run_b = block_exclusive_scan(local_b, warp_tot);
     for (int s = s_lo; s < s_hi; ++s) {
-      off_lo[s] = run_lo;
-      run_lo += chunks_of(s) * split16 / 16;
+      ob[s] = run_b;
+      run_b += lead(s);
     }
-    if (s_hi == n_seq && s_lo < s_hi) off_lo[n_seq] = run_lo;
-    if (n_seq == 0 && tid == 0) off_lo[0] = 0;
+    if (s_hi == n_seq && s_lo < s_hi) ob[n_seq] = run_b;
+    if (n_seq == 0 && tid == 0) ob[0] = 0;
   }
   if (n_seq == 0 && tid == 0) off[0] = 0;
   if (order) {
@@ -140,7 +145,6 @@ __global__ void __launch_bounds__(1024) kda_chunk_table(const int32_t *cu, int n
   if (tid == 0) {
     meta->invalid = bad;
     meta->total_chunks = bad ? 0 : off[n_seq];
-    meta->lo_chunks = (bad || !off_lo) ? 0 : off_lo[n_seq];
     if (bad) set_err(kErrBadSeqlens);
   }
 }
@@ -782,8 +786,10 @@ cudaError_t launch_chunk_table(const int32_t *cu, int n_seq, int64_t T_total, co
                                cudaStream_t st) {
   // one thread per sequence up to 1024 (a warp at least): few sequences, few barrier members
   const int threads = n_seq >= 1024 ? 1024 : ((n_seq + 31) / 32) * 32 + (n_seq == 0 ? 32 : 0);
-  kda_chunk_table<<<1, threads, 0, st>>>(cu, n_seq, T_total, ws.meta, ws.seq_chunk_off,
-                                         ws.split16, ws.seq_chunk_lo, ws.seq_order);
+  const int nb = ws.nparts > 1 ? ws.nparts - 1 : 0;
+  const int4 b = make_int4(ws.bound64[1], ws.bound64[2], 0, 0);
+  kda_chunk_table<<<1, threads, 0, st>>>(cu, n_seq, T_total, ws.meta, ws.seq_chunk_off, nb, b,
+                                         ws.seq_chunk_b, ws.seq_order);
   return cudaGetLastError();
 }
 

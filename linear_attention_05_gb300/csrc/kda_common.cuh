@@ -64,8 +64,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 struct ChunkMeta {
   int total_chunks;  // sum over sequences of ceil(len / 64)
   int invalid;       // non-zero: cu_seqlens rejected; every kernel exits
-  int lo_chunks;     // split prefill: chunks in the leading parts of all sequences
-  int pad[61];
+  int pad[62];
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) {
@@ -125,18 +124,23 @@ __device__ __forceinline__ float *ckpt_after_chunk(const CkptOut &ck, int s, int
 // Launchers and error-word accessors defined in the kernel translation units.
 namespace kda {
 
+constexpr int kMaxParts = 3;
 struct ChunkWs {
   ChunkMeta *meta;
   int *seq_chunk_off;  // [n_seq + 1]
   float *W, *U, *Q, *Kd, *P, *D;  // SIMT path
   uint8_t *cards;                 // tensor-core path: one update card per (chunk, head)
   int max_chunks;
-  // Split prefill (tensor-core path): each sequence's first floor(n_s * split16 / 16) chunks
-  // form its leading part. seq_chunk_lo [n_seq + 1] holds the leading parts' offsets and mid
-  // [n_seq, H, 128, 128] the state between the parts. split16 = 0: no split.
-  int split16;
-  int *seq_chunk_lo;
-  float *mid;
+  // Split prefill (tensor-core path): part p < nparts of a sequence with n chunks holds its
+  // chunks [floor(n * bound64[p] / 64), floor(n * bound64[p + 1] / 64)), bound64[0] = 0 and
+  // bound64[nparts] = 64. seq_chunk_b [nparts - 1][n_seq + 1] holds, for each inner boundary,
+  // the running sum over the sequences of floor(n * bound64[p] / 64) (with cu_seqlens); part p
+  // leaves its state in mid[p & 1] ([n_seq, H, 128, 128]), where part p + 1 starts.
+  // nparts = 0: no split.
+  int nparts;
+  int bound64[kMaxParts + 1];
+  int *seq_chunk_b;
+  float *mid[2];
   // tensor-core path: sequences by decreasing chunk count (ties by index) when there are at
   // most kOrderMax of them, else in index order. The state pass takes its chains in this
   // order, so the longest chains start in the first wave of CTAs.
@@ -198,13 +202,14 @@ cudaError_t launch_scan_combine(const float *X, const float *Z, int n_seg,
 bool tc_path(int dk, int dv, kda_dtype dt);
 // 2D tensor map over `rows` rows of 128 fp32 values: box 32 columns x 128 rows, 128-byte swizzle.
 bool make_rows_map_f32(CUtensorMap *m, const void *base, uint64_t rows);
-// Split prefill: sixteenths of each sequence's chunks in its leading part, or 0 when the
-// state pass would leave too few SMs idle for the trailing cards to use.
-int tc_split16(int64_t T_total, int n_seq, int H);
+// Split prefill: the number of parts the prefill splits each sequence into (writing their
+// boundaries in 64ths to bound64[0 .. parts]), or 0 when the state pass would leave too few
+// SMs idle for the cards of the later parts to use.
+int tc_split_parts(int64_t T_total, int n_seq, int H, int *bound64 = nullptr);
 size_t tc_ws_bytes(int64_t T_total, int n_seq, int H);
 ChunkWs tc_ws_carve(void *ws, int64_t T_total, int n_seq, int H);
-// part -1: every chunk; 0 / 1: the leading / trailing parts of a split prefill (ws.split16 > 0).
-// The state pass of part 0 leaves its state in ws.mid, where part 1 starts.
+// part -1: every chunk; p >= 0: part p of a split prefill (ws.nparts > 0). The state pass of
+// part p leaves its state in ws.mid[p & 1], where part p + 1 starts.
 cudaError_t launch_card_tc(const void *q, const void *k, const void *v, const void *la,
                            const void *beta, const int32_t *cu, int n_seq, int64_t T_total,
                            int H, unsigned flags, const ChunkWs &ws, cudaStream_t st,

@@ -235,7 +235,7 @@ cudaError_t launch_prefill_fused(const void *q, const void *k, const void *v, co
   FusedArgs a;
   a.st = tsb::StateIn{0, flags, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final,
                       nullptr, nullptr, nullptr, n_seq, L, H, scale, ws.meta, ws.seq_chunk_off,
-                      ws.cards, ck, -1, 0, nullptr, nullptr};
+                      ws.cards, ck, -1, 0, 64, nullptr, nullptr, nullptr};
   a.beta = (const __nv_bfloat16 *)beta;
   a.n_chunks = n_chunks;
   a.total = n_chunks * n_chains;

@@ -54,9 +54,14 @@ cudaError_t launch_state_tc(int mode, unsigned flags, const void *gate, void *ou
   auto launch = [&](auto kernel, int dyn) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
     if (e != cudaSuccess) return e;
+    // part p of a split prefill starts from mid[(p - 1) & 1] and leaves its state in mid[p & 1]
+    const bool split = part >= 0;
     const StateIn p{mode, flags, (const __nv_bfloat16 *)gate, (__nv_bfloat16 *)out, S0, S_final,
                     X_out, Z_out, cu, n_seq, fixed_len, H, scale, ws.meta, ws.seq_chunk_off,
-                    ws.cards, ck, part, ws.split16, ws.mid, ws.seq_order};
+                    ws.cards, ck, part, split ? ws.bound64[part] : 0,
+                    split ? ws.bound64[part + 1] : 64,
+                    split && part > 0 ? ws.mid[(part - 1) & 1] : nullptr,
+                    split && part + 1 < ws.nparts ? ws.mid[part & 1] : nullptr, ws.seq_order};
     kernel<<<dim3(n_seq * H, 1), kThreads, dyn, st>>>(p);
     return cudaSuccess;
   };

@@ -82,8 +82,11 @@ struct StateIn {
   const int *off;
   const uint8_t *cards;
   CkptOut ck;
-  int part, split16;
-  float *mid;
+  // split prefill: part >= 0 walks each sequence's chunks [n * b_lo / 64, n * b_hi / 64),
+  // starting from mid_in (else S0) and leaving its state in mid_out (else S_final)
+  int part, b_lo, b_hi;
+  const float *mid_in;
+  float *mid_out;
   const int *seq_order;
 };
 
@@ -137,8 +140,7 @@ __device__ __forceinline__ void state_body(const StateIn &p, const StateShared &
   const int *__restrict__ off = p.off;
   const uint8_t *__restrict__ cards = p.cards;
   const CkptOut &ck = p.ck;
-  const int part = p.part, split16 = p.split16;
-  float *__restrict__ mid = p.mid;
+  const int part = p.part;
   const int *__restrict__ seq_order = p.seq_order;
   using G = Geo<SUMMARY>;
   constexpr int B_NSTAGE = G::NST;
@@ -167,20 +169,15 @@ __device__ __forceinline__ void state_body(const StateIn &p, const StateShared &
   const int64_t ls_seq = ls;
   int nchunks = (int)((ls + C - 1) / C);
   const int seq_off = cu ? off[s] : s * nchunks;  // first global chunk of the sequence
-  // a split prefill walks the first nchunks * split16 / 16 chunks (part 0), handing its
-  // state over in `mid`, then the rest (part 1); chunk n below is chunk n_lo + n of the sequence
+  // a split prefill walks the sequence in parts, each a range of its chunks, handing the state
+  // from one part to the next through a buffer; chunk n below is chunk n_lo + n of the sequence
   int n_lo = 0;
   if (part >= 0) {
-    const int m = nchunks * split16 / 16;
-    if (part == 0) {
-      nchunks = m;
-      ls = (int64_t)m * C;
-    } else {
-      n_lo = m;
-      nchunks -= m;
-      ts += (int64_t)m * C;
-      ls -= (int64_t)m * C;
-    }
+    const int lo = (int)((int64_t)nchunks * p.b_lo / 64), hi = (int)((int64_t)nchunks * p.b_hi / 64);
+    n_lo = lo;
+    ls = min(ls, (int64_t)hi * C) - (int64_t)lo * C;
+    ts += (int64_t)lo * C;
+    nchunks = hi - lo;
   }
   const int cbase = nchunks > 0 ? seq_off + n_lo : 0;
   auto card_of = [&](int n) { return cards + ((size_t)(cbase + n) * H + h) * CARD_BYTES; };
@@ -196,8 +193,8 @@ __device__ __forceinline__ void state_body(const StateIn &p, const StateShared &
     atomicOr(sh.err, kErrTimeout);
     return false;
   };
-  const float *S_entry = part == 1 ? mid : S0;
-  float *S_exit = part == 0 ? mid : S_final;
+  const float *S_entry = p.mid_in ? p.mid_in : S0;
+  float *S_exit = p.mid_out ? p.mid_out : S_final;
   // element (c, j) of the entry state, and where element (c, j) of the result goes
   auto entry = [&](int c) -> float {
     if (mode == 0) return S_entry ? S_entry[(((size_t)s * H + h) * DD + c) * DD + j] : 0.f;
