@@ -449,22 +449,24 @@ def run_gpu(args, rank, world, local):
                               "peak": pk["bf16_tflops"], "frac": round(tf / pk["bf16_tflops"], 4),
                               "flop_per_chunk_head": card_flop + state_flop, "over": "step"}
 
-    # end to end through the public API: pinned host inputs -> device -> host. HostPipeline
-    # copies each sequence in, computes it and copies it out on three streams, so the transfers
-    # of one sequence overlap the work on its neighbours. The last sequence is computed in four
-    # time slices, so that little compute and copy-out is left after the last copy in (2.08 ->
-    # 1.95 ms); cutting every sequence costs more host time to issue than it saves.
-    from linear_attention_05_gb300.pipeline import HostPipeline
+    # end to end through the C ABI with host buffers: kda_chunk_fwd_host copies each sequence's
+    # page-locked inputs in, computes it and copies its outputs back (copies on the library's
+    # two copy streams, compute on this stream), so the transfers of one sequence overlap the
+    # work on its neighbours; the last sequence is computed in four time slices, so that little
+    # compute and copy-back is left after the last copy in.
     host = {k: v.to("cpu").pin_memory() for k, v in x.items() if k != "cu_seqlens" and v is not None}
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     fs_h = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_h.numel() * out_h.element_size() + fs_h.numel() * fs_h.element_size()
-    pl = HostPipeline(n_seq, PREFILL["T"], H, d, d, dtype=torch.bfloat16, device=dev,
-                      groups=n_seq, tail_parts=4)
+    tail = 4
+    dbuf = torch.empty(kda.kda_chunk_fwd_host_buffer_size(T, n_seq, H, d, d, tail_slices=tail),
+                       dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        pl.run(host, out_h, fs_h)
+        kda.kda_chunk_fwd_host(host["q"], host["k"], host["v"], host["log_alpha"], host["beta"],
+                               host["gate"], out_h, host["S0"], fs_h, n_seq, tail_slices=tail,
+                               device_buffer=dbuf, stream=stream)
 
     for _ in range(2):
         e2e_step()
@@ -479,9 +481,9 @@ def run_gpu(args, rank, world, local):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     e2e = {"value": round(world * TOKENS_PER_STEP / (e2e_ms * 1e-3) / 1e6, 3), "unit": "Mtok/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": round(e2e_ms, 4),
+           "ms_per_step": round(e2e_ms, 4), "api": "kda_chunk_fwd_host",
            "overlap": "per-sequence copy/compute pipeline, last sequence in 4 time slices"}
-    del host, pl
+    del host, dbuf
 
     line = {
         "metric": METRIC,

@@ -269,6 +269,47 @@ kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                                  kda_dtype dtype, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd on host-resident buffers: each sequence's inputs are copied
+ * to the device, computed and its outputs copied back, the copies of one
+ * sequence overlapped with the compute of its neighbours (three streams: the
+ * caller's for the compute, two library-owned ones per device for the
+ * copies). It serves callers whose activations live in host memory. The K3
+ * pages have no counterpart to this entry point.
+ *
+ * Arguments and results of kda_chunk_fwd for fixed-length sequences (no
+ * cu_seqlens: n_seq sequences of T_total / n_seq tokens), except:
+ *  q, k, v, log_alpha, beta, gate, out, initial_state, final_state :
+ *      page-locked host memory (cudaHostAlloc, cudaHostRegister), the same
+ *      layouts. Other memory returns KDA_ERR_INVALID_ARG.
+ *  tail_slices   : 1 to 16. The last sequence is computed in this many time
+ *                  slices of equal length, each starting from the state the
+ *                  slice before left, so that less compute and copy-out is left
+ *                  after its last copy in. Its length must be a multiple of
+ *                  64 * tail_slices.
+ *  device_buffer : device memory of at least kda_chunk_fwd_host_buffer_size()
+ *                  bytes, 256-byte aligned: the inputs' and outputs' device
+ *                  copies and the compute's workspace.
+ * Work is ordered after `stream`, and `stream` waits for the last copy back:
+ * the host outputs are complete once the work queued on `stream` so far has
+ * finished. Results are bitwise those of kda_chunk_fwd on the same values in
+ * device memory.
+ */
+kda_status kda_chunk_fwd_host(const void *q, const void *k, const void *v,
+                              const void *log_alpha, const void *beta,
+                              const void *gate, void *out,
+                              const float *initial_state, float *final_state,
+                              int n_seq, int64_t T_total, int H, int dk, int dv,
+                              int chunk, float scale, unsigned flags,
+                              kda_dtype dtype, int tail_slices,
+                              void *device_buffer, size_t device_bytes,
+                              kda_stream_t stream);
+
+/* Bytes of device_buffer kda_chunk_fwd_host needs; 0 for an invalid problem. */
+size_t kda_chunk_fwd_host_buffer_size(int64_t T_total, int n_seq, int H, int dk,
+                                      int dv, int chunk, kda_dtype dtype,
+                                      int tail_slices);
+
+/*
  * One decode step for N sequences, one new token each, against fp32 states
  * resident in device memory (the recurrence above, applied once).
  * Source: K3 explainer section 2 (one corrective write per token) and the

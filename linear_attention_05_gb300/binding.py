@@ -83,6 +83,9 @@ def load(path: str = LIB_PATH):
             "kda_chunk_fwd_checkpoints": ([P, P, P, P, P, P, P, P, P, P, I64, I, P, I, I64, I, I,
                                            I, I, F, U, I, P, SZ, P], I),
             "kda_chunk_fwd_noalloc": ([P, P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, P], I),
+            "kda_chunk_fwd_host": ([P, P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, U, I, I, P,
+                                    SZ, P], I),
+            "kda_chunk_fwd_host_buffer_size": ([I64, I, I, I, I, I, I, I], SZ),
             "kda_decode_step": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, U, I, P], I),
             "kda_segment_summary": ([P, P, P, P, P, I, I64, I, I, I, I, U, I, P, P, P, SZ, P], I),
             "kda_segment_summary_workspace_size": ([I64, I, I, I, I, I, I], SZ),
@@ -300,6 +303,54 @@ def kda_chunk_fwd_noalloc(q, k, v, log_alpha, beta, gate, out, initial_state, fi
                                    _ptr(gate), _ptr(out), _ptr(initial_state), _ptr(final_state),
                                    _ptr(cu_seqlens), n_seq, T, H, dk, dv, chunk, float(scale),
                                    int(flags), _dtype_code(k), _stream(stream))
+    _check(lib, st)
+    return out, final_state
+
+
+def _host_ptr(t):
+    """Address of a contiguous CPU tensor (the library checks that it is page-locked)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor or None")
+    if t.is_cuda:
+        raise ValueError("tensor must be in host memory")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def kda_chunk_fwd_host_buffer_size(T_total, n_seq, H, dk, dv, chunk=CHUNK,
+                                   dtype=KDA_DTYPE_BF16, tail_slices=1):
+    return int(load().kda_chunk_fwd_host_buffer_size(T_total, n_seq, H, dk, dv, chunk, dtype,
+                                                     tail_slices))
+
+
+def kda_chunk_fwd_host(q, k, v, log_alpha, beta, gate, out, initial_state, final_state, n_seq,
+                       scale=1.0, flags=KDA_QK_L2NORM, tail_slices=1, device_buffer=None,
+                       stream=None, chunk=CHUNK, device=None):
+    """Prefill of ``n_seq`` equal-length sequences held in page-locked host tensors (e.g.
+    ``torch.Tensor.pin_memory()``); writes the host tensors ``out`` and (if given)
+    ``final_state``. The copies and the compute are queued on ``stream`` (and the library's
+    copy streams); the host outputs are complete once ``stream`` has drained.
+    ``device_buffer``: a CUDA uint8 tensor of at least kda_chunk_fwd_host_buffer_size bytes,
+    allocated on ``device`` (default: the current device) when None."""
+    lib = load()
+    T, H, dk = k.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(k)
+    _f32_or_none(initial_state, "initial_state")
+    _f32_or_none(final_state, "final_state")
+    need = lib.kda_chunk_fwd_host_buffer_size(T, n_seq, H, dk, dv, chunk, dt, tail_slices)
+    if device_buffer is None:
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        device_buffer = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    nb = device_buffer.numel() * device_buffer.element_size()
+    st = lib.kda_chunk_fwd_host(_host_ptr(q), _host_ptr(k), _host_ptr(v), _host_ptr(log_alpha),
+                                _host_ptr(beta), _host_ptr(gate), _host_ptr(out),
+                                _host_ptr(initial_state), _host_ptr(final_state), n_seq, T, H, dk,
+                                dv, chunk, float(scale), int(flags), dt, int(tail_slices),
+                                _ptr(device_buffer), nb, _stream(stream))
     _check(lib, st)
     return out, final_state
 

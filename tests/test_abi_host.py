@@ -257,3 +257,48 @@ def test_missing_library_fails_loudly(tmp_path):
                        timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "not found" in r.stdout
+
+
+def host_fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, la=FAKE, beta=FAKE, gate=None, out=FAKE, s0=None, sf=None,
+             n_seq=2, T=256, H=2, dk=64, dv=64, chunk=64, scale=1.0, flags=1, dtype=1, tail=1,
+             buf=None, bufb=0, stream=None)
+    a.update(kw)
+    return lib.kda_chunk_fwd_host(a["q"], a["k"], a["v"], a["la"], a["beta"], a["gate"],
+                                  a["out"], a["s0"], a["sf"], a["n_seq"], a["T"], a["H"], a["dk"],
+                                  a["dv"], a["chunk"], a["scale"], a["flags"], a["dtype"],
+                                  a["tail"], a["buf"], a["bufb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dk=96), B.KDA_ERR_UNSUPPORTED),
+    (dict(chunk=32), B.KDA_ERR_UNSUPPORTED),
+    (dict(n_seq=0), B.KDA_ERR_INVALID_ARG),
+    (dict(n_seq=3), B.KDA_ERR_INVALID_ARG),           # 256 tokens do not split into 3
+    (dict(tail=0), B.KDA_ERR_INVALID_ARG),
+    (dict(tail=17), B.KDA_ERR_INVALID_ARG),
+    (dict(tail=4), B.KDA_ERR_INVALID_ARG),            # 128 tokens a sequence: not 4 x 64
+    (dict(buf=None, bufb=0), B.KDA_ERR_WORKSPACE),
+    (dict(buf=FAKE, bufb=100), B.KDA_ERR_WORKSPACE),
+])
+def test_chunk_fwd_host_rejects(lib, kw, status):
+    """kda_chunk_fwd_host's argument errors, all found before any CUDA call."""
+    assert host_fwd(lib, **kw) == status
+    assert b"kda_chunk_fwd_host" in lib.kda_last_error_string()
+
+
+def test_chunk_fwd_host_buffer_size(lib):
+    """The device buffer holds a slot per sequence for every tensor (256-byte aligned), the
+    states and one sequence's workspace; invalid problems give 0."""
+    S = B.kda_chunk_fwd_host_buffer_size
+    n, L, H, d = 4, 4096, 16, 128
+    size = S(n * L, n, H, d, d, tail_slices=4)
+    staging = n * L * H * (5 * d + 1 + d) * 2 + 2 * n * H * d * d * 4
+    ws = B.kda_chunk_fwd_workspace_size(L, 1, H, d, d)   # one sequence's update cards
+    assert staging + ws <= size < staging + ws + (4 << 20)  # + the two hand-over states
+    assert S(n * L, n, H, d, d, tail_slices=1) > 0
+    assert S(3 * 77, 3, 5, 64, 64, tail_slices=1) > 0      # any length with one slice
+    assert S(3 * 77, 3, 5, 64, 64, tail_slices=2) == 0     # slices need 64-token multiples
+    assert S(n * L, n, H, 96, d) == 0
+    assert S(n * L + 1, n, H, d, d) == 0
+    assert S(n * L, n, H, d, d, tail_slices=32) == 0
