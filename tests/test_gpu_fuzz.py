@@ -71,7 +71,7 @@ def _inputs(i):
     return x, S0, cu, fixed, dtype, scale, l2norm
 
 
-@pytest.mark.parametrize("i", range(12), ids=_case_id)
+@pytest.mark.parametrize("i", range(48), ids=_case_id)
 def test_forward_random_case(i):
     x, S0, cu, fixed, dtype, scale, l2norm = _inputs(i)
     n_seq = len(cu) - 1
@@ -89,7 +89,7 @@ def test_forward_random_case(i):
     assert rel_err(np32(fs), rs) <= TOL[dtype]
 
 
-@pytest.mark.parametrize("i", [2, 6, 9, 10], ids=_case_id)
+@pytest.mark.parametrize("i", [2, 6, 9, 10, 14, 18, 22, 27], ids=_case_id)
 def test_backward_random_case(i):
     x, S0, cu, fixed, dtype, scale, l2norm = _inputs(i)
     n_seq = len(cu) - 1
