@@ -95,3 +95,38 @@ def test_pageable_memory_is_rejected():
                              None, None, n_seq)
     assert ei.value.status == B.KDA_ERR_INVALID_ARG
     assert "page-locked" in str(ei.value)
+
+
+def _fuzz_fixed_cases():
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(__file__))
+    from test_gpu_fuzz import _draw
+    return [i for i in range(48) if _draw(i)[1]]
+
+
+@pytest.mark.parametrize("i", _fuzz_fixed_cases())
+def test_fuzz_fixed_lengths_bitwise(i):
+    """The fixed-length cases of the seeded fuzz generator (every head-dim pair, fp32 and bf16,
+    with and without gate and initial state): each sequence computed on its own, the last one
+    in time slices where its length allows, equals the batch computed in one device call."""
+    from test_gpu_fuzz import _draw
+    lengths, fixed, H, dk, dv, dtype, scale, gate, l2norm, with_init = _draw(i)
+    n_seq, L = len(lengths), lengths[0]
+    x = inputs.tokens(n_seq * L, H, dk, dv, dtype, seed=9100 + i, device="cuda", with_gate=gate)
+    S0 = inputs.state(n_seq, H, dk, dv, seed=9200 + i, device="cuda") if with_init else None
+    flags = B.KDA_QK_L2NORM if l2norm else 0
+    out_d, fs_d = B.chunk_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["gate"], S0,
+                              None, n_seq=n_seq, scale=scale, l2norm=l2norm)
+    torch.cuda.synchronize()
+    tail = next((t for t in (4, 2) if L % (64 * t) == 0), 1)
+    h = {n: (x[n].cpu().pin_memory() if x[n] is not None else None) for n in _TOKEN}
+    out_h = torch.empty((n_seq * L, H, dv), dtype=dtype).pin_memory()
+    fs_h = torch.empty((n_seq, H, dk, dv)).pin_memory()
+    B.kda_chunk_fwd_host(h["q"], h["k"], h["v"], h["log_alpha"], h["beta"], h["gate"], out_h,
+                         S0.cpu().pin_memory() if S0 is not None else None, fs_h, n_seq,
+                         scale=scale, flags=flags, tail_slices=tail)
+    torch.cuda.synchronize()
+    assert B.kda_get_error() == B.KDA_OK
+    assert torch.equal(out_h, out_d.cpu())
+    assert torch.equal(fs_h, fs_d.cpu())
