@@ -280,6 +280,9 @@ def host_fwd(lib, **kw):
     (dict(tail=4), B.KDA_ERR_INVALID_ARG),            # 128 tokens a sequence: not 4 x 64
     (dict(buf=None, bufb=0), B.KDA_ERR_WORKSPACE),
     (dict(buf=FAKE, bufb=100), B.KDA_ERR_WORKSPACE),
+    (dict(buf=FAKE + 16, bufb=1 << 40), B.KDA_ERR_INVALID_ARG),   # not 256-byte aligned
+    (dict(q=None, buf=FAKE, bufb=1 << 40), B.KDA_ERR_INVALID_ARG),
+    (dict(out=None, buf=FAKE, bufb=1 << 40), B.KDA_ERR_INVALID_ARG),
 ])
 def test_chunk_fwd_host_rejects(lib, kw, status):
     """kda_chunk_fwd_host's argument errors, all found before any CUDA call."""
