@@ -293,6 +293,12 @@ kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
  * the host outputs are complete once the work queued on `stream` so far has
  * finished. Results are bitwise those of kda_chunk_fwd on the same values in
  * device memory.
+ * Status: KDA_ERR_UNSUPPORTED for dk, dv, chunk or dtype; KDA_ERR_INVALID_ARG
+ * for unequal lengths, a bad tail_slices, a missing or pageable buffer or a
+ * misaligned device_buffer; KDA_ERR_WORKSPACE when device_buffer is NULL or
+ * too small (all before any copy or launch); KDA_ERR_CUDA when a copy, event or
+ * launch fails, after the copy streams are joined back into `stream`; and
+ * kda_chunk_fwd's own codes for the compute.
  */
 kda_status kda_chunk_fwd_host(const void *q, const void *k, const void *v,
                               const void *log_alpha, const void *beta,
